@@ -1,0 +1,82 @@
+"""The oracle against its pins, and the pins against planted mistakes.
+
+Runs on the CPU only.  Each pin is defined in ``tests/oracle_pins.py``.  The
+planted-mistake test compiles altered copies of the oracle source (in a
+temporary directory, never in the tree) and requires every alteration to be
+caught by at least one pin.
+"""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "qsa_oracle.c")
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+# (name, text in the oracle source, replacement).  Each is a plausible slip:
+# a dropped term, a wrong sign or index, an operand taken from the wrong array.
+MUTANTS = [
+    ("drop_v_scale", "++d) out[d] += w * (vs * (double)v_row[d]);",
+     "++d) out[d] += w * ((double)v_row[d]);"),
+    ("partial_drops_v_scale", "o_out[d] += w * (vs * (double)v_row[d]);",
+     "o_out[d] += w * ((double)v_row[d]);"),
+    ("partial_l_off_by_max", "double w = exp(s[i] - m);\n            l += w;",
+     "double w = exp(s[i] - m);\n            l += 1.0;"),
+    ("drop_k_scale", "double k_hat = (double)k_scale * (double)k_row[d];",
+     "double k_hat = (double)k_row[d];"),
+    ("drop_softmax_scale", "return softmax_scale * dot;", "return dot;"),
+    ("flip_exp_sign", "double w = exp(s[i] - m);\n            L += w;",
+     "double w = exp(m - s[i]);\n            L += w;"),
+    ("no_max_shift", "double w = exp(s[i] - m);\n            L += w;",
+     "double w = exp(s[i]);\n            L += w;"),
+    ("position_not_slot", "cell_score(D, q, k_codes + (size_t)slot * D",
+     "cell_score(D, q, k_codes + (size_t)(sel[start + i] % pool_cells) * D"),
+    ("k_from_v_pool", "int err = score_range(D, pool_cells, page_table_len, q, k_codes, k_scale, page_table,\n                          sel, 0, n_sel",
+     "int err = score_range(D, pool_cells, page_table_len, q, v_codes, k_scale, page_table,\n                          sel, 0, n_sel"),
+    ("masked_as_slot0", "if (s == -1) { *slot = -1; return ORACLE_OK; }",
+     "if (s == -1) { *slot = 0; return ORACLE_OK; }"),
+    ("chunk_ignores_start", "sel[start + i], &slot", "sel[i], &slot"),
+    ("merge_no_rescale", "double f = exp(m[c] - M);", "double f = 1.0;"),
+    ("kv_head_by_modulo", "int g = h / H;", "int g = h % G;"),
+    ("normaliser_dropped", "for (int d = 0; d < D; ++d) out[d] /= L;\n    }\n    free(slots);",
+     "\n    }\n    free(slots);"),
+    ("v_row_from_position", "const int8_t *v_row = v_codes + (size_t)slots[i] * D;\n            double vs = (double)v_scale[slots[i]];\n            for (int d = 0; d < D; ++d) out[d]",
+     "const int8_t *v_row = v_codes + (size_t)(sel[i] % pool_cells) * D;\n            double vs = (double)v_scale[slots[i]];\n            for (int d = 0; d < D; ++d) out[d]"),
+]
+
+
+def test_mutants_are_distinct_edits():
+    src = open(ORACLE_SRC).read()
+    for name, old, _ in MUTANTS:
+        assert src.count(old) == 1, f"mutant {name}: anchor found {src.count(old)} times"
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1
+    tmp = tempfile.mkdtemp(prefix="oracle_mutant_")
+    try:
+        path = os.path.join(tmp, "mutant.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        lib_path = oracle.compile_library(path, os.path.join(tmp, f"lib_{name}.so"))
+        lib = oracle.load(lib_path)
+        failed = []
+        for pin in PINS:
+            try:
+                pin(lib)
+            except (AssertionError, oracle.OracleError, FloatingPointError, ValueError):
+                failed.append(pin.__name__)
+        assert failed, f"no pin catches the planted mistake {name}"
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
