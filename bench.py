@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""Benchmark of QSA decode attention over INT8 K/V pools.
+
+Headline workload: the pages' kernel-table shape -- 1 KV head x 12 query
+heads, head_dim 256, a 32,768-cell INT8 pool with per-cell scales, a
+permuted page table, 2,051 selected cells, chunk 128 -- with the MTP verify
+window swept over 1/2/3/4 queries.  One step = the four calls (T = 1, 2, 3,
+4), each a CUDA graph of one library call (chunk kernel + merge kernel).
+
+Metric: selected KV cells/s (sum of selected cells over the step's calls
+divided by the step time), with the achieved HBM GB/s of the calls against
+the measured HBM peak.  L2 is flushed (a 512 MB write) before every timed
+step, so every call reads its cells from HBM.  Inputs are synthetic and
+seeded; nothing is read from disk.
+
+Arms:
+  default            the CUDA library (this repo), N GPUs via torchrun
+  --impl reference   the fp64 CPU oracle on the host cores (rank 0 only)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "selected KV cells/s and achieved HBM GB/s (% of roofline) per decode-attn call"
+UNIT = "cells/s"
+WORKLOAD = ("qsa_decode: 1 KV head x 12 query heads, head_dim 256, INT8 K/V pool of 32768 "
+            "cells with per-cell fp32 scales, permuted page table, 2051 selected cells, "
+            "queries swept 1/2/3/4 (one call each), chunk 128, fp32 output")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20
+SWEEP = (1, 2, 3, 4)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def algorithmic_bytes(p) -> int:
+    """Bytes one call must move at minimum: per selected cell and KV head the
+    K and V rows (256 B each) and the two fp32 scales; per selected cell the
+    list entry and page entry (4 B each); the queries (read) and outputs
+    (written) once."""
+    n_total = int(p.n_selected.sum())
+    q_bytes = p.q.size * (2 if p.q_dtype == "bf16" else 4)
+    out_bytes = p.n_seq * p.n_queries * p.n_kv_heads * p.q_per_kv * p.head_dim * 4
+    per_cell = p.n_kv_heads * (2 * p.head_dim + 8) + 8
+    return n_total * per_cell + q_bytes + out_bytes
+
+
+def flops(p) -> int:
+    """Multiply-adds of the two contractions (scores and P.V), x2."""
+    n_total = int(p.n_selected.sum())
+    return 2 * 2 * n_total * p.n_kv_heads * p.rows_per_kv * p.head_dim
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.1)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_selection_int8_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# DRAM traffic per call of the dominant kernel from an ncu capture, valid
+# only while the kernel source hashes to the recorded digest.
+TRAFFIC = {}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle arm
+
+def oracle_sample(problems, seconds: float):
+    """Run the oracle over whole calls of the workload until `seconds` of wall
+    time pass (at least one full sweep); returns (cells/s, cores, sample)."""
+    import oracle
+    oracle.build()
+    cells = 0
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        for p in problems:
+            oracle.decode_attn(p)
+            cells += int(p.n_selected.sum())
+            calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return cells / el, oracle.threads(), f"{calls} whole calls of the T=1..4 sweep in {el:.1f} s"
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import qsa_workloads as wl
+    import oracle
+    oracle.build()
+    problems = [wl.qsa_decode(T) for T in SWEEP]
+    for _ in range(max(args.warmup, 0)):
+        for p in problems:
+            oracle.decode_attn(p)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for p in problems:
+            oracle.decode_attn(p)
+        times.append(time.perf_counter() - t0)
+        if sum(times) > 120:
+            break
+    step = statistics.mean(times)
+    cells = sum(int(p.n_selected.sum()) for p in problems)
+    value = cells / step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+        "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "arm": "fp64 CPU oracle (unchunked softmax), host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{len(times)} whole T=1..4 sweeps (every output row)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def time_graphs(torch, graphs, flush, steps, warmup, stream):
+    """Replay each graph in order per step; L2 flushed before each step.
+    Returns per-step lists of per-graph durations in ms."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+    for _ in range(warmup):
+        flush.zero_()
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    per_step = []
+    pending = []
+    for s in range(steps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+        evs[0].record(stream)
+        for i, g in enumerate(graphs):
+            g.replay()
+            evs[i + 1].record(stream)
+        pending.append(evs)
+        if len(pending) >= 256:
+            torch.cuda.synchronize()
+            for e in pending:
+                per_step.append([e[i].elapsed_time(e[i + 1]) for i in range(len(graphs))])
+            pending = []
+    torch.cuda.synchronize()
+    for e in pending:
+        per_step.append([e[i].elapsed_time(e[i + 1]) for i in range(len(graphs))])
+    del ev
+    return per_step
+
+
+def capture(torch, dp, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        dp.run()  # warm (no allocation inside the library)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        dp.run()
+    return g
+
+
+def measure_extra(torch, qsa, wl, flush, stream, hbm_peak, tflops_peak, budget_s=60.0):
+    """µs per call and roofline of the other workloads (context, not the headline)."""
+    res = {}
+    t_start = time.perf_counter()
+    specs = [("tiny_decode", wl.tiny_decode, 200), ("batched_decode", wl.batched_decode, 100),
+             ("long_context", wl.long_context, 50), ("prompt_shaped", wl.prompt_shaped, 5)]
+    for name, make, iters in specs:
+        if time.perf_counter() - t_start > budget_s:
+            res[name] = {"skipped": "time budget"}
+            continue
+        p = make()
+        dp = qsa.DeviceProblem(p)
+        g = capture(torch, dp, stream)
+        per = time_graphs(torch, [g], flush, iters, 3, stream)
+        us = statistics.median([x[0] for x in per]) * 1e3
+        cells = int(p.n_selected.sum())
+        ab = algorithmic_bytes(p)
+        entry = {"us_per_call": round(us, 2), "cells_per_s": cells / (us * 1e-6),
+                 "algorithmic_bytes": ab, "hbm_gbs": ab / (us * 1e-6) / 1e9}
+        entry["hbm_frac"] = entry["hbm_gbs"] / hbm_peak
+        if name == "prompt_shaped":
+            entry["tflops"] = flops(p) / (us * 1e-6) / 1e12
+            entry["tensor_frac_bf16"] = entry["tflops"] / tflops_peak
+        res[name] = entry
+        del dp, g
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("the CUDA arm needs a GPU")
+    torch.cuda.set_device(local)
+    from sparse_selection_int8_gb300 import build as qsa_build
+    if rank == 0:
+        qsa_build.build()
+    dist_barrier(world)
+    import sparse_selection_int8_gb300 as qsa
+    import qsa_workloads as wl
+
+    hbm_peak, tflops_peak, peak_src = measured_peaks()
+    stream = torch.cuda.Stream()
+    problems = [wl.qsa_decode(T) for T in SWEEP]
+    dps = [qsa.DeviceProblem(p) for p in problems]
+    graphs = [capture(torch, dp, stream) for dp in dps]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        per_step = time_graphs(torch, graphs, flush, args.steps, args.warmup, stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+
+    step_ms = [sum(x) for x in per_step]
+    total_ms = dist_max(sum(step_ms), world)
+    ms_per_step = total_ms / len(step_ms)
+    cells_step = sum(int(p.n_selected.sum()) for p in problems)
+    value = world * cells_step * len(step_ms) / (total_ms * 1e-3)
+    call_ms = [statistics.mean([x[i] for x in per_step]) for i in range(len(SWEEP))]
+    bytes_step = sum(algorithmic_bytes(p) for p in problems)
+    achieved = bytes_step / (sum(call_ms) * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: per step, the
+    # queries and selection lists go host->device from pinned memory and the
+    # outputs come back; the pools and page tables stay resident.
+    h_q = [torch.from_numpy(p.q).pin_memory() for p in problems]
+    h_sel = [torch.from_numpy(p.sel).pin_memory() for p in problems]
+    h_out = [torch.empty(dp.out.shape, dtype=torch.float32).pin_memory() for dp in dps]
+    h2d = sum(x.numel() * x.element_size() for x in h_q + h_sel)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    e2e_steps = max(50, min(args.steps, 500))
+    e2e_times = []
+    with torch.cuda.stream(stream):
+        for s in range(e2e_steps + 5):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i, dp in enumerate(dps):
+                dp.q.copy_(h_q[i], non_blocking=True)
+                dp.sel.copy_(h_sel[i], non_blocking=True)
+                dp.run(stream=stream)
+                h_out[i].copy_(dp.out, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if s >= 5:
+                e2e_times.append(e0.elapsed_time(e1))
+    e2e_ms = dist_max(statistics.mean(e2e_times), world)
+    e2e_value = world * cells_step / (e2e_ms * 1e-3)
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = measure_extra(torch, qsa, wl, flush, stream, hbm_peak, tflops_peak)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cps, cores, sample = oracle_sample(problems, args.cpu_seconds)
+        cpu = {"value": cps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    digest = source_digest("qsa_chunk_simt.cu")
+    traffic = TRAFFIC.get(digest)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": len(step_ms), "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "flushed (512 MB write) before every timed step",
+                       "launch": "one CUDA graph per call, replayed", "parallelism":
+                       f"replica per GPU x{world}" if world > 1 else "1 GPU"},
+            "us_per_call": {f"T{T}": round(ms * 1e3, 3) for T, ms in zip(SWEEP, call_ms)},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                         "peak_source": peak_src,
+                         "timed_unit": "one library call (chunk kernel + merge kernel)"},
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * len(SWEEP) * len(step_ms),
+            "cpu_baseline": cpu,
+            "other_workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    dist_barrier(world)
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,170 @@
+/*
+ * qsa.h -- C ABI of the QSA decode-attention library (libqsa.so).
+ *
+ * QSA decode attention: a handful of decode/verify queries (1-4 per step, the
+ * MTP window) attend to a sparse selection of cells (one cell = one token's
+ * K/V entry) drawn from INT8 K/V pools.  Cells are reached through a permuted
+ * page table; each KV head is shared by q_per_kv query heads (12 on the
+ * pages) at head_dim 256.  The selected list is split into chunks; each chunk
+ * emits partials (running max m, sum of exponentials l, unnormalised P.V o)
+ * and a merge combines them by log-sum-exp rescaling into the fp32 output.
+ *
+ * Defining passages: "Strata PR #2220, attn_chunk_q8_v3_kernel" (opening
+ * description: decode attention over the QSA selection, INT8 pools, 12 query
+ * heads, chunk partials and merged output, the two entry points
+ * qsa_decode_attn_step / qsa_decode_attn_batch; kernel table: permuted page
+ * table, 600 / 2,051 selected cells, 1-4 queries; prompt-shaped parity:
+ * 2,048 queries against 32K INT8 cells), and "Strata issue #8, round 9:
+ * performance candidate set on v0.2.9", R9-gpu-11 (page -1 masking; partial
+ * accumulators, maxima and denominators; 0/1/2/3/63/64/65 selected cells).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument of a compute call is a DEVICE pointer, except the
+ *     qsa_shape pointer, which is host memory read during the call only.
+ *   - The caller owns every buffer.  The library allocates nothing, never
+ *     synchronises, and is stateless and thread-safe; calls are asynchronous
+ *     on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Host-visible argument errors return a negative qsa_status and launch
+ *     nothing.  A failed launch returns QSA_ERR_CUDA.
+ *   - Device-side input errors never trap: an out-of-range list entry or page
+ *     slot is treated as masked and raises a bit in the optional status word.
+ *
+ * Dequantised values: k_hat = k_scale[cell] * K[cell][d] (same for V), a
+ * symmetric per-cell fp32 scale with no zero point.  Scores
+ * s = softmax_scale * (q . k_hat).  A page entry of -1 masks its cell: the
+ * cell is left out of the softmax exactly as if it were not listed.  A row
+ * with no valid cell outputs zeros.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qsa_status {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned buffer */
+    QSA_ERR_UNSUPPORTED = -2, /* a shape outside what the kernels implement */
+    QSA_ERR_WORKSPACE = -3,   /* workspace smaller than qsa_workspace_bytes() */
+    QSA_ERR_CUDA = -4         /* a CUDA launch or runtime call failed */
+} qsa_status;
+
+typedef enum qsa_dtype {
+    QSA_F32 = 0,  /* fp32 queries (decode) */
+    QSA_BF16 = 1  /* bf16 queries (the prompt-shaped case) */
+} qsa_dtype;
+
+/* Which kernel family runs the chunk step.  AUTO picks by shape: the
+ * cells-on-M tensor-core kernel for decode windows (q_per_kv * n_queries
+ * <= 64 rows), the rows-on-M tensor-core kernel for prompt-shaped calls.
+ * SIMT forces the CUDA-core kernel (kept as an independent second path). */
+typedef enum qsa_algo {
+    QSA_ALGO_AUTO = 0,
+    QSA_ALGO_SIMT = 1,
+    QSA_ALGO_TCGEN05 = 2
+} qsa_algo;
+
+/* Bits of the optional device status word (OR-ed in by the kernels; the
+ * library never clears it -- the caller zeroes it when it wants a fresh read). */
+#define QSA_STATUS_BAD_POSITION 0x1u /* a selected position outside [0, page_table_len) */
+#define QSA_STATUS_BAD_SLOT 0x2u     /* a page entry outside [0, pool_cells) and not -1 */
+#define QSA_STATUS_BAD_OFFSETS 0x4u  /* batch offsets decreasing or a list above max_selected */
+
+typedef struct qsa_shape {
+    int32_t n_kv_heads;     /* G: KV heads per sequence (>= 1) */
+    int32_t q_per_kv;       /* H: query heads per KV head (1..64; 12 on the pages) */
+    int32_t head_dim;       /* D: must be 256 */
+    int32_t n_queries;      /* T: queries per sequence (1-4 decode; up to 65536) */
+    int32_t pool_cells;     /* N_pool: pool rows per (sequence, KV head) (>= 1) */
+    int32_t page_table_len; /* N_log: page-table entries per sequence (>= 1) */
+    int32_t chunk_cells;    /* C: selected-list positions per chunk (>= 1) */
+    float softmax_scale;    /* multiplies q . k_hat (1/16 on the pages' shapes) */
+    int32_t q_dtype;        /* qsa_dtype */
+    int32_t algo;           /* qsa_algo */
+} qsa_shape;
+
+/*
+ * Workspace size for a call with this shape, n_seq sequences and at most
+ * max_selected selected cells per sequence.  Writes the byte count to
+ * *bytes.  The workspace holds the chunk partials (and, for prompt-shaped
+ * calls, converted operand images).  It needs no initialisation and no
+ * clearing between calls; its base must be 256-byte aligned.
+ * Errors: QSA_ERR_INVALID_ARG for a null pointer or a non-positive field;
+ * QSA_ERR_UNSUPPORTED for head_dim != 256 or sizes beyond the limits above.
+ */
+qsa_status qsa_workspace_bytes(const qsa_shape *shape, int32_t n_seq, int32_t max_selected,
+                               size_t *bytes);
+
+/*
+ * One sequence.
+ *   q          [T][G*H][D]  fp32 or bf16 (per shape->q_dtype); query head j
+ *              of KV head g is head index g*H + j.  16-byte aligned.
+ *   k_pool     [G][pool_cells][D] int8 codes; v_pool the same.  16-byte aligned.
+ *   k_scale    [G][pool_cells] fp32 per-cell scales; v_scale the same.
+ *   page_table [page_table_len] int32: pool slot of each logical position,
+ *              or -1 (masked).
+ *   sel        [n_sel] int32 logical positions (the QSA selection), in list
+ *              order; chunk c covers list positions [c*C, min((c+1)*C, n_sel)).
+ *   out        [T][G*H][D] fp32, fully written (zeros for rows with no valid
+ *              cell).  Must not alias any input.
+ *   workspace  >= qsa_workspace_bytes(shape, 1, n_sel) bytes.
+ *   status     optional (may be NULL) device uint32 word; see QSA_STATUS_*.
+ *   stream     cudaStream_t.
+ * n_sel = 0 is valid and writes zeros.
+ */
+qsa_status qsa_decode_attn_step(const qsa_shape *shape, const void *q, const int8_t *k_pool,
+                                const int8_t *v_pool, const float *k_scale,
+                                const float *v_scale, const int32_t *page_table,
+                                const int32_t *sel, int32_t n_sel, float *out, void *workspace,
+                                size_t workspace_bytes, uint32_t *status, void *stream);
+
+/*
+ * n_seq independent sequences in one launch sequence.
+ *   q          [n_seq][T][G*H][D]
+ *   k_pool     [n_seq][G][pool_cells][D] (v_pool the same)
+ *   k_scale    [n_seq][G][pool_cells]    (v_scale the same)
+ *   page_table [n_seq][page_table_len]
+ *   sel        concatenated lists; sequence b uses
+ *              sel[sel_offsets[b] .. sel_offsets[b+1]).
+ *   sel_offsets [n_seq+1] int32, device, non-decreasing, sel_offsets[0] = 0.
+ *   max_selected  host-side upper bound on every list length; it sizes the
+ *              grid and the workspace, so one captured CUDA graph serves any
+ *              lists within the bound.  A longer list is clamped to
+ *              max_selected and raises QSA_STATUS_BAD_OFFSETS.
+ *   out        [n_seq][T][G*H][D] fp32.
+ *   workspace  >= qsa_workspace_bytes(shape, n_seq, max_selected) bytes.
+ */
+qsa_status qsa_decode_attn_batch(const qsa_shape *shape, int32_t n_seq, const void *q,
+                                 const int8_t *k_pool, const int8_t *v_pool,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *page_table, const int32_t *sel,
+                                 const int32_t *sel_offsets, int32_t max_selected, float *out,
+                                 void *workspace, size_t workspace_bytes, uint32_t *status,
+                                 void *stream);
+
+/*
+ * Where the chunk partials of the last call with this (shape, n_seq,
+ * max_selected) sit inside `workspace` (device pointers, read-only).
+ *   m, l  [n_seq][G][n_chunks][T*H]      fp32; row r = t*H + j
+ *   o     [n_seq][G][n_chunks][T*H][D]   fp32
+ * with n_chunks = ceil(max_selected / chunk_cells).  For chunk c of sequence
+ * b: m = max score (natural-log units, -inf when the chunk has no valid
+ * cell), l = sum exp(s - m), o = sum exp(s - m) * v_hat.  Chunks at or past
+ * ceil(n_b / C) are not written.  Any of m, l, o may be NULL.
+ */
+qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_selected,
+                             const void *workspace, const float **m, const float **l,
+                             const float **o, int32_t *n_chunks);
+
+/* Static description of a status code. */
+const char *qsa_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -1,0 +1,178 @@
+// qsa_api.cu -- the C ABI declared in include/qsa.h: argument checks,
+// workspace carve-up, kernel choice and launches.  Nothing here allocates,
+// synchronises or keeps state between calls.
+#include <math.h>
+#include <string.h>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kMaxRowsPerKv = 64 * 65536; // q_per_kv <= 64, n_queries <= 65536
+constexpr size_t kWorkspaceAlign = 256;
+
+bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+qsa_status check_shape(const qsa_shape *s)
+{
+    if (!s) return QSA_ERR_INVALID_ARG;
+    if (s->n_kv_heads < 1 || s->q_per_kv < 1 || s->n_queries < 1 || s->pool_cells < 1 ||
+        s->page_table_len < 1 || s->chunk_cells < 1)
+        return QSA_ERR_INVALID_ARG;
+    if (!isfinite(s->softmax_scale)) return QSA_ERR_INVALID_ARG;
+    if (s->q_dtype != QSA_F32 && s->q_dtype != QSA_BF16) return QSA_ERR_INVALID_ARG;
+    if (s->algo != QSA_ALGO_AUTO && s->algo != QSA_ALGO_SIMT && s->algo != QSA_ALGO_TCGEN05)
+        return QSA_ERR_INVALID_ARG;
+    if (s->head_dim != kHeadDim) return QSA_ERR_UNSUPPORTED;
+    if (s->q_per_kv > 64 || s->n_queries > 65536 || s->n_kv_heads > 65535)
+        return QSA_ERR_UNSUPPORTED;
+    if ((long long)s->q_per_kv * s->n_queries > kMaxRowsPerKv) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+Workspace carve(const qsa_shape *s, int n_seq, int max_selected)
+{
+    Workspace w{};
+    const size_t R = (size_t)s->q_per_kv * s->n_queries;
+    const size_t n_chunks = max_selected > 0 ? ((size_t)max_selected + s->chunk_cells - 1) / s->chunk_cells : 0;
+    const size_t rows = (size_t)n_seq * s->n_kv_heads * n_chunks * R;
+    w.off_m = 0;
+    w.off_l = align_up(w.off_m + rows * sizeof(float), kWorkspaceAlign);
+    w.off_o = align_up(w.off_l + rows * sizeof(float), kWorkspaceAlign);
+    w.off_extra = align_up(w.off_o + rows * kHeadDim * sizeof(float), kWorkspaceAlign);
+    w.total = w.off_extra;
+    return w;
+}
+
+qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_pool,
+               const int8_t *v_pool, const float *k_scale, const float *v_scale,
+               const int32_t *page_table, const int32_t *sel, const int32_t *sel_offsets,
+               int n_sel_single, int max_selected, float *out, void *workspace,
+               size_t workspace_bytes, uint32_t *status, void *stream)
+{
+    qsa_status st = check_shape(s);
+    if (st != QSA_OK) return st;
+    if (n_seq < 1 || n_seq > 65535 || max_selected < 0) return QSA_ERR_INVALID_ARG;
+    if (!q || !k_pool || !v_pool || !k_scale || !v_scale || !page_table || !out)
+        return QSA_ERR_INVALID_ARG;
+    if (max_selected > 0 && !sel) return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+        !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(page_table, 4) ||
+        (sel && !aligned(sel, 4)) || (status && !aligned(status, 4)))
+        return QSA_ERR_INVALID_ARG;
+    if ((const void *)out == q || (const void *)out == (const void *)k_pool ||
+        (const void *)out == (const void *)v_pool)
+        return QSA_ERR_INVALID_ARG;
+    const Workspace w = carve(s, n_seq, max_selected);
+    if (w.total > 0 && (!workspace || !aligned(workspace, kWorkspaceAlign)))
+        return QSA_ERR_INVALID_ARG;
+    if (workspace_bytes < w.total) return QSA_ERR_WORKSPACE;
+
+    Params p{};
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.page_table = page_table;
+    p.sel = sel;
+    p.sel_offsets = sel_offsets;
+    p.out = out;
+    char *ws = static_cast<char *>(workspace);
+    p.part_m = reinterpret_cast<float *>(ws + w.off_m);
+    p.part_l = reinterpret_cast<float *>(ws + w.off_l);
+    p.part_o = reinterpret_cast<float *>(ws + w.off_o);
+    p.status = status;
+    p.n_sel_single = n_sel_single;
+    p.n_seq = n_seq;
+    p.G = s->n_kv_heads;
+    p.H = s->q_per_kv;
+    p.T = s->n_queries;
+    p.R = s->q_per_kv * s->n_queries;
+    p.pool_cells = s->pool_cells;
+    p.page_table_len = s->page_table_len;
+    p.chunk_cells = s->chunk_cells;
+    p.max_selected = max_selected;
+    p.n_chunks = max_selected > 0 ? (max_selected + s->chunk_cells - 1) / s->chunk_cells : 0;
+    p.q_bf16 = s->q_dtype == QSA_BF16;
+    p.scale_log2 = s->softmax_scale * kLog2e;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_chunk_simt(p, cs);
+    if (e != cudaSuccess) return QSA_ERR_CUDA;
+    e = launch_merge(p, cs);
+    if (e != cudaSuccess) return QSA_ERR_CUDA;
+    return QSA_OK;
+}
+
+} // namespace
+} // namespace qsa
+
+extern "C" {
+
+qsa_status qsa_workspace_bytes(const qsa_shape *shape, int32_t n_seq, int32_t max_selected,
+                               size_t *bytes)
+{
+    qsa_status st = qsa::check_shape(shape);
+    if (st != QSA_OK) return st;
+    if (!bytes || n_seq < 1 || max_selected < 0) return QSA_ERR_INVALID_ARG;
+    *bytes = qsa::carve(shape, n_seq, max_selected).total;
+    return QSA_OK;
+}
+
+qsa_status qsa_decode_attn_step(const qsa_shape *shape, const void *q, const int8_t *k_pool,
+                                const int8_t *v_pool, const float *k_scale,
+                                const float *v_scale, const int32_t *page_table,
+                                const int32_t *sel, int32_t n_sel, float *out, void *workspace,
+                                size_t workspace_bytes, uint32_t *status, void *stream)
+{
+    if (n_sel < 0) return QSA_ERR_INVALID_ARG;
+    return qsa::run(shape, 1, q, k_pool, v_pool, k_scale, v_scale, page_table, sel, nullptr,
+                    n_sel, n_sel, out, workspace, workspace_bytes, status, stream);
+}
+
+qsa_status qsa_decode_attn_batch(const qsa_shape *shape, int32_t n_seq, const void *q,
+                                 const int8_t *k_pool, const int8_t *v_pool,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *page_table, const int32_t *sel,
+                                 const int32_t *sel_offsets, int32_t max_selected, float *out,
+                                 void *workspace, size_t workspace_bytes, uint32_t *status,
+                                 void *stream)
+{
+    if (!sel_offsets || !qsa::aligned(sel_offsets, 4)) return QSA_ERR_INVALID_ARG;
+    return qsa::run(shape, n_seq, q, k_pool, v_pool, k_scale, v_scale, page_table, sel,
+                    sel_offsets, 0, max_selected, out, workspace, workspace_bytes, status,
+                    stream);
+}
+
+qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_selected,
+                             const void *workspace, const float **m, const float **l,
+                             const float **o, int32_t *n_chunks)
+{
+    qsa_status st = qsa::check_shape(shape);
+    if (st != QSA_OK) return st;
+    if (n_seq < 1 || max_selected < 0 || !workspace) return QSA_ERR_INVALID_ARG;
+    const qsa::Workspace w = qsa::carve(shape, n_seq, max_selected);
+    const char *ws = static_cast<const char *>(workspace);
+    if (m) *m = reinterpret_cast<const float *>(ws + w.off_m);
+    if (l) *l = reinterpret_cast<const float *>(ws + w.off_l);
+    if (o) *o = reinterpret_cast<const float *>(ws + w.off_o);
+    if (n_chunks)
+        *n_chunks = max_selected > 0 ? (max_selected + shape->chunk_cells - 1) / shape->chunk_cells : 0;
+    return QSA_OK;
+}
+
+const char *qsa_status_string(int32_t status)
+{
+    switch (status) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case QSA_ERR_WORKSPACE: return "workspace too small";
+    case QSA_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+    }
+}
+
+} // extern "C"

@@ -1,0 +1,125 @@
+// qsa_internal.cuh -- shared definitions of the QSA decode-attention kernels.
+//
+// Path of one call (the pages' "chunk kernel + merge", "Strata PR #2220,
+// attn_chunk_q8_v3_kernel", opening description):
+//   a1  selected list entry -> page-table slot (-1 masks the cell)
+//   a2  INT8 K/V row gather + dequantise with the per-cell scales
+//   a3  scores of every query row against every cell of the chunk
+//   a4  chunk online softmax and P.V -> partials (m, l, o)
+//   a5  split-K merge of the partials by log-sum-exp rescaling -> output
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+constexpr int kHeadDim = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Everything a kernel needs about one call; passed by value.
+struct Params {
+    const void *q;             // [n_seq][T][G*H][D] f32 or bf16
+    const int8_t *k_pool;      // [n_seq][G][pool][D]
+    const int8_t *v_pool;
+    const float *k_scale;      // [n_seq][G][pool]
+    const float *v_scale;
+    const int32_t *page_table; // [n_seq][N_log]
+    const int32_t *sel;        // concatenated lists
+    const int32_t *sel_offsets; // [n_seq+1] or nullptr (single sequence)
+    float *out;                // [n_seq][T][G*H][D]
+    float *part_m;             // [n_seq][G][n_chunks][R]
+    float *part_l;
+    float *part_o;             // [n_seq][G][n_chunks][R][D]
+    uint32_t *status;          // optional
+    int32_t n_sel_single;      // list length when sel_offsets == nullptr
+    int32_t n_seq, G, H, T, R; // R = T*H rows per KV head
+    int32_t pool_cells, page_table_len, chunk_cells, n_chunks, max_selected;
+    int32_t q_bf16;
+    float scale_log2;          // softmax_scale * log2(e)
+};
+
+// Workspace carve-up shared by the host code of every path.
+struct Workspace {
+    size_t off_m, off_l, off_o, off_extra, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__device__ __forceinline__ void raise_status(const Params &p, uint32_t bits)
+{
+    if (p.status) atomicOr(p.status, bits);
+}
+
+// List range of sequence b: [*start, *start + *n).  Bad offsets are clamped
+// and reported instead of trusted.
+__device__ __forceinline__ void seq_range(const Params &p, int b, int *start, int *n)
+{
+    if (p.sel_offsets == nullptr) {
+        *start = 0;
+        *n = p.n_sel_single;
+        return;
+    }
+    int o0 = __ldg(p.sel_offsets + b);
+    int o1 = __ldg(p.sel_offsets + b + 1);
+    int len = o1 - o0;
+    if (o0 < 0 || len < 0) {
+        raise_status(p, QSA_STATUS_BAD_OFFSETS);
+        *start = 0;
+        *n = 0;
+        return;
+    }
+    if (len > p.max_selected) {
+        raise_status(p, QSA_STATUS_BAD_OFFSETS);
+        len = p.max_selected;
+    }
+    *start = o0;
+    *n = len;
+}
+
+// Step a1: logical position -> pool slot of sequence b; -1 when masked or
+// out of range (out-of-range entries also raise a status bit).
+__device__ __forceinline__ int resolve_slot(const Params &p, int b, int pos)
+{
+    if (pos < 0 || pos >= p.page_table_len) {
+        raise_status(p, QSA_STATUS_BAD_POSITION);
+        return -1;
+    }
+    int slot = __ldg(p.page_table + (size_t)b * p.page_table_len + pos);
+    if (slot == -1) return -1;
+    if (slot < 0 || slot >= p.pool_cells) {
+        raise_status(p, QSA_STATUS_BAD_SLOT);
+        return -1;
+    }
+    return slot;
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *ptr)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
+{
+    return __uint_as_float(bits16 << 16);
+}
+
+// Host-side launchers (defined in the kernel translation units).
+cudaError_t launch_chunk_simt(const Params &p, cudaStream_t stream);
+cudaError_t launch_merge(const Params &p, cudaStream_t stream);
+
+} // namespace qsa

@@ -1,0 +1,109 @@
+"""Device-resident problem: uploads host arrays with torch and calls the C ABI.
+
+Only marshalling lives here: torch allocates device memory and copies the
+host arrays; every computation is a libqsa kernel launched through
+``qsa_decode_attn_step`` / ``qsa_decode_attn_batch``.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+from . import (QSA_ALGO_AUTO, QSA_BF16, QSA_F32, make_shape, qsa_decode_attn_batch,
+               qsa_decode_attn_step, qsa_partials_view, qsa_workspace_bytes)
+
+
+def _to_dev(torch, a: np.ndarray, device, pin: bool = False):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if pin:
+        t = t.pin_memory()
+    return t.to(device, non_blocking=pin)
+
+
+class DeviceProblem:
+    """A problem (as drawn by the input generator) resident in device memory.
+
+    Attributes mirror the C ABI arguments; ``out`` and ``workspace`` are
+    allocated once and reused by every ``run``.
+    """
+
+    def __init__(self, p, device: str = "cuda", algo: int = QSA_ALGO_AUTO,
+                 max_selected: Optional[int] = None):
+        import torch
+        self.p = p
+        self.device = device
+        if p.q_dtype == "bf16":
+            self.q = _to_dev(torch, np.asarray(p.q).view(np.int16), device).view(torch.bfloat16)
+        else:
+            self.q = _to_dev(torch, p.q.astype(np.float32), device)
+        self.k_pool = _to_dev(torch, p.k_pool, device)
+        self.v_pool = _to_dev(torch, p.v_pool, device)
+        self.k_scale = _to_dev(torch, p.k_scale, device)
+        self.v_scale = _to_dev(torch, p.v_scale, device)
+        self.page_table = _to_dev(torch, p.page_table, device)
+        self.sel = _to_dev(torch, p.sel if p.sel.size else np.zeros(1, np.int32), device)
+        self.sel_offsets = _to_dev(torch, p.sel_offsets, device)
+        self.n_seq = p.n_seq
+        self.max_selected = p.max_selected if max_selected is None else max_selected
+        self.shape = make_shape(n_kv_heads=p.n_kv_heads, q_per_kv=p.q_per_kv,
+                                n_queries=p.n_queries, pool_cells=p.pool_cells,
+                                page_table_len=p.page_table_len, chunk_cells=p.chunk_cells,
+                                softmax_scale=p.softmax_scale,
+                                q_dtype=QSA_BF16 if p.q_dtype == "bf16" else QSA_F32,
+                                algo=algo, head_dim=p.head_dim)
+        self.ws_bytes = qsa_workspace_bytes(self.shape, self.n_seq, self.max_selected)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.out = torch.empty((p.n_seq, p.n_queries, p.n_kv_heads * p.q_per_kv, p.head_dim),
+                               dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run(self, batch: Optional[bool] = None, stream=None, out=None):
+        """One call.  ``batch=None`` uses the step entry for one sequence and
+        the batch entry otherwise."""
+        out = self.out if out is None else out
+        if batch is None:
+            batch = self.n_seq != 1
+        if batch:
+            qsa_decode_attn_batch(self.shape, self.n_seq, self.q, self.k_pool, self.v_pool,
+                                  self.k_scale, self.v_scale, self.page_table, self.sel,
+                                  self.sel_offsets, self.max_selected, out, self.workspace,
+                                  self.ws_bytes, self.status, stream)
+        else:
+            assert self.n_seq == 1
+            qsa_decode_attn_step(self.shape, self.q, self.k_pool, self.v_pool, self.k_scale,
+                                 self.v_scale, self.page_table, self.sel,
+                                 int(self.p.sel.shape[0]), out, self.workspace, self.ws_bytes,
+                                 self.status, stream)
+        return out
+
+
+def run_problem(p, algo: int = QSA_ALGO_AUTO, batch: Optional[bool] = None) -> np.ndarray:
+    """Upload, run once, and return the output as a float32 numpy array."""
+    import torch
+    dp = DeviceProblem(p, algo=algo)
+    out = dp.run(batch=batch)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def partials_of(dp: DeviceProblem):
+    """Copy the chunk partials of the last call to host: (m, l, o) with shapes
+    [n_seq][G][n_chunks][R] and [n_seq][G][n_chunks][R][D]."""
+    import torch
+    m_ptr, l_ptr, o_ptr, n_chunks = qsa_partials_view(dp.shape, dp.n_seq, dp.max_selected,
+                                                      dp.workspace)
+    p = dp.p
+    R = p.n_queries * p.q_per_kv
+    rows = dp.n_seq * p.n_kv_heads * n_chunks * R
+    base = dp.workspace.data_ptr()
+    ws = dp.workspace
+
+    def view(ptr, count):
+        off = ptr - base
+        return ws[off:off + count * 4].view(torch.float32).cpu().numpy()
+
+    m = view(m_ptr, rows).reshape(dp.n_seq, p.n_kv_heads, n_chunks, R)
+    l = view(l_ptr, rows).reshape(dp.n_seq, p.n_kv_heads, n_chunks, R)
+    o = view(o_ptr, rows * p.head_dim).reshape(dp.n_seq, p.n_kv_heads, n_chunks, R, p.head_dim)
+    return m, l, o

@@ -1,0 +1,154 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+function ``include/qsa.h`` declares, sizes its workspace as documented and
+rejects bad arguments before any CUDA call.  No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_selection_int8_gb300 as qsa
+from sparse_selection_int8_gb300 import build as qsa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qsa_build.build()
+    return qsa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(qsa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("qsa_decode_attn_step", "qsa_decode_attn_batch", "qsa_workspace_bytes",
+                     "qsa_partials_view", "qsa_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(qsa.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def shape(**kw):
+    base = dict(n_kv_heads=1, q_per_kv=12, n_queries=1, pool_cells=4096, page_table_len=4096,
+                chunk_cells=64, softmax_scale=1 / 16)
+    base.update(kw)
+    return qsa.make_shape(**base)
+
+
+def test_workspace_bytes_layout(lib):
+    s = shape(n_queries=4, chunk_cells=128)
+    n_chunks = (2051 + 127) // 128
+    rows = n_chunks * 48
+    got = qsa.qsa_workspace_bytes(s, 1, 2051)
+    assert got >= rows * 4 * 2 + rows * 256 * 4
+    assert got % 256 == 0
+    assert qsa.qsa_workspace_bytes(s, 1, 0) == 0
+    # grows linearly with sequences
+    assert qsa.qsa_workspace_bytes(s, 8, 2051) >= 8 * rows * 258 * 4
+
+
+def test_partials_view_offsets(lib):
+    s = shape(n_queries=2, chunk_cells=256, n_kv_heads=2)
+    base = 1 << 20
+    m, l, o, n = qsa.qsa_partials_view(s, 8, 16384, base)
+    assert n == 64
+    rows = 8 * 2 * 64 * 24
+    assert m == base and l >= m + rows * 4 and o >= l + rows * 4
+    assert (l - base) % 256 == 0 and (o - base) % 256 == 0
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 128, qsa.QSA_ERR_UNSUPPORTED),
+    ("q_per_kv", 0, qsa.QSA_ERR_INVALID_ARG),
+    ("q_per_kv", 65, qsa.QSA_ERR_UNSUPPORTED),
+    ("n_queries", 0, qsa.QSA_ERR_INVALID_ARG),
+    ("chunk_cells", 0, qsa.QSA_ERR_INVALID_ARG),
+    ("pool_cells", -1, qsa.QSA_ERR_INVALID_ARG),
+    ("q_dtype", 7, qsa.QSA_ERR_INVALID_ARG),
+    ("algo", 9, qsa.QSA_ERR_INVALID_ARG),
+    ("softmax_scale", float("nan"), qsa.QSA_ERR_INVALID_ARG),
+])
+def test_bad_shape_rejected(lib, field, value, code):
+    s = shape()
+    setattr(s, field, value)
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_workspace_bytes(s, 1, 100)
+    assert e.value.code == code
+
+
+FAKE = 1 << 32  # an aligned, never-dereferenced address: every call below fails its checks
+
+
+def step_args(**over):
+    a = dict(q=FAKE, k_pool=FAKE, v_pool=FAKE, k_scale=FAKE, v_scale=FAKE, page_table=FAKE,
+             sel=FAKE, n_sel=100, out=FAKE + 4096, workspace=FAKE, workspace_bytes=1 << 30)
+    a.update(over)
+    return a
+
+
+def call_step(lib, s, a):
+    return lib.qsa_decode_attn_step(ctypes.byref(s), a["q"], a["k_pool"], a["v_pool"],
+                                    a["k_scale"], a["v_scale"], a["page_table"], a["sel"],
+                                    a["n_sel"], a["out"], a["workspace"], a["workspace_bytes"],
+                                    None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(k_pool=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(out=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(sel=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(n_sel=-1), qsa.QSA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), qsa.QSA_ERR_INVALID_ARG),          # misaligned queries
+    (dict(k_pool=FAKE + 4), qsa.QSA_ERR_INVALID_ARG),     # misaligned pool
+    (dict(workspace=FAKE + 16), qsa.QSA_ERR_INVALID_ARG), # workspace not 256-aligned
+    (dict(workspace=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(workspace_bytes=64), qsa.QSA_ERR_WORKSPACE),
+    (dict(out=FAKE), qsa.QSA_ERR_INVALID_ARG),            # out aliases q
+])
+def test_step_rejects_before_launch(lib, over, code):
+    assert call_step(lib, shape(), step_args(**over)) == code
+
+
+def test_batch_rejects_before_launch(lib):
+    s = shape()
+    args = [ctypes.byref(s), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]
+    # null offsets
+    assert lib.qsa_decode_attn_batch(*args, None, 100, FAKE + 4096, FAKE, 1 << 30, None,
+                                     None) == qsa.QSA_ERR_INVALID_ARG
+    # zero sequences
+    args0 = [ctypes.byref(s), 0] + args[2:]
+    assert lib.qsa_decode_attn_batch(*args0, FAKE, 100, FAKE + 4096, FAKE, 1 << 30, None,
+                                     None) == qsa.QSA_ERR_INVALID_ARG
+    # negative bound
+    assert lib.qsa_decode_attn_batch(*args, FAKE, -5, FAKE + 4096, FAKE, 1 << 30, None,
+                                     None) == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert qsa.qsa_status_string(code)
+    assert qsa.qsa_status_string(12345) == "unknown status"
+
+
+def test_binding_has_no_cpu_path():
+    """The product package never imports the oracle."""
+    pkg = os.path.dirname(qsa.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "qsa_oracle" not in text, f

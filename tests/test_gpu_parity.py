@@ -1,0 +1,308 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every configuration of the workload set, the pages' edge cases (0/1/2/3/63/
+64/65 selected cells, page -1 masking), chunk sizes around the tile sizes,
+ragged batches, out-of-range indices, determinism of the chunk partials and
+bit-exact index handling.  Tolerance: ``tests/parity.py``.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import qsa_workloads as wl
+from parity import assert_parity, errors
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+ALGOS = ["auto", "simt", "tcgen05"]
+
+
+def algo_code(name):
+    import sparse_selection_int8_gb300 as qsa
+    return {"auto": qsa.QSA_ALGO_AUTO, "simt": qsa.QSA_ALGO_SIMT,
+            "tcgen05": qsa.QSA_ALGO_TCGEN05}[name]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_selection_int8_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def run(p, algo="auto", batch=None, poison=True, max_selected=None):
+    import sparse_selection_int8_gb300 as qsa
+    dp = qsa.DeviceProblem(p, algo=algo_code(algo), max_selected=max_selected)
+    if poison:
+        dp.workspace.fill_(0xFF)   # NaN bytes: any read of an unwritten partial shows
+        dp.out.fill_(float("nan"))
+    dp.run(batch=batch)
+    torch.cuda.synchronize()
+    return dp, dp.out.cpu().numpy()
+
+
+def check_full(p, algo, what):
+    dp, out = run(p, algo)
+    ref = oracle.decode_attn(p)
+    e = assert_parity(out, ref, what)
+    assert int(dp.status.item()) == 0
+    return e
+
+
+# ---------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tiny_decode(algo):
+    check_full(wl.tiny_decode(), algo, "tiny_decode")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_qsa_decode(algo, T):
+    check_full(wl.qsa_decode(T), algo, f"qsa_decode T={T}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_batched_decode(algo):
+    check_full(wl.batched_decode(), algo, "batched_decode")
+
+
+@pytest.mark.parametrize("algo", ["auto"])
+def test_long_context(algo):
+    check_full(wl.long_context(), algo, "long_context")
+
+
+@pytest.mark.parametrize("algo", ["auto", "simt"])
+def test_prompt_shaped_sampled_rows(algo):
+    """Full size (2,048 bf16 queries x 32,768 cells); the oracle computes a
+    sample of output rows one by one."""
+    p = wl.prompt_shaped()
+    dp, out = run(p, algo)
+    rng = np.random.Generator(np.random.PCG64(5))
+    GH = p.n_kv_heads * p.q_per_kv
+    ts = np.concatenate([[0, p.n_queries - 1], rng.integers(0, p.n_queries, 30)])
+    hs = rng.integers(0, GH, ts.shape[0])
+    rows = [oracle.flat_row(p, 0, int(t), int(h)) for t, h in zip(ts, hs)]
+    ref = oracle.decode_attn(p, rows=rows)
+    got = np.stack([out[0, t, h] for t, h in zip(ts, hs)])
+    assert_parity(got, ref, "prompt_shaped")
+    assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("algo", ["auto"])
+def test_prompt_shaped_small_full(algo):
+    """A smaller prompt-shaped call (256 bf16 queries x 4,096 cells, two
+    chunks with a ragged tail) checked on every output row."""
+    p = wl.prompt_shaped(n_queries=256, pool_cells=4096, chunk_cells=3000)
+    check_full(p, algo, "prompt_small")
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 63, 64, 65, 127, 128, 129, 300])
+def test_selected_counts(algo, n):
+    p = wl.make_problem(n_queries=2, pool_cells=1024, n_selected=n, chunk_cells=64,
+                        seed=7000 + n)
+    dp, out = run(p, algo)
+    ref = oracle.decode_attn(p)
+    assert_parity(out, ref, f"n={n}")
+    if n == 0:
+        assert np.array_equal(out, np.zeros_like(out))
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("C", [1, 7, 64, 127, 128, 129, 256, 2051, 5000])
+def test_chunk_sizes(algo, C):
+    p = wl.make_problem(n_queries=2, pool_cells=8192, n_selected=2051, chunk_cells=C,
+                        seed=7100 + C)
+    check_full(p, algo, f"C={C}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("T", [1, 3, 5])
+def test_query_counts_and_heads(algo, T):
+    p = wl.make_problem(n_queries=T, q_per_kv=12, n_kv_heads=3, pool_cells=2048,
+                        n_selected=700, chunk_cells=128, seed=7200 + T)
+    check_full(p, algo, f"T={T} G=3")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_page_minus_one_masking(algo):
+    p = wl.make_problem(n_queries=4, pool_cells=4096, n_selected=1500, chunk_cells=128,
+                        mask_fraction=0.4, seed=7300)
+    check_full(p, algo, "masked")
+    # every selected cell masked -> zeros
+    p.page_table[:] = -1
+    dp, out = run(p, algo)
+    assert np.array_equal(out, np.zeros_like(out))
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_out_of_range_entries_are_masked_and_reported(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_queries=2, pool_cells=2048, n_selected=600, chunk_cells=64,
+                        seed=7400)
+    clean_sel = p.sel.copy()
+    bad_pos = [5, 77, 300]
+    bad_slot_pos = [10, 200]
+    p.sel[bad_pos] = [-3, 2048, 99999]
+    for i in bad_slot_pos:
+        p.page_table[0, p.sel[i]] = 5000 if i == 10 else -7
+    dp, out = run(p, algo)
+    st = int(dp.status.item())
+    assert st & qsa.QSA_STATUS_BAD_POSITION and st & qsa.QSA_STATUS_BAD_SLOT
+    keep = np.ones(600, bool)
+    keep[bad_pos + bad_slot_pos] = False
+    q = wl.make_problem(n_queries=2, pool_cells=2048, n_selected=600, chunk_cells=64,
+                        seed=7400)
+    q.sel = clean_sel[keep]
+    q.sel_offsets = np.array([0, keep.sum()], np.int32)
+    ref = oracle.decode_attn(q)
+    assert_parity(out, ref, "bad entries")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_ragged_batch_with_empty_sequences(algo):
+    lens = [0, 1, 65, 600, 0, 2051, 129, 3]
+    p = wl.make_problem(n_seq=len(lens), n_kv_heads=2, n_queries=3, pool_cells=4096,
+                        n_selected=lens, chunk_cells=128, seed=7500)
+    dp, out = run(p, algo, max_selected=2100)
+    assert_parity(out, oracle.decode_attn(p), "ragged")
+    assert np.array_equal(out[0], np.zeros_like(out[0]))
+    assert np.array_equal(out[4], np.zeros_like(out[4]))
+
+
+@pytest.mark.parametrize("algo", ["auto", "simt"])
+def test_batch_list_above_bound_is_clamped(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_seq=2, n_queries=1, pool_cells=2048, n_selected=[300, 500],
+                        chunk_cells=64, seed=7600)
+    dp, out = run(p, algo, max_selected=400)
+    assert int(dp.status.item()) & qsa.QSA_STATUS_BAD_OFFSETS
+    q = wl.make_problem(n_seq=2, n_queries=1, pool_cells=2048, n_selected=[300, 500],
+                        chunk_cells=64, seed=7600)
+    q.sel = np.concatenate([q.sel_of(0), q.sel_of(1)[:400]])
+    q.sel_offsets = np.array([0, 300, 700], np.int32)
+    assert_parity(out, oracle.decode_attn(q), "clamped")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_output_guard_untouched(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_queries=2, pool_cells=1024, n_selected=200, chunk_cells=64,
+                        seed=7700)
+    dp = qsa.DeviceProblem(p, algo=algo_code(algo))
+    n = dp.out.numel()
+    big = torch.full((n + 2048,), 12345.0, device="cuda")
+    view = big[1024:1024 + n].view_as(dp.out)
+    dp.run(out=view)
+    torch.cuda.synchronize()
+    b = big.cpu().numpy()
+    assert np.all(b[:1024] == 12345.0) and np.all(b[1024 + n:] == 12345.0)
+    assert_parity(view.cpu().numpy(), oracle.decode_attn(p), "guard")
+
+
+# ------------------------------------------------- determinism and indexing
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_partials_bit_identical_across_runs(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.qsa_decode(4)
+    dp = qsa.DeviceProblem(p, algo=algo_code(algo))
+    dp.run()
+    torch.cuda.synchronize()
+    m0, l0, o0 = qsa.partials_of(dp)
+    out0 = dp.out.cpu().numpy()
+    side = torch.cuda.Stream()
+    for i in range(10):
+        dp.workspace.fill_(0xFF)
+        if i % 2:
+            with torch.cuda.stream(side):
+                dp.run(stream=side)
+            side.synchronize()
+        else:
+            dp.run()
+            torch.cuda.synchronize()
+        m, l, o = qsa.partials_of(dp)
+        assert m.tobytes() == m0.tobytes() and l.tobytes() == l0.tobytes()
+        assert o.tobytes() == o0.tobytes()
+        assert dp.out.cpu().numpy().tobytes() == out0.tobytes()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_partials_against_oracle(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_queries=2, pool_cells=4096, n_selected=700, chunk_cells=128,
+                        mask_fraction=0.1, seed=7800)
+    dp = qsa.DeviceProblem(p, algo=algo_code(algo))
+    dp.run()
+    torch.cuda.synchronize()
+    m, l, o = qsa.partials_of(dp)
+    qd = oracle.widen_queries(p.q, p.q_dtype)
+    H = p.q_per_kv
+    for r in range(p.n_queries * H):
+        t, j = divmod(r, H)
+        om, ol, oo = oracle.row_partials(qd[0, t, j], p.k_pool[0, 0], p.v_pool[0, 0],
+                                         p.k_scale[0, 0], p.v_scale[0, 0], p.page_table[0],
+                                         p.sel, p.chunk_cells, p.softmax_scale)
+        for c in range(len(om)):
+            if ol[c] == 0:
+                assert l[0, 0, c, r] == 0 and m[0, 0, c, r] == -np.inf
+                continue
+            assert abs(m[0, 0, c, r] - om[c]) <= 2e-3, (r, c)
+            # the normalised chunk output and the denominator relative to the max
+            assert abs(l[0, 0, c, r] / ol[c] - 1) <= 1e-2, (r, c)
+            assert_parity(o[0, 0, c, r] / l[0, 0, c, r], oo[c] / ol[c], f"chunk {c} row {r}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_step_and_batch_agree_bitwise(algo):
+    p = wl.qsa_decode(3)
+    _, a = run(p, algo, batch=False)
+    _, b = run(p, algo, batch=True)
+    assert a.tobytes() == b.tobytes()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_page_table_relabelling_bit_identical(algo):
+    """Permuting the pool rows and rewriting the page table consistently gives
+    the same bits: the kernels see the same values in the same order."""
+    p = wl.make_problem(n_queries=4, pool_cells=4096, n_selected=1000, chunk_cells=128,
+                        mask_fraction=0.05, seed=7900)
+    _, a = run(p, algo)
+    rng = np.random.Generator(np.random.PCG64(7901))
+    perm = rng.permutation(p.pool_cells)
+    inv = np.argsort(perm)
+    p.k_pool[0, 0] = p.k_pool[0, 0][inv]
+    p.v_pool[0, 0] = p.v_pool[0, 0][inv]
+    p.k_scale[0, 0] = p.k_scale[0, 0][inv]
+    p.v_scale[0, 0] = p.v_scale[0, 0][inv]
+    pt = p.page_table[0]
+    p.page_table[0] = np.where(pt >= 0, perm[np.maximum(pt, 0)], -1)
+    _, b = run(p, algo)
+    assert a.tobytes() == b.tobytes()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_single_cell_gather_is_exact(algo):
+    """Each sequence selects one cell whose V row encodes its slot; with a
+    power-of-two V scale the output must equal scale x code exactly."""
+    n_seq, pool = 64, 512
+    p = wl.make_problem(n_seq=n_seq, n_kv_heads=2, n_queries=2, pool_cells=pool,
+                        n_selected=1, chunk_cells=64, seed=8000)
+    d = np.arange(256)
+    for s in range(pool):
+        p.v_pool[:, :, s, :] = ((s * 7 + d * 13) % 255 - 127).astype(np.int8)
+    p.v_scale[:] = 2.0 ** -6
+    _, out = run(p, algo)
+    for b in range(n_seq):
+        slot = p.page_table[b, p.sel[b]]
+        expect = (((slot * 7 + d * 13) % 255) - 127) * 2.0 ** -6
+        for t in range(2):
+            for h in range(24):
+                assert np.array_equal(out[b, t, h], expect.astype(np.float32)), (b, t, h)
