@@ -248,7 +248,10 @@ def run_reference(args, world, rank):
 
 def time_graphs(torch, graphs, flush, steps, warmup, stream):
     """Replay each graph in order per step; L2 flushed before each step.
+    Must run with `stream` as torch's current stream: CUDAGraph.replay() and
+    the flush launch on the current stream, the events are recorded on it.
     Returns per-step lists of per-graph durations in ms."""
+    assert torch.cuda.current_stream() == stream
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
     for _ in range(warmup):
         flush.zero_()
@@ -300,7 +303,8 @@ def measure_extra(torch, qsa, wl, flush, stream, hbm_peak, tflops_peak, budget_s
         p = make()
         dp = qsa.DeviceProblem(p)
         g = capture(torch, dp, stream)
-        per = time_graphs(torch, [g], flush, iters, 3, stream)
+        with torch.cuda.stream(stream):
+            per = time_graphs(torch, [g], flush, iters, 3, stream)
         us = statistics.median([x[0] for x in per]) * 1e3
         cells = int(p.n_selected.sum())
         ab = algorithmic_bytes(p)
@@ -338,7 +342,7 @@ def run_ours(args, world, rank, local):
 
     dist_barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk, torch.cuda.stream(stream):
         per_step = time_graphs(torch, graphs, flush, args.steps, args.warmup, stream)
     torch.cuda.synchronize()
     dist_barrier(world)

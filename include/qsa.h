@@ -73,6 +73,7 @@ typedef enum qsa_algo {
 #define QSA_STATUS_BAD_POSITION 0x1u /* a selected position outside [0, page_table_len) */
 #define QSA_STATUS_BAD_SLOT 0x2u     /* a page entry outside [0, pool_cells) and not -1 */
 #define QSA_STATUS_BAD_OFFSETS 0x4u  /* batch offsets decreasing or a list above max_selected */
+#define QSA_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait ran out: outputs invalid */
 
 typedef struct qsa_shape {
     int32_t n_kv_heads;     /* G: KV heads per sequence (>= 1) */

@@ -32,6 +32,7 @@ QSA_ALGO_TCGEN05 = 2
 QSA_STATUS_BAD_POSITION = 0x1
 QSA_STATUS_BAD_SLOT = 0x2
 QSA_STATUS_BAD_OFFSETS = 0x4
+QSA_STATUS_TIMEOUT = 0x8
 
 HEAD_DIM = 256
 

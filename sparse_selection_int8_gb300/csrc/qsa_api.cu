@@ -99,7 +99,10 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.scale_log2 = s->softmax_scale * kLog2e;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_chunk_simt(p, cs);
+    const bool tc_ok = chunk_tc_supports(p);
+    if (s->algo == QSA_ALGO_TCGEN05 && !tc_ok) return QSA_ERR_UNSUPPORTED;
+    const bool use_tc = s->algo != QSA_ALGO_SIMT && tc_ok;
+    cudaError_t e = use_tc ? launch_chunk_tc(p, cs) : launch_chunk_simt(p, cs);
     if (e != cudaSuccess) return QSA_ERR_CUDA;
     e = launch_merge(p, cs);
     if (e != cudaSuccess) return QSA_ERR_CUDA;

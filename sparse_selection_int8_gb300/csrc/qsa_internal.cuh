@@ -120,6 +120,8 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
 
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_chunk_simt(const Params &p, cudaStream_t stream);
+bool chunk_tc_supports(const Params &p);
+cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream);
 cudaError_t launch_merge(const Params &p, cudaStream_t stream);
 
 } // namespace qsa
