@@ -18,21 +18,29 @@
 // to f16; the group's largest scale multiplies the fp32 result.  Queries are
 // rounded to f16.  Accumulation is fp32 in tensor memory.
 //
-// CTA = 1 producer warp + 8 consumer warps, persistent over a contiguous
-// range of non-empty (sequence, KV head, chunk) items:
-//   producer  resolves list entry -> page slot (a1) and streams the cells' K
-//             and V rows (256 B each) with bulk async copies into a ring of
-//             raw stages, plus the two per-cell scales with 4-byte cp.async;
-//   consumers dequantise a stage into an f16 tile in the tensor cores'
-//             128-byte-swizzled layout, issue tcgen05.mma from one thread,
-//             and run the softmax (max via redux, sum via a reduce-scatter
-//             butterfly), all in a fixed order, so partials are bit-identical
-//             run to run.
-// A chunk is processed in groups of up to 256 cells (two M tiles) that share
-// one max; longer chunks combine their groups in registers.
+// One persistent CTA of 16 warps per SM walks a contiguous range of
+// non-empty (sequence, KV head, chunk) items as a sequence of ops: for every
+// group of up to 256 cells (two M tiles sharing one max), its K tiles, then
+// its V tiles.  Every warp takes part in every phase:
+//   gather   the rows of op k+2 are copied with 16-byte cp.async into a ring
+//            of three raw stages while op k is computed (random 256-byte rows
+//            need many warps issuing copies: one warp tops out near 8 GB/s
+//            per SM; one TMA bulk copy per row was ~10x slower still);
+//   resolve  list entry -> page slot (a1) runs two groups ahead: the list
+//            reads are issued at a group's first K op, the page-table reads
+//            after its softmax max pass, and the checked slots are stored at
+//            the group's end;
+//   convert  a raw stage becomes an f16 tile in the tensor cores'
+//            128-byte-swizzled layout (no bank conflicts on either side);
+//   MMA      one thread issues tcgen05.mma; completion on an mbarrier;
+//   softmax  warp (quadrant q, quarter c) owns cells 32q..32q+31 of a tile
+//            and a quarter of the rows: max via redux, sums via a
+//            reduce-scatter butterfly, all in a fixed order, so partials are
+//            bit-identical run to run.
 //
-// Every wait is bounded; a wait that runs out raises QSA_STATUS_TIMEOUT and
-// the kernel runs to its end without further waiting.
+// The only wait that is not a CTA barrier is the MMA-completion wait; it is
+// bounded, and a wait that runs out raises QSA_STATUS_TIMEOUT and the kernel
+// runs to its end without further waiting.
 #include <cuda_fp16.h>
 
 #include "qsa_internal.cuh"
@@ -46,9 +54,9 @@ using namespace sm100;
 constexpr int kTile = 128;          // cells per MMA tile (M)
 constexpr int kMaxTiles = 2;        // tiles per softmax group
 constexpr int kGroupCells = kTile * kMaxTiles;
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlotRing = 4;        // groups of resolved slots kept
 constexpr uint32_t kOddRows = 64 * 256 + 64;        // odd rows start 64 B past a 128-B line
 constexpr uint32_t kStageRowBytes = kOddRows + 64 * 256;
 constexpr uint32_t kStageSlots = kStageRowBytes;     // int32[128]
@@ -62,19 +70,20 @@ struct Layout {
     uint32_t off_kv, off_q, off_p, off_raw, n_stages, off_misc, total;
 };
 
-// Misc area: per-group cell info, reduction scratch, per-row values, barriers.
+// Misc area: slot ring, per-group cell info, reduction scratch, per-row values.
 struct Misc {
+    int32_t ring[kSlotRing][kGroupCells];
     int32_t cell_slot[kMaxTiles][kTile];
     float cell_ks[kMaxTiles][kTile];
     float cell_vs[kMaxTiles][kTile];
-    float red_max[2][4][32];
-    float red_sum[2][4][32];
-    float red_vs[2][4];
-    float row_fa[64], row_fb[64], row_m[64], row_l[64], row_mrun[64], row_lrun[64];
+    float red_max[4][4][16]; // [row quarter][lane quadrant][row within quarter]
+    float red_sum[4][4][16];
+    float red_vs[kWarps];
+    float row_fa[64], row_fb[64], row_mrun[64], row_lrun[64];
     float sigma;
     int32_t abort;
     uint32_t tmem;
-    uint64_t full[4], empty[4], mma;
+    uint64_t mma;
 };
 
 __host__ __device__ inline Layout make_layout(int N, int n_stages)
@@ -139,23 +148,31 @@ __device__ __forceinline__ float from_ordered_key(int k)
     return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// NC consecutive columns of tensor memory (a multiple of 4) into v.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v)
+{
+#pragma unroll
+    for (int j = 0; j + 8 <= NC; j += 8) tmem_ld8(taddr + j, v + j);
+    if (NC % 8) tmem_ld4(taddr + (NC / 8) * 8, v + (NC / 8) * 8);
 }
 
 // ---------------------------------------------------------------- work list
 
 // Non-empty (sequence, KV head, chunk) items in sequence-major order; each
-// CTA takes a contiguous range.  Producer and consumers walk it identically.
+// CTA takes a contiguous range (consecutive chunks share their queries).
 struct Cursor {
     int b, g, c, nch, start, n;
     int remaining;
@@ -176,9 +193,7 @@ __device__ inline void cursor_init(const Params &p, Cursor &cur)
     long long lo = per * blockIdx.x;
     const long long hi = min(lo + per, total);
     cur.remaining = lo < hi ? (int)(hi - lo) : 0;
-    cur.b = 0;
-    cur.g = cur.c = 0;
-    cur.nch = 0;
+    cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
     if (cur.remaining == 0) return;
     for (int b = 0; b < p.n_seq; ++b) {
         const int nch = seq_chunks(p, b, &s, &n);
@@ -218,119 +233,155 @@ __device__ inline void cursor_next(const Params &p, Cursor &cur)
     cur.remaining = 0;
 }
 
-// ---------------------------------------------------------------- producer
-
-__device__ void run_producer(const Params &p, uint8_t *smem, const Layout &L, Misc &ms)
-{
-    const int lane = threadIdx.x & 31;
-    const uint32_t raw_base = smem_u32(smem + L.off_raw);
-    uint32_t op = 0;
+// The ops of the work range: for every group (up to two tiles of one
+// chunk), its K tiles, then its V tiles.  Groups are numbered by gi in the
+// same order everywhere (slot ring index = gi % kSlotRing).
+struct OpIter {
     Cursor cur;
-    cursor_init(p, cur);
-    for (; cur.remaining > 0; cursor_next(p, cur)) {
-        const int c0 = cur.c * p.chunk_cells;
-        const int nc = min(p.chunk_cells, cur.n - c0);
-        const size_t kv_base = ((size_t)cur.b * p.G + cur.g) * p.pool_cells;
-        for (int gs = 0; gs < nc; gs += kGroupCells) {
-            const int gn = min(kGroupCells, nc - gs);
-            const int tiles = (gn + kTile - 1) / kTile;
-            int slots[kMaxTiles][4];
-#pragma unroll
-            for (int t = 0; t < kMaxTiles; ++t) {
-                int pos[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = t * kTile + lane * 4 + e;
-                    pos[e] = (t < tiles && i < gn) ? __ldg(p.sel + cur.start + c0 + gs + i) : INT_MIN;
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    slots[t][e] = pos[e] == INT_MIN ? -1 : resolve_slot(p, cur.b, pos[e]);
-            }
-            for (int kind = 0; kind < 2; ++kind) {
-                for (int t = 0; t < tiles; ++t, ++op) {
-                    const uint32_t s = op % L.n_stages;
-                    const uint32_t round = op / L.n_stages;
-                    if (ms.abort) continue; // stop issuing copies after a timeout
-                    if (!mbar_wait(&ms.empty[s], (round & 1) ^ 1)) {
-                        atomicExch(&ms.abort, 1);
-                        raise_status(p, QSA_STATUS_TIMEOUT);
-                        continue;
-                    }
-                    const uint32_t st = raw_base + s * kStageBytes;
-                    int sl[4]; // this tile's slots (kept in registers: t is 0 or 1)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sl[e] = t == 0 ? slots[0][e] : slots[1][e];
-                    int nvalid = 0;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) nvalid += sl[e] >= 0;
-                    if (kind == 0) {
-                        const int c = lane * 4;
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(st + kStageSlots + c * 4),
-                                     "r"(sl[0]), "r"(sl[1]), "r"(sl[2]), "r"(sl[3])
-                                     : "memory");
-                    }
-                    __syncwarp();
-                    const int total = __reduce_add_sync(0xffffffffu, nvalid);
-                    if (lane == 0) mbar_arrive_expect_tx(&ms.full[s], (uint32_t)total * 256u);
-                    const int8_t *pool = kind == 0 ? p.k_pool : p.v_pool;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = lane * 4 + e;
-                        const int slot = sl[e];
-                        if (slot < 0) continue;
-                        bulk_g2s(smem + L.off_raw + s * kStageBytes + row_offset(c),
-                                 pool + (kv_base + slot) * kHeadDim, 256, &ms.full[s]);
-                        if (kind == 0) {
-                            cp_async4(st + kStageKs + c * 4, p.k_scale + kv_base + slot);
-                            cp_async4(st + kStageVs + c * 4, p.v_scale + kv_base + slot);
-                        }
-                    }
-                    cp_async_arrive_noinc(&ms.full[s]);
-                }
-            }
-        }
+    int nc;      // cells of the current item (chunk)
+    int gs;      // first cell of the current group within the item
+    int tiles;   // tiles of the current group
+    int kind;    // 0 = K tile, 1 = V tile
+    int t;       // tile within the group
+    uint32_t gi; // group counter
+    bool valid;
+};
+
+__device__ inline void op_setup_item(const Params &p, OpIter &it)
+{
+    it.nc = min(p.chunk_cells, it.cur.n - it.cur.c * p.chunk_cells);
+    it.gs = 0;
+    it.kind = 0;
+    it.t = 0;
+    it.tiles = (min(kGroupCells, it.nc) + kTile - 1) / kTile;
+}
+
+__device__ inline void op_init(const Params &p, OpIter &it)
+{
+    cursor_init(p, it.cur);
+    it.gi = 0;
+    it.valid = it.cur.remaining > 0;
+    if (it.valid) op_setup_item(p, it);
+}
+
+// Advance to the first op of the next group.
+__device__ inline void op_next_group(const Params &p, OpIter &it)
+{
+    it.t = 0;
+    it.kind = 0;
+    ++it.gi;
+    it.gs += kGroupCells;
+    if (it.gs < it.nc) {
+        it.tiles = (min(kGroupCells, it.nc - it.gs) + kTile - 1) / kTile;
+        return;
     }
-    // After a timeout the consumers stop waiting; before the CTA may exit,
-    // wait (bounded) for the copies this warp issued into the last stages.
-    if (ms.abort) {
-        const uint32_t n = op < L.n_stages ? op : L.n_stages;
-        for (uint32_t i = 1; i <= n; ++i) {
-            const uint32_t k = op - i;
-            mbar_wait(&ms.full[k % L.n_stages], (k / L.n_stages) & 1, 1u << 22);
+    cursor_next(p, it.cur);
+    it.valid = it.cur.remaining > 0;
+    if (it.valid) op_setup_item(p, it);
+}
+
+__device__ inline void op_next(const Params &p, OpIter &it)
+{
+    if (++it.t < it.tiles) return;
+    it.t = 0;
+    if (++it.kind < 2) return;
+    op_next_group(p, it);
+}
+
+// ---------------------------------------------------------------- phases
+
+// Step a1 for one cell of a group, split in three so the two dependent reads
+// overlap other work: list entry, page entry, then the checks.
+__device__ __forceinline__ int resolve_list(const Params &p, const OpIter &g, int i)
+{
+    if (!g.valid || i >= min(kGroupCells, g.nc - g.gs)) return INT_MIN;
+    return __ldg(p.sel + g.cur.start + g.cur.c * p.chunk_cells + g.gs + i);
+}
+
+// INT_MIN marks a position outside the page table; -1 a cell past the group.
+__device__ __forceinline__ int resolve_page(const Params &p, const OpIter &g, int pos)
+{
+    if (pos == INT_MIN) return -1;
+    if (pos < 0 || pos >= p.page_table_len) return INT_MIN;
+    return __ldg(p.page_table + (size_t)g.cur.b * p.page_table_len + pos);
+}
+
+__device__ __forceinline__ int resolve_check(const Params &p, int raw)
+{
+    if (raw == INT_MIN) {
+        raise_status(p, QSA_STATUS_BAD_POSITION);
+        return -1;
+    }
+    if (raw == -1) return -1;
+    if (raw < 0 || raw >= p.pool_cells) {
+        raise_status(p, QSA_STATUS_BAD_SLOT);
+        return -1;
+    }
+    return raw;
+}
+
+// Copies of one op into a raw stage: warp w moves rows 8w..8w+7, two per
+// instruction (16 lanes x 16 B per 256-byte row).  For a K op the first 128
+// threads also publish their cell's slot and copy its two scales.  Masked
+// cells are not copied: their stale bytes are finite codes that get zero
+// weight.
+__device__ __forceinline__ void issue_op(const Params &p, uint8_t *smem, const Misc &ms,
+                                         const OpIter &it, uint32_t st_off, int tid)
+{
+    const int w = tid >> 5, lane = tid & 31;
+    const int *tslots = ms.ring[it.gi % kSlotRing] + it.t * kTile;
+    const size_t kv_base = ((size_t)it.cur.b * p.G + it.cur.g) * p.pool_cells;
+    const int8_t *pool = (it.kind == 0 ? p.k_pool : p.v_pool) + kv_base * kHeadDim + (lane & 15) * 16;
+    const uint32_t st = smem_u32(smem) + st_off;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = 8 * w + 2 * i + (lane >> 4);
+        const int slot = tslots[row];
+        if (slot >= 0) cp_async16(st + row_offset(row) + (lane & 15) * 16, pool + (size_t)slot * kHeadDim);
+    }
+    if (it.kind == 0 && tid < kTile) {
+        const int slot = tslots[tid];
+        *reinterpret_cast<int *>(smem + st_off + kStageSlots + tid * 4) = slot;
+        if (slot >= 0) {
+            cp_async4(st + kStageKs + tid * 4, p.k_scale + kv_base + slot);
+            cp_async4(st + kStageVs + tid * 4, p.v_scale + kv_base + slot);
         }
     }
 }
 
-// ---------------------------------------------------------------- consumers
-
-// Dequantise one raw stage (128 rows) into the f16 tile.  32 threads cover
-// two rows x sixteen 16-byte pieces; even and odd rows sit in regions 64 B
-// apart modulo 128, so both the reads and the swizzled writes are free of
-// bank conflicts.
-__device__ __forceinline__ void convert_tile(uint32_t stage, uint32_t tile, int cw, int lane)
+// Dequantise one raw stage (128 rows) into the f16 tile.  Warp w converts
+// row pairs 4w..4w+3; 32 threads cover two rows x sixteen 16-byte pieces.
+// Even and odd rows sit in regions 64 B apart modulo 128, so both the reads
+// and the swizzled writes are free of bank conflicts.
+__device__ __forceinline__ void convert_tile(uint32_t stage, uint32_t tile, int w, int lane)
 {
     const int qlo = lane & 3, rsel = (lane >> 2) & 1, qhi = lane >> 3;
     const int q = qhi * 4 + qlo;
-#pragma unroll 4
-    for (int it = 0; it < 8; ++it) {
-        const int rp = cw * 8 + it;
-        const int row = 2 * rp + rsel;
-        const uint4 raw = lds128(stage + (rsel ? kOddRows : 0u) + (uint32_t)rp * 256u + q * 16u);
+    // row = 2*(4w + it) + rsel: row/8 = w and row%8 = 2*it + rsel
+    const uint32_t src0 = stage + (rsel ? kOddRows : 0u) + (uint32_t)(w * 4) * 256u + q * 16u;
+    const uint32_t dst0 = tile + (uint32_t)qhi * (kTile * 128) + (uint32_t)w * 1024u + (uint32_t)rsel * 128u;
+    uint4 raw[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) raw[it] = lds128(src0 + it * 256u);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const uint32_t r8 = 2u * it + rsel;
+        const uint32_t dst = dst0 + 2u * it * 128u;
         uint4 a, b;
-        i8x4_to_f16x4(raw.x, a.x, a.y);
-        i8x4_to_f16x4(raw.y, a.z, a.w);
-        i8x4_to_f16x4(raw.z, b.x, b.y);
-        i8x4_to_f16x4(raw.w, b.z, b.w);
-        sts128(tile + kmajor_sw128_off(row, 16 * q, kTile), a);
-        sts128(tile + kmajor_sw128_off(row, 16 * q + 8, kTile), b);
+        i8x4_to_f16x4(raw[it].x, a.x, a.y);
+        i8x4_to_f16x4(raw[it].y, a.z, a.w);
+        i8x4_to_f16x4(raw[it].z, b.x, b.y);
+        i8x4_to_f16x4(raw[it].w, b.z, b.w);
+        sts128(dst + (((2u * qlo) ^ r8) << 4), a);
+        sts128(dst + (((2u * qlo + 1u) ^ r8) << 4), b);
     }
 }
 
-__device__ __forceinline__ void load_queries(const Params &p, uint32_t sq, int b, int g, int N, int ct)
+// Queries of (sequence b, KV head g) as the f16 B operand (rows >= R zero).
+__device__ __forceinline__ void load_queries(const Params &p, uint32_t sq, int b, int g, int N, int tid)
 {
     const int GH = p.G * p.H;
-    for (int e = ct; e < N * 32; e += kConsumers) {
+    for (int e = tid; e < N * 32; e += kThreads) {
         const int r = e >> 5, piece = e & 31;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (r < p.R) {
@@ -339,11 +390,11 @@ __device__ __forceinline__ void load_queries(const Params &p, uint32_t sq, int b
             float f[8];
             if (p.q_bf16) {
                 const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) + off);
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    f[2 * e2] = bf16_bits_to_f32(w[e2] & 0xffff);
-                    f[2 * e2 + 1] = bf16_bits_to_f32(w[e2] >> 16);
+                    f[2 * e2] = bf16_bits_to_f32(wv[e2] & 0xffff);
+                    f[2 * e2 + 1] = bf16_bits_to_f32(wv[e2] >> 16);
                 }
             } else {
                 const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.q) + off);
@@ -362,28 +413,52 @@ __device__ __forceinline__ void load_queries(const Params &p, uint32_t sq, int b
     }
 }
 
-template <int N>
-__device__ void run_consumers(const Params &p, uint8_t *smem, const Layout &L, Misc &ms)
+__device__ __forceinline__ void cta_sync()
 {
-    constexpr int NH = N / 2;                   // columns per warp half
-    constexpr int NHP = NH <= 8 ? 8 : (NH <= 16 ? 16 : 32);
-    const int ct = threadIdx.x - 32;            // consumer thread 0..255
-    const int cw = ct >> 5, lane = ct & 31;
-    const int qd = (cw + 1) & 3;                // TMEM lane quadrant of this warp
-    const int ch = cw >> 2;                     // column half / d half
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params p, int n_stages)
+{
+    constexpr int NQ = N / 4;                   // rows per warp in the softmax
+    constexpr int NQP = NQ <= 4 ? 4 : (NQ <= 8 ? 8 : 16);
+    constexpr int NO = N / 2;                   // rows per thread in the fold
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + pad;
+    const Layout L = make_layout(N, n_stages);
+    Misc &ms = *reinterpret_cast<Misc *>(smem + L.off_misc);
+    const int tid = threadIdx.x;
+    const int w = tid >> 5, lane = tid & 31;
+    const int qd = w & 3;                       // TMEM lane quadrant of this warp
+    const int rq = w >> 2;                      // softmax row quarter
+    const int oh = (w >> 2) & 1, oc = w >> 3;   // fold: d half, row half
     const uint32_t s_kv = smem_u32(smem + L.off_kv);
     const uint32_t s_q = smem_u32(smem + L.off_q);
     const uint32_t s_p = smem_u32(smem + L.off_p);
-    const uint32_t raw_base = smem_u32(smem + L.off_raw);
-    const uint32_t tmem = ms.tmem;
     const uint32_t t_lane = (uint32_t)(32 * qd) << 16;
     const uint32_t o_base = kMaxTiles * N;
     const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
     const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
+    const uint32_t ahead = (uint32_t)n_stages - 1; // ops whose copies are in flight
 
-    uint32_t op = 0, mma_phase = 0;
-    int cur_bg = -1;
-
+    if (tid == 0) {
+        mbar_init(&ms.mma, 1);
+        ms.abort = 0;
+        fence_mbar_init();
+    }
+    if (w == 0) {
+        tmem_alloc(&ms.tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    cta_sync();
+    const uint32_t tmem = ms.tmem;
+    uint32_t mma_phase = 0;
     auto wait_mma = [&]() {
         if (!ms.abort && !mbar_wait(&ms.mma, mma_phase)) {
             atomicExch(&ms.abort, 1);
@@ -392,261 +467,247 @@ __device__ void run_consumers(const Params &p, uint8_t *smem, const Layout &L, M
         mma_phase ^= 1;
         tc_fence_after();
     };
-    auto wait_full = [&](uint32_t s, uint32_t round) {
-        if (!ms.abort && !mbar_wait(&ms.full[s], round & 1)) {
-            atomicExch(&ms.abort, 1);
-            raise_status(p, QSA_STATUS_TIMEOUT);
-        }
-    };
 
-    Cursor cur;
-    cursor_init(p, cur);
-    for (; cur.remaining > 0; cursor_next(p, cur)) {
-        const int c0 = cur.c * p.chunk_cells;
-        const int nc = min(p.chunk_cells, cur.n - c0);
-        const int bg = cur.b * p.G + cur.g;
-        if (bg != cur_bg) {
-            load_queries(p, s_q, cur.b, cur.g, N, ct);
-            fence_proxy_async_smem();
-            cur_bg = bg;
+    // ---- resolve the first two groups; later groups are resolved two ahead
+    OpIter rg; // the group being resolved
+    op_init(p, rg);
+    for (int k = 0; k < 2; ++k) {
+        if (tid < kGroupCells) {
+            const int pos = resolve_list(p, rg, tid);
+            ms.ring[rg.gi % kSlotRing][tid] = resolve_check(p, resolve_page(p, rg, pos));
         }
-        if (ct < 64) {
-            ms.row_mrun[ct] = -INFINITY;
-            ms.row_lrun[ct] = 0.f;
+        if (rg.valid) op_next_group(p, rg);
+    }
+    __syncthreads();
+
+    OpIter is, cs; // issue side (`ahead` ops in front) and compute side
+    op_init(p, is);
+    op_init(p, cs);
+    for (uint32_t k = 0; k < ahead; ++k) {
+        if (is.valid) {
+            issue_op(p, smem, ms, is, L.off_raw + (k % n_stages) * kStageBytes, tid);
+            op_next(p, is);
         }
-        for (int gs = 0; gs < nc; gs += kGroupCells) {
-            const int gn = min(kGroupCells, nc - gs);
-            const int tiles = (gn + kTile - 1) / kTile;
-            // ---- scores: one K tile at a time
-            for (int t = 0; t < tiles; ++t, ++op) {
-                const uint32_t s = op % L.n_stages, round = op / L.n_stages;
-                const uint32_t st = raw_base + s * kStageBytes;
-                wait_full(s, round);
-                convert_tile(st, s_kv, cw, lane);
-                if (ct < kTile) {
-                    const int slot = *reinterpret_cast<const int *>(smem + L.off_raw + s * kStageBytes + kStageSlots + ct * 4);
-                    ms.cell_slot[t][ct] = slot;
-                    ms.cell_ks[t][ct] = *reinterpret_cast<const float *>(smem + L.off_raw + s * kStageBytes + kStageKs + ct * 4) * p.scale_log2;
-                    ms.cell_vs[t][ct] = *reinterpret_cast<const float *>(smem + L.off_raw + s * kStageBytes + kStageVs + ct * 4);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                consumer_sync();
-                tc_fence_after();
-                if (ct == 0) {
-                    mbar_arrive(&ms.empty[s]);
-#pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                        const uint64_t ad = smem_desc(s_kv + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc(s_q + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-                        mma_f16_ss(tmem + t * N, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        cp_async_commit();
+    }
+
+    int cur_bg = -1;
+    int r_pos = INT_MIN, r_raw = -1; // this thread's cell of the group being resolved
+    for (uint32_t op = 0; cs.valid; ++op) {
+        if (is.valid) {
+            issue_op(p, smem, ms, is, L.off_raw + ((op + ahead) % n_stages) * kStageBytes, tid);
+            op_next(p, is);
+        }
+        cp_async_commit();
+        if (ahead == 2)
+            asm volatile("cp.async.wait_group 2;" ::: "memory");
+        else
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        cta_sync(); // this op's rows and scales have landed, for every thread
+
+        const uint32_t st_off = L.off_raw + (op % n_stages) * kStageBytes;
+        const uint32_t st = smem_u32(smem) + st_off;
+        const int t = cs.t;
+        const bool last_tile = t == cs.tiles - 1;
+        if (cs.kind == 0) {
+            // ---- scores of one K tile
+            if (t == 0) {
+                if (tid < kGroupCells) r_pos = resolve_list(p, rg, tid);
+                if (cs.gs == 0) {
+                    const int bg = cs.cur.b * p.G + cs.cur.g;
+                    if (bg != cur_bg) {
+                        load_queries(p, s_q, cs.cur.b, cs.cur.g, N, tid);
+                        cur_bg = bg;
                     }
-                    mma_commit(&ms.mma);
+                    if (tid < 64) {
+                        ms.row_mrun[tid] = -INFINITY;
+                        ms.row_lrun[tid] = 0.f;
+                    }
                 }
-                wait_mma();
             }
-            // ---- softmax over the group
-            const int cell = 32 * qd + lane;
-            float mx[NH];
-#pragma unroll
-            for (int j = 0; j < NH; ++j) mx[j] = -INFINITY;
-            float vsabs = 0.f;
-            for (int t = 0; t < tiles; ++t) {
-                float sv[NH];
-#pragma unroll
-                for (int j = 0; j < NH; j += 8) tmem_ld8(tmem + t_lane + t * N + ch * NH + j, sv + j);
-                tmem_wait_ld();
-                const bool ok = ms.cell_slot[t][cell] >= 0;
-                const float ksc = ms.cell_ks[t][cell];
-                if (ok) vsabs = fmaxf(vsabs, fabsf(ms.cell_vs[t][cell]));
-#pragma unroll
-                for (int j = 0; j < NH; ++j) mx[j] = fmaxf(mx[j], ok ? sv[j] * ksc : -INFINITY);
+            convert_tile(st, s_kv, w, lane);
+            if (tid < kTile) {
+                const int slot = *reinterpret_cast<const int *>(smem + st_off + kStageSlots + tid * 4);
+                ms.cell_slot[t][tid] = slot;
+                ms.cell_ks[t][tid] = *reinterpret_cast<const float *>(smem + st_off + kStageKs + tid * 4) * p.scale_log2;
+                ms.cell_vs[t][tid] = *reinterpret_cast<const float *>(smem + st_off + kStageVs + tid * 4);
             }
+            fence_proxy_async_smem();
+            cta_sync();
+            if (tid == 0) {
 #pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                const int key = __reduce_max_sync(0xffffffffu, ordered_key(mx[j]));
-                if (lane == j) ms.red_max[ch][qd][j] = from_ordered_key(key);
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint64_t ad = smem_desc(s_kv + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc(s_q + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_f16_ss(tmem + t * N, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&ms.mma);
             }
-            {
-                const unsigned u = __reduce_max_sync(0xffffffffu, __float_as_uint(vsabs));
-                if (lane == 0) ms.red_vs[ch][qd] = __uint_as_float(u);
+            wait_mma();
+            if (last_tile) {
+                // ---- softmax over the group: warp (qd, rq) owns cells
+                // 32qd..32qd+31 of each tile and rows rq*NQ..rq*NQ+NQ-1
+                const int cell = 32 * qd + lane;
+                float mx[NQ];
+#pragma unroll
+                for (int j = 0; j < NQ; ++j) mx[j] = -INFINITY;
+                float vsabs = 0.f;
+                for (int tt = 0; tt < cs.tiles; ++tt) {
+                    float sv[NQ];
+                    tmem_ld_cols<NQ>(tmem + t_lane + tt * N + rq * NQ, sv);
+                    tmem_wait_ld();
+                    const bool ok = ms.cell_slot[tt][cell] >= 0;
+                    const float ksc = ms.cell_ks[tt][cell];
+                    if (ok) vsabs = fmaxf(vsabs, fabsf(ms.cell_vs[tt][cell]));
+#pragma unroll
+                    for (int j = 0; j < NQ; ++j) mx[j] = fmaxf(mx[j], ok ? __fmul_rn(sv[j], ksc) : -INFINITY);
+                }
+#pragma unroll
+                for (int j = 0; j < NQ; ++j) {
+                    const int key = __reduce_max_sync(0xffffffffu, ordered_key(mx[j]));
+                    if (lane == j) ms.red_max[rq][qd][j] = from_ordered_key(key);
+                }
+                {
+                    const unsigned u = __reduce_max_sync(0xffffffffu, __float_as_uint(vsabs));
+                    if (lane == 0) ms.red_vs[w] = __uint_as_float(u);
+                }
+                // the group two ahead: its page-table reads go out now
+                if (tid < kGroupCells) r_raw = resolve_page(p, rg, r_pos);
+                cta_sync();
+                float m2[NQ];
+#pragma unroll
+                for (int j = 0; j < NQ; ++j)
+                    m2[j] = fmaxf(fmaxf(ms.red_max[rq][0][j], ms.red_max[rq][1][j]),
+                                  fmaxf(ms.red_max[rq][2][j], ms.red_max[rq][3][j]));
+                float sigma = fmaxf(fmaxf(ms.red_vs[0], ms.red_vs[1]), fmaxf(ms.red_vs[2], ms.red_vs[3]));
+                if (!(sigma > 0.f)) sigma = 1.f;
+                const float inv_sigma = 1.f / sigma;
+                float ls[NQP];
+#pragma unroll
+                for (int j = 0; j < NQP; ++j) ls[j] = 0.f;
+                for (int tt = 0; tt < cs.tiles; ++tt) {
+                    float sv[NQ];
+                    tmem_ld_cols<NQ>(tmem + t_lane + tt * N + rq * NQ, sv);
+                    tmem_wait_ld();
+                    const bool ok = ms.cell_slot[tt][cell] >= 0;
+                    const float ksc = ms.cell_ks[tt][cell];
+                    const float vsn = ok ? ms.cell_vs[tt][cell] * inv_sigma : 0.f;
+                    const uint32_t ptile = s_p + tt * (N * kTile * 2);
+#pragma unroll
+                    for (int j = 0; j < NQ; ++j) {
+                        // the same rounded product as in the max pass (no FMA
+                        // contraction), so the max cell gets exactly 2^0 = 1
+                        const float pr = ok ? fast_exp2(__fmul_rn(sv[j], ksc) - m2[j]) : 0.f;
+                        ls[j] += pr;
+                        const __half h = __float2half_rn(pr * vsn);
+                        sts16(ptile + kmajor_sw128_off(rq * NQ + j, cell, N),
+                              *reinterpret_cast<const uint16_t *>(&h));
+                    }
+                }
+                // reduce-scatter of the NQ row sums over the warp's 32 cells
+#pragma unroll
+                for (int o = 16, cnt = NQP; o >= 1; o >>= 1) {
+                    if (cnt > 1) {
+                        const int half = cnt / 2;
+                        const bool up = (lane & o) != 0;
+#pragma unroll
+                        for (int i = 0; i < half; ++i) {
+                            const float send = up ? ls[i] : ls[i + half];
+                            const float keep = up ? ls[i + half] : ls[i];
+                            ls[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
+                        cnt = half;
+                    } else {
+                        ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], o);
+                    }
+                }
+                {
+                    constexpr int lanes_per_col = 32 / NQP;
+                    const int col = lane / lanes_per_col;
+                    if (lane % lanes_per_col == 0 && col < NQ) ms.red_sum[rq][qd][col] = ls[0];
+                }
+                if (tid == 0) ms.sigma = sigma;
+                fence_proxy_async_smem();
+                cta_sync();
+                // per-row group values and their combination with earlier groups
+                if (tid < N) {
+                    const int r = tid, hr = r / NQ, jr = r % NQ;
+                    const float mg = fmaxf(fmaxf(ms.red_max[hr][0][jr], ms.red_max[hr][1][jr]),
+                                           fmaxf(ms.red_max[hr][2][jr], ms.red_max[hr][3][jr]));
+                    const float lg = ((ms.red_sum[hr][0][jr] + ms.red_sum[hr][1][jr]) + ms.red_sum[hr][2][jr]) +
+                                     ms.red_sum[hr][3][jr];
+                    const float mr = ms.row_mrun[r];
+                    const float mn = fmaxf(mr, mg);
+                    float fa = 0.f, fb = 0.f;
+                    if (mn > -INFINITY) {
+                        fa = mr == mn ? 1.f : (mr > -INFINITY ? fast_exp2(mr - mn) : 0.f);
+                        fb = mg == mn ? 1.f : (mg > -INFINITY ? fast_exp2(mg - mn) : 0.f);
+                    }
+                    ms.row_fa[r] = fa;
+                    ms.row_fb[r] = fb;
+                    ms.row_mrun[r] = mn;
+                    ms.row_lrun[r] = ms.row_lrun[r] * fa + lg * fb;
+                }
             }
-            tc_fence_before();
-            consumer_sync();
-            tc_fence_after();
-            float m2[NH];
-#pragma unroll
-            for (int j = 0; j < NH; ++j)
-                m2[j] = fmaxf(fmaxf(ms.red_max[ch][0][j], ms.red_max[ch][1][j]),
-                              fmaxf(ms.red_max[ch][2][j], ms.red_max[ch][3][j]));
-            float sigma = fmaxf(fmaxf(ms.red_vs[ch][0], ms.red_vs[ch][1]), fmaxf(ms.red_vs[ch][2], ms.red_vs[ch][3]));
-            if (!(sigma > 0.f)) sigma = 1.f;
-            const float inv_sigma = 1.f / sigma;
-            float ls[NHP];
-#pragma unroll
-            for (int j = 0; j < NHP; ++j) ls[j] = 0.f;
-            for (int t = 0; t < tiles; ++t) {
-                float sv[NH];
-#pragma unroll
-                for (int j = 0; j < NH; j += 8) tmem_ld8(tmem + t_lane + t * N + ch * NH + j, sv + j);
-                tmem_wait_ld();
-                const bool ok = ms.cell_slot[t][cell] >= 0;
-                const float ksc = ms.cell_ks[t][cell];
-                const float vsn = ok ? ms.cell_vs[t][cell] * inv_sigma : 0.f;
+        } else {
+            // ---- P.V of one V tile
+            convert_tile(st, s_kv, w, lane);
+            fence_proxy_async_smem();
+            cta_sync();
+            if (tid == 0) {
                 const uint32_t ptile = s_p + t * (N * kTile * 2);
 #pragma unroll
-                for (int j = 0; j < NH; ++j) {
-                    const float pr = ok ? fast_exp2(sv[j] * ksc - m2[j]) : 0.f;
-                    ls[j] += pr;
-                    const __half h = __float2half_rn(pr * vsn);
-                    sts16(ptile + kmajor_sw128_off(ch * NH + j, cell, N), *reinterpret_cast<const uint16_t *>(&h));
-                }
-            }
-            // reduce-scatter of the NH column sums over the warp's 32 cells
+                for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int o = 16, cnt = NHP; o >= 1; o >>= 1) {
-                if (cnt > 1) {
-                    const int half = cnt / 2;
-                    const bool up = (lane & o) != 0;
-#pragma unroll
-                    for (int i = 0; i < half; ++i) {
-                        const float send = up ? ls[i] : ls[i + half];
-                        const float keep = up ? ls[i + half] : ls[i];
-                        ls[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t ad = smem_desc(s_kv + (2 * h) * (kTile * 128) + kk * 2048, kTile * 128, 1024);
+                        const uint64_t bd = smem_desc(ptile + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+                        mma_f16_ss(tmem + o_base + h * N, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
                     }
-                    cnt = half;
-                } else {
-                    ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], o);
                 }
+                mma_commit(&ms.mma);
             }
-            {
-                constexpr int lanes_per_col = 32 / NHP;
-                const int col = lane / lanes_per_col;
-                if (lane % lanes_per_col == 0 && col < NH) ms.red_sum[ch][qd][col] = ls[0];
-            }
-            if (ct == 0) ms.sigma = sigma;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            consumer_sync();
-            tc_fence_after();
-            // per-row group values and their combination with earlier groups
-            if (ct < N) {
-                const int r = ct, hr = r / NH, jr = r % NH;
-                const float mg = fmaxf(fmaxf(ms.red_max[hr][0][jr], ms.red_max[hr][1][jr]),
-                                       fmaxf(ms.red_max[hr][2][jr], ms.red_max[hr][3][jr]));
-                const float lg = ((ms.red_sum[hr][0][jr] + ms.red_sum[hr][1][jr]) + ms.red_sum[hr][2][jr]) +
-                                 ms.red_sum[hr][3][jr];
-                const float mr = ms.row_mrun[r];
-                const float mn = fmaxf(mr, mg);
-                float fa = 0.f, fb = 0.f;
-                if (mn > -INFINITY) {
-                    fa = mr == mn ? 1.f : (mr > -INFINITY ? fast_exp2(mr - mn) : 0.f);
-                    fb = mg == mn ? 1.f : (mg > -INFINITY ? fast_exp2(mg - mn) : 0.f);
-                }
-                ms.row_fa[r] = fa;
-                ms.row_fb[r] = fb;
-                ms.row_mrun[r] = mn;
-                ms.row_lrun[r] = ms.row_lrun[r] * fa + lg * fb;
-            }
-            // ---- P.V: one V tile at a time
-            for (int t = 0; t < tiles; ++t, ++op) {
-                const uint32_t s = op % L.n_stages, round = op / L.n_stages;
-                const uint32_t st = raw_base + s * kStageBytes;
-                wait_full(s, round);
-                convert_tile(st, s_kv, cw, lane);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                consumer_sync();
-                tc_fence_after();
-                if (ct == 0) {
-                    mbar_arrive(&ms.empty[s]);
-                    const uint32_t ptile = s_p + t * (N * kTile * 2);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk) {
-                            const uint64_t ad = smem_desc(s_kv + (2 * h) * (kTile * 128) + kk * 2048, kTile * 128, 1024);
-                            const uint64_t bd = smem_desc(ptile + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-                            mma_f16_ss(tmem + o_base + h * N, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(&ms.mma);
-                }
-                wait_mma();
-            }
-            // ---- fold the group's O into the chunk partial.  The first group
-            // writes it; a later group (chunks longer than 256 cells) rescales
-            // the partial already written by this thread and adds to it.
-            {
-                const int d = ch * 128 + 32 * qd + lane;
-                const size_t base = (((size_t)cur.b * p.G + cur.g) * p.n_chunks + cur.c) * p.R;
-                const float sg = ms.sigma;
-#pragma unroll
-                for (int j0 = 0; j0 < N; j0 += 16) {
-                    float ov[16];
-                    tmem_ld16(tmem + t_lane + o_base + ch * N + j0, ov);
+            wait_mma();
+            if (last_tile) {
+                // the group two ahead: checked slots into the ring
+                if (tid < kGroupCells && rg.valid) ms.ring[rg.gi % kSlotRing][tid] = resolve_check(p, r_raw);
+                if (rg.valid) op_next_group(p, rg);
+                r_pos = INT_MIN;
+                r_raw = -1;
+                // ---- fold the group's O into the chunk partial.  The first
+                // group writes it; a later group (chunks longer than 256
+                // cells) rescales the partial this thread wrote and adds.
+                {
+                    const int d = oh * 128 + 32 * qd + lane;
+                    const size_t base = (((size_t)cs.cur.b * p.G + cs.cur.g) * p.n_chunks + cs.cur.c) * p.R;
+                    const float sg = ms.sigma;
+                    float ov[NO];
+                    tmem_ld_cols<NO>(tmem + t_lane + o_base + oh * N + oc * NO, ov);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int r = j0 + i;
+                    for (int i = 0; i < NO; ++i) {
+                        const int r = oc * NO + i;
                         if (r >= p.R) continue;
-                        float* dst = p.part_o + (base + r) * kHeadDim + d;
+                        float *dst = p.part_o + (base + r) * kHeadDim + d;
                         float v = ov[i] * sg * ms.row_fb[r];
-                        if (gs > 0) v = fmaf(*dst, ms.row_fa[r], v);
+                        if (cs.gs > 0) v = fmaf(*dst, ms.row_fa[r], v);
                         *dst = v;
                     }
                 }
+                if (cs.gs + kGroupCells >= cs.nc && tid < p.R) {
+                    // ---- item epilogue: the chunk's max and denominator
+                    const size_t base = (((size_t)cs.cur.b * p.G + cs.cur.g) * p.n_chunks + cs.cur.c) * p.R;
+                    p.part_m[base + tid] = ms.row_mrun[tid] * kLn2;
+                    p.part_l[base + tid] = ms.row_lrun[tid];
+                }
+                cta_sync();
             }
-            tc_fence_before();
-            consumer_sync();
-            tc_fence_after();
         }
-        // ---- item epilogue: the chunk's max and denominator
-        if (ct < p.R) {
-            const size_t base = (((size_t)cur.b * p.G + cur.g) * p.n_chunks + cur.c) * p.R;
-            p.part_m[base + ct] = ms.row_mrun[ct] * kLn2;
-            p.part_l[base + ct] = ms.row_lrun[ct];
-        }
-        consumer_sync();
+        op_next(p, cs);
     }
-}
-
-template <int N>
-__global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params p, int n_stages)
-{
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + pad;
-    const Layout L = make_layout(N, n_stages);
-    Misc &ms = *reinterpret_cast<Misc *>(smem + L.off_misc);
-    const int warp = threadIdx.x >> 5;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < n_stages; ++s) {
-            mbar_init(&ms.full[s], 33);
-            mbar_init(&ms.empty[s], 1);
-        }
-        mbar_init(&ms.mma, 1);
-        ms.abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(&ms.tmem, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    if (warp == 0)
-        run_producer(p, smem, L, ms);
-    else
-        run_consumers<N>(p, smem, L, ms);
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(ms.tmem, kTmemCols);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    cta_sync();
+    if (w == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int N>
