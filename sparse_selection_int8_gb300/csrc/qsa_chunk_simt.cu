@@ -37,6 +37,7 @@ qsa_chunk_simt_kernel(const Params p, int n_row_blocks)
     __shared__ float s_ks[kStage];
     __shared__ float s_vs[kStage];
 
+    cudaTriggerProgrammaticLaunchCompletion(); // the merge kernel waits for this grid anyway
     const int chunk = blockIdx.x / n_row_blocks;
     const int rb = blockIdx.x % n_row_blocks;
     const int g = blockIdx.y;

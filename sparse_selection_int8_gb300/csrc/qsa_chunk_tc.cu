@@ -70,6 +70,12 @@ struct Layout {
     uint32_t off_kv, off_q, off_p, off_raw, n_stages, off_misc, total;
 };
 
+// Position in the work list (see cursor_init_warp / cursor_next).
+struct Cursor {
+    int b, g, c, nch, start, n;
+    int remaining;
+};
+
 // Misc area: slot ring, per-group cell info, reduction scratch, per-row values.
 struct Misc {
     int32_t ring[kSlotRing][kGroupCells];
@@ -83,6 +89,7 @@ struct Misc {
     float sigma;
     int32_t abort;
     uint32_t tmem;
+    Cursor first; // this CTA's first item
     uint64_t mma;
 };
 
@@ -173,10 +180,6 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v)
 
 // Non-empty (sequence, KV head, chunk) items in sequence-major order; each
 // CTA takes a contiguous range (consecutive chunks share their queries).
-struct Cursor {
-    int b, g, c, nch, start, n;
-    int remaining;
-};
 
 __device__ inline int seq_chunks(const Params &p, int b, int *start, int *n)
 {
@@ -184,30 +187,48 @@ __device__ inline int seq_chunks(const Params &p, int b, int *start, int *n)
     return *n > 0 ? (*n + p.chunk_cells - 1) / p.chunk_cells : 0;
 }
 
-__device__ inline void cursor_init(const Params &p, Cursor &cur)
+// Position of this CTA's first item, computed by one full warp: lanes read
+// the sequences' list offsets in parallel, a warp scan finds the sequence
+// that holds item `lo`.
+__device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
 {
     long long total = 0;
     int s, n;
-    for (int b = 0; b < p.n_seq; ++b) total += (long long)p.G * seq_chunks(p, b, &s, &n);
+    for (int b = lane; b < p.n_seq; b += 32) total += (long long)p.G * seq_chunks(p, b, &s, &n);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     const long long per = (total + gridDim.x - 1) / gridDim.x;
-    long long lo = per * blockIdx.x;
+    const long long lo = per * blockIdx.x;
     const long long hi = min(lo + per, total);
     cur.remaining = lo < hi ? (int)(hi - lo) : 0;
     cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
     if (cur.remaining == 0) return;
-    for (int b = 0; b < p.n_seq; ++b) {
-        const int nch = seq_chunks(p, b, &s, &n);
+    long long before = 0; // items of the sequences already passed
+    for (int b0 = 0; b0 < p.n_seq; b0 += 32) {
+        const int b = b0 + lane;
+        int st = 0, len = 0, nch = 0;
+        if (b < p.n_seq) nch = seq_chunks(p, b, &st, &len);
         const long long items = (long long)p.G * nch;
-        if (lo < items) {
-            cur.b = b;
-            cur.nch = nch;
-            cur.start = s;
-            cur.n = n;
-            cur.g = (int)(lo / nch);
-            cur.c = (int)(lo % nch);
+        long long incl = items;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const long long excl = incl - items;
+        const unsigned hit = __ballot_sync(0xffffffffu, items > 0 && before + excl <= lo && lo < before + incl);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const long long off = lo - before - __shfl_sync(0xffffffffu, excl, src);
+            cur.b = b0 + src;
+            cur.nch = __shfl_sync(0xffffffffu, nch, src);
+            cur.start = __shfl_sync(0xffffffffu, st, src);
+            cur.n = __shfl_sync(0xffffffffu, len, src);
+            cur.g = (int)(off / cur.nch);
+            cur.c = (int)(off % cur.nch);
             return;
         }
-        lo -= items;
+        before += __shfl_sync(0xffffffffu, incl, 31);
     }
     cur.remaining = 0;
 }
@@ -256,9 +277,9 @@ __device__ inline void op_setup_item(const Params &p, OpIter &it)
     it.tiles = (min(kGroupCells, it.nc) + kTile - 1) / kTile;
 }
 
-__device__ inline void op_init(const Params &p, OpIter &it)
+__device__ inline void op_init(const Params &p, OpIter &it, const Cursor &first)
 {
-    cursor_init(p, it.cur);
+    it.cur = first;
     it.gi = 0;
     it.valid = it.cur.remaining > 0;
     if (it.valid) op_setup_item(p, it);
@@ -456,8 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         tmem_alloc(&ms.tmem, kTmemCols);
         tmem_relinquish();
     }
+    if (w == 1) cursor_init_warp(p, ms.first, lane);
     cta_sync();
+    // the merge kernel may be scheduled now; it waits for this grid's results
+    cudaTriggerProgrammaticLaunchCompletion();
     const uint32_t tmem = ms.tmem;
+    const Cursor first = ms.first;
     uint32_t mma_phase = 0;
     auto wait_mma = [&]() {
         if (!ms.abort && !mbar_wait(&ms.mma, mma_phase)) {
@@ -470,19 +495,22 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 
     // ---- resolve the first two groups; later groups are resolved two ahead
     OpIter rg; // the group being resolved
-    op_init(p, rg);
-    for (int k = 0; k < 2; ++k) {
-        if (tid < kGroupCells) {
-            const int pos = resolve_list(p, rg, tid);
-            ms.ring[rg.gi % kSlotRing][tid] = resolve_check(p, resolve_page(p, rg, pos));
-        }
+    op_init(p, rg, first);
+    {
+        OpIter g1 = rg; // threads 0..255 resolve group 0, threads 256..511 group 1
+        if (g1.valid) op_next_group(p, g1);
+        const OpIter &mine = tid < kGroupCells ? rg : g1;
+        const int pos = resolve_list(p, mine, tid & (kGroupCells - 1));
+        const int slot = resolve_check(p, resolve_page(p, mine, pos));
+        if (mine.valid) ms.ring[mine.gi % kSlotRing][tid & (kGroupCells - 1)] = slot;
+        rg = g1;
         if (rg.valid) op_next_group(p, rg);
     }
     __syncthreads();
 
     OpIter is, cs; // issue side (`ahead` ops in front) and compute side
-    op_init(p, is);
-    op_init(p, cs);
+    op_init(p, is, first);
+    op_init(p, cs, first);
     for (uint32_t k = 0; k < ahead; ++k) {
         if (is.valid) {
             issue_op(p, smem, ms, is, L.off_raw + (k % n_stages) * kStageBytes, tid);

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(kBlock) qsa_merge_kernel(const Params p)
     const int g = blockIdx.y;
     const int b = blockIdx.z;
     const int d = threadIdx.x;
+    // launched as a programmatic dependent of the chunk kernel: wait until
+    // that grid has finished and its partials are visible
+    cudaGridDependencySynchronize();
     int start, n;
     seq_range(p, b, &start, &n);
     const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
@@ -82,9 +85,17 @@ __global__ void __launch_bounds__(kBlock) qsa_merge_kernel(const Params p)
 
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
-    dim3 grid((unsigned)p.R, (unsigned)p.G, (unsigned)p.n_seq);
-    qsa_merge_kernel<<<grid, kBlock, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.R, (unsigned)p.G, (unsigned)p.n_seq);
+    cfg.blockDim = dim3(kBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel, p);
 }
 
 } // namespace qsa
