@@ -161,6 +161,31 @@ qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_
                              const void *workspace, const float **m, const float **l,
                              const float **o, int32_t *n_chunks);
 
+/*
+ * qsa_decode_attn_step without a workspace, for callers that cannot allocate
+ * device memory where they run this call (a serving path whose memory budget
+ * is fixed after start-up, or a plugin inside an application that owns all
+ * device memory).  The pages have no counterpart; this is an addition of
+ * this library.
+ *   Arguments are those of qsa_decode_attn_step minus workspace and
+ *   workspace_bytes.  The chunk partials go to a fixed 8 MiB array that the
+ *   library keeps in every GPU that loads it, until the process exits.
+ *   A call whose qsa_workspace_bytes(shape, 1, n_sel) exceeds 8 MiB returns
+ *   QSA_ERR_WORKSPACE and launches nothing (e.g. 48 query rows at chunk 128
+ *   fit about 21,000 selected cells).
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls share the array: calls whose kernels may overlap on the GPU
+ *   (different streams) race and must be ordered by the caller.
+ *   It allocates nothing and calls no allocating routine.
+ */
+qsa_status qsa_decode_attn_step_noalloc(const qsa_shape *shape, const void *q,
+                                        const int8_t *k_pool, const int8_t *v_pool,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *page_table, const int32_t *sel,
+                                        int32_t n_sel, float *out, uint32_t *status,
+                                        void *stream);
+
 /* Static description of a status code. */
 const char *qsa_status_string(int32_t status);
 

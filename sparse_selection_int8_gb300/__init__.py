@@ -82,6 +82,8 @@ _SIG = {
                            ctypes.POINTER(_VP), ctypes.POINTER(_VP), ctypes.POINTER(_VP),
                            ctypes.POINTER(ctypes.c_int32)], ctypes.c_int32),
     "qsa_status_string": ([ctypes.c_int32], ctypes.c_char_p),
+    "qsa_decode_attn_step_noalloc": ([ctypes.POINTER(qsa_shape), _VP, _VP, _VP, _VP, _VP, _VP,
+                                      _VP, ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int32),
 }
 
 
@@ -164,6 +166,17 @@ def qsa_decode_attn_batch(shape: qsa_shape, n_seq: int, q, k_pool, v_pool, k_sca
         _ptr(v_scale), _ptr(page_table), _ptr(sel), _ptr(sel_offsets), int(max_selected),
         _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
         "qsa_decode_attn_batch")
+
+
+def qsa_decode_attn_step_noalloc(shape: qsa_shape, q, k_pool, v_pool, k_scale, v_scale,
+                                 page_table, sel, n_sel: int, out, status=None,
+                                 stream=None) -> None:
+    """qsa_decode_attn_step with the library's fixed scratch array instead of
+    a workspace (for callers that cannot allocate device memory)."""
+    _check(load_library().qsa_decode_attn_step_noalloc(
+        ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(page_table), _ptr(sel), int(n_sel), _ptr(out), _ptr(status),
+        _stream(stream)), "qsa_decode_attn_step_noalloc")
 
 
 def qsa_partials_view(shape: qsa_shape, n_seq: int, max_selected: int, workspace):
