@@ -53,7 +53,30 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline")
+    ap.add_argument("--case", default=None,
+                    help="run one workload --reps times and exit (for profiler captures): "
+                         "tiny_decode, qsa_decode1..4, batched_decode, long_context, prompt_shaped")
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tcgen05"])
     return ap.parse_args()
+
+
+def run_case(args):
+    """One workload, --reps calls, no timing: the command profiler captures wrap."""
+    import torch
+    import qsa_workloads as wl
+    from sparse_selection_int8_gb300 import build as qsa_build
+    qsa_build.build()
+    import sparse_selection_int8_gb300 as qsa
+    name = args.case
+    p = wl.qsa_decode(int(name[-1])) if name.startswith("qsa_decode") else getattr(wl, name)()
+    algo = {"auto": qsa.QSA_ALGO_AUTO, "simt": qsa.QSA_ALGO_SIMT, "tcgen05": qsa.QSA_ALGO_TCGEN05}[args.algo]
+    dp = qsa.DeviceProblem(p, algo=algo)
+    for _ in range(args.reps):
+        dp.run()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": name, "reps": args.reps, "status": int(dp.status.item())}))
+    return 0
 
 
 # ------------------------------------------------------------------ helpers
@@ -423,6 +446,8 @@ def run_ours(args, world, rank, local):
 
 def main():
     args = parse()
+    if args.case:
+        return run_case(args)
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":
