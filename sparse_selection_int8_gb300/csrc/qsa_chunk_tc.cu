@@ -18,25 +18,27 @@
 // to f16; the group's largest scale multiplies the fp32 result.  Queries are
 // rounded to f16.  Accumulation is fp32 in tensor memory.
 //
-// One persistent CTA of 16 warps per SM walks a contiguous range of
-// non-empty (sequence, KV head, chunk) items as a sequence of ops: for every
-// group of up to 256 cells (two M tiles sharing one max), its K tiles, then
-// its V tiles.  Every warp takes part in every phase:
-//   gather   the rows of op k+2 are copied with 16-byte cp.async into a ring
-//            of three raw stages while op k is computed (random 256-byte rows
-//            need many warps issuing copies: one warp tops out near 8 GB/s
-//            per SM; one TMA bulk copy per row was ~10x slower still);
-//   resolve  list entry -> page slot (a1) runs two groups ahead: the list
-//            reads are issued at a group's first K op, the page-table reads
-//            after its softmax max pass, and the checked slots are stored at
-//            the group's end;
-//   convert  a raw stage becomes an f16 tile in the tensor cores'
-//            128-byte-swizzled layout (no bank conflicts on either side);
+// Two persistent CTAs of 8 warps share each SM (about 110 KB of shared
+// memory and 256 TMEM columns each), so one CTA's dependent phases overlap
+// the other's.  A CTA walks a contiguous range of non-empty (sequence, KV
+// head, chunk) items as a sequence of ops: for every group of up to 256
+// cells (two M tiles sharing one max), its K tiles, then its V tiles.
+//   gather   each op's 128 rows (256 B each) are loaded straight into
+//            registers with 16-byte read-only loads one op ahead (8 x 16 B
+//            per thread, issued as soon as the previous op is converted);
+//            16 lanes cover a row, so every load instruction moves two whole
+//            rows; the op after that is prefetched into L2 at the same time,
+//            so the register loads mostly hit L2;
+//   resolve  list entry -> page slot (a1) runs two groups ahead: list reads
+//            at a group's first K op, page-table reads after its max pass,
+//            the checked slots stored in a small ring at the group's end;
+//   convert  registers -> f16 tile in the tensor cores' 128-byte-swizzled
+//            layout (the lane mapping makes the stores conflict-free);
 //   MMA      one thread issues tcgen05.mma; completion on an mbarrier;
-//   softmax  warp (quadrant q, quarter c) owns cells 32q..32q+31 of a tile
-//            and a quarter of the rows: max via redux, sums via a
-//            reduce-scatter butterfly, all in a fixed order, so partials are
-//            bit-identical run to run.
+//   softmax  warp (quadrant q, half h) owns cells 32q..32q+31 and half the
+//            rows, eight rows at a time: max via redux, P built per tile
+//            right before its P.V MMA, sums via a reduce-scatter butterfly,
+//            all in a fixed order, so partials are bit-identical run to run.
 //
 // The only wait that is not a CTA barrier is the MMA-completion wait; it is
 // bounded, and a wait that runs out raises QSA_STATUS_TIMEOUT and the kernel
@@ -54,20 +56,14 @@ using namespace sm100;
 constexpr int kTile = 128;          // cells per MMA tile (M)
 constexpr int kMaxTiles = 2;        // tiles per softmax group
 constexpr int kGroupCells = kTile * kMaxTiles;
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlotRing = 4;        // groups of resolved slots kept
-constexpr uint32_t kOddRows = 64 * 256 + 64;        // odd rows start 64 B past a 128-B line
-constexpr uint32_t kStageRowBytes = kOddRows + 64 * 256;
-constexpr uint32_t kStageSlots = kStageRowBytes;     // int32[128]
-constexpr uint32_t kStageKs = kStageSlots + 512;     // f32[128]
-constexpr uint32_t kStageVs = kStageKs + 512;        // f32[128]
-constexpr uint32_t kStageBytes = ((kStageVs + 512) + 127) / 128 * 128;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTileF16Bytes = kTile * kHeadDim * 2; // 64 KB
 
 struct Layout {
-    uint32_t off_kv, off_q, off_p, off_raw, n_stages, off_misc, total;
+    uint32_t off_kv, off_q, off_p, off_misc, total;
 };
 
 // Position in the work list (see cursor_init_warp / cursor_next).
@@ -82,33 +78,25 @@ struct Misc {
     int32_t cell_slot[kMaxTiles][kTile];
     float cell_ks[kMaxTiles][kTile];
     float cell_vs[kMaxTiles][kTile];
-    float red_max[4][4][16]; // [row quarter][lane quadrant][row within quarter]
-    float red_sum[4][4][16];
+    float red_max[2][32][4]; // [row half][row within half][lane quadrant]
+    float red_sum[2][32][4];
     float red_vs[kWarps];
     float row_fa[64], row_fb[64], row_mrun[64], row_lrun[64];
-    float sigma;
     int32_t abort;
     uint32_t tmem;
     Cursor first; // this CTA's first item
     uint64_t mma;
 };
 
-__host__ __device__ inline Layout make_layout(int N, int n_stages)
+__host__ __device__ inline Layout make_layout(int N)
 {
     Layout L;
     L.off_kv = 0;
     L.off_q = kTileF16Bytes;
     L.off_p = L.off_q + (uint32_t)N * kHeadDim * 2;
-    L.off_raw = L.off_p + (uint32_t)kMaxTiles * N * kTile * 2;
-    L.n_stages = (uint32_t)n_stages;
-    L.off_misc = L.off_raw + (uint32_t)n_stages * kStageBytes;
+    L.off_misc = L.off_p + (uint32_t)N * kTile * 2;
     L.total = L.off_misc + (uint32_t)((sizeof(Misc) + 127) / 128 * 128);
     return L;
-}
-
-__device__ __forceinline__ uint32_t row_offset(int c)
-{
-    return (c & 1) ? kOddRows + (uint32_t)(c >> 1) * 256u : (uint32_t)(c >> 1) * 256u;
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
@@ -116,15 +104,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
 }
 
 __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v)
@@ -154,18 +133,6 @@ __device__ __forceinline__ float from_ordered_key(int k)
 {
     return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
 }
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // NC consecutive columns of tensor memory (a multiple of 4) into v.
 template <int NC>
@@ -341,61 +308,83 @@ __device__ __forceinline__ int resolve_check(const Params &p, int raw)
     return raw;
 }
 
-// Copies of one op into a raw stage: warp w moves rows 8w..8w+7, two per
-// instruction (16 lanes x 16 B per 256-byte row).  For a K op the first 128
-// threads also publish their cell's slot and copy its two scales.  Masked
-// cells are not copied: their stale bytes are finite codes that get zero
-// weight.
-__device__ __forceinline__ void issue_op(const Params &p, uint8_t *smem, const Misc &ms,
-                                         const OpIter &it, uint32_t st_off, int tid)
+// One op's rows in registers: warp w loads row pairs 8w..8w+7; lane
+// (qhi, rsel, qlo) takes piece q = 4*qhi + qlo (16 B) of row 2*rp + rsel.
+// Cells that are masked load nothing (zeros).  For a K op the first 128
+// threads also load their cell's two scales.
+struct OpRegs {
+    uint4 raw[8];
+    float ks, vs;
+};
+
+__device__ __forceinline__ void load_op(const Params &p, const Misc &ms, const OpIter &it, int tid,
+                                        OpRegs &r)
 {
     const int w = tid >> 5, lane = tid & 31;
+    const int rsel = (lane >> 2) & 1, q = (lane >> 3) * 4 + (lane & 3);
     const int *tslots = ms.ring[it.gi % kSlotRing] + it.t * kTile;
     const size_t kv_base = ((size_t)it.cur.b * p.G + it.cur.g) * p.pool_cells;
-    const int8_t *pool = (it.kind == 0 ? p.k_pool : p.v_pool) + kv_base * kHeadDim + (lane & 15) * 16;
-    const uint32_t st = smem_u32(smem) + st_off;
+    const int8_t *pool = (it.kind == 0 ? p.k_pool : p.v_pool) + kv_base * kHeadDim + q * 16;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = 8 * w + 2 * i + (lane >> 4);
-        const int slot = tslots[row];
-        if (slot >= 0) cp_async16(st + row_offset(row) + (lane & 15) * 16, pool + (size_t)slot * kHeadDim);
+    for (int i = 0; i < 8; ++i) {
+        const int slot = tslots[2 * (8 * w + i) + rsel];
+        r.raw[i] = slot >= 0 ? ldg_nc_v4(pool + (size_t)slot * kHeadDim) : make_uint4(0, 0, 0, 0);
     }
+    r.ks = r.vs = 0.f;
     if (it.kind == 0 && tid < kTile) {
         const int slot = tslots[tid];
-        *reinterpret_cast<int *>(smem + st_off + kStageSlots + tid * 4) = slot;
         if (slot >= 0) {
-            cp_async4(st + kStageKs + tid * 4, p.k_scale + kv_base + slot);
-            cp_async4(st + kStageVs + tid * 4, p.v_scale + kv_base + slot);
+            r.ks = __ldg(p.k_scale + kv_base + slot);
+            r.vs = __ldg(p.v_scale + kv_base + slot);
         }
     }
 }
 
-// Dequantise one raw stage (128 rows) into the f16 tile.  Warp w converts
-// row pairs 4w..4w+3; 32 threads cover two rows x sixteen 16-byte pieces.
-// Even and odd rows sit in regions 64 B apart modulo 128, so both the reads
-// and the swizzled writes are free of bank conflicts.
-__device__ __forceinline__ void convert_tile(uint32_t stage, uint32_t tile, int w, int lane)
+// Warm L2 with the rows (and, for a K op, the scales) of an op that is
+// loaded into registers one op later: thread i prefetches 128-byte line
+// i % 2 of row i / 2.  No registers or shared memory are held.
+__device__ __forceinline__ void prefetch_op(const Params &p, const Misc &ms, const OpIter &it, int tid)
 {
+    const int *tslots = ms.ring[it.gi % kSlotRing] + it.t * kTile;
+    const size_t kv_base = ((size_t)it.cur.b * p.G + it.cur.g) * p.pool_cells;
+    const int slot = tslots[tid >> 1];
+    if (slot >= 0) {
+        const int8_t *row = (it.kind == 0 ? p.k_pool : p.v_pool) + (kv_base + slot) * kHeadDim + (tid & 1) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+        if (it.kind == 0) {
+            const float *sc = (tid & 1) ? p.v_scale : p.k_scale;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(sc + kv_base + slot));
+        }
+    }
+}
+
+// Registers -> f16 tile: row = 2*(8w + i) + rsel, so row/8 = 2w + i/4 and
+// row%8 = 2*(i%4) + rsel; the two 16-byte f16 chunks of piece q land in
+// chunks 2*qlo and 2*qlo+1 of their 64-column block, XOR-swizzled by row%8.
+__device__ __forceinline__ void convert_op(const OpRegs &r, uint32_t tile, int tid)
+{
+    const int w = tid >> 5, lane = tid & 31;
     const int qlo = lane & 3, rsel = (lane >> 2) & 1, qhi = lane >> 3;
-    const int q = qhi * 4 + qlo;
-    // row = 2*(4w + it) + rsel: row/8 = w and row%8 = 2*it + rsel
-    const uint32_t src0 = stage + (rsel ? kOddRows : 0u) + (uint32_t)(w * 4) * 256u + q * 16u;
-    const uint32_t dst0 = tile + (uint32_t)qhi * (kTile * 128) + (uint32_t)w * 1024u + (uint32_t)rsel * 128u;
-    uint4 raw[4];
+    const uint32_t dst0 = tile + (uint32_t)qhi * (kTile * 128) + (uint32_t)(2 * w) * 1024u + (uint32_t)rsel * 128u;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) raw[it] = lds128(src0 + it * 256u);
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const uint32_t r8 = 2u * it + rsel;
-        const uint32_t dst = dst0 + 2u * it * 128u;
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t r8 = 2u * (i & 3) + rsel;
+        const uint32_t dst = dst0 + (uint32_t)(i >> 2) * 1024u + 2u * (i & 3) * 128u;
         uint4 a, b;
-        i8x4_to_f16x4(raw[it].x, a.x, a.y);
-        i8x4_to_f16x4(raw[it].y, a.z, a.w);
-        i8x4_to_f16x4(raw[it].z, b.x, b.y);
-        i8x4_to_f16x4(raw[it].w, b.z, b.w);
+        i8x4_to_f16x4(r.raw[i].x, a.x, a.y);
+        i8x4_to_f16x4(r.raw[i].y, a.z, a.w);
+        i8x4_to_f16x4(r.raw[i].z, b.x, b.y);
+        i8x4_to_f16x4(r.raw[i].w, b.z, b.w);
         sts128(dst + (((2u * qlo) ^ r8) << 4), a);
         sts128(dst + (((2u * qlo + 1u) ^ r8) << 4), b);
     }
+}
+
+__device__ __forceinline__ void cta_sync()
+{
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 }
 
 // Queries of (sequence b, KV head g) as the f16 B operand (rows >= R zero).
@@ -434,31 +423,21 @@ __device__ __forceinline__ void load_queries(const Params &p, uint32_t sq, int b
     }
 }
 
-__device__ __forceinline__ void cta_sync()
-{
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-}
-
 // ---------------------------------------------------------------- kernel
 
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params p, int n_stages)
+__global__ void __launch_bounds__(kThreads, 2) qsa_chunk_tc_kernel(const Params p)
 {
-    constexpr int NQ = N / 4;                   // rows per warp in the softmax
-    constexpr int NQP = NQ <= 4 ? 4 : (NQ <= 8 ? 8 : 16);
-    constexpr int NO = N / 2;                   // rows per thread in the fold
+    constexpr int NH = N / 2; // rows per warp half (a multiple of 8)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
     uint8_t *smem = smem_raw + pad;
-    const Layout L = make_layout(N, n_stages);
+    const Layout L = make_layout(N);
     Misc &ms = *reinterpret_cast<Misc *>(smem + L.off_misc);
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
-    const int qd = w & 3;                       // TMEM lane quadrant of this warp
-    const int rq = w >> 2;                      // softmax row quarter
-    const int oh = (w >> 2) & 1, oc = w >> 3;   // fold: d half, row half
+    const int qd = w & 3;  // TMEM lane quadrant of this warp
+    const int ch = w >> 2; // row half (softmax) and d half (fold)
     const uint32_t s_kv = smem_u32(smem + L.off_kv);
     const uint32_t s_q = smem_u32(smem + L.off_q);
     const uint32_t s_p = smem_u32(smem + L.off_p);
@@ -466,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     const uint32_t o_base = kMaxTiles * N;
     const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
     const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
-    const uint32_t ahead = (uint32_t)n_stages - 1; // ops whose copies are in flight
+    const int cell = 32 * qd + lane; // softmax: this thread's cell within a tile
 
     if (tid == 0) {
         mbar_init(&ms.mma, 1);
@@ -493,48 +472,34 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         tc_fence_after();
     };
 
-    // ---- resolve the first two groups; later groups are resolved two ahead
-    OpIter rg; // the group being resolved
+    // ---- resolve the first two groups (one per half of the threads)
+    OpIter rg; // the group being resolved (two ahead of the one computed)
     op_init(p, rg, first);
     {
-        OpIter g1 = rg; // threads 0..255 resolve group 0, threads 256..511 group 1
+        OpIter g1 = rg;
         if (g1.valid) op_next_group(p, g1);
-        const OpIter &mine = tid < kGroupCells ? rg : g1;
-        const int pos = resolve_list(p, mine, tid & (kGroupCells - 1));
-        const int slot = resolve_check(p, resolve_page(p, mine, pos));
-        if (mine.valid) ms.ring[mine.gi % kSlotRing][tid & (kGroupCells - 1)] = slot;
+        const OpIter &mine = tid < kTile ? rg : g1;
+        for (int i = tid & (kTile - 1); i < kGroupCells; i += kTile) {
+            const int pos = resolve_list(p, mine, i);
+            const int slot = resolve_check(p, resolve_page(p, mine, pos));
+            if (mine.valid) ms.ring[mine.gi % kSlotRing][i] = slot;
+        }
         rg = g1;
         if (rg.valid) op_next_group(p, rg);
     }
     __syncthreads();
 
-    OpIter is, cs; // issue side (`ahead` ops in front) and compute side
+    OpIter is, cs; // loads run one op ahead of the compute side
     op_init(p, is, first);
     op_init(p, cs, first);
-    for (uint32_t k = 0; k < ahead; ++k) {
-        if (is.valid) {
-            issue_op(p, smem, ms, is, L.off_raw + (k % n_stages) * kStageBytes, tid);
-            op_next(p, is);
-        }
-        cp_async_commit();
-    }
+    OpRegs rr; // the rows of the next op to convert
+    if (is.valid) { load_op(p, ms, is, tid, rr); op_next(p, is); }
+    if (is.valid) prefetch_op(p, ms, is, tid);
 
     int cur_bg = -1;
     int r_pos = INT_MIN, r_raw = -1; // this thread's cell of the group being resolved
+    float sigma = 1.f, inv_sigma = 1.f;
     for (uint32_t op = 0; cs.valid; ++op) {
-        if (is.valid) {
-            issue_op(p, smem, ms, is, L.off_raw + ((op + ahead) % n_stages) * kStageBytes, tid);
-            op_next(p, is);
-        }
-        cp_async_commit();
-        if (ahead == 2)
-            asm volatile("cp.async.wait_group 2;" ::: "memory");
-        else
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        cta_sync(); // this op's rows and scales have landed, for every thread
-
-        const uint32_t st_off = L.off_raw + (op % n_stages) * kStageBytes;
-        const uint32_t st = smem_u32(smem) + st_off;
         const int t = cs.t;
         const bool last_tile = t == cs.tiles - 1;
         if (cs.kind == 0) {
@@ -553,12 +518,16 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     }
                 }
             }
-            convert_tile(st, s_kv, w, lane);
+            convert_op(rr, s_kv, tid);
             if (tid < kTile) {
-                const int slot = *reinterpret_cast<const int *>(smem + st_off + kStageSlots + tid * 4);
-                ms.cell_slot[t][tid] = slot;
-                ms.cell_ks[t][tid] = *reinterpret_cast<const float *>(smem + st_off + kStageKs + tid * 4) * p.scale_log2;
-                ms.cell_vs[t][tid] = *reinterpret_cast<const float *>(smem + st_off + kStageVs + tid * 4);
+                ms.cell_slot[t][tid] = ms.ring[cs.gi % kSlotRing][t * kTile + tid];
+                ms.cell_ks[t][tid] = rr.ks * p.scale_log2;
+                ms.cell_vs[t][tid] = rr.vs;
+            }
+            if (is.valid) {
+                load_op(p, ms, is, tid, rr);
+                op_next(p, is);
+                if (is.valid) prefetch_op(p, ms, is, tid);
             }
             fence_proxy_async_smem();
             cta_sync();
@@ -573,27 +542,30 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
             wait_mma();
             if (last_tile) {
-                // ---- softmax over the group: warp (qd, rq) owns cells
-                // 32qd..32qd+31 of each tile and rows rq*NQ..rq*NQ+NQ-1
-                const int cell = 32 * qd + lane;
-                float mx[NQ];
-#pragma unroll
-                for (int j = 0; j < NQ; ++j) mx[j] = -INFINITY;
+                // ---- max pass over the group, eight rows at a time: warp
+                // (qd, ch) owns cells 32qd..32qd+31 and rows ch*NH..ch*NH+NH-1
                 float vsabs = 0.f;
-                for (int tt = 0; tt < cs.tiles; ++tt) {
-                    float sv[NQ];
-                    tmem_ld_cols<NQ>(tmem + t_lane + tt * N + rq * NQ, sv);
-                    tmem_wait_ld();
-                    const bool ok = ms.cell_slot[tt][cell] >= 0;
-                    const float ksc = ms.cell_ks[tt][cell];
-                    if (ok) vsabs = fmaxf(vsabs, fabsf(ms.cell_vs[tt][cell]));
+                for (int tt = 0; tt < cs.tiles; ++tt)
+                    if (ms.cell_slot[tt][cell] >= 0) vsabs = fmaxf(vsabs, fabsf(ms.cell_vs[tt][cell]));
 #pragma unroll
-                    for (int j = 0; j < NQ; ++j) mx[j] = fmaxf(mx[j], ok ? __fmul_rn(sv[j], ksc) : -INFINITY);
-                }
+                for (int j0 = 0; j0 < NH; j0 += 8) {
+                    float mx[8];
 #pragma unroll
-                for (int j = 0; j < NQ; ++j) {
-                    const int key = __reduce_max_sync(0xffffffffu, ordered_key(mx[j]));
-                    if (lane == j) ms.red_max[rq][qd][j] = from_ordered_key(key);
+                    for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
+                    for (int tt = 0; tt < cs.tiles; ++tt) {
+                        float sv[8];
+                        tmem_ld8(tmem + t_lane + tt * N + ch * NH + j0, sv);
+                        tmem_wait_ld();
+                        const bool ok = ms.cell_slot[tt][cell] >= 0;
+                        const float ksc = ms.cell_ks[tt][cell];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], ok ? __fmul_rn(sv[j], ksc) : -INFINITY);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int key = __reduce_max_sync(0xffffffffu, ordered_key(mx[j]));
+                        if (lane == j) ms.red_max[ch][j0 + j][qd] = from_ordered_key(key);
+                    }
                 }
                 {
                     const unsigned u = __reduce_max_sync(0xffffffffu, __float_as_uint(vsabs));
@@ -602,68 +574,86 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 // the group two ahead: its page-table reads go out now
                 if (tid < kGroupCells) r_raw = resolve_page(p, rg, r_pos);
                 cta_sync();
-                float m2[NQ];
-#pragma unroll
-                for (int j = 0; j < NQ; ++j)
-                    m2[j] = fmaxf(fmaxf(ms.red_max[rq][0][j], ms.red_max[rq][1][j]),
-                                  fmaxf(ms.red_max[rq][2][j], ms.red_max[rq][3][j]));
-                float sigma = fmaxf(fmaxf(ms.red_vs[0], ms.red_vs[1]), fmaxf(ms.red_vs[2], ms.red_vs[3]));
+                sigma = fmaxf(fmaxf(ms.red_vs[0], ms.red_vs[1]), fmaxf(ms.red_vs[2], ms.red_vs[3]));
                 if (!(sigma > 0.f)) sigma = 1.f;
-                const float inv_sigma = 1.f / sigma;
-                float ls[NQP];
+                inv_sigma = 1.f / sigma;
+            }
+        } else {
+            // ---- P of one tile, then P.V
+            {
+                const bool ok = ms.cell_slot[t][cell] >= 0;
+                const float ksc = ms.cell_ks[t][cell];
+                const float vsn = ok ? ms.cell_vs[t][cell] * inv_sigma : 0.f;
 #pragma unroll
-                for (int j = 0; j < NQP; ++j) ls[j] = 0.f;
-                for (int tt = 0; tt < cs.tiles; ++tt) {
-                    float sv[NQ];
-                    tmem_ld_cols<NQ>(tmem + t_lane + tt * N + rq * NQ, sv);
+                for (int j0 = 0; j0 < NH; j0 += 8) {
+                    float sv[8], ls[8];
+                    tmem_ld8(tmem + t_lane + t * N + ch * NH + j0, sv);
                     tmem_wait_ld();
-                    const bool ok = ms.cell_slot[tt][cell] >= 0;
-                    const float ksc = ms.cell_ks[tt][cell];
-                    const float vsn = ok ? ms.cell_vs[tt][cell] * inv_sigma : 0.f;
-                    const uint32_t ptile = s_p + tt * (N * kTile * 2);
 #pragma unroll
-                    for (int j = 0; j < NQ; ++j) {
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 q4 = *reinterpret_cast<const float4 *>(ms.red_max[ch][j0 + j]);
+                        const float m2 = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
                         // the same rounded product as in the max pass (no FMA
                         // contraction), so the max cell gets exactly 2^0 = 1
-                        const float pr = ok ? fast_exp2(__fmul_rn(sv[j], ksc) - m2[j]) : 0.f;
-                        ls[j] += pr;
+                        const float pr = ok ? fast_exp2(__fmul_rn(sv[j], ksc) - m2) : 0.f;
+                        ls[j] = pr;
                         const __half h = __float2half_rn(pr * vsn);
-                        sts16(ptile + kmajor_sw128_off(rq * NQ + j, cell, N),
+                        sts16(s_p + kmajor_sw128_off(ch * NH + j0 + j, cell, N),
                               *reinterpret_cast<const uint16_t *>(&h));
                     }
-                }
-                // reduce-scatter of the NQ row sums over the warp's 32 cells
+                    // reduce-scatter of the eight row sums over the warp's 32 cells:
+                    // lane pairs (4c, 4c+1, 4c+2, 4c+3) end with row j0 + c
 #pragma unroll
-                for (int o = 16, cnt = NQP; o >= 1; o >>= 1) {
-                    if (cnt > 1) {
-                        const int half = cnt / 2;
-                        const bool up = (lane & o) != 0;
+                    for (int o = 16, cnt = 8; o >= 1; o >>= 1) {
+                        if (cnt > 1) {
+                            const int half = cnt / 2;
+                            const bool up = (lane & o) != 0;
 #pragma unroll
-                        for (int i = 0; i < half; ++i) {
-                            const float send = up ? ls[i] : ls[i + half];
-                            const float keep = up ? ls[i + half] : ls[i];
-                            ls[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                            for (int i = 0; i < half; ++i) {
+                                const float send = up ? ls[i] : ls[i + half];
+                                const float keep = up ? ls[i + half] : ls[i];
+                                ls[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                            }
+                            cnt = half;
+                        } else {
+                            ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], o);
                         }
-                        cnt = half;
-                    } else {
-                        ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], o);
+                    }
+                    if ((lane & 3) == 0) {
+                        float &acc = ms.red_sum[ch][j0 + (lane >> 2)][qd];
+                        acc = t == 0 ? ls[0] : acc + ls[0];
                     }
                 }
-                {
-                    constexpr int lanes_per_col = 32 / NQP;
-                    const int col = lane / lanes_per_col;
-                    if (lane % lanes_per_col == 0 && col < NQ) ms.red_sum[rq][qd][col] = ls[0];
+            }
+            convert_op(rr, s_kv, tid);
+            if (is.valid) {
+                load_op(p, ms, is, tid, rr);
+                op_next(p, is);
+                if (is.valid) prefetch_op(p, ms, is, tid);
+            }
+            fence_proxy_async_smem();
+            cta_sync();
+            if (tid == 0) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t ad = smem_desc(s_kv + (2 * h) * (kTile * 128) + kk * 2048, kTile * 128, 1024);
+                        const uint64_t bd = smem_desc(s_p + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+                        mma_f16_ss(tmem + o_base + h * N, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                if (tid == 0) ms.sigma = sigma;
-                fence_proxy_async_smem();
-                cta_sync();
+                mma_commit(&ms.mma);
+            }
+            wait_mma();
+            if (last_tile) {
                 // per-row group values and their combination with earlier groups
                 if (tid < N) {
-                    const int r = tid, hr = r / NQ, jr = r % NQ;
-                    const float mg = fmaxf(fmaxf(ms.red_max[hr][0][jr], ms.red_max[hr][1][jr]),
-                                           fmaxf(ms.red_max[hr][2][jr], ms.red_max[hr][3][jr]));
-                    const float lg = ((ms.red_sum[hr][0][jr] + ms.red_sum[hr][1][jr]) + ms.red_sum[hr][2][jr]) +
-                                     ms.red_sum[hr][3][jr];
+                    const int r = tid, hr = r / NH, jr = r % NH;
+                    const float4 m4 = *reinterpret_cast<const float4 *>(ms.red_max[hr][jr]);
+                    const float4 l4 = *reinterpret_cast<const float4 *>(ms.red_sum[hr][jr]);
+                    const float mg = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+                    const float lg = ((l4.x + l4.y) + l4.z) + l4.w;
                     const float mr = ms.row_mrun[r];
                     const float mn = fmaxf(mr, mg);
                     float fa = 0.f, fb = 0.f;
@@ -676,50 +666,32 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     ms.row_mrun[r] = mn;
                     ms.row_lrun[r] = ms.row_lrun[r] * fa + lg * fb;
                 }
-            }
-        } else {
-            // ---- P.V of one V tile
-            convert_tile(st, s_kv, w, lane);
-            fence_proxy_async_smem();
-            cta_sync();
-            if (tid == 0) {
-                const uint32_t ptile = s_p + t * (N * kTile * 2);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t ad = smem_desc(s_kv + (2 * h) * (kTile * 128) + kk * 2048, kTile * 128, 1024);
-                        const uint64_t bd = smem_desc(ptile + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-                        mma_f16_ss(tmem + o_base + h * N, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                mma_commit(&ms.mma);
-            }
-            wait_mma();
-            if (last_tile) {
                 // the group two ahead: checked slots into the ring
                 if (tid < kGroupCells && rg.valid) ms.ring[rg.gi % kSlotRing][tid] = resolve_check(p, r_raw);
                 if (rg.valid) op_next_group(p, rg);
                 r_pos = INT_MIN;
                 r_raw = -1;
+                cta_sync();
                 // ---- fold the group's O into the chunk partial.  The first
                 // group writes it; a later group (chunks longer than 256
                 // cells) rescales the partial this thread wrote and adds.
                 {
-                    const int d = oh * 128 + 32 * qd + lane;
+                    const int d = ch * 128 + 32 * qd + lane;
                     const size_t base = (((size_t)cs.cur.b * p.G + cs.cur.g) * p.n_chunks + cs.cur.c) * p.R;
-                    const float sg = ms.sigma;
-                    float ov[NO];
-                    tmem_ld_cols<NO>(tmem + t_lane + o_base + oh * N + oc * NO, ov);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < NO; ++i) {
-                        const int r = oc * NO + i;
-                        if (r >= p.R) continue;
-                        float *dst = p.part_o + (base + r) * kHeadDim + d;
-                        float v = ov[i] * sg * ms.row_fb[r];
-                        if (cs.gs > 0) v = fmaf(*dst, ms.row_fa[r], v);
-                        *dst = v;
+                    for (int j0 = 0; j0 < N; j0 += 16) {
+                        float ov[16];
+                        tmem_ld16(tmem + t_lane + o_base + ch * N + j0, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int r = j0 + i;
+                            if (r >= p.R) continue;
+                            float *dst = p.part_o + (base + r) * kHeadDim + d;
+                            float v = ov[i] * sigma * ms.row_fb[r];
+                            if (cs.gs > 0) v = fmaf(*dst, ms.row_fa[r], v);
+                            *dst = v;
+                        }
                     }
                 }
                 if (cs.gs + kGroupCells >= cs.nc && tid < p.R) {
@@ -733,7 +705,6 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         }
         op_next(p, cs);
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
     cta_sync();
     if (w == 0) tmem_dealloc(tmem, kTmemCols);
 }
@@ -741,25 +712,25 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 template <int N>
 cudaError_t launch_n(const Params &p, cudaStream_t stream)
 {
-    int dev = 0, sms = 0, max_smem = 0;
+    int dev = 0, sms = 0, max_smem = 0, sm_smem = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    int n_stages = 3;
-    uint32_t bytes = make_layout(N, n_stages).total + 1024;
-    if ((int)bytes > max_smem) {
-        n_stages = 2;
-        bytes = make_layout(N, n_stages).total + 1024;
-    }
+    if ((e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+        return e;
+    const uint32_t bytes = make_layout(N).total + 1024;
     if ((int)bytes > max_smem) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)bytes)) != cudaSuccess)
         return e;
+    // two CTAs per SM when their shared memory fits (1 KB per CTA is reserved)
+    const int per_sm = 2 * ((int)bytes + 1024) <= sm_smem ? 2 : 1;
     const long long items = (long long)p.n_seq * p.G * p.n_chunks;
-    const int grid = (int)(items < (long long)sms ? items : (long long)sms);
-    qsa_chunk_tc_kernel<N><<<grid, kThreads, bytes, stream>>>(p, n_stages);
+    const long long slots = (long long)sms * per_sm;
+    const int grid = (int)(items < slots ? items : slots);
+    qsa_chunk_tc_kernel<N><<<grid, kThreads, bytes, stream>>>(p);
     return cudaGetLastError();
 }
 
