@@ -31,6 +31,21 @@ qsa_status check_shape(const qsa_shape *s)
     return QSA_OK;
 }
 
+enum Path { kPathSimt = 0, kPathDecodeTc = 1, kPathPromptTc = 2, kPathNone = -1 };
+
+// Kernel family by shape: the cells-on-M tensor-core kernel for decode
+// windows (at most 64 query rows per KV head), the rows-on-M tensor-core
+// kernel for prompt-shaped calls (chunks of at least one 128-cell tile), the
+// CUDA-core kernel otherwise or when asked for.
+Path select_path(const qsa_shape *s)
+{
+    const long long R = (long long)s->q_per_kv * s->n_queries;
+    if (s->algo == QSA_ALGO_SIMT) return kPathSimt;
+    if (R <= 64) return kPathDecodeTc;
+    if (s->chunk_cells >= 128) return kPathPromptTc;
+    return s->algo == QSA_ALGO_TCGEN05 ? kPathNone : kPathSimt;
+}
+
 Workspace carve(const qsa_shape *s, int n_seq, int max_selected)
 {
     Workspace w{};
@@ -40,9 +55,36 @@ Workspace carve(const qsa_shape *s, int n_seq, int max_selected)
     w.off_m = 0;
     w.off_l = align_up(w.off_m + rows * sizeof(float), kWorkspaceAlign);
     w.off_o = align_up(w.off_l + rows * sizeof(float), kWorkspaceAlign);
-    w.off_extra = align_up(w.off_o + rows * kHeadDim * sizeof(float), kWorkspaceAlign);
+    w.off_extra = align_up(w.off_o + rows * kHeadDim * sizeof(float), 1024);
     w.total = w.off_extra;
+    if (select_path(s) == kPathPromptTc && n_chunks > 0) {
+        size_t kb, qb, cb;
+        prompt_image_bytes(n_seq, s->n_kv_heads, (int)R, s->chunk_cells, (int)n_chunks, &kb, &qb, &cb);
+        w.total = w.off_extra + 2 * align_up(kb, 1024) + align_up(qb, 1024) + 2 * align_up(cb, 1024);
+    }
     return w;
+}
+
+PromptImages prompt_images(const qsa_shape *s, int n_seq, int max_selected, char *ws, const Workspace &w)
+{
+    PromptImages im{};
+    const int R = s->q_per_kv * s->n_queries;
+    const int n_chunks = max_selected > 0 ? (max_selected + s->chunk_cells - 1) / s->chunk_cells : 0;
+    size_t kb, qb, cb;
+    prompt_image_bytes(n_seq, s->n_kv_heads, R, s->chunk_cells, n_chunks, &kb, &qb, &cb);
+    size_t off = w.off_extra;
+    im.k = ws + off;
+    off += align_up(kb, 1024);
+    im.v = ws + off;
+    off += align_up(kb, 1024);
+    im.q = ws + off;
+    off += align_up(qb, 1024);
+    im.ksc = reinterpret_cast<float *>(ws + off);
+    off += align_up(cb, 1024);
+    im.bias = reinterpret_cast<float *>(ws + off);
+    im.tiles_per_chunk = (s->chunk_cells + 127) / 128;
+    im.row_tiles = (R + 127) / 128;
+    return im;
 }
 
 qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_pool,
@@ -99,10 +141,15 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.scale_log2 = s->softmax_scale * kLog2e;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const bool tc_ok = chunk_tc_supports(p);
-    if (s->algo == QSA_ALGO_TCGEN05 && !tc_ok) return QSA_ERR_UNSUPPORTED;
-    const bool use_tc = s->algo != QSA_ALGO_SIMT && tc_ok;
-    cudaError_t e = use_tc ? launch_chunk_tc(p, cs) : launch_chunk_simt(p, cs);
+    const Path path = select_path(s);
+    if (path == kPathNone) return QSA_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (path == kPathDecodeTc)
+        e = launch_chunk_tc(p, cs);
+    else if (path == kPathPromptTc)
+        e = launch_prompt_tc(p, prompt_images(s, n_seq, max_selected, ws, w), cs);
+    else
+        e = launch_chunk_simt(p, cs);
     if (e != cudaSuccess) return QSA_ERR_CUDA;
     e = launch_merge(p, cs);
     if (e != cudaSuccess) return QSA_ERR_CUDA;

@@ -42,6 +42,17 @@ struct Params {
     float scale_log2;          // softmax_scale * log2(e)
 };
 
+// Tensor-core-ready operand images of the prompt-shaped path (workspace).
+struct PromptImages {
+    void *k;     // [n_seq][G][n_chunks][tiles_per_chunk] 64 KB tiles: K codes (bf16|f16)
+    void *v;     // same tiles: f16(V code * v_scale)
+    void *q;     // [n_seq][G][row_tiles] 64 KB tiles: queries (bf16|f16)
+    float *ksc;  // [..][tiles_per_chunk][128]: k_scale * softmax_scale * log2(e), 0 if masked
+    float *bias; // same: 0, or -inf for a masked cell
+    int tiles_per_chunk;
+    int row_tiles;
+};
+
 // Workspace carve-up shared by the host code of every path.
 struct Workspace {
     size_t off_m, off_l, off_o, off_extra, total;
@@ -122,6 +133,10 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
 cudaError_t launch_chunk_simt(const Params &p, cudaStream_t stream);
 bool chunk_tc_supports(const Params &p);
 cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream);
+bool prompt_tc_supports(const Params &p);
+size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks, size_t *k_bytes,
+                          size_t *q_bytes, size_t *cell_bytes);
+cudaError_t launch_prompt_tc(const Params &p, const PromptImages &im, cudaStream_t stream);
 cudaError_t launch_merge(const Params &p, cudaStream_t stream);
 
 } // namespace qsa

@@ -1,0 +1,416 @@
+// qsa_prompt_tc.cu -- tensor-core path for prompt-shaped calls (step a6).
+//
+// The pages run a prompt chunk through the decode kernel ("Strata PR #2220,
+// attn_chunk_q8_v3_kernel", prompt-shaped parity: 2,048 queries against 32K
+// INT8 cells).  With thousands of query rows per KV head the two
+// contractions are dense, so this path puts the query rows on the MMA's M
+// dimension and streams the selected cells through it, flash-attention
+// style:
+//
+//   staging   one pass resolves every listed cell through the page table
+//             (a1) and writes tensor-core-ready images to the workspace:
+//             K codes as 16-bit floats (exact), V as f16(code x v_scale),
+//             per-cell k_scale*softmax_scale*log2(e) and a 0/-inf mask
+//             bias, and the queries, each 128-row or 128-cell tile a
+//             contiguous 64 KB block in the 128-byte-swizzled layout;
+//   main      one CTA per (128-row query tile, chunk) loads image tiles with
+//             bulk async copies and runs, per 128-cell tile,
+//               S = Q . K_code^T        (M=128 rows, N=128 cells, K=256)
+//               P = 2^(S*ksc + bias - m_ref)      (online softmax)
+//               O += P . V_hat          (M=128 rows, N=256 d, K=128 cells)
+//             with S and O in tensor memory.  O is rescaled only when a
+//             row's max grows by more than 2^8 over its reference, so P
+//             stays below 256 and f16 holds it; the partial is brought to
+//             the true running max at the end.
+// The partials have the decode path's layout and go to the same merge.
+//
+// Queries keep their own 16-bit type (bf16 queries with bf16 K codes; f32
+// queries are rounded to f16 and use f16 K codes), since one tcgen05.mma
+// takes A and B of the same type.  V_hat = f16(code * v_scale) needs
+// |v_scale| * 127 < 65504.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qsa_internal.cuh"
+#include "qsa_sm100.cuh"
+
+namespace qsa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTile = 128;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2; // 64 KB image tile
+constexpr uint32_t kPBytes = kTile * kTile * 2;       // 32 KB P tile
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    if (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ---------------------------------------------------------------- staging
+
+// One CTA per 128-cell image tile of (chunk c, tile j) of one (sequence, KV
+// head).  Cells past the chunk or the list are masked (zero rows, bias -inf).
+template <bool QBF16>
+__global__ void __launch_bounds__(256) qsa_prompt_stage_kv(const Params p, const PromptImages im)
+{
+    __shared__ int s_slot[kTile];
+    __shared__ float s_vs[kTile];
+    const int tile = blockIdx.x;
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int c = tile / im.tiles_per_chunk, j = tile % im.tiles_per_chunk;
+    int start, n;
+    seq_range(p, b, &start, &n);
+    const size_t kv_base = ((size_t)b * p.G + g) * p.pool_cells;
+    const size_t tile_id = (((size_t)b * p.G + g) * p.n_chunks + c) * im.tiles_per_chunk + j;
+    const long long c0 = (long long)c * p.chunk_cells;
+    const long long lo = c0 + (long long)j * kTile;
+    const long long hi = min(min(c0 + p.chunk_cells, (long long)n), lo + kTile);
+    const int tid = threadIdx.x;
+    if (tid < kTile) {
+        int slot = -1;
+        if (lo + tid < hi) slot = resolve_slot(p, b, __ldg(p.sel + start + lo + tid));
+        s_slot[tid] = slot;
+        s_vs[tid] = slot >= 0 ? __ldg(p.v_scale + kv_base + slot) : 0.f;
+        im.ksc[tile_id * kTile + tid] = slot >= 0 ? __ldg(p.k_scale + kv_base + slot) * p.scale_log2 : 0.f;
+        im.bias[tile_id * kTile + tid] = slot >= 0 ? 0.f : -INFINITY;
+    }
+    __syncthreads();
+    uint8_t *kimg = static_cast<uint8_t *>(im.k) + tile_id * kTileBytes;
+    uint8_t *vimg = static_cast<uint8_t *>(im.v) + tile_id * kTileBytes;
+    for (int e = tid; e < kTile * 16; e += blockDim.x) {
+        const int cell = e >> 4, piece = e & 15; // 16 codes = d 16*piece .. +15
+        const int slot = s_slot[cell];
+        uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
+        if (slot >= 0) {
+            kr = ldg_nc_v4(p.k_pool + (kv_base + slot) * kHeadDim + piece * 16);
+            vr = ldg_nc_v4(p.v_pool + (kv_base + slot) * kHeadDim + piece * 16);
+        }
+        const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, vw[4] = {vr.x, vr.y, vr.z, vr.w};
+        const float vsc = s_vs[cell];
+        uint32_t ko[8], vo[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float k0 = (float)(int8_t)(kw[q] & 0xff), k1 = (float)(int8_t)((kw[q] >> 8) & 0xff);
+            const float k2 = (float)(int8_t)((kw[q] >> 16) & 0xff), k3 = (float)(int8_t)(kw[q] >> 24);
+            ko[2 * q] = pack2<QBF16>(k0, k1);
+            ko[2 * q + 1] = pack2<QBF16>(k2, k3);
+            const float v0 = (float)(int8_t)(vw[q] & 0xff) * vsc, v1 = (float)(int8_t)((vw[q] >> 8) & 0xff) * vsc;
+            const float v2 = (float)(int8_t)((vw[q] >> 16) & 0xff) * vsc, v3 = (float)(int8_t)(vw[q] >> 24) * vsc;
+            vo[2 * q] = pack2<false>(v0, v1);
+            vo[2 * q + 1] = pack2<false>(v2, v3);
+        }
+        const uint32_t off0 = kmajor_sw128_off(cell, piece * 16, kTile);
+        const uint32_t off1 = kmajor_sw128_off(cell, piece * 16 + 8, kTile);
+        *reinterpret_cast<uint4 *>(kimg + off0) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+        *reinterpret_cast<uint4 *>(kimg + off1) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+        *reinterpret_cast<uint4 *>(vimg + off0) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+        *reinterpret_cast<uint4 *>(vimg + off1) = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+    }
+}
+
+// One CTA per 128-row query tile of one (sequence, KV head); row r = t*H + j.
+template <bool QBF16>
+__global__ void __launch_bounds__(256) qsa_prompt_stage_q(const Params p, const PromptImages im)
+{
+    const int mt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    uint8_t *qimg = static_cast<uint8_t *>(im.q) + (((size_t)b * p.G + g) * im.row_tiles + mt) * kTileBytes;
+    const int GH = p.G * p.H;
+    for (int e = threadIdx.x; e < kTile * 32; e += blockDim.x) {
+        const int row = e >> 5, piece = e & 31; // 8 values = d 8*piece .. +7
+        const int r = mt * kTile + row;
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (r < p.R) {
+            const int t = r / p.H, j = r % p.H;
+            const size_t off = (((size_t)b * p.T + t) * GH + (size_t)g * p.H + j) * kHeadDim + piece * 8;
+            if (p.q_bf16) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) + off);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    f[2 * q] = bf16_bits_to_f32(w[q] & 0xffff);
+                    f[2 * q + 1] = bf16_bits_to_f32(w[q] >> 16);
+                }
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.q) + off);
+                const float4 x = src[0], y = src[1];
+                f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+                f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+            }
+        }
+        const uint4 v = make_uint4(pack2<QBF16>(f[0], f[1]), pack2<QBF16>(f[2], f[3]),
+                                   pack2<QBF16>(f[4], f[5]), pack2<QBF16>(f[6], f[7]));
+        *reinterpret_cast<uint4 *>(qimg + kmajor_sw128_off(row, piece * 8, kTile)) = v;
+    }
+}
+
+// ---------------------------------------------------------------- main
+
+struct PromptSmem {
+    float ksc[kTile];
+    float bias[kTile];
+    uint64_t bar_q, bar_k, bar_v, bar_mma;
+    uint32_t tmem;
+    int32_t abort;
+};
+
+__device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64_t *bar, uint32_t parity)
+{
+    if (ms.abort) return false;
+    if (!mbar_wait(bar, parity)) {
+        atomicExch(&ms.abort, 1);
+        raise_status(p, QSA_STATUS_TIMEOUT);
+        return false;
+    }
+    return true;
+}
+
+// 128 threads: thread i owns query row i of the tile (TMEM lane i).
+template <bool QBF16>
+__global__ void __launch_bounds__(kTile, 1) qsa_prompt_tc_kernel(const Params p, const PromptImages im)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t s_q = smem_u32(smem), s_k = s_q + kTileBytes, s_v = s_k + kTileBytes;
+    const uint32_t s_p = s_v + kTileBytes;
+    PromptSmem &ms = *reinterpret_cast<PromptSmem *>(smem + 3 * kTileBytes + kPBytes);
+    const int tid = threadIdx.x, w = tid >> 5;
+    const int mt = blockIdx.x / p.n_chunks, c = blockIdx.x % p.n_chunks;
+    const int g = blockIdx.y, b = blockIdx.z;
+    int start, n;
+    seq_range(p, b, &start, &n);
+    cudaTriggerProgrammaticLaunchCompletion();
+    if ((long long)c * p.chunk_cells >= n) return; // no such chunk: the merge skips it
+    const int cells = (int)min((long long)p.chunk_cells, (long long)n - (long long)c * p.chunk_cells);
+    const int n_tiles = (cells + kTile - 1) / kTile;
+    const size_t tile0 = (((size_t)b * p.G + g) * p.n_chunks + c) * im.tiles_per_chunk;
+    const uint8_t *kimg = static_cast<const uint8_t *>(im.k) + tile0 * kTileBytes;
+    const uint8_t *vimg = static_cast<const uint8_t *>(im.v) + tile0 * kTileBytes;
+    const uint8_t *qimg = static_cast<const uint8_t *>(im.q) + (((size_t)b * p.G + g) * im.row_tiles + mt) * kTileBytes;
+    const float *kscg = im.ksc + tile0 * kTile, *biasg = im.bias + tile0 * kTile;
+    const uint32_t idesc_s = idesc_f16(kTile, kTile, QBF16, QBF16, false, false);
+    const uint32_t idesc_o = idesc_f16(kTile, kHeadDim, false, false, false, true);
+
+    if (tid == 0) {
+        mbar_init(&ms.bar_q, 1);
+        mbar_init(&ms.bar_k, 1);
+        mbar_init(&ms.bar_v, 1);
+        mbar_init(&ms.bar_mma, 1);
+        ms.abort = 0;
+        fence_mbar_init();
+    }
+    if (w == 0) {
+        tmem_alloc(&ms.tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem, t_s = tmem, t_o = tmem + kTile;
+    const uint32_t t_lane = (uint32_t)(32 * w) << 16;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&ms.bar_q, kTileBytes);
+        bulk_g2s(smem, qimg, kTileBytes, &ms.bar_q);
+        mbar_arrive_expect_tx(&ms.bar_k, kTileBytes + 2 * kTile * 4);
+        bulk_g2s(smem + kTileBytes, kimg, kTileBytes, &ms.bar_k);
+        bulk_g2s(ms.ksc, kscg, kTile * 4, &ms.bar_k);
+        bulk_g2s(ms.bias, biasg, kTile * 4, &ms.bar_k);
+        mbar_arrive_expect_tx(&ms.bar_v, kTileBytes);
+        bulk_g2s(smem + 2 * kTileBytes, vimg, kTileBytes, &ms.bar_v);
+    }
+    wait_bar(p, ms, &ms.bar_q, 0);
+
+    float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
+    uint32_t mma_phase = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+        wait_bar(p, ms, &ms.bar_k, j & 1);
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                const uint64_t ad = smem_desc(s_q + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc(s_k + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                mma_f16_ss(t_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&ms.bar_mma);
+        }
+        wait_bar(p, ms, &ms.bar_mma, mma_phase);
+        mma_phase ^= 1;
+        tc_fence_after();
+        // ---- row max of this tile (scaled, masked), then P
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c16 = 0; c16 < kTile / 16; ++c16) {
+            float sv[16];
+            tmem_ld16(t_s + t_lane + c16 * 16, sv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                mx = fmaxf(mx, fmaf(sv[i], ms.ksc[c16 * 16 + i], ms.bias[c16 * 16 + i]));
+        }
+        // rescale O (and l) when this row's max outgrows its reference by 2^8
+        bool rescale = false;
+        float factor = 1.f;
+        if (mx > -INFINITY) {
+            if (m_ref == -INFINITY) {
+                m_ref = mx;
+            } else if (mx > m_ref + 8.f) {
+                factor = fast_exp2(m_ref - mx);
+                l *= factor;
+                m_ref = mx;
+                rescale = true;
+            }
+            m_run = fmaxf(m_run, mx);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
+                float ov[16];
+                tmem_ld16(t_o + t_lane + c16 * 16, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ov[i] *= factor;
+                tmem_st16(t_o + t_lane + c16 * 16, ov);
+            }
+            tmem_wait_st();
+        }
+#pragma unroll
+        for (int c16 = 0; c16 < kTile / 16; ++c16) {
+            float sv[16];
+            tmem_ld16(t_s + t_lane + c16 * 16, sv);
+            tmem_wait_ld();
+            uint32_t hw[8];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float s0 = fmaf(sv[i], ms.ksc[c16 * 16 + i], ms.bias[c16 * 16 + i]);
+                const float s1 = fmaf(sv[i + 1], ms.ksc[c16 * 16 + i + 1], ms.bias[c16 * 16 + i + 1]);
+                const float p0 = m_ref > -INFINITY ? fast_exp2(s0 - m_ref) : 0.f;
+                const float p1 = m_ref > -INFINITY ? fast_exp2(s1 - m_ref) : 0.f;
+                l += p0 + p1;
+                hw[i / 2] = pack2<false>(p0, p1);
+            }
+            sts128(s_p + kmajor_sw128_off(tid, c16 * 16, kTile), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+            sts128(s_p + kmajor_sw128_off(tid, c16 * 16 + 8, kTile), make_uint4(hw[4], hw[5], hw[6], hw[7]));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads(); // P written, S and the scale vectors read, O rescaled
+        tc_fence_after();
+        if (tid == 0 && j + 1 < n_tiles && !ms.abort) {
+            mbar_arrive_expect_tx(&ms.bar_k, kTileBytes + 2 * kTile * 4);
+            bulk_g2s(smem + kTileBytes, kimg + (size_t)(j + 1) * kTileBytes, kTileBytes, &ms.bar_k);
+            bulk_g2s(ms.ksc, kscg + (size_t)(j + 1) * kTile, kTile * 4, &ms.bar_k);
+            bulk_g2s(ms.bias, biasg + (size_t)(j + 1) * kTile, kTile * 4, &ms.bar_k);
+        }
+        wait_bar(p, ms, &ms.bar_v, j & 1);
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint64_t ad = smem_desc(s_p + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc(s_v + kk * 2048, kTile * 128, 1024);
+                mma_f16_ss(t_o, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&ms.bar_mma);
+        }
+        wait_bar(p, ms, &ms.bar_mma, mma_phase);
+        mma_phase ^= 1;
+        tc_fence_after();
+        if (tid == 0 && j + 1 < n_tiles && !ms.abort) {
+            mbar_arrive_expect_tx(&ms.bar_v, kTileBytes);
+            bulk_g2s(smem + 2 * kTileBytes, vimg + (size_t)(j + 1) * kTileBytes, kTileBytes, &ms.bar_v);
+        }
+    }
+
+    // ---- the partial relative to the row's true maximum
+    const int r = mt * kTile + tid;
+    const size_t base = (((size_t)b * p.G + g) * p.n_chunks + c) * p.R;
+    const float fin = (m_run > -INFINITY && m_ref < m_run) ? fast_exp2(m_ref - m_run) : 1.f;
+    if (r < p.R) {
+        p.part_m[base + r] = m_run > -INFINITY ? m_run * kLn2 : -INFINITY;
+        p.part_l[base + r] = m_run > -INFINITY ? l * fin : 0.f;
+    }
+#pragma unroll 1
+    for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
+        float ov[16];
+        tmem_ld16(t_o + t_lane + c16 * 16, ov);
+        tmem_wait_ld();
+        if (r < p.R) {
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + (base + r) * kHeadDim + c16 * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float a0 = m_run > -INFINITY ? ov[4 * i] * fin : 0.f;
+                const float a1 = m_run > -INFINITY ? ov[4 * i + 1] * fin : 0.f;
+                const float a2 = m_run > -INFINITY ? ov[4 * i + 2] * fin : 0.f;
+                const float a3 = m_run > -INFINITY ? ov[4 * i + 3] * fin : 0.f;
+                dst[i] = make_float4(a0, a1, a2, a3);
+            }
+        }
+    }
+    // bulk copies still in flight after a timeout must land before exit
+    if (tid == 0 && ms.abort) {
+        mbar_wait(&ms.bar_k, n_tiles & 1, 1u << 22);
+        mbar_wait(&ms.bar_v, n_tiles & 1, 1u << 22);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (w == 0) tmem_dealloc(tmem, 512);
+}
+
+template <bool QBF16>
+cudaError_t launch_prompt(const Params &p, const PromptImages &im, cudaStream_t stream)
+{
+    dim3 gkv((unsigned)(p.n_chunks * im.tiles_per_chunk), (unsigned)p.G, (unsigned)p.n_seq);
+    qsa_prompt_stage_kv<QBF16><<<gkv, 256, 0, stream>>>(p, im);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 gq((unsigned)im.row_tiles, (unsigned)p.G, (unsigned)p.n_seq);
+    qsa_prompt_stage_q<QBF16><<<gq, 256, 0, stream>>>(p, im);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int bytes = (int)(3 * kTileBytes + kPBytes + sizeof(PromptSmem) + 1024);
+    if ((e = cudaFuncSetAttribute(qsa_prompt_tc_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  bytes)) != cudaSuccess)
+        return e;
+    dim3 gm((unsigned)(im.row_tiles * p.n_chunks), (unsigned)p.G, (unsigned)p.n_seq);
+    qsa_prompt_tc_kernel<QBF16><<<gm, kTile, bytes, stream>>>(p, im);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+bool prompt_tc_supports(const Params &p) { return p.R > 64 && p.chunk_cells >= kTile; }
+
+size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks, size_t *k_bytes,
+                          size_t *q_bytes, size_t *cell_bytes)
+{
+    const size_t tpc = ((size_t)chunk_cells + kTile - 1) / kTile;
+    const size_t row_tiles = ((size_t)R + kTile - 1) / kTile;
+    *k_bytes = (size_t)n_seq * G * n_chunks * tpc * kTileBytes;
+    *q_bytes = (size_t)n_seq * G * row_tiles * kTileBytes;
+    *cell_bytes = (size_t)n_seq * G * n_chunks * tpc * kTile * sizeof(float);
+    return 2 * *k_bytes + *q_bytes + 2 * *cell_bytes;
+}
+
+cudaError_t launch_prompt_tc(const Params &p, const PromptImages &im, cudaStream_t stream)
+{
+    if (p.n_chunks == 0) return cudaSuccess;
+    return p.q_bf16 ? launch_prompt<true>(p, im, stream) : launch_prompt<false>(p, im, stream);
+}
+
+} // namespace qsa
