@@ -416,14 +416,14 @@ def run_ours(args, world, rank, local):
         cps, cores, sample = oracle_sample(problems, args.cpu_seconds)
         cpu = {"value": cps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
-    digest = source_digest("qsa_chunk_simt.cu")
+    digest = source_digest("qsa_chunk_tc.cu", "qsa_merge.cu")
     traffic = TRAFFIC.get(digest)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": len(step_ms), "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "f16 (int8 codes exact) x f16 -> f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "flushed (512 MB write) before every timed step",
                        "launch": "one CUDA graph per call, replayed", "parallelism":
                        f"replica per GPU x{world}" if world > 1 else "1 GPU"},

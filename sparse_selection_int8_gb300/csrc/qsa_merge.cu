@@ -5,80 +5,109 @@
 // of a row carries (m_c, l_c, o_c) with m in natural-log units; the merge is
 //   M = max_{c: l_c > 0} m_c,  L = sum_c l_c e^{m_c - M},
 //   out = sum_c o_c e^{m_c - M} / L   (zeros when no chunk holds a cell).
-// One CTA per (row, KV head, sequence).  The chunks' (m, l) pairs are read
-// in parallel, 256 chunks at a time, into shared memory; the weights
-// e^{m_c - M} are formed once per chunk; thread d then sums o_c[d] times its
-// weight with independent loads.  Every sum runs in ascending chunk order,
-// so the result is deterministic.
+// One warp per query row: lane k owns output dimensions 8k..8k+7.  The
+// lanes read the chunks' (m, l) pairs 32 at a time, form the weights
+// e^{m_c - M} once, and broadcast them by shuffle while every lane sums its
+// eight dimensions over the chunks with independent 16-byte loads.  All sums
+// run in a fixed order (ascending chunks; a fixed shuffle tree for L), so the
+// result is deterministic.
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kBlock = kHeadDim; // one thread per output dimension
+constexpr int kWarpsPerBlock = 8;
 
-__global__ void __launch_bounds__(kBlock) qsa_merge_kernel(const Params p)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) qsa_merge_kernel(const Params p)
 {
-    __shared__ float s_w[kBlock];   // weights e^{m_c - M} (0 for empty chunks)
-    __shared__ float s_lw[kBlock];  // l_c * weight
-    __shared__ float s_red[kBlock / 32];
-    const int r = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int g = blockIdx.y;
     const int b = blockIdx.z;
-    const int d = threadIdx.x;
     // launched as a programmatic dependent of the chunk kernel: wait until
     // that grid has finished and its partials are visible
     cudaGridDependencySynchronize();
+    if (r >= p.R) return;
     int start, n;
     seq_range(p, b, &start, &n);
     const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
     const size_t base = ((size_t)b * p.G + g) * p.n_chunks * p.R + r;
+    const size_t stride = (size_t)p.R; // chunk stride of m and l
 
-    // M: every thread takes chunks d, d+256, ...; then a block max (exact)
     float M = -INFINITY;
-    for (int c = d; c < n_chunks; c += kBlock) {
-        const size_t idx = base + (size_t)c * p.R;
+    for (int c = lane; c < n_chunks; c += 32) {
+        const size_t idx = base + (size_t)c * stride;
         if (p.part_l[idx] > 0.f) M = fmaxf(M, p.part_m[idx]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((d & 31) == 0) s_red[d >> 5] = M;
-    __syncthreads();
-    M = s_red[0];
-#pragma unroll
-    for (int i = 1; i < kBlock / 32; ++i) M = fmaxf(M, s_red[i]);
 
-    float acc = 0.f, L = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float Lpart = 0.f;
     if (M > -INFINITY) {
-        for (int c0 = 0; c0 < n_chunks; c0 += kBlock) {
-            const int cnt = min(kBlock, n_chunks - c0);
-            __syncthreads(); // the previous block's weights are consumed
-            if (d < cnt) {
-                const size_t idx = base + (size_t)(c0 + d) * p.R;
+        for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+            const int cnt = min(32, n_chunks - c0);
+            float wgt = 0.f;
+            if (lane < cnt) {
+                const size_t idx = base + (size_t)(c0 + lane) * stride;
                 const float lc = p.part_l[idx];
-                const float wgt = lc > 0.f ? expf(p.part_m[idx] - M) : 0.f;
-                s_w[d] = wgt;
-                s_lw[d] = lc > 0.f ? lc * wgt : 0.f;
+                if (lc > 0.f) {
+                    wgt = expf(p.part_m[idx] - M);
+                    Lpart = fmaf(lc, wgt, Lpart);
+                }
             }
-            __syncthreads();
-            const float *o = p.part_o + (base + (size_t)c0 * p.R) * kHeadDim + d;
-            const size_t stride = (size_t)p.R * kHeadDim;
+            const float *o = p.part_o + (base + (size_t)c0 * stride) * kHeadDim + lane * 8;
+            const size_t ostride = stride * kHeadDim;
             int c = 0;
             for (; c + 4 <= cnt; c += 4) {
-                const float o0 = o[(size_t)c * stride], o1 = o[(size_t)(c + 1) * stride];
-                const float o2 = o[(size_t)(c + 2) * stride], o3 = o[(size_t)(c + 3) * stride];
-                acc = fmaf(o0, s_w[c], acc);
-                acc = fmaf(o1, s_w[c + 1], acc);
-                acc = fmaf(o2, s_w[c + 2], acc);
-                acc = fmaf(o3, s_w[c + 3], acc);
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)(c + u) * ostride);
+                    v[2 * u] = src[0];
+                    v[2 * u + 1] = src[1];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float wu = __shfl_sync(0xffffffffu, wgt, c + u);
+                    acc[0] = fmaf(v[2 * u].x, wu, acc[0]);
+                    acc[1] = fmaf(v[2 * u].y, wu, acc[1]);
+                    acc[2] = fmaf(v[2 * u].z, wu, acc[2]);
+                    acc[3] = fmaf(v[2 * u].w, wu, acc[3]);
+                    acc[4] = fmaf(v[2 * u + 1].x, wu, acc[4]);
+                    acc[5] = fmaf(v[2 * u + 1].y, wu, acc[5]);
+                    acc[6] = fmaf(v[2 * u + 1].z, wu, acc[6]);
+                    acc[7] = fmaf(v[2 * u + 1].w, wu, acc[7]);
+                }
             }
-            for (; c < cnt; ++c) acc = fmaf(o[(size_t)c * stride], s_w[c], acc);
-            for (int cc = 0; cc < cnt; ++cc) L += s_lw[cc];
+            for (; c < cnt; ++c) {
+                const float wu = __shfl_sync(0xffffffffu, wgt, c);
+                const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)c * ostride);
+                const float4 a = src[0], b4 = src[1];
+                acc[0] = fmaf(a.x, wu, acc[0]);
+                acc[1] = fmaf(a.y, wu, acc[1]);
+                acc[2] = fmaf(a.z, wu, acc[2]);
+                acc[3] = fmaf(a.w, wu, acc[3]);
+                acc[4] = fmaf(b4.x, wu, acc[4]);
+                acc[5] = fmaf(b4.y, wu, acc[5]);
+                acc[6] = fmaf(b4.z, wu, acc[6]);
+                acc[7] = fmaf(b4.w, wu, acc[7]);
+            }
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lpart += __shfl_xor_sync(0xffffffffu, Lpart, o);
+    const float L = Lpart;
     const int t = r / p.H, j = r % p.H;
-    const size_t out_idx = (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim + d;
-    p.out[out_idx] = L > 0.f ? acc / L : 0.f;
+    float4 *dst = reinterpret_cast<float4 *>(
+        p.out + (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim + lane * 8);
+    if (L > 0.f) {
+        dst[0] = make_float4(acc[0] / L, acc[1] / L, acc[2] / L, acc[3] / L);
+        dst[1] = make_float4(acc[4] / L, acc[5] / L, acc[6] / L, acc[7] / L);
+    } else {
+        dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
 } // namespace
@@ -86,8 +115,8 @@ __global__ void __launch_bounds__(kBlock) qsa_merge_kernel(const Params p)
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.R, (unsigned)p.G, (unsigned)p.n_seq);
-    cfg.blockDim = dim3(kBlock);
+    cfg.gridDim = dim3((unsigned)((p.R + kWarpsPerBlock - 1) / kWarpsPerBlock), (unsigned)p.G, (unsigned)p.n_seq);
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

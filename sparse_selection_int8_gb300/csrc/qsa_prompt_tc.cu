@@ -160,9 +160,12 @@ __global__ void __launch_bounds__(256) qsa_prompt_stage_q(const Params p, const 
 
 // ---------------------------------------------------------------- main
 
+constexpr int kThreads = 2 * kTile; // two threads per query row (column halves)
+
 struct PromptSmem {
     float ksc[kTile];
     float bias[kTile];
+    float rowmax[2][kTile]; // row maxima of the two column halves (rows' sums at the end)
     uint64_t bar_q, bar_k, bar_v, bar_mma;
     uint32_t tmem;
     int32_t abort;
@@ -179,13 +182,19 @@ __device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64
     return true;
 }
 
-// 128 threads: thread i owns query row i of the tile (TMEM lane i).
+// 256 threads: warp w owns query rows 32*(w%4)..+31 (its TMEM lanes) and
+// column half w/4 of S (cells) and of O (dimensions).
 template <bool QBF16>
-__global__ void __launch_bounds__(kTile, 1) qsa_prompt_tc_kernel(const Params p, const PromptImages im)
+__global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params p, const PromptImages im)
 {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + pad;
+    // The operand tiles need 1024-byte alignment (128-byte swizzle atoms);
+    // the dynamic shared memory of a kernel without static shared memory
+    // starts there.  The check keeps a misplaced window from being used.
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) raise_status(p, QSA_STATUS_TIMEOUT);
+        return;
+    }
     const uint32_t s_q = smem_u32(smem), s_k = s_q + kTileBytes, s_v = s_k + kTileBytes;
     const uint32_t s_p = s_v + kTileBytes;
     PromptSmem &ms = *reinterpret_cast<PromptSmem *>(smem + 3 * kTileBytes + kPBytes);
@@ -222,7 +231,8 @@ __global__ void __launch_bounds__(kTile, 1) qsa_prompt_tc_kernel(const Params p,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms.tmem, t_s = tmem, t_o = tmem + kTile;
-    const uint32_t t_lane = (uint32_t)(32 * w) << 16;
+    const int row = 32 * (w & 3) + (tid & 31), hc = w >> 2;
+    const uint32_t t_lane = (uint32_t)(32 * (w & 3)) << 16;
     if (tid == 0) {
         mbar_arrive_expect_tx(&ms.bar_q, kTileBytes);
         bulk_g2s(smem, qimg, kTileBytes, &ms.bar_q);
@@ -252,17 +262,20 @@ __global__ void __launch_bounds__(kTile, 1) qsa_prompt_tc_kernel(const Params p,
         wait_bar(p, ms, &ms.bar_mma, mma_phase);
         mma_phase ^= 1;
         tc_fence_after();
-        // ---- row max of this tile (scaled, masked), then P
+        // ---- this thread's 64 scaled, masked scores, the row max, then P
+        float sv[64];
+#pragma unroll
+        for (int c16 = 0; c16 < 4; ++c16) tmem_ld16(t_s + t_lane + hc * 64 + c16 * 16, sv + c16 * 16);
+        tmem_wait_ld();
         float mx = -INFINITY;
 #pragma unroll
-        for (int c16 = 0; c16 < kTile / 16; ++c16) {
-            float sv[16];
-            tmem_ld16(t_s + t_lane + c16 * 16, sv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                mx = fmaxf(mx, fmaf(sv[i], ms.ksc[c16 * 16 + i], ms.bias[c16 * 16 + i]));
+        for (int i = 0; i < 64; ++i) {
+            sv[i] = fmaf(sv[i], ms.ksc[hc * 64 + i], ms.bias[hc * 64 + i]);
+            mx = fmaxf(mx, sv[i]);
         }
+        ms.rowmax[hc][row] = mx;
+        __syncthreads();
+        mx = fmaxf(ms.rowmax[0][row], ms.rowmax[1][row]);
         // rescale O (and l) when this row's max outgrows its reference by 2^8
         bool rescale = false;
         float factor = 1.f;
@@ -279,33 +292,27 @@ __global__ void __launch_bounds__(kTile, 1) qsa_prompt_tc_kernel(const Params p,
         }
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-            for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
+            for (int c16 = 0; c16 < 8; ++c16) {
                 float ov[16];
-                tmem_ld16(t_o + t_lane + c16 * 16, ov);
+                tmem_ld16(t_o + t_lane + hc * 128 + c16 * 16, ov);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) ov[i] *= factor;
-                tmem_st16(t_o + t_lane + c16 * 16, ov);
+                tmem_st16(t_o + t_lane + hc * 128 + c16 * 16, ov);
             }
             tmem_wait_st();
         }
 #pragma unroll
-        for (int c16 = 0; c16 < kTile / 16; ++c16) {
-            float sv[16];
-            tmem_ld16(t_s + t_lane + c16 * 16, sv);
-            tmem_wait_ld();
-            uint32_t hw[8];
+        for (int c8 = 0; c8 < 8; ++c8) {
+            uint32_t hw[4];
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const float s0 = fmaf(sv[i], ms.ksc[c16 * 16 + i], ms.bias[c16 * 16 + i]);
-                const float s1 = fmaf(sv[i + 1], ms.ksc[c16 * 16 + i + 1], ms.bias[c16 * 16 + i + 1]);
-                const float p0 = m_ref > -INFINITY ? fast_exp2(s0 - m_ref) : 0.f;
-                const float p1 = m_ref > -INFINITY ? fast_exp2(s1 - m_ref) : 0.f;
+            for (int i = 0; i < 8; i += 2) {
+                const float p0 = m_ref > -INFINITY ? fast_exp2(sv[c8 * 8 + i] - m_ref) : 0.f;
+                const float p1 = m_ref > -INFINITY ? fast_exp2(sv[c8 * 8 + i + 1] - m_ref) : 0.f;
                 l += p0 + p1;
                 hw[i / 2] = pack2<false>(p0, p1);
             }
-            sts128(s_p + kmajor_sw128_off(tid, c16 * 16, kTile), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-            sts128(s_p + kmajor_sw128_off(tid, c16 * 16 + 8, kTile), make_uint4(hw[4], hw[5], hw[6], hw[7]));
+            sts128(s_p + kmajor_sw128_off(row, hc * 64 + c8 * 8, kTile), make_uint4(hw[0], hw[1], hw[2], hw[3]));
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -338,20 +345,22 @@ __global__ void __launch_bounds__(kTile, 1) qsa_prompt_tc_kernel(const Params p,
     }
 
     // ---- the partial relative to the row's true maximum
-    const int r = mt * kTile + tid;
+    ms.rowmax[hc][row] = l; // reused for the two halves' sums
+    __syncthreads();
+    const int r = mt * kTile + row;
     const size_t base = (((size_t)b * p.G + g) * p.n_chunks + c) * p.R;
     const float fin = (m_run > -INFINITY && m_ref < m_run) ? fast_exp2(m_ref - m_run) : 1.f;
-    if (r < p.R) {
+    if (r < p.R && hc == 0) {
         p.part_m[base + r] = m_run > -INFINITY ? m_run * kLn2 : -INFINITY;
-        p.part_l[base + r] = m_run > -INFINITY ? l * fin : 0.f;
+        p.part_l[base + r] = m_run > -INFINITY ? (ms.rowmax[0][row] + ms.rowmax[1][row]) * fin : 0.f;
     }
 #pragma unroll 1
-    for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
+    for (int c16 = 0; c16 < 8; ++c16) {
         float ov[16];
-        tmem_ld16(t_o + t_lane + c16 * 16, ov);
+        tmem_ld16(t_o + t_lane + hc * 128 + c16 * 16, ov);
         tmem_wait_ld();
         if (r < p.R) {
-            float4 *dst = reinterpret_cast<float4 *>(p.part_o + (base + r) * kHeadDim + c16 * 16);
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + (base + r) * kHeadDim + hc * 128 + c16 * 16);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float a0 = m_run > -INFINITY ? ov[4 * i] * fin : 0.f;
@@ -383,12 +392,12 @@ cudaError_t launch_prompt(const Params &p, const PromptImages &im, cudaStream_t 
     dim3 gq((unsigned)im.row_tiles, (unsigned)p.G, (unsigned)p.n_seq);
     qsa_prompt_stage_q<QBF16><<<gq, 256, 0, stream>>>(p, im);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int bytes = (int)(3 * kTileBytes + kPBytes + sizeof(PromptSmem) + 1024);
+    const int bytes = (int)(3 * kTileBytes + kPBytes + sizeof(PromptSmem));
     if ((e = cudaFuncSetAttribute(qsa_prompt_tc_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   bytes)) != cudaSuccess)
         return e;
     dim3 gm((unsigned)(im.row_tiles * p.n_chunks), (unsigned)p.G, (unsigned)p.n_seq);
-    qsa_prompt_tc_kernel<QBF16><<<gm, kTile, bytes, stream>>>(p, im);
+    qsa_prompt_tc_kernel<QBF16><<<gm, kThreads, bytes, stream>>>(p, im);
     return cudaGetLastError();
 }
 

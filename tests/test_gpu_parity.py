@@ -306,3 +306,55 @@ def test_single_cell_gather_is_exact(algo):
         for t in range(2):
             for h in range(24):
                 assert np.array_equal(out[b, t, h], expect.astype(np.float32)), (b, t, h)
+
+
+# ------------------------------------------------- prompt-shaped path (rows on M)
+
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+@pytest.mark.parametrize("q_dtype", ["bf16", "f32"])
+def test_prompt_path_masked_ragged(algo, q_dtype):
+    """Many query rows per KV head (the rows-on-M tensor-core path) with
+    page -1 masking, a chunk that is not a multiple of 128 cells, a row count
+    that is not a multiple of 128, and both query types."""
+    p = wl.make_problem(n_queries=13, q_per_kv=12, pool_cells=3000, n_selected=2500,
+                        chunk_cells=1000, q_dtype=q_dtype, mask_fraction=0.2, seed=8100)
+    check_full(p, algo, f"prompt masked {q_dtype}")
+
+
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+def test_prompt_path_ragged_batch(algo):
+    lens = [0, 700, 129, 1500]
+    p = wl.make_problem(n_seq=4, n_kv_heads=2, n_queries=7, q_per_kv=12, pool_cells=2048,
+                        n_selected=lens, chunk_cells=512, q_dtype="bf16", seed=8200)
+    dp, out = run(p, algo, max_selected=1600)
+    assert_parity(out, oracle.decode_attn(p), "prompt ragged batch")
+    assert np.array_equal(out[0], np.zeros_like(out[0]))
+
+
+@pytest.mark.parametrize("algo", ["auto"])
+def test_prompt_path_partials_bit_identical(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.prompt_shaped(n_queries=64, pool_cells=2048, chunk_cells=1024)
+    dp = qsa.DeviceProblem(p, algo=algo_code(algo))
+    dp.run()
+    torch.cuda.synchronize()
+    m0, l0, o0 = qsa.partials_of(dp)
+    for _ in range(3):
+        dp.workspace.fill_(0xFF)
+        dp.run()
+        torch.cuda.synchronize()
+        m, l, o = qsa.partials_of(dp)
+        assert m.tobytes() == m0.tobytes() and l.tobytes() == l0.tobytes() and o.tobytes() == o0.tobytes()
+
+
+def test_prompt_path_growing_scores():
+    """K scales that grow along the list make each row's running max climb by
+    tens of log2 units across the tiles, which forces the rescaling of O in
+    tensor memory (the reference moves when the max grows by more than 2^8).
+    bf16 queries meet bf16 K codes exactly, so only fp32 accumulation and the
+    f16 P and V_hat roundings differ from the oracle."""
+    p = wl.make_problem(n_queries=16, q_per_kv=12, pool_cells=4096, n_selected=4096,
+                        chunk_cells=4096, q_dtype="bf16", selection="full", seed=8300)
+    ks = np.linspace(0.005, 0.1, p.pool_cells, dtype=np.float32)
+    p.k_scale[0, 0] = ks[p.page_table[0].argsort()]  # cell at list position i gets ks[i]
+    check_full(p, "auto", "prompt growing scores")
