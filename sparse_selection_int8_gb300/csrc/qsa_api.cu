@@ -57,6 +57,8 @@ Workspace carve(const qsa_shape *s, int n_seq, int max_selected)
     w.off_o = align_up(w.off_l + rows * sizeof(float), kWorkspaceAlign);
     w.off_extra = align_up(w.off_o + rows * kHeadDim * sizeof(float), 1024);
     w.total = w.off_extra;
+    if (select_path(s) == kPathDecodeTc && n_chunks > 0)
+        w.total = w.off_extra + align_up(chunk_tc_query_image_bytes(n_seq, s->n_kv_heads, (int)R), 1024);
     if (select_path(s) == kPathPromptTc && n_chunks > 0) {
         size_t kb, qb, cb;
         prompt_image_bytes(n_seq, s->n_kv_heads, (int)R, s->chunk_cells, (int)n_chunks, &kb, &qb, &cb);
@@ -126,6 +128,7 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.part_l = reinterpret_cast<float *>(ws + w.off_l);
     p.part_o = reinterpret_cast<float *>(ws + w.off_o);
     p.status = status;
+    p.q_img = ws + w.off_extra;
     p.n_sel_single = n_sel_single;
     p.n_seq = n_seq;
     p.G = s->n_kv_heads;

@@ -9,40 +9,40 @@
 // cells on the MMA's M dimension, because a decode window has only 12-64
 // query rows:
 //
-//   S^T[cell][row] = K_hat[cell][:] . Q[row][:]       M=128 cells, N=rows, K=256
-//   O^T[d][row]    = V_hat^T[d][cell] . P^T[cell][row] M=128 d (x2), N=rows, K=128 cells
+//   S^T[cell][row] = K_code[cell][:] . Q[row][:]      M=128 cells, N=rows, K=256
+//   O^T[d][row]   += V_code^T[d][cell] . P'^T[cell][row]   M=128 d (x2), N=rows, K=128 cells
 //
-// INT8 codes convert exactly to f16 (|code| <= 127); the K scale multiplies
-// the fp32 score after the MMA, and the V scale (divided by the group's
-// largest V scale, so P stays in [0, 1]) multiplies P before it is rounded
-// to f16; the group's largest scale multiplies the fp32 result.  Queries are
-// rounded to f16.  Accumulation is fp32 in tensor memory.
+// INT8 codes convert exactly to f16 (|code| <= 127).  The K scale (times the
+// softmax scale and log2 e) multiplies the fp32 score after the MMA; the V
+// scale, divided by a per-chunk reference sigma, multiplies the probability
+// before it is rounded to f16 (P' = p * v_scale / sigma), and sigma
+// multiplies the fp32 result.  Queries are rounded to f16.
 //
-// Two persistent CTAs of 8 warps share each SM (about 110 KB of shared
-// memory and 256 TMEM columns each), so one CTA's dependent phases overlap
-// the other's.  A CTA walks a contiguous range of non-empty (sequence, KV
-// head, chunk) items as a sequence of ops: for every group of up to 256
-// cells (two M tiles sharing one max), its K tiles, then its V tiles.
-//   gather   each op's 128 rows (256 B each) are loaded straight into
-//            registers with 16-byte read-only loads one op ahead (8 x 16 B
-//            per thread, issued as soon as the previous op is converted);
-//            16 lanes cover a row, so every load instruction moves two whole
-//            rows; the op after that is prefetched into L2 at the same time,
-//            so the register loads mostly hit L2;
-//   resolve  list entry -> page slot (a1) runs two groups ahead: list reads
-//            at a group's first K op, page-table reads after its max pass,
-//            the checked slots stored in a small ring at the group's end;
-//   convert  registers -> f16 tile in the tensor cores' 128-byte-swizzled
-//            layout (the lane mapping makes the stores conflict-free);
-//   MMA      one thread issues tcgen05.mma; completion on an mbarrier;
-//   softmax  warp (quadrant q, half h) owns cells 32q..32q+31 and half the
-//            rows, eight rows at a time: max via redux, P built per tile
-//            right before its P.V MMA, sums via a reduce-scatter butterfly,
-//            all in a fixed order, so partials are bit-identical run to run.
+// One persistent CTA per SM walks a contiguous range of non-empty (sequence,
+// KV head, chunk) items as a stream of 128-cell tiles, with warp roles that
+// run concurrently and hand tiles over through mbarrier rings:
 //
-// The only wait that is not a CTA barrier is the MMA-completion wait; it is
-// bounded, and a wait that runs out raises QSA_STATUS_TIMEOUT and the kernel
-// runs to its end without further waiting.
+//   loader warps 0-7  (warp w: cells 32(w%4)..+31, row half w/4).  A software
+//            pipeline, one tile per step: list entries four tiles ahead,
+//            page-table entries three ahead, slot checks and L2 prefetch of
+//            the K/V rows two ahead, 32-byte register loads of the rows one
+//            ahead; the current tile's K codes go to tensor memory as the
+//            MMA's A operand (tcgen05.st), its V codes to a double-buffered
+//            shared-memory tile in the MN-major 128-byte-swizzled layout, its
+//            scales and validity bits to a small double-buffered ring.
+//   softmax warps 8-11 (thread = cell).  Per tile: max of every row over the
+//            128 cells (redux), per-row decisions by the row's own thread
+//            (running max; the reference max moves, and O is rescaled in
+//            tensor memory, only when the max grows by more than 2^8), then
+//            P' written to shared memory as the second MMA's B operand and
+//            row sums by a reduce-scatter butterfly.  At the end of a chunk
+//            they read O from tensor memory and write the partials.
+//   MMA warp 12 (one thread) issues S = K.Q^T for tile i+1 before
+//            O += V^T.P'^T for tile i; completion is signalled by
+//            tcgen05.commit on the rings' "empty" and "full" barriers.
+//
+// Every wait is bounded; a wait that runs out raises QSA_STATUS_TIMEOUT and
+// makes all later waits of the CTA return at once, so the kernel always ends.
 #include <cuda_fp16.h>
 
 #include "qsa_internal.cuh"
@@ -53,18 +53,22 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTile = 128;          // cells per MMA tile (M)
-constexpr int kMaxTiles = 2;        // tiles per softmax group
-constexpr int kGroupCells = kTile * kMaxTiles;
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kSlotRing = 4;        // groups of resolved slots kept
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTileF16Bytes = kTile * kHeadDim * 2; // 64 KB
-
-struct Layout {
-    uint32_t off_kv, off_q, off_p, off_misc, total;
-};
+constexpr int kTile = 128;                        // cells per tile (MMA M)
+constexpr int kLoadWarps = 8;
+constexpr int kSoftWarps = 4;
+constexpr int kMmaWarp = kLoadWarps + kSoftWarps; // 12
+constexpr int kThreads = (kMmaWarp + 1) * 32;     // 416
+constexpr int kLoadThreads = kLoadWarps * 32;
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kScaleThreads = kLoadThreads / 4;   // loader threads that write the scales
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColK = 0;   // K codes, 128 columns (two f16 per column)
+constexpr uint32_t kColS = 128; // scores, two buffers of 64 columns
+constexpr uint32_t kColO = 256; // O^T, two chunk buffers x two d halves x 64 columns
+constexpr uint32_t kStageBytes = kTile * kHeadDim * 2; // one f16 V tile, 64 KB
+constexpr uint32_t kBarSoft = 1;                       // named barrier of the softmax warps
+constexpr float kRescaleLog2 = 8.f; // O is rescaled when a row max grows past 2^8
+constexpr float kSigmaGrow = 16.f;  // ... or a V scale exceeds 16 x the reference
 
 // Position in the work list (see cursor_init_warp / cursor_next).
 struct Cursor {
@@ -72,43 +76,43 @@ struct Cursor {
     int remaining;
 };
 
-// Misc area: slot ring, per-group cell info, reduction scratch, per-row values.
 struct Misc {
-    int32_t ring[kSlotRing][kGroupCells];
-    int32_t cell_slot[kMaxTiles][kTile];
-    float cell_ks[kMaxTiles][kTile];
-    float cell_vs[kMaxTiles][kTile];
-    float red_max[2][32][4]; // [row half][row within half][lane quadrant]
-    float red_sum[2][32][4];
-    float red_vs[kWarps];
-    float row_fa[64], row_fb[64], row_mrun[64], row_lrun[64];
-    int32_t abort;
+    float sc_ks[2][kTile];   // k_scale * softmax_scale * log2(e) per cell
+    float sc_vs[2][kTile];   // v_scale per cell
+    uint8_t sc_ok[2][kTile]; // cell holds a valid slot
+    __align__(16) float red_max[2][65][4]; // [tile parity][row; 64 = |v_scale| max][lane quadrant]
+    __align__(16) float red_sum[2][64][4];
+    float st_mrun[2][64];    // running max (log2 units) after the tile of that parity
+    __align__(16) float st_mref[2][64]; // reference max the tile's P' were formed against
+    float st_fac[64];        // O/l factor of the current tile
+    float st_fin[64];        // 2^(mref - mrun) at the end of a chunk
+    float st_sig[2];         // sigma reference after the tile of that parity
+    float st_fs[2];          // sigma factor of the tile
+    int st_any[2];           // tile index whose O needs rescaling
+    Cursor first;
     uint32_t tmem;
-    Cursor first; // this CTA's first item
-    uint64_t mma;
+    int abort;
+    uint64_t k_full, k_empty, done;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t v_full[2], v_empty[2], sc_full[2], sc_empty[2];
+    uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
 };
 
-__host__ __device__ inline Layout make_layout(int N)
-{
-    Layout L;
-    L.off_kv = 0;
-    L.off_q = kTileF16Bytes;
-    L.off_p = L.off_q + (uint32_t)N * kHeadDim * 2;
-    L.off_misc = L.off_p + (uint32_t)N * kTile * 2;
-    L.total = L.off_misc + (uint32_t)((sizeof(Misc) + 127) / 128 * 128);
-    return L;
-}
+template <int N>
+struct Lay {
+    static constexpr int PB = N <= 48 ? 2 : 1; // P' buffers
+    static constexpr uint32_t v = 0;
+    static constexpr uint32_t q = 2 * kStageBytes;
+    static constexpr uint32_t pb = q + 2u * N * 512u;
+    static constexpr uint32_t misc = pb + PB * N * 256u;
+    static constexpr uint32_t total = misc + (uint32_t)((sizeof(Misc) + 127) / 128 * 128);
+};
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
-}
-
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v)
-{
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 // Four int8 codes -> four f16 values (exact): bias the bytes to u = code+128,
@@ -134,19 +138,27 @@ __device__ __forceinline__ float from_ordered_key(int k)
     return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
 }
 
-// NC consecutive columns of tensor memory (a multiple of 4) into v.
-template <int NC>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v)
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b)
 {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// One stage of a reduce-scatter over the warp: values [0, 2*HALF) -> [0, HALF);
+// a lane keeps the half selected by its bit `o` and adds the partner's.
+template <int HALF>
+__device__ __forceinline__ void rs_stage(float *e, int lane, int o)
+{
+    const bool up = (lane & o) != 0;
 #pragma unroll
-    for (int j = 0; j + 8 <= NC; j += 8) tmem_ld8(taddr + j, v + j);
-    if (NC % 8) tmem_ld4(taddr + (NC / 8) * 8, v + (NC / 8) * 8);
+    for (int x = 0; x < HALF; ++x) {
+        const float send = up ? e[x] : e[x + HALF];
+        const float keep = up ? e[x + HALF] : e[x];
+        e[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
 }
 
 // ---------------------------------------------------------------- work list
-
-// Non-empty (sequence, KV head, chunk) items in sequence-major order; each
-// CTA takes a contiguous range (consecutive chunks share their queries).
 
 __device__ inline int seq_chunks(const Params &p, int b, int *start, int *n)
 {
@@ -156,7 +168,8 @@ __device__ inline int seq_chunks(const Params &p, int b, int *start, int *n)
 
 // Position of this CTA's first item, computed by one full warp: lanes read
 // the sequences' list offsets in parallel, a warp scan finds the sequence
-// that holds item `lo`.
+// that holds item `lo`.  Items are (sequence, KV head, chunk) in that order;
+// each CTA takes a contiguous range (consecutive chunks share their queries).
 __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
 {
     long long total = 0;
@@ -170,7 +183,7 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
     cur.remaining = lo < hi ? (int)(hi - lo) : 0;
     cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
     if (cur.remaining == 0) return;
-    long long before = 0; // items of the sequences already passed
+    long long before = 0;
     for (int b0 = 0; b0 < p.n_seq; b0 += 32) {
         const int b = b0 + lane;
         int st = 0, len = 0, nch = 0;
@@ -221,522 +234,727 @@ __device__ inline void cursor_next(const Params &p, Cursor &cur)
     cur.remaining = 0;
 }
 
-// The ops of the work range: for every group (up to two tiles of one
-// chunk), its K tiles, then its V tiles.  Groups are numbered by gi in the
-// same order everywhere (slot ring index = gi % kSlotRing).
-struct OpIter {
+// First item of the next (sequence, KV head) pair in the range, if any.
+__device__ inline Cursor next_segment(const Params &p, Cursor cur)
+{
+    const int left = cur.nch - 1 - cur.c; // later items of the same pair
+    if (cur.remaining - 1 <= left) {
+        cur.remaining = 0;
+        return cur;
+    }
+    cur.remaining -= left;
+    cur.c = cur.nch - 1;
+    cursor_next(p, cur);
+    return cur;
+}
+
+// The tile stream: every item's chunk in 128-cell tiles; a segment is a run
+// of tiles of one (sequence, KV head) pair (one query block).
+struct TileIt {
     Cursor cur;
-    int nc;      // cells of the current item (chunk)
-    int gs;      // first cell of the current group within the item
-    int tiles;   // tiles of the current group
-    int kind;    // 0 = K tile, 1 = V tile
-    int t;       // tile within the group
-    uint32_t gi; // group counter
+    int ti, nt, nc; // tile within the chunk, tiles of the chunk, cells of the chunk
+    int seg;
     bool valid;
 };
 
-__device__ inline void op_setup_item(const Params &p, OpIter &it)
+__device__ __forceinline__ void tile_setup(const Params &p, TileIt &t)
 {
-    it.nc = min(p.chunk_cells, it.cur.n - it.cur.c * p.chunk_cells);
-    it.gs = 0;
-    it.kind = 0;
-    it.t = 0;
-    it.tiles = (min(kGroupCells, it.nc) + kTile - 1) / kTile;
+    t.nc = min(p.chunk_cells, t.cur.n - t.cur.c * p.chunk_cells);
+    t.nt = (t.nc + kTile - 1) / kTile;
+    t.ti = 0;
 }
 
-__device__ inline void op_init(const Params &p, OpIter &it, const Cursor &first)
+__device__ __forceinline__ void tile_init(const Params &p, TileIt &t, const Cursor &first)
 {
-    it.cur = first;
-    it.gi = 0;
-    it.valid = it.cur.remaining > 0;
-    if (it.valid) op_setup_item(p, it);
+    t.cur = first;
+    t.seg = 0;
+    t.valid = first.remaining > 0;
+    if (t.valid) tile_setup(p, t);
 }
 
-// Advance to the first op of the next group.
-__device__ inline void op_next_group(const Params &p, OpIter &it)
+__device__ __forceinline__ void tile_next(const Params &p, TileIt &t)
 {
-    it.t = 0;
-    it.kind = 0;
-    ++it.gi;
-    it.gs += kGroupCells;
-    if (it.gs < it.nc) {
-        it.tiles = (min(kGroupCells, it.nc - it.gs) + kTile - 1) / kTile;
-        return;
-    }
-    cursor_next(p, it.cur);
-    it.valid = it.cur.remaining > 0;
-    if (it.valid) op_setup_item(p, it);
+    if (++t.ti < t.nt) return;
+    const int b = t.cur.b, g = t.cur.g;
+    cursor_next(p, t.cur);
+    t.valid = t.cur.remaining > 0;
+    if (!t.valid) return;
+    tile_setup(p, t);
+    if (t.cur.b != b || t.cur.g != g) ++t.seg;
 }
 
-__device__ inline void op_next(const Params &p, OpIter &it)
+__device__ __forceinline__ int tile_cells(const TileIt &t) { return min(kTile, t.nc - t.ti * kTile); }
+
+__device__ __forceinline__ int tile_base(const Params &p, const TileIt &t)
 {
-    if (++it.t < it.tiles) return;
-    it.t = 0;
-    if (++it.kind < 2) return;
-    op_next_group(p, it);
+    return t.cur.start + t.cur.c * p.chunk_cells + t.ti * kTile;
 }
 
-// ---------------------------------------------------------------- phases
+// ---------------------------------------------------------------- step a1
 
-// Step a1 for one cell of a group, split in three so the two dependent reads
-// overlap other work: list entry, page entry, then the checks.
-__device__ __forceinline__ int resolve_list(const Params &p, const OpIter &g, int i)
+constexpr int kBadPos = INT_MIN;
+
+// Page-table entry of list entry `pos` (has = the tile holds this cell).
+__device__ __forceinline__ int page_entry(const Params &p, int b, int pos, bool has)
 {
-    if (!g.valid || i >= min(kGroupCells, g.nc - g.gs)) return INT_MIN;
-    return __ldg(p.sel + g.cur.start + g.cur.c * p.chunk_cells + g.gs + i);
+    if (!has) return -1;
+    if (pos < 0 || pos >= p.page_table_len) return kBadPos;
+    return __ldg(p.page_table + (size_t)b * p.page_table_len + pos);
 }
 
-// INT_MIN marks a position outside the page table; -1 a cell past the group.
-__device__ __forceinline__ int resolve_page(const Params &p, const OpIter &g, int pos)
+// Checked pool slot, -1 when masked or out of range; `report` raises the
+// status bits (one of the two threads of a cell reports).
+__device__ __forceinline__ int slot_of(const Params &p, int raw, bool report)
 {
-    if (pos == INT_MIN) return -1;
-    if (pos < 0 || pos >= p.page_table_len) return INT_MIN;
-    return __ldg(p.page_table + (size_t)g.cur.b * p.page_table_len + pos);
-}
-
-__device__ __forceinline__ int resolve_check(const Params &p, int raw)
-{
-    if (raw == INT_MIN) {
-        raise_status(p, QSA_STATUS_BAD_POSITION);
+    if (raw == kBadPos) {
+        if (report) raise_status(p, QSA_STATUS_BAD_POSITION);
         return -1;
     }
     if (raw == -1) return -1;
     if (raw < 0 || raw >= p.pool_cells) {
-        raise_status(p, QSA_STATUS_BAD_SLOT);
+        if (report) raise_status(p, QSA_STATUS_BAD_SLOT);
         return -1;
     }
     return raw;
 }
 
-// One op's rows in registers: warp w loads row pairs 8w..8w+7; lane
-// (qhi, rsel, qlo) takes piece q = 4*qhi + qlo (16 B) of row 2*rp + rsel.
-// Cells that are masked load nothing (zeros).  For a K op the first 128
-// threads also load their cell's two scales.
-struct OpRegs {
-    uint4 raw[8];
-    float ks, vs;
-};
+// ---------------------------------------------------------------- queries
 
-__device__ __forceinline__ void load_op(const Params &p, const Misc &ms, const OpIter &it, int tid,
-                                        OpRegs &r)
+// Element offset of query row r (= t*H + j) of (sequence b, KV head g).
+__device__ __forceinline__ size_t q_row_offset(const Params &p, int b, int g, int r)
 {
-    const int w = tid >> 5, lane = tid & 31;
-    const int rsel = (lane >> 2) & 1, q = (lane >> 3) * 4 + (lane & 3);
-    const int *tslots = ms.ring[it.gi % kSlotRing] + it.t * kTile;
-    const size_t kv_base = ((size_t)it.cur.b * p.G + it.cur.g) * p.pool_cells;
-    const int8_t *pool = (it.kind == 0 ? p.k_pool : p.v_pool) + kv_base * kHeadDim + q * 16;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int slot = tslots[2 * (8 * w + i) + rsel];
-        r.raw[i] = slot >= 0 ? ldg_nc_v4(pool + (size_t)slot * kHeadDim) : make_uint4(0, 0, 0, 0);
-    }
-    r.ks = r.vs = 0.f;
-    if (it.kind == 0 && tid < kTile) {
-        const int slot = tslots[tid];
-        if (slot >= 0) {
-            r.ks = __ldg(p.k_scale + kv_base + slot);
-            r.vs = __ldg(p.v_scale + kv_base + slot);
-        }
-    }
+    const int t = r / p.H, j = r % p.H;
+    return (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim;
 }
 
-// Warm L2 with the rows (and, for a K op, the scales) of an op that is
-// loaded into registers one op later: thread i prefetches 128-byte line
-// i % 2 of row i / 2.  No registers or shared memory are held.
-__device__ __forceinline__ void prefetch_op(const Params &p, const Misc &ms, const OpIter &it, int tid)
+// The K codes sit in tensor memory with the contraction index permuted (the
+// loader's 16x256b stores, see the loader): tensor-memory dimension
+// 16k + 4u + e holds byte (k < 8 ? 32u + 4k : 128 + 32u + 4(k - 8)) + e of
+// the K row.  The query tile is stored in the same order, so the dot product
+// is unchanged.  Piece pc (dimensions 8pc..8pc+7) of a query row takes the
+// four elements at s0 and the four at s0 + 32.
+__device__ __forceinline__ int q_piece_source(int pc)
 {
-    const int *tslots = ms.ring[it.gi % kSlotRing] + it.t * kTile;
-    const size_t kv_base = ((size_t)it.cur.b * p.G + it.cur.g) * p.pool_cells;
-    const int slot = tslots[tid >> 1];
-    if (slot >= 0) {
-        const int8_t *row = (it.kind == 0 ? p.k_pool : p.v_pool) + (kv_base + slot) * kHeadDim + (tid & 1) * 128;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
-        if (it.kind == 0) {
-            const float *sc = (tid & 1) ? p.v_scale : p.k_scale;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(sc + kv_base + slot));
-        }
-    }
+    const int k = pc >> 1, u0 = (pc & 1) * 2;
+    return (k < 8 ? 4 * k : 128 + 4 * (k - 8)) + 32 * u0;
 }
 
-// Registers -> f16 tile: row = 2*(8w + i) + rsel, so row/8 = 2w + i/4 and
-// row%8 = 2*(i%4) + rsel; the two 16-byte f16 chunks of piece q land in
-// chunks 2*qlo and 2*qlo+1 of their 64-column block, XOR-swizzled by row%8.
-__device__ __forceinline__ void convert_op(const OpRegs &r, uint32_t tile, int tid)
+// Query piece pc of the row at `row` (f32 or bf16 elements) -> f16x8.
+__device__ __forceinline__ uint4 q_piece_f16(const Params &p, const uint8_t *row, int pc)
 {
-    const int w = tid >> 5, lane = tid & 31;
-    const int qlo = lane & 3, rsel = (lane >> 2) & 1, qhi = lane >> 3;
-    const uint32_t dst0 = tile + (uint32_t)qhi * (kTile * 128) + (uint32_t)(2 * w) * 1024u + (uint32_t)rsel * 128u;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t r8 = 2u * (i & 3) + rsel;
-        const uint32_t dst = dst0 + (uint32_t)(i >> 2) * 1024u + 2u * (i & 3) * 128u;
-        uint4 a, b;
-        i8x4_to_f16x4(r.raw[i].x, a.x, a.y);
-        i8x4_to_f16x4(r.raw[i].y, a.z, a.w);
-        i8x4_to_f16x4(r.raw[i].z, b.x, b.y);
-        i8x4_to_f16x4(r.raw[i].w, b.z, b.w);
-        sts128(dst + (((2u * qlo) ^ r8) << 4), a);
-        sts128(dst + (((2u * qlo + 1u) ^ r8) << 4), b);
+    const int s0 = q_piece_source(pc);
+    float f[8];
+    if (p.q_bf16) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(row + 2 * s0);
+        const uint2 b = *reinterpret_cast<const uint2 *>(row + 2 * (s0 + 32));
+        f[0] = bf16_bits_to_f32(a.x & 0xffff); f[1] = bf16_bits_to_f32(a.x >> 16);
+        f[2] = bf16_bits_to_f32(a.y & 0xffff); f[3] = bf16_bits_to_f32(a.y >> 16);
+        f[4] = bf16_bits_to_f32(b.x & 0xffff); f[5] = bf16_bits_to_f32(b.x >> 16);
+        f[6] = bf16_bits_to_f32(b.y & 0xffff); f[7] = bf16_bits_to_f32(b.y >> 16);
+    } else {
+        const float4 a = *reinterpret_cast<const float4 *>(row + 4 * s0);
+        const float4 b = *reinterpret_cast<const float4 *>(row + 4 * (s0 + 32));
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
     }
+    return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                      pack_f16x2(f[6], f[7]));
 }
 
-__device__ __forceinline__ void cta_sync()
+// Query tiles of every (sequence, KV head) pair, written once per call into
+// the workspace in exactly the shared-memory layout the MMA reads (f16,
+// K-major, 128-byte swizzle, contraction index permuted as above, rows >= R
+// zero), so the chunk kernel brings a pair's tile in with one bulk copy.
+// One thread per 16-byte piece.
+template <int N>
+__global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
 {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-}
-
-// Queries of (sequence b, KV head g) as the f16 B operand (rows >= R zero).
-__device__ __forceinline__ void load_queries(const Params &p, uint32_t sq, int b, int g, int N, int tid)
-{
-    const int GH = p.G * p.H;
-    for (int e = tid; e < N * 32; e += kThreads) {
-        const int r = e >> 5, piece = e & 31;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < p.R) {
-            const int t = r / p.H, j = r % p.H;
-            const size_t off = (((size_t)b * p.T + t) * GH + (size_t)g * p.H + j) * kHeadDim + piece * 8;
-            float f[8];
-            if (p.q_bf16) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) + off);
-                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    f[2 * e2] = bf16_bits_to_f32(wv[e2] & 0xffff);
-                    f[2 * e2 + 1] = bf16_bits_to_f32(wv[e2] >> 16);
-                }
-            } else {
-                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.q) + off);
-                const float4 x = src[0], y = src[1];
-                f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
-                f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
-            }
-            __half2 h0 = __floats2half2_rn(f[0], f[1]), h1 = __floats2half2_rn(f[2], f[3]);
-            __half2 h2 = __floats2half2_rn(f[4], f[5]), h3 = __floats2half2_rn(f[6], f[7]);
-            v.x = *reinterpret_cast<uint32_t *>(&h0);
-            v.y = *reinterpret_cast<uint32_t *>(&h1);
-            v.z = *reinterpret_cast<uint32_t *>(&h2);
-            v.w = *reinterpret_cast<uint32_t *>(&h3);
-        }
-        sts128(sq + kmajor_sw128_off(r, piece * 8, N), v);
+    // the chunk kernel may launch now; it waits for this grid before reading
+    cudaTriggerProgrammaticLaunchCompletion();
+    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long pieces = (long long)p.n_seq * p.G * N * 32;
+    if (e >= pieces) return;
+    const int bg = (int)(e / (N * 32));
+    const int r = (int)((e / 32) % N), pc = (int)(e % 32);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < p.R) {
+        const int esz = p.q_bf16 ? 2 : 4;
+        v = q_piece_f16(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, r) * esz, pc);
     }
+    *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.q_img) + (size_t)bg * N * 512 + kmajor_sw128_off(r, pc * 8, N)) = v;
 }
 
 // ---------------------------------------------------------------- kernel
 
 template <int N>
-__global__ void __launch_bounds__(kThreads, 2) qsa_chunk_tc_kernel(const Params p)
+__global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params p)
 {
-    constexpr int NH = N / 2; // rows per warp half (a multiple of 8)
+    using L = Lay<N>;
+    constexpr int PB = L::PB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
     uint8_t *smem = smem_raw + pad;
-    const Layout L = make_layout(N);
-    Misc &ms = *reinterpret_cast<Misc *>(smem + L.off_misc);
+    Misc &ms = *reinterpret_cast<Misc *>(smem + L::misc);
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
-    const int qd = w & 3;  // TMEM lane quadrant of this warp
-    const int ch = w >> 2; // row half (softmax) and d half (fold)
-    const uint32_t s_kv = smem_u32(smem + L.off_kv);
-    const uint32_t s_q = smem_u32(smem + L.off_q);
-    const uint32_t s_p = smem_u32(smem + L.off_p);
-    const uint32_t t_lane = (uint32_t)(32 * qd) << 16;
-    const uint32_t o_base = kMaxTiles * N;
-    const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
-    const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
-    const int cell = 32 * qd + lane; // softmax: this thread's cell within a tile
+    const uint32_t s_v = smem_u32(smem + L::v);
+    const uint32_t s_q = smem_u32(smem + L::q);
+    const uint32_t s_p = smem_u32(smem + L::pb);
+    volatile int *abort_flag = &ms.abort;
 
     if (tid == 0) {
-        mbar_init(&ms.mma, 1);
+        mbar_init(&ms.k_full, kLoadThreads);
+        mbar_init(&ms.k_empty, 1);
+        mbar_init(&ms.done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.v_full[i], kLoadThreads);
+            mbar_init(&ms.v_empty[i], 1);
+            mbar_init(&ms.sc_full[i], kScaleThreads);
+            mbar_init(&ms.sc_empty[i], kSoftThreads);
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.s_empty[i], kSoftThreads);
+            mbar_init(&ms.p_full[i], kSoftThreads);
+            mbar_init(&ms.p_empty[i], 1);
+            mbar_init(&ms.o_full[i], 1);
+            mbar_init(&ms.o_empty[i], kSoftThreads);
+            mbar_init(&ms.q_full[i], 1);
+            mbar_init(&ms.q_empty[i], 1);
+            ms.st_any[i] = -1;
+            ms.st_sig[i] = 1.f;
+            ms.st_fs[i] = 1.f;
+        }
         ms.abort = 0;
         fence_mbar_init();
     }
-    if (w == 0) {
+    if (w == kMmaWarp) {
         tmem_alloc(&ms.tmem, kTmemCols);
         tmem_relinquish();
     }
-    if (w == 1) cursor_init_warp(p, ms.first, lane);
-    cta_sync();
+    if (w == kLoadWarps) cursor_init_warp(p, ms.first, lane);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     // the merge kernel may be scheduled now; it waits for this grid's results
     cudaTriggerProgrammaticLaunchCompletion();
     const uint32_t tmem = ms.tmem;
     const Cursor first = ms.first;
-    uint32_t mma_phase = 0;
-    auto wait_mma = [&]() {
-        if (!ms.abort && !mbar_wait(&ms.mma, mma_phase)) {
-            atomicExch(&ms.abort, 1);
+
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait(bar, parity)) {
+            *abort_flag = 1;
             raise_status(p, QSA_STATUS_TIMEOUT);
         }
-        mma_phase ^= 1;
-        tc_fence_after();
     };
 
-    // ---- resolve the first two groups (one per half of the threads)
-    OpIter rg; // the group being resolved (two ahead of the one computed)
-    op_init(p, rg, first);
-    {
-        OpIter g1 = rg;
-        if (g1.valid) op_next_group(p, g1);
-        const OpIter &mine = tid < kTile ? rg : g1;
-        for (int i = tid & (kTile - 1); i < kGroupCells; i += kTile) {
-            const int pos = resolve_list(p, mine, i);
-            const int slot = resolve_check(p, resolve_page(p, mine, pos));
-            if (mine.valid) ms.ring[mine.gi % kSlotRing][i] = slot;
-        }
-        rg = g1;
-        if (rg.valid) op_next_group(p, rg);
-    }
-    __syncthreads();
-
-    OpIter is, cs; // loads run one op ahead of the compute side
-    op_init(p, is, first);
-    op_init(p, cs, first);
-    OpRegs rr; // the rows of the next op to convert
-    if (is.valid) { load_op(p, ms, is, tid, rr); op_next(p, is); }
-    if (is.valid) prefetch_op(p, ms, is, tid);
-
-    int cur_bg = -1;
-    int r_pos = INT_MIN, r_raw = -1; // this thread's cell of the group being resolved
-    float sigma = 1.f, inv_sigma = 1.f;
-    for (uint32_t op = 0; cs.valid; ++op) {
-        const int t = cs.t;
-        const bool last_tile = t == cs.tiles - 1;
-        if (cs.kind == 0) {
-            // ---- scores of one K tile
-            if (t == 0) {
-                if (tid < kGroupCells) r_pos = resolve_list(p, rg, tid);
-                if (cs.gs == 0) {
-                    const int bg = cs.cur.b * p.G + cs.cur.g;
-                    if (bg != cur_bg) {
-                        load_queries(p, s_q, cs.cur.b, cs.cur.g, N, tid);
-                        cur_bg = bg;
-                    }
-                    if (tid < 64) {
-                        ms.row_mrun[tid] = -INFINITY;
-                        ms.row_lrun[tid] = 0.f;
-                    }
-                }
-            }
-            convert_op(rr, s_kv, tid);
-            if (tid < kTile) {
-                ms.cell_slot[t][tid] = ms.ring[cs.gi % kSlotRing][t * kTile + tid];
-                ms.cell_ks[t][tid] = rr.ks * p.scale_log2;
-                ms.cell_vs[t][tid] = rr.vs;
-            }
-            if (is.valid) {
-                load_op(p, ms, is, tid, rr);
-                op_next(p, is);
-                if (is.valid) prefetch_op(p, ms, is, tid);
-            }
-            fence_proxy_async_smem();
-            cta_sync();
-            if (tid == 0) {
+    if (w < kLoadWarps) {
+        // ================================================================ loaders
+        // Warp w covers the 16 tile rows (cells) R0 = 32(w%4) + 16(w/4) .. R0+15.
+        // K: thread t holds cells A = R0 + t/4 and B = A + 8 and, of each, the
+        // 32-byte pieces at bytes 32u and 128 + 32u (u = t%4): every warp load
+        // reads 8 whole 128-byte lines, and the pieces land in tensor memory by
+        // 16x256b stores (lanes t/4 and 8 + t/4, columns 8k + 2u, +1).
+        // V: thread t holds cells A' = R0 + t%8 and B' = A' + 8, pieces at
+        // 32v and 128 + 32v (v = t/8), so the 16-byte swizzled shared-memory
+        // stores of 8 consecutive threads hit 8 different bank groups.
+        const int R0 = 32 * (w & 3) + 16 * (w >> 2);
+        const int u = lane & 3, cA = R0 + (lane >> 2), cB = cA + 8;
+        const int vr = lane & 7, vu = lane >> 3, vA = R0 + vr, vB = vA + 8;
+        const int src_k = 4 * vr; // K-mapping thread holding the V rows' slots
+        const bool scl = u == 0;  // writes the scales of cells A and B, reports status
+        const uint32_t t_lane = (uint32_t)R0 << 16;
+        // pipeline stage info: bg = b * G + g, mt = cells of the tile (0 = no tile)
+        int bg0 = 0, bg1 = 0, bg2 = 0, bg3 = 0, bg4 = 0;
+        int mt0 = 0, mt1 = 0, mt2 = 0, mt3 = 0, mt4 = 0;
+        int selA3 = 0, selB3 = 0, selA4 = 0, selB4 = 0;
+        int pgA2 = -1, pgB2 = -1, pgA3 = -1, pgB3 = -1;
+        int slA0 = -1, slB0 = -1, slA1 = -1, slB1 = -1, slA2 = -1, slB2 = -1;
+        float ksA0 = 0.f, vsA0 = 0.f, ksB0 = 0.f, vsB0 = 0.f, ksA1 = 0.f, vsA1 = 0.f, ksB1 = 0.f, vsB1 = 0.f;
+        uint32_t rk[32], rv[32]; // K: A p0, A p1, B p0, B p1; V: A' p0, A' p1, B' p0, B' p1
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint64_t ad = smem_desc(s_kv + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(s_q + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_f16_ss(tmem + t * N, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&ms.mma);
-            }
-            wait_mma();
-            if (last_tile) {
-                // ---- max pass over the group, eight rows at a time: warp
-                // (qd, ch) owns cells 32qd..32qd+31 and rows ch*NH..ch*NH+NH-1
-                float vsabs = 0.f;
-                for (int tt = 0; tt < cs.tiles; ++tt)
-                    if (ms.cell_slot[tt][cell] >= 0) vsabs = fmaxf(vsabs, fabsf(ms.cell_vs[tt][cell]));
+        for (int e = 0; e < 32; ++e) rk[e] = rv[e] = 0u;
+        TileIt head;
+        tile_init(p, head, first);
+        for (int j = -4;; ++j) {
+            // ---- tile j -> tensor memory / shared memory; after each half, the
+            // registers it frees take tile j+1's rows (mostly L2 hits by now)
+            if (mt0) {
+                if (j >= 1) wait(&ms.k_empty, (uint32_t)(j - 1) & 1u);
+                tc_fence_after();
 #pragma unroll
-                for (int j0 = 0; j0 < NH; j0 += 8) {
-                    float mx[8];
+                for (int pc = 0; pc < 2; ++pc) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
-                    for (int tt = 0; tt < cs.tiles; ++tt) {
-                        float sv[8];
-                        tmem_ld8(tmem + t_lane + tt * N + ch * NH + j0, sv);
-                        tmem_wait_ld();
-                        const bool ok = ms.cell_slot[tt][cell] >= 0;
-                        const float ksc = ms.cell_ks[tt][cell];
+                    for (int hq = 0; hq < 2; ++hq) {
+                        uint32_t f[16];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], ok ? __fmul_rn(sv[j], ksc) : -INFINITY);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int key = __reduce_max_sync(0xffffffffu, ordered_key(mx[j]));
-                        if (lane == j) ms.red_max[ch][j0 + j][qd] = from_ordered_key(key);
+                        for (int k = 0; k < 4; ++k) {
+                            i8x4_to_f16x4(rk[8 * pc + 4 * hq + k], f[4 * k], f[4 * k + 1]);
+                            i8x4_to_f16x4(rk[16 + 8 * pc + 4 * hq + k], f[4 * k + 2], f[4 * k + 3]);
+                        }
+                        tmem_st_16x256b_x4(tmem + t_lane + kColK + 64u * pc + 32u * hq, f);
                     }
                 }
-                {
-                    const unsigned u = __reduce_max_sync(0xffffffffu, __float_as_uint(vsabs));
-                    if (lane == 0) ms.red_vs[w] = __uint_as_float(u);
-                }
-                // the group two ahead: its page-table reads go out now
-                if (tid < kGroupCells) r_raw = resolve_page(p, rg, r_pos);
-                cta_sync();
-                sigma = fmaxf(fmaxf(ms.red_vs[0], ms.red_vs[1]), fmaxf(ms.red_vs[2], ms.red_vs[3]));
-                if (!(sigma > 0.f)) sigma = 1.f;
-                inv_sigma = 1.f / sigma;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&ms.k_full);
+            } else if (j >= 0) {
+                break;
             }
-        } else {
-            // ---- P of one tile, then P.V
+            const size_t kvb1 = (size_t)bg1 * p.pool_cells;
+            if (mt1) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int sk = rr ? slB1 : slA1;
+#pragma unroll
+                    for (int pc = 0; pc < 2; ++pc) {
+                        if (sk >= 0) {
+                            ldg256_stream(p.k_pool + (kvb1 + sk) * kHeadDim + 128 * pc + 32 * u, rk + 16 * rr + 8 * pc);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) rk[16 * rr + 8 * pc + e] = 0u;
+                        }
+                    }
+                }
+            }
+            if (mt0) {
+                const int jb = j & 1;
+                if (scl) {
+                    if (j >= 2) wait(&ms.sc_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
+                    ms.sc_ks[jb][cA] = ksA0 * p.scale_log2;
+                    ms.sc_vs[jb][cA] = vsA0;
+                    ms.sc_ok[jb][cA] = slA0 >= 0;
+                    ms.sc_ks[jb][cB] = ksB0 * p.scale_log2;
+                    ms.sc_vs[jb][cB] = vsB0;
+                    ms.sc_ok[jb][cB] = slB0 >= 0;
+                    mbar_arrive(&ms.sc_full[jb]);
+                }
+                if (j >= 2) wait(&ms.v_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
+                uint8_t *sv = smem + L::v + (size_t)jb * kStageBytes;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int c = rr ? vB : vA;
+#pragma unroll
+                    for (int pc = 0; pc < 2; ++pc) {
+                        // 32 dims at byte 128pc + 32vu: d-block 2pc + vu/2, chunks 4(vu&1)..+3
+                        uint8_t *line = sv + (size_t)(2 * pc + (vu >> 1)) * 16384 + (c >> 3) * 1024 + (c & 7) * 128;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint4 v;
+                            i8x4_to_f16x4(rv[16 * rr + 8 * pc + 2 * i], v.x, v.y);
+                            i8x4_to_f16x4(rv[16 * rr + 8 * pc + 2 * i + 1], v.z, v.w);
+                            *reinterpret_cast<uint4 *>(line + (((4 * (vu & 1) + i) ^ (c & 7)) << 4)) = v;
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&ms.v_full[jb]);
+            }
             {
-                const bool ok = ms.cell_slot[t][cell] >= 0;
-                const float ksc = ms.cell_ks[t][cell];
-                const float vsn = ok ? ms.cell_vs[t][cell] * inv_sigma : 0.f;
+                const int va = __shfl_sync(0xffffffffu, slA1, src_k);
+                const int vb = __shfl_sync(0xffffffffu, slB1, src_k);
+                if (mt1) {
 #pragma unroll
-                for (int j0 = 0; j0 < NH; j0 += 8) {
-                    float sv[8], ls[8];
-                    tmem_ld8(tmem + t_lane + t * N + ch * NH + j0, sv);
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int sv2 = rr ? vb : va;
+#pragma unroll
+                        for (int pc = 0; pc < 2; ++pc) {
+                            if (sv2 >= 0) {
+                                ldg256_stream(p.v_pool + (kvb1 + sv2) * kHeadDim + 128 * pc + 32 * vu, rv + 16 * rr + 8 * pc);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) rv[16 * rr + 8 * pc + e] = 0u;
+                            }
+                        }
+                    }
+                    if (scl) {
+                        ksA1 = slA1 >= 0 ? __ldg(p.k_scale + kvb1 + slA1) : 0.f;
+                        vsA1 = slA1 >= 0 ? __ldg(p.v_scale + kvb1 + slA1) : 0.f;
+                        ksB1 = slB1 >= 0 ? __ldg(p.k_scale + kvb1 + slB1) : 0.f;
+                        vsB1 = slB1 >= 0 ? __ldg(p.v_scale + kvb1 + slB1) : 0.f;
+                    }
+                }
+            }
+            // ---- list entries of tile j+4
+            mt4 = 0;
+            if (head.valid) {
+                const int nc = tile_cells(head);
+                bg4 = head.cur.b * p.G + head.cur.g;
+                mt4 = nc;
+                const int base = tile_base(p, head);
+                selA4 = cA < nc ? __ldg(p.sel + base + cA) : 0;
+                selB4 = cB < nc ? __ldg(p.sel + base + cB) : 0;
+                tile_next(p, head);
+            }
+            // ---- page-table entries of tile j+3
+            if (mt3) {
+                const int b3 = bg3 / p.G, nc = mt3;
+                pgA3 = page_entry(p, b3, selA3, cA < nc);
+                pgB3 = page_entry(p, b3, selB3, cB < nc);
+            }
+            // ---- slots of tile j+2; its rows (and scales) prefetched into L2
+            if (mt2) {
+                slA2 = slot_of(p, pgA2, scl);
+                slB2 = slot_of(p, pgB2, scl);
+                const int sa = __shfl_sync(0xffffffffu, slA2, 4 * (lane & 7));
+                const int sb = __shfl_sync(0xffffffffu, slB2, 4 * (lane & 7));
+                const int sl = (lane & 8) ? sb : sa; // slot of cell R0 + lane%16
+                if (sl >= 0) {
+                    const size_t cell = (size_t)bg2 * p.pool_cells + sl;
+                    prefetch_l2(p.k_pool + cell * kHeadDim + 128 * (lane >> 4));
+                    prefetch_l2(p.v_pool + cell * kHeadDim + 128 * (lane >> 4));
+                }
+                if (scl) {
+                    const size_t kvb = (size_t)bg2 * p.pool_cells;
+                    if (slA2 >= 0) { prefetch_l2(p.k_scale + kvb + slA2); prefetch_l2(p.v_scale + kvb + slA2); }
+                    if (slB2 >= 0) { prefetch_l2(p.k_scale + kvb + slB2); prefetch_l2(p.v_scale + kvb + slB2); }
+                }
+            }
+            // shift the pipeline by one tile
+            bg0 = bg1; bg1 = bg2; bg2 = bg3; bg3 = bg4;
+            mt0 = mt1; mt1 = mt2; mt2 = mt3; mt3 = mt4;
+            slA0 = slA1; slB0 = slB1; ksA0 = ksA1; vsA0 = vsA1; ksB0 = ksB1; vsB0 = vsB1;
+            slA1 = slA2; slB1 = slB2; pgA2 = pgA3; pgB2 = pgB3; selA3 = selA4; selB3 = selB4;
+        }
+    } else if (w < kMmaWarp) {
+        // ================================================================ softmax
+        const int q = w & 3, c = 32 * q + lane;
+        const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+        struct Pend {
+            int b, g, c, cp, par;
+            bool on;
+        };
+        Pend pend{0, 0, 0, 0, 0, false};
+        float l_own = 0.f, l_fin = 0.f;
+        int cp = -1;
+        TileIt it;
+        tile_init(p, it, first);
+
+        // partials of the chunk that ended at the previous tile
+        auto epilogue = [&](const Pend &e) {
+            wait(&ms.o_full[e.cp & 1], (uint32_t)(e.cp >> 1) & 1u);
+            tc_fence_after();
+            const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R;
+            const float sig = ms.st_sig[e.par];
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
+                for (int r0 = 0; r0 < N; r0 += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + t_lane + kColO + 128u * (e.cp & 1) + 64u * hh + r0, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 q4 = *reinterpret_cast<const float4 *>(ms.red_max[ch][j0 + j]);
-                        const float m2 = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
-                        // the same rounded product as in the max pass (no FMA
-                        // contraction), so the max cell gets exactly 2^0 = 1
-                        const float pr = ok ? fast_exp2(__fmul_rn(sv[j], ksc) - m2) : 0.f;
-                        ls[j] = pr;
-                        const __half h = __float2half_rn(pr * vsn);
-                        sts16(s_p + kmajor_sw128_off(ch * NH + j0 + j, cell, N),
-                              *reinterpret_cast<const uint16_t *>(&h));
-                    }
-                    // reduce-scatter of the eight row sums over the warp's 32 cells:
-                    // lane pairs (4c, 4c+1, 4c+2, 4c+3) end with row j0 + c
-#pragma unroll
-                    for (int o = 16, cnt = 8; o >= 1; o >>= 1) {
-                        if (cnt > 1) {
-                            const int half = cnt / 2;
-                            const bool up = (lane & o) != 0;
-#pragma unroll
-                            for (int i = 0; i < half; ++i) {
-                                const float send = up ? ls[i] : ls[i + half];
-                                const float keep = up ? ls[i + half] : ls[i];
-                                ls[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                            }
-                            cnt = half;
-                        } else {
-                            ls[0] += __shfl_xor_sync(0xffffffffu, ls[0], o);
-                        }
-                    }
-                    if ((lane & 3) == 0) {
-                        float &acc = ms.red_sum[ch][j0 + (lane >> 2)][qd];
-                        acc = t == 0 ? ls[0] : acc + ls[0];
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int r = r0 + jj;
+                        if (r < p.R) p.part_o[(base + r) * kHeadDim + 128 * hh + c] = v[jj] * sig * ms.st_fin[r];
                     }
                 }
             }
-            convert_op(rr, s_kv, tid);
-            if (is.valid) {
-                load_op(p, ms, is, tid, rr);
-                op_next(p, is);
-                if (is.valid) prefetch_op(p, ms, is, tid);
+            tc_fence_before();
+            mbar_arrive(&ms.o_empty[e.cp & 1]);
+            if (c < p.R) {
+                p.part_m[base + c] = ms.st_mrun[e.par][c] * kLn2;
+                p.part_l[base + c] = l_fin * ms.st_fin[c];
             }
-            fence_proxy_async_smem();
-            cta_sync();
-            if (tid == 0) {
+        };
+
+        for (int i = 0; it.valid; ++i) {
+            const int par = i & 1;
+            const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
+            if (first_t) ++cp;
+            wait(&ms.sc_full[par], (uint32_t)(i >> 1) & 1u);
+            const bool ok = ms.sc_ok[par][c] != 0;
+            const float ks = ms.sc_ks[par][c], vs = ms.sc_vs[par][c];
+            mbar_arrive(&ms.sc_empty[par]);
+            wait(&ms.s_full[par], (uint32_t)(i >> 1) & 1u);
+            tc_fence_after();
+            const uint32_t sb = tmem + t_lane + kColS + 64u * par;
+            // ---- pass 1: tile max of every row
+#pragma unroll 1
+            for (int r0 = 0; r0 < N; r0 += 16) {
+                float v[16];
+                tmem_ld16(sb + r0, v);
+                tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t ad = smem_desc(s_kv + (2 * h) * (kTile * 128) + kk * 2048, kTile * 128, 1024);
-                        const uint64_t bd = smem_desc(s_p + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-                        mma_f16_ss(tmem + o_base + h * N, ad, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int jj = 0; jj < 16; ++jj) {
+                    // the same rounded product as in pass 2 (no FMA
+                    // contraction), so the max cell gets exactly 2^0 = 1
+                    const int key = __reduce_max_sync(0xffffffffu, ordered_key(ok ? __fmul_rn(v[jj], ks) : -INFINITY));
+                    if (lane == jj) ms.red_max[par][r0 + jj][q] = from_ordered_key(key);
+                }
+            }
+            {
+                const unsigned u = __reduce_max_sync(0xffffffffu, ok ? __float_as_uint(fabsf(vs)) : 0u);
+                if (lane == 0) ms.red_max[par][64][q] = __uint_as_float(u);
+            }
+            named_bar(kBarSoft, kSoftThreads);
+            // ---- per-row decisions (thread c owns row c)
+            if (c < N) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(ms.red_max[par][c]);
+                const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+                const float mo = ms.st_mrun[par ^ 1][c], mref = ms.st_mref[par ^ 1][c];
+                if (i >= 1) {
+                    const float4 s4 = *reinterpret_cast<const float4 *>(ms.red_sum[par ^ 1][c]);
+                    l_own += ((s4.x + s4.y) + s4.z) + s4.w;
+                }
+                if (pend.on) {
+                    l_fin = l_own;
+                    ms.st_fin[c] = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
+                }
+                float mrun_n, mref_n, fac;
+                if (first_t) {
+                    mrun_n = mref_n = mt;
+                    fac = 0.f;
+                } else {
+                    mrun_n = fmaxf(mo, mt);
+                    if (mref == -INFINITY) {
+                        mref_n = mrun_n; // nothing accumulated yet
+                        fac = 0.f;
+                    } else if (mrun_n > mref + kRescaleLog2) {
+                        mref_n = mrun_n;
+                        fac = fast_exp2(mref - mref_n);
+                        ms.st_any[par] = i;
+                    } else {
+                        mref_n = mref;
+                        fac = 1.f;
                     }
                 }
-                mma_commit(&ms.mma);
+                l_own *= fac;
+                ms.st_mrun[par][c] = mrun_n;
+                ms.st_mref[par][c] = mref_n;
+                ms.st_fac[c] = fac;
             }
-            wait_mma();
-            if (last_tile) {
-                // per-row group values and their combination with earlier groups
-                if (tid < N) {
-                    const int r = tid, hr = r / NH, jr = r % NH;
-                    const float4 m4 = *reinterpret_cast<const float4 *>(ms.red_max[hr][jr]);
-                    const float4 l4 = *reinterpret_cast<const float4 *>(ms.red_sum[hr][jr]);
-                    const float mg = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
-                    const float lg = ((l4.x + l4.y) + l4.z) + l4.w;
-                    const float mr = ms.row_mrun[r];
-                    const float mn = fmaxf(mr, mg);
-                    float fa = 0.f, fb = 0.f;
-                    if (mn > -INFINITY) {
-                        fa = mr == mn ? 1.f : (mr > -INFINITY ? fast_exp2(mr - mn) : 0.f);
-                        fb = mg == mn ? 1.f : (mg > -INFINITY ? fast_exp2(mg - mn) : 0.f);
-                    }
-                    ms.row_fa[r] = fa;
-                    ms.row_fb[r] = fb;
-                    ms.row_mrun[r] = mn;
-                    ms.row_lrun[r] = ms.row_lrun[r] * fa + lg * fb;
+            if (c == N) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(ms.red_max[par][64]);
+                const float st = fmaxf(fmaxf(g4.x, g4.y), fmaxf(g4.z, g4.w));
+                const float so = ms.st_sig[par ^ 1];
+                float sn = so, fs = 1.f;
+                if (first_t) {
+                    sn = st > 0.f ? st : 1.f;
+                } else if (st > so * kSigmaGrow) {
+                    sn = st;
+                    fs = so / st;
+                    ms.st_any[par] = i;
                 }
-                // the group two ahead: checked slots into the ring
-                if (tid < kGroupCells && rg.valid) ms.ring[rg.gi % kSlotRing][tid] = resolve_check(p, r_raw);
-                if (rg.valid) op_next_group(p, rg);
-                r_pos = INT_MIN;
-                r_raw = -1;
-                cta_sync();
-                // ---- fold the group's O into the chunk partial.  The first
-                // group writes it; a later group (chunks longer than 256
-                // cells) rescales the partial this thread wrote and adds.
-                {
-                    const int d = ch * 128 + 32 * qd + lane;
-                    const size_t base = (((size_t)cs.cur.b * p.G + cs.cur.g) * p.n_chunks + cs.cur.c) * p.R;
+                ms.st_sig[par] = sn;
+                ms.st_fs[par] = fs;
+            }
+            named_bar(kBarSoft, kSoftThreads);
+            const float vsn = ok ? vs / ms.st_sig[par] : 0.f;
+            const bool resc = ms.st_any[par] == i;
+            const int pbi = i % PB;
+            if (i >= PB) wait(&ms.p_empty[pbi], (uint32_t)((i - PB) / PB) & 1u);
+            uint8_t *p_tile = smem + L::pb + (size_t)pbi * N * 256;
+            // ---- pass 2: P' (f16, B operand of the P.V MMA) and row sums
+#pragma unroll 1
+            for (int r0 = 0; r0 < N; r0 += 16) {
+                float v[16];
+                tmem_ld16(sb + r0, v);
+                tmem_wait_ld();
+                if (r0 + 16 == N) {
+                    tc_fence_before();
+                    mbar_arrive(&ms.s_empty[par]);
+                }
+                float e[16];
+                const float4 *mr4 = reinterpret_cast<const float4 *>(&ms.st_mref[par][r0]);
+                const float4 ma = mr4[0], mb = mr4[1], mc = mr4[2], md = mr4[3];
+                const float mr[16] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w,
+                                      mc.x, mc.y, mc.z, mc.w, md.x, md.y, md.z, md.w};
 #pragma unroll
-                    for (int j0 = 0; j0 < N; j0 += 16) {
-                        float ov[16];
-                        tmem_ld16(tmem + t_lane + o_base + ch * N + j0, ov);
+                for (int jj = 0; jj < 16; ++jj) e[jj] = ok ? fast_exp2(__fmul_rn(v[jj], ks) - mr[jj]) : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const __half hv = __float2half_rn(e[jj] * vsn);
+                    *reinterpret_cast<__half *>(p_tile + kmajor_sw128_off(r0 + jj, c, N)) = hv;
+                }
+                // reduce-scatter of the 16 row sums over the warp's 32 cells:
+                // lanes 2k and 2k+1 end with row r0 + k
+                rs_stage<8>(e, lane, 16);
+                rs_stage<4>(e, lane, 8);
+                rs_stage<2>(e, lane, 4);
+                rs_stage<1>(e, lane, 2);
+                e[0] += __shfl_xor_sync(0xffffffffu, e[0], 1);
+                if ((lane & 1) == 0) ms.red_sum[par][r0 + (lane >> 1)][q] = e[0];
+            }
+            // ---- lazy rescale of the chunk's O (rows whose max moved, or sigma)
+            if (resc) {
+                if (PB == 2) wait(&ms.p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u); // P.V of tile i-1 done
+                tc_fence_after();
+                const float fs = ms.st_fs[par];
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
+                    for (int r0 = 0; r0 < N; r0 += 16) {
+                        const uint32_t ta = tmem + t_lane + kColO + 128u * (cp & 1) + 64u * hh + r0;
+                        float v[16];
+                        tmem_ld16(ta, v);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int r = j0 + i;
-                            if (r >= p.R) continue;
-                            float *dst = p.part_o + (base + r) * kHeadDim + d;
-                            float v = ov[i] * sigma * ms.row_fb[r];
-                            if (cs.gs > 0) v = fmaf(*dst, ms.row_fa[r], v);
-                            *dst = v;
-                        }
+                        for (int jj = 0; jj < 16; ++jj) v[jj] *= ms.st_fac[r0 + jj] * fs;
+                        tmem_st16(ta, v);
                     }
                 }
-                if (cs.gs + kGroupCells >= cs.nc && tid < p.R) {
-                    // ---- item epilogue: the chunk's max and denominator
-                    const size_t base = (((size_t)cs.cur.b * p.G + cs.cur.g) * p.n_chunks + cs.cur.c) * p.R;
-                    p.part_m[base + tid] = ms.row_mrun[tid] * kLn2;
-                    p.part_l[base + tid] = ms.row_lrun[tid];
-                }
-                cta_sync();
+                tmem_wait_st();
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&ms.p_full[pbi]);
+            if (pend.on) {
+                epilogue(pend);
+                pend.on = false;
+            }
+            if (last_t) pend = Pend{it.cur.b, it.cur.g, it.cur.c, cp, par, true};
+            tile_next(p, it);
         }
-        op_next(p, cs);
+        if (pend.on) {
+            named_bar(kBarSoft, kSoftThreads);
+            if (c < N) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(ms.red_sum[pend.par][c]);
+                l_own += ((s4.x + s4.y) + s4.z) + s4.w;
+                l_fin = l_own;
+                const float mo = ms.st_mrun[pend.par][c], mref = ms.st_mref[pend.par][c];
+                ms.st_fin[c] = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
+            }
+            named_bar(kBarSoft, kSoftThreads);
+            epilogue(pend);
+        }
+    } else {
+        // ================================================================ MMA warp
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
+            const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
+            struct PvT {
+                int i, cp;
+                bool first, last;
+            };
+            auto issue_pv = [&](const PvT &t) {
+                wait(&ms.p_full[t.i % PB], (uint32_t)(t.i / PB) & 1u);
+                wait(&ms.v_full[t.i & 1], (uint32_t)(t.i >> 1) & 1u);
+                if (t.first && t.cp >= 2) wait(&ms.o_empty[t.cp & 1], (uint32_t)((t.cp - 2) >> 1) & 1u);
+                tc_fence_after();
+                // descriptors built once; a K step only moves the start address
+                // (field [0,14) in 16-byte units, no carry for shared addresses)
+                const uint64_t ad0 = smem_desc(s_v + (uint32_t)(t.i & 1) * kStageBytes, 16384, 1024);
+                const uint64_t bd0 = smem_desc(s_p + (uint32_t)(t.i % PB) * N * 256u, 16, 1024);
+                const uint32_t d0 = tmem + kColO + 128u * (t.cp & 1);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    // the two d halves interleaved: independent accumulators
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint64_t ad = ad0 + (uint64_t)(((uint32_t)(2 * hh) * 16384u + (uint32_t)kk * 2048u) >> 4);
+                        const uint64_t bd = bd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
+                        mma_f16_ss(d0 + 64u * hh, ad, bd, idesc_o, (t.first && kk == 0) ? 0u : 1u);
+                    }
+                }
+                mma_commit(&ms.v_empty[t.i & 1]);
+                mma_commit(&ms.p_empty[t.i % PB]);
+                if (t.last) mma_commit(&ms.o_full[t.cp & 1]);
+            };
+            TileIt it;
+            tile_init(p, it, first);
+            // query tiles: one bulk copy per segment into buffer seg % 2; the
+            // first two now, segment s + 1 once segment s has started (its
+            // buffer was segment s - 1's, free after that segment's last QK)
+            auto load_q = [&](const Cursor &sc, int seg) {
+                const uint32_t bytes = (uint32_t)N * 512u;
+                mbar_arrive_expect_tx(&ms.q_full[seg & 1], bytes);
+                bulk_g2s(smem + L::q + (size_t)(seg & 1) * N * 512,
+                         static_cast<const uint8_t *>(p.q_img) + ((size_t)sc.b * p.G + sc.g) * N * 512, bytes,
+                         &ms.q_full[seg & 1]);
+            };
+            Cursor qnext = first;
+            int qseg = 0; // next segment whose tile is to be loaded
+            if (it.valid) {
+                cudaGridDependencySynchronize(); // the tiles come from the staging kernel
+                for (; qseg < 2 && qnext.remaining > 0; ++qseg) {
+                    load_q(qnext, qseg);
+                    qnext = next_segment(p, qnext);
+                }
+            }
+            int cp = -1, i = 0, cur_seg = -1;
+            PvT prev{0, 0, false, false};
+            for (; it.valid; ++i) {
+                const int seg = it.seg;
+                const bool seg_start = seg != cur_seg;
+                if (seg_start) wait(&ms.q_full[seg & 1], (uint32_t)(seg >> 1) & 1u);
+                cur_seg = seg;
+                wait(&ms.k_full, (uint32_t)i & 1u);
+                if (i >= 2) wait(&ms.s_empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u);
+                tc_fence_after();
+                const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg & 1) * N * 512u, 16, 1024);
+                const uint32_t sd = tmem + kColS + 64u * (i & 1);
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint64_t bd = qd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
+                    mma_f16_ts(sd, tmem + kColK + 8u * kk, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&ms.k_empty);
+                mma_commit(&ms.s_full[i & 1]);
+                const bool first_t = it.ti == 0;
+                if (first_t) ++cp;
+                if (i >= 1) issue_pv(prev);
+                prev = PvT{i, cp, first_t, it.ti == it.nt - 1};
+                tile_next(p, it);
+                if (!it.valid || it.seg != seg) mma_commit(&ms.q_empty[seg & 1]);
+                if (seg_start && seg >= 1 && qnext.remaining > 0) {
+                    wait(&ms.q_empty[(seg - 1) & 1], (uint32_t)((seg - 1) >> 1) & 1u);
+                    load_q(qnext, qseg);
+                    ++qseg;
+                    qnext = next_segment(p, qnext);
+                }
+            }
+            if (i >= 1) issue_pv(prev);
+            mma_commit(&ms.done);
+            wait(&ms.done, 0);
+        }
+        __syncwarp();
     }
-    cta_sync();
-    if (w == 0) tmem_dealloc(tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (w == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int N>
 cudaError_t launch_n(const Params &p, cudaStream_t stream)
 {
-    int dev = 0, sms = 0, max_smem = 0, sm_smem = 0;
+    int dev = 0, sms = 0, max_smem = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    if ((e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
-        return e;
-    const uint32_t bytes = make_layout(N).total + 1024;
+    const uint32_t bytes = Lay<N>::total + 1024;
     if ((int)bytes > max_smem) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)bytes)) != cudaSuccess)
         return e;
-    // two CTAs per SM when their shared memory fits (1 KB per CTA is reserved)
-    const int per_sm = 2 * ((int)bytes + 1024) <= sm_smem ? 2 : 1;
+    const long long pieces = (long long)p.n_seq * p.G * N * 32;
+    qsa_query_stage_kernel<N><<<(unsigned)((pieces + 255) / 256), 256, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long items = (long long)p.n_seq * p.G * p.n_chunks;
-    const long long slots = (long long)sms * per_sm;
-    const int grid = (int)(items < slots ? items : slots);
-    qsa_chunk_tc_kernel<N><<<grid, kThreads, bytes, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qsa_chunk_tc_kernel<N>, p);
 }
 
 } // namespace
 
 bool chunk_tc_supports(const Params &p) { return p.R <= 64; }
+
+size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
+{
+    const size_t N = (size_t)(R + 15) / 16 * 16;
+    return (size_t)n_seq * G * N * 512;
+}
 
 cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream)
 {

@@ -35,6 +35,7 @@ struct Params {
     float *part_l;
     float *part_o;             // [n_seq][G][n_chunks][R][D]
     uint32_t *status;          // optional
+    void *q_img;               // decode tensor-core path: [n_seq][G] f16 query tiles (workspace)
     int32_t n_sel_single;      // list length when sel_offsets == nullptr
     int32_t n_seq, G, H, T, R; // R = T*H rows per KV head
     int32_t pool_cells, page_table_len, chunk_cells, n_chunks, max_selected;
@@ -132,6 +133,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_chunk_simt(const Params &p, cudaStream_t stream);
 bool chunk_tc_supports(const Params &p);
+size_t chunk_tc_query_image_bytes(int n_seq, int G, int R);
 cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream);
 bool prompt_tc_supports(const Params &p);
 size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks, size_t *k_bytes,

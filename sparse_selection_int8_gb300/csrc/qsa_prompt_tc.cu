@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     }
     // bulk copies still in flight after a timeout must land before exit
     if (tid == 0 && ms.abort) {
-        mbar_wait(&ms.bar_k, n_tiles & 1, 1u << 22);
-        mbar_wait(&ms.bar_v, n_tiles & 1, 1u << 22);
+        mbar_wait(&ms.bar_k, n_tiles & 1, 1ll << 26);
+        mbar_wait(&ms.bar_v, n_tiles & 1, 1ll << 26);
     }
     tc_fence_before();
     __syncthreads();

@@ -41,25 +41,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+// Test for completion of phase `parity`; a thread whose phase is not yet
+// complete is suspended for up to `suspend_ns` (woken earlier when the phase
+// completes), so waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t suspend_ns)
 {
     uint32_t ok;
     asm volatile("{\n .reg .pred p;\n"
-                 " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
                  " selp.u32 %0, 1, 0, p;\n}"
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
                  : "memory");
     return ok != 0;
 }
 
-// Bounded wait on phase `parity`; false when the spin limit ran out.
+// Bounded wait on phase `parity`: false once about `max_cycles` SM clock
+// cycles (default 2^32, about two seconds) have passed without completion.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          uint32_t max_spins = (1u << 26))
+                                          long long max_cycles = (1ll << 32))
 {
-    for (uint32_t i = 0; i < max_spins; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity, 200000u))
+        if (clock64() - t0 > max_cycles) return false;
+    return true;
 }
 
 // ------------------------------------------------------------- bulk copies
@@ -148,6 +154,17 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem]^T: A (M rows in M lanes, K packed two
+// 16-bit values per 32-bit column) read from tensor memory at `a_tmem`.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
@@ -206,7 +223,62 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v)
                  : "memory");
 }
 
+// registers -> 32 lanes x 32-bit, 16 consecutive columns per thread (raw bits).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                   "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                   "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
+// registers -> 16 lanes x 256 bits, four repetitions (32 columns).  Thread
+// t writes lanes base + t/4 (v[4k], v[4k+1]) and base + 8 + t/4 (v[4k+2],
+// v[4k+3]) at columns 8k + 2(t%4) and 8k + 2(t%4) + 1, k = 0..3.
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                   "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                   "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------- misc
+
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), no registers held.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// 32-byte read-only global load that does not allocate in L1 (streamed data).
+__device__ __forceinline__ void ldg256_stream(const void *ptr, uint32_t *r)
+{
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "l"(ptr));
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *ptr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
 
 // ------------------------------------------------------------- layouts
 
