@@ -80,8 +80,8 @@ struct Misc {
     float sc_ks[2][kTile];   // k_scale * softmax_scale * log2(e) per cell
     float sc_vs[2][kTile];   // v_scale per cell
     uint8_t sc_ok[2][kTile]; // cell holds a valid slot
-    __align__(16) float red_max[2][65][4]; // [tile parity][row; 64 = |v_scale| max][lane quadrant]
-    __align__(16) float red_sum[2][64][4];
+    __align__(16) float red_max[2][4][68]; // [tile parity][warp quadrant][row; 64 = |v_scale| max]
+    __align__(16) float red_sum[2][4][64];
     float st_mrun[2][64];    // running max (log2 units) after the tile of that parity
     __align__(16) float st_mref[2][64]; // reference max the tile's P' were formed against
     float st_fac[64];        // O/l factor of the current tile
@@ -618,6 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     } else if (w < kMmaWarp) {
         // ================================================================ softmax
         const int q = w & 3, c = 32 * q + lane;
+        const int u = lane & 3, ra = lane >> 2; // 16x256b: rows 8k + 2u + e, cells 32q + 8i + ra
+        constexpr int NK = N / 8;               // 16x256b repetitions over the score columns
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
         struct Pend {
             int b, g, c, cp, par;
@@ -662,40 +664,72 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
             if (first_t) ++cp;
             wait(&ms.sc_full[par], (uint32_t)(i >> 1) & 1u);
-            const bool ok = ms.sc_ok[par][c] != 0;
-            const float ks = ms.sc_ks[par][c], vs = ms.sc_vs[par][c];
+            // this thread's four cells (16x256b layout): cell(i) = 32q + 8i + t/4,
+            // i = 2L + B for lane group L (lanes +16) and row half B (+8)
+            float ksc[4], vsc[4];
+            bool okc[4];
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+                const int cc = 32 * q + 8 * ci + ra;
+                okc[ci] = ms.sc_ok[par][cc] != 0;
+                ksc[ci] = ms.sc_ks[par][cc];
+                vsc[ci] = ms.sc_vs[par][cc];
+            }
             mbar_arrive(&ms.sc_empty[par]);
             wait(&ms.s_full[par], (uint32_t)(i >> 1) & 1u);
             tc_fence_after();
-            const uint32_t sb = tmem + t_lane + kColS + 64u * par;
-            // ---- pass 1: tile max of every row
-#pragma unroll 1
-            for (int r0 = 0; r0 < N; r0 += 16) {
-                float v[16];
-                tmem_ld16(sb + r0, v);
-                tmem_wait_ld();
+            // scores: x[L][4k + 2B + e] = cell 2L+B, row 8k + 2u + e (log2 units)
+            float x[2][4 * NK];
+            tmem_ld_16x256b<NK>(tmem + ((uint32_t)(32 * q) << 16) + kColS + 64u * par, x[0]);
+            tmem_ld_16x256b<NK>(tmem + ((uint32_t)(32 * q + 16) << 16) + kColS + 64u * par, x[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&ms.s_empty[par]); // the scores live in registers from here on
+            // ---- pass 1: tile max of every row.  The same rounded product is
+            // used in pass 2 (no FMA contraction), so the max cell gets 2^0 = 1.
+            float mrow[2 * NK];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    // the same rounded product as in pass 2 (no FMA
-                    // contraction), so the max cell gets exactly 2^0 = 1
-                    const int key = __reduce_max_sync(0xffffffffu, ordered_key(ok ? __fmul_rn(v[jj], ks) : -INFINITY));
-                    if (lane == jj) ms.red_max[par][r0 + jj][q] = from_ordered_key(key);
+            for (int k = 0; k < NK; ++k) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float m = -INFINITY;
+#pragma unroll
+                    for (int L = 0; L < 2; ++L) {
+#pragma unroll
+                        for (int B = 0; B < 2; ++B) {
+                            const int ci = 2 * L + B;
+                            float &xv = x[L][4 * k + 2 * B + e];
+                            xv = okc[ci] ? __fmul_rn(xv, ksc[ci]) : -INFINITY;
+                            m = fmaxf(m, xv);
+                        }
+                    }
+                    mrow[2 * k + e] = m;
                 }
             }
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+#pragma unroll
+                for (int jr = 0; jr < 2 * NK; ++jr) mrow[jr] = fmaxf(mrow[jr], __shfl_xor_sync(0xffffffffu, mrow[jr], o));
+            }
+#pragma unroll
+            for (int k = 0; k < NK; ++k)
+                if (ra == k) *reinterpret_cast<float2 *>(&ms.red_max[par][q][8 * k + 2 * u]) = make_float2(mrow[2 * k], mrow[2 * k + 1]);
             {
-                const unsigned u = __reduce_max_sync(0xffffffffu, ok ? __float_as_uint(fabsf(vs)) : 0u);
-                if (lane == 0) ms.red_max[par][64][q] = __uint_as_float(u);
+                float va = 0.f;
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) va = fmaxf(va, okc[ci] ? fabsf(vsc[ci]) : 0.f);
+                const unsigned uu = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
+                if (lane == 0) ms.red_max[par][q][64] = __uint_as_float(uu);
             }
             named_bar(kBarSoft, kSoftThreads);
             // ---- per-row decisions (thread c owns row c)
             if (c < N) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(ms.red_max[par][c]);
-                const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+                const float mt = fmaxf(fmaxf(ms.red_max[par][0][c], ms.red_max[par][1][c]),
+                                       fmaxf(ms.red_max[par][2][c], ms.red_max[par][3][c]));
                 const float mo = ms.st_mrun[par ^ 1][c], mref = ms.st_mref[par ^ 1][c];
-                if (i >= 1) {
-                    const float4 s4 = *reinterpret_cast<const float4 *>(ms.red_sum[par ^ 1][c]);
-                    l_own += ((s4.x + s4.y) + s4.z) + s4.w;
-                }
+                if (i >= 1)
+                    l_own += ((ms.red_sum[par ^ 1][0][c] + ms.red_sum[par ^ 1][1][c]) + ms.red_sum[par ^ 1][2][c]) +
+                             ms.red_sum[par ^ 1][3][c];
                 if (pend.on) {
                     l_fin = l_own;
                     ms.st_fin[c] = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
@@ -724,8 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 ms.st_fac[c] = fac;
             }
             if (c == N) {
-                const float4 g4 = *reinterpret_cast<const float4 *>(ms.red_max[par][64]);
-                const float st = fmaxf(fmaxf(g4.x, g4.y), fmaxf(g4.z, g4.w));
+                const float st = fmaxf(fmaxf(ms.red_max[par][0][64], ms.red_max[par][1][64]),
+                                       fmaxf(ms.red_max[par][2][64], ms.red_max[par][3][64]));
                 const float so = ms.st_sig[par ^ 1];
                 float sn = so, fs = 1.f;
                 if (first_t) {
@@ -739,42 +773,49 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 ms.st_fs[par] = fs;
             }
             named_bar(kBarSoft, kSoftThreads);
-            const float vsn = ok ? vs / ms.st_sig[par] : 0.f;
+            const float inv_sig = 1.f / ms.st_sig[par];
             const bool resc = ms.st_any[par] == i;
             const int pbi = i % PB;
             if (i >= PB) wait(&ms.p_empty[pbi], (uint32_t)((i - PB) / PB) & 1u);
             uint8_t *p_tile = smem + L::pb + (size_t)pbi * N * 256;
-            // ---- pass 2: P' (f16, B operand of the P.V MMA) and row sums
-#pragma unroll 1
-            for (int r0 = 0; r0 < N; r0 += 16) {
-                float v[16];
-                tmem_ld16(sb + r0, v);
-                tmem_wait_ld();
-                if (r0 + 16 == N) {
-                    tc_fence_before();
-                    mbar_arrive(&ms.s_empty[par]);
-                }
-                float e[16];
-                const float4 *mr4 = reinterpret_cast<const float4 *>(&ms.st_mref[par][r0]);
-                const float4 ma = mr4[0], mb = mr4[1], mc = mr4[2], md = mr4[3];
-                const float mr[16] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w,
-                                      mc.x, mc.y, mc.z, mc.w, md.x, md.y, md.z, md.w};
+            // ---- pass 2: P' = f16(p * v_scale / sigma) into the B operand of
+            // the P.V MMA (K-major [rows][cells]), and row sums
+            float lrow[2 * NK], mref_r[2 * NK];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) e[jj] = ok ? fast_exp2(__fmul_rn(v[jj], ks) - mr[jj]) : 0.f;
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const __half hv = __float2half_rn(e[jj] * vsn);
-                    *reinterpret_cast<__half *>(p_tile + kmajor_sw128_off(r0 + jj, c, N)) = hv;
-                }
-                // reduce-scatter of the 16 row sums over the warp's 32 cells:
-                // lanes 2k and 2k+1 end with row r0 + k
-                rs_stage<8>(e, lane, 16);
-                rs_stage<4>(e, lane, 8);
-                rs_stage<2>(e, lane, 4);
-                rs_stage<1>(e, lane, 2);
-                e[0] += __shfl_xor_sync(0xffffffffu, e[0], 1);
-                if ((lane & 1) == 0) ms.red_sum[par][r0 + (lane >> 1)][q] = e[0];
+            for (int k = 0; k < NK; ++k) {
+                // reference maxima of this thread's rows, read once (the P'
+                // stores below could otherwise force re-reads)
+                const float2 m2 = *reinterpret_cast<const float2 *>(&ms.st_mref[par][8 * k + 2 * u]);
+                mref_r[2 * k] = m2.x;
+                mref_r[2 * k + 1] = m2.y;
+                lrow[2 * k] = lrow[2 * k + 1] = 0.f;
             }
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+                const int cc = 32 * q + 8 * ci + ra;
+                const float vsn = okc[ci] ? vsc[ci] * inv_sig : 0.f;
+                const int L = ci >> 1, B = ci & 1;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    // element (row 8k + 2u + e, cell cc) at pe + 1024k
+                    const int r7 = 2 * u + e;
+                    uint8_t *pe = p_tile + (cc >> 6) * N * 128 + r7 * 128 + ((((cc & 63) >> 3) ^ r7) << 4) + (cc & 7) * 2;
+#pragma unroll
+                    for (int k = 0; k < NK; ++k) {
+                        const float pr = okc[ci] ? fast_exp2(x[L][4 * k + 2 * B + e] - mref_r[2 * k + e]) : 0.f;
+                        lrow[2 * k + e] += pr;
+                        *reinterpret_cast<__half *>(pe + 1024 * k) = __float2half_rn(pr * vsn);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+#pragma unroll
+                for (int jr = 0; jr < 2 * NK; ++jr) lrow[jr] += __shfl_xor_sync(0xffffffffu, lrow[jr], o);
+            }
+#pragma unroll
+            for (int k = 0; k < NK; ++k)
+                if (ra == k) *reinterpret_cast<float2 *>(&ms.red_sum[par][q][8 * k + 2 * u]) = make_float2(lrow[2 * k], lrow[2 * k + 1]);
             // ---- lazy rescale of the chunk's O (rows whose max moved, or sigma)
             if (resc) {
                 if (PB == 2) wait(&ms.p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u); // P.V of tile i-1 done
@@ -808,8 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         if (pend.on) {
             named_bar(kBarSoft, kSoftThreads);
             if (c < N) {
-                const float4 s4 = *reinterpret_cast<const float4 *>(ms.red_sum[pend.par][c]);
-                l_own += ((s4.x + s4.y) + s4.z) + s4.w;
+                l_own += ((ms.red_sum[pend.par][0][c] + ms.red_sum[pend.par][1][c]) + ms.red_sum[pend.par][2][c]) +
+                         ms.red_sum[pend.par][3][c];
                 l_fin = l_own;
                 const float mo = ms.st_mrun[pend.par][c], mref = ms.st_mref[pend.par][c];
                 ms.st_fin[c] = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;

@@ -208,6 +208,43 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 lanes x 256 bits per repetition, loaded: thread t gets lanes base + t/4
+// (v[4k], v[4k+1]) and base + 8 + t/4 (v[4k+2], v[4k+3]) at columns
+// 8k + 2(t%4) and 8k + 2(t%4) + 1 of repetition k.
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, float *v)
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, float *v)
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// NK repetitions (NK in {2, 4, 6, 8}) starting at taddr's column.
+template <int NK>
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, float *v)
+{
+    if constexpr (NK >= 4) {
+        tmem_ld_16x256b_x4(taddr, v);
+        if constexpr (NK >= 8) tmem_ld_16x256b_x4(taddr + 32, v + 16);
+        else if constexpr (NK == 6) tmem_ld_16x256b_x2(taddr + 32, v + 16);
+    } else {
+        tmem_ld_16x256b_x2(taddr, v);
+    }
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // registers -> 32 lanes x 32-bit, 16 consecutive columns per thread.
