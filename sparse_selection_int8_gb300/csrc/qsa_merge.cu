@@ -5,23 +5,29 @@
 // of a row carries (m_c, l_c, o_c) with m in natural-log units; the merge is
 //   M = max_{c: l_c > 0} m_c,  L = sum_c l_c e^{m_c - M},
 //   out = sum_c o_c e^{m_c - M} / L   (zeros when no chunk holds a cell).
-// One warp per query row: lane k owns output dimensions 8k..8k+7.  The
-// lanes read the chunks' (m, l) pairs 32 at a time, form the weights
-// e^{m_c - M} once, and broadcast them by shuffle while every lane sums its
-// eight dimensions over the chunks with independent 16-byte loads.  All sums
-// run in a fixed order (ascending chunks; a fixed shuffle tree for L), so the
-// result is deterministic.
+// A CTA of four warps covers four query rows with one warp each when a row
+// has at most four chunks, or one row with all four warps otherwise (warp w
+// takes chunks w, w+4, ...).  Lane k owns output dimensions 8k..8k+7.  Each
+// warp forms its own (M_w, L_w, acc_w) with the chunk weights computed once
+// per chunk by one lane and broadcast by shuffle, and independent 16-byte
+// loads of o; with four warps per row their results are then combined in
+// shared memory.  Every sum runs in a fixed order, so the output is
+// bit-identical from run to run.
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
+constexpr int kMergeWarps = 4;
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) qsa_merge_kernel(const Params p)
+template <int WPR> // warps per row: 1 or kMergeWarps
+__global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Params p)
 {
+    __shared__ float s_acc[kMergeWarps][kHeadDim];
+    __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
     const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int w = WPR == 1 ? 0 : threadIdx.x >> 5; // this warp's first chunk
+    const int r = WPR == 1 ? blockIdx.x * kMergeWarps + (threadIdx.x >> 5) : blockIdx.x;
     const int g = blockIdx.y;
     const int b = blockIdx.z;
     // launched as a programmatic dependent of the chunk kernel: wait until
@@ -33,10 +39,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qsa_merge_kernel(const Pa
     const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
     const size_t base = ((size_t)b * p.G + g) * p.n_chunks * p.R + r;
     const size_t stride = (size_t)p.R; // chunk stride of m and l
+    const int mine = n_chunks > w ? (n_chunks - w + WPR - 1) / WPR : 0; // chunks of this warp
 
     float M = -INFINITY;
-    for (int c = lane; c < n_chunks; c += 32) {
-        const size_t idx = base + (size_t)c * stride;
+    for (int i = lane; i < mine; i += 32) {
+        const size_t idx = base + (size_t)(w + WPR * i) * stride;
         if (p.part_l[idx] > 0.f) M = fmaxf(M, p.part_m[idx]);
     }
 #pragma unroll
@@ -45,19 +52,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qsa_merge_kernel(const Pa
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float Lpart = 0.f;
     if (M > -INFINITY) {
-        for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-            const int cnt = min(32, n_chunks - c0);
+        const size_t ostride = WPR * stride * kHeadDim; // between this warp's chunks
+        for (int i0 = 0; i0 < mine; i0 += 32) {
+            const int cnt = min(32, mine - i0);
             float wgt = 0.f;
             if (lane < cnt) {
-                const size_t idx = base + (size_t)(c0 + lane) * stride;
+                const size_t idx = base + (size_t)(w + WPR * (i0 + lane)) * stride;
                 const float lc = p.part_l[idx];
                 if (lc > 0.f) {
                     wgt = expf(p.part_m[idx] - M);
                     Lpart = fmaf(lc, wgt, Lpart);
                 }
             }
-            const float *o = p.part_o + (base + (size_t)c0 * stride) * kHeadDim + lane * 8;
-            const size_t ostride = stride * kHeadDim;
+            const float *o = p.part_o + (base + (size_t)(w + WPR * i0) * stride) * kHeadDim + lane * 8;
             int c = 0;
             for (; c + 4 <= cnt; c += 4) {
                 float4 v[8];
@@ -97,26 +104,57 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qsa_merge_kernel(const Pa
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Lpart += __shfl_xor_sync(0xffffffffu, Lpart, o);
-    const float L = Lpart;
     const int t = r / p.H, j = r % p.H;
-    float4 *dst = reinterpret_cast<float4 *>(
-        p.out + (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim + lane * 8);
-    if (L > 0.f) {
-        dst[0] = make_float4(acc[0] / L, acc[1] / L, acc[2] / L, acc[3] / L);
-        dst[1] = make_float4(acc[4] / L, acc[5] / L, acc[6] / L, acc[7] / L);
-    } else {
-        dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float *orow = p.out + (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim;
+    if (WPR == 1) {
+        float4 *dst = reinterpret_cast<float4 *>(orow + lane * 8);
+        const float L = Lpart;
+        if (L > 0.f) {
+            dst[0] = make_float4(acc[0] / L, acc[1] / L, acc[2] / L, acc[3] / L);
+            dst[1] = make_float4(acc[4] / L, acc[5] / L, acc[6] / L, acc[7] / L);
+        } else {
+            dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
     }
+    *reinterpret_cast<float4 *>(&s_acc[w][lane * 8]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(&s_acc[w][lane * 8 + 4]) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (lane == 0) {
+        s_m[w] = M;
+        s_l[w] = Lpart;
+    }
+    __syncthreads();
+
+    // combine the warps' results (fixed order); thread t owns dimensions 2t, 2t+1
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < kMergeWarps; ++x)
+        if (s_l[x] > 0.f) Mt = fmaxf(Mt, s_m[x]);
+    float L = 0.f, o0 = 0.f, o1 = 0.f;
+    if (Mt > -INFINITY) {
+#pragma unroll
+        for (int x = 0; x < kMergeWarps; ++x) {
+            if (!(s_l[x] > 0.f)) continue;
+            const float f = s_m[x] == Mt ? 1.f : expf(s_m[x] - Mt);
+            L = fmaf(s_l[x], f, L);
+            o0 = fmaf(s_acc[x][2 * threadIdx.x], f, o0);
+            o1 = fmaf(s_acc[x][2 * threadIdx.x + 1], f, o1);
+        }
+    }
+    float2 *dst = reinterpret_cast<float2 *>(orow + 2 * threadIdx.x);
+    *dst = L > 0.f ? make_float2(o0 / L, o1 / L) : make_float2(0.f, 0.f);
 }
 
 } // namespace
 
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
+    // one warp per row when rows have few chunks, four otherwise
+    const bool wide = p.n_chunks > kMergeWarps;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.R + kWarpsPerBlock - 1) / kWarpsPerBlock), (unsigned)p.G, (unsigned)p.n_seq);
-    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.gridDim = dim3((unsigned)(wide ? p.R : (p.R + kMergeWarps - 1) / kMergeWarps), (unsigned)p.G, (unsigned)p.n_seq);
+    cfg.blockDim = dim3(kMergeWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -124,7 +162,8 @@ cudaError_t launch_merge(const Params &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel, p);
+    return wide ? cudaLaunchKernelEx(&cfg, qsa_merge_kernel<kMergeWarps>, p)
+                : cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1>, p);
 }
 
 } // namespace qsa
