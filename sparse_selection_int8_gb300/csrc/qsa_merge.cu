@@ -8,11 +8,10 @@
 // A CTA of four warps covers four query rows with one warp each when a row
 // has at most four chunks, or one row with all four warps otherwise (warp w
 // takes chunks w, w+4, ...).  Lane k owns output dimensions 8k..8k+7.  Each
-// warp forms its own (M_w, L_w, acc_w) with the chunk weights computed once
-// per chunk by one lane and broadcast by shuffle, and independent 16-byte
-// loads of o; with four warps per row their results are then combined in
-// shared memory.  Every sum runs in a fixed order, so the output is
-// bit-identical from run to run.
+// warp forms its own (M_w, L_w, acc_w), four chunks at a time with all their
+// loads in flight together and a running maximum; with four warps per row
+// their results are then combined in shared memory.  Every sum runs in a
+// fixed order, so the output is bit-identical from run to run.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -34,76 +33,63 @@ __global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Param
     // that grid has finished and its partials are visible
     cudaGridDependencySynchronize();
     if (r >= p.R) return;
-    int start, n;
-    seq_range(p, b, &start, &n);
-    const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
     const size_t base = ((size_t)b * p.G + g) * p.n_chunks * p.R + r;
     const size_t stride = (size_t)p.R; // chunk stride of m and l
-    const int mine = n_chunks > w ? (n_chunks - w + WPR - 1) / WPR : 0; // chunks of this warp
-
-    float M = -INFINITY;
-    for (int i = lane; i < mine; i += 32) {
-        const size_t idx = base + (size_t)(w + WPR * i) * stride;
-        if (p.part_l[idx] > 0.f) M = fmaxf(M, p.part_m[idx]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
+    // chunks are taken four at a time with every load of a group issued
+    // together (the list length is only needed to mask the group, so its
+    // read overlaps the first group's), combined with a running maximum
+    int start, n;
+    seq_range(p, b, &start, &n);
+    float M = -INFINITY, Lpart = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float Lpart = 0.f;
-    if (M > -INFINITY) {
-        const size_t ostride = WPR * stride * kHeadDim; // between this warp's chunks
-        for (int i0 = 0; i0 < mine; i0 += 32) {
-            const int cnt = min(32, mine - i0);
-            float wgt = 0.f;
-            if (lane < cnt) {
-                const size_t idx = base + (size_t)(w + WPR * (i0 + lane)) * stride;
-                const float lc = p.part_l[idx];
-                if (lc > 0.f) {
-                    wgt = expf(p.part_m[idx] - M);
-                    Lpart = fmaf(lc, wgt, Lpart);
-                }
-            }
-            const float *o = p.part_o + (base + (size_t)(w + WPR * i0) * stride) * kHeadDim + lane * 8;
-            int c = 0;
-            for (; c + 4 <= cnt; c += 4) {
-                float4 v[8];
+    for (int c0 = w; c0 < p.n_chunks; c0 += 4 * WPR) {
+        float mu[4], lu[4];
+        float4 ou[4][2];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)(c + u) * ostride);
-                    v[2 * u] = src[0];
-                    v[2 * u + 1] = src[1];
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float wu = __shfl_sync(0xffffffffu, wgt, c + u);
-                    acc[0] = fmaf(v[2 * u].x, wu, acc[0]);
-                    acc[1] = fmaf(v[2 * u].y, wu, acc[1]);
-                    acc[2] = fmaf(v[2 * u].z, wu, acc[2]);
-                    acc[3] = fmaf(v[2 * u].w, wu, acc[3]);
-                    acc[4] = fmaf(v[2 * u + 1].x, wu, acc[4]);
-                    acc[5] = fmaf(v[2 * u + 1].y, wu, acc[5]);
-                    acc[6] = fmaf(v[2 * u + 1].z, wu, acc[6]);
-                    acc[7] = fmaf(v[2 * u + 1].w, wu, acc[7]);
-                }
-            }
-            for (; c < cnt; ++c) {
-                const float wu = __shfl_sync(0xffffffffu, wgt, c);
-                const float4 *src = reinterpret_cast<const float4 *>(o + (size_t)c * ostride);
-                const float4 a = src[0], b4 = src[1];
-                acc[0] = fmaf(a.x, wu, acc[0]);
-                acc[1] = fmaf(a.y, wu, acc[1]);
-                acc[2] = fmaf(a.z, wu, acc[2]);
-                acc[3] = fmaf(a.w, wu, acc[3]);
-                acc[4] = fmaf(b4.x, wu, acc[4]);
-                acc[5] = fmaf(b4.y, wu, acc[5]);
-                acc[6] = fmaf(b4.z, wu, acc[6]);
-                acc[7] = fmaf(b4.w, wu, acc[7]);
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * WPR;
+            mu[u] = -INFINITY;
+            lu[u] = 0.f;
+            if (c < p.n_chunks) {
+                const size_t idx = base + (size_t)c * stride;
+                mu[u] = p.part_m[idx];
+                lu[u] = p.part_l[idx];
+                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * kHeadDim + lane * 8);
+                ou[u][0] = src[0];
+                ou[u][1] = src[1];
             }
         }
-    }
+        const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
+        bool ok[4];
+        float gm = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lpart += __shfl_xor_sync(0xffffffffu, Lpart, o);
+        for (int u = 0; u < 4; ++u) {
+            ok[u] = c0 + u * WPR < n_chunks && lu[u] > 0.f;
+            if (ok[u]) gm = fmaxf(gm, mu[u]);
+        }
+        if (gm > M) {
+            const float f = M == -INFINITY ? 0.f : expf(M - gm);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= f;
+            Lpart *= f;
+            M = gm;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!ok[u]) continue;
+            const float wu = mu[u] == M ? 1.f : expf(mu[u] - M);
+            Lpart = fmaf(lu[u], wu, Lpart);
+            acc[0] = fmaf(ou[u][0].x, wu, acc[0]);
+            acc[1] = fmaf(ou[u][0].y, wu, acc[1]);
+            acc[2] = fmaf(ou[u][0].z, wu, acc[2]);
+            acc[3] = fmaf(ou[u][0].w, wu, acc[3]);
+            acc[4] = fmaf(ou[u][1].x, wu, acc[4]);
+            acc[5] = fmaf(ou[u][1].y, wu, acc[5]);
+            acc[6] = fmaf(ou[u][1].z, wu, acc[6]);
+            acc[7] = fmaf(ou[u][1].w, wu, acc[7]);
+        }
+        if (c0 + 4 * WPR >= n_chunks) break;
+    }
     const int t = r / p.H, j = r % p.H;
     float *orow = p.out + (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim;
     if (WPR == 1) {
