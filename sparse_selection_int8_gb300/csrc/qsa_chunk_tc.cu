@@ -85,7 +85,7 @@ struct Misc {
     float st_mrun[2][64];    // running max (log2 units) after the tile of that parity
     __align__(16) float st_mref[2][64]; // reference max the tile's P' were formed against
     float st_fac[64];        // O/l factor of the current tile
-    float st_fin[64];        // 2^(mref - mrun) at the end of a chunk
+    float st_fin[64];        // sigma * 2^(mref - mrun) at the end of a chunk
     float st_sig[2];         // sigma reference after the tile of that parity
     float st_fs[2];          // sigma factor of the tile
     int st_any[2];           // tile index whose O needs rescaling
@@ -619,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         // ================================================================ softmax
         const int q = w & 3, c = 32 * q + lane;
         const int u = lane & 3, ra = lane >> 2; // 16x256b: rows 8k + 2u + e, cells 32q + 8i + ra
+        const int orow = 4 * lane + q;          // the row this thread owns (running values, decisions)
         constexpr int NK = N / 8;               // 16x256b repetitions over the score columns
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
         struct Pend {
@@ -636,7 +637,6 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             wait(&ms.o_full[e.cp & 1], (uint32_t)(e.cp >> 1) & 1u);
             tc_fence_after();
             const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R;
-            const float sig = ms.st_sig[e.par];
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 1
@@ -647,15 +647,15 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int r = r0 + jj;
-                        if (r < p.R) p.part_o[(base + r) * kHeadDim + 128 * hh + c] = v[jj] * sig * ms.st_fin[r];
+                        if (r < p.R) p.part_o[(base + r) * kHeadDim + 128 * hh + c] = v[jj] * ms.st_fin[r];
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&ms.o_empty[e.cp & 1]);
-            if (c < p.R) {
-                p.part_m[base + c] = ms.st_mrun[e.par][c] * kLn2;
-                p.part_l[base + c] = l_fin * ms.st_fin[c];
+            if (orow < p.R) {
+                p.part_m[base + orow] = ms.st_mrun[e.par][orow] * kLn2;
+                p.part_l[base + orow] = l_fin;
             }
         };
 
@@ -723,7 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
             named_bar(kBarSoft, kSoftThreads);
             // ---- per-row decisions (thread c owns row c)
-            if (c < N) {
+            if (orow < N) {
+                const int c = orow;
                 const float mt = fmaxf(fmaxf(ms.red_max[par][0][c], ms.red_max[par][1][c]),
                                        fmaxf(ms.red_max[par][2][c], ms.red_max[par][3][c]));
                 const float mo = ms.st_mrun[par ^ 1][c], mref = ms.st_mref[par ^ 1][c];
@@ -731,8 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     l_own += ((ms.red_sum[par ^ 1][0][c] + ms.red_sum[par ^ 1][1][c]) + ms.red_sum[par ^ 1][2][c]) +
                              ms.red_sum[par ^ 1][3][c];
                 if (pend.on) {
-                    l_fin = l_own;
-                    ms.st_fin[c] = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
+                    // the chunk that ended at the previous tile: its partials are
+                    // o * sigma * 2^(mref - mrun), l * 2^(mref - mrun)
+                    const float fin = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
+                    l_fin = l_own * fin;
+                    ms.st_fin[c] = fin * ms.st_sig[par ^ 1];
                 }
                 float mrun_n, mref_n, fac;
                 if (first_t) {
@@ -757,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 ms.st_mref[par][c] = mref_n;
                 ms.st_fac[c] = fac;
             }
-            if (c == N) {
+            if (c == kSoftThreads - 1) { // owns no row (N <= 64)
                 const float st = fmaxf(fmaxf(ms.red_max[par][0][64], ms.red_max[par][1][64]),
                                        fmaxf(ms.red_max[par][2][64], ms.red_max[par][3][64]));
                 const float so = ms.st_sig[par ^ 1];
@@ -848,12 +852,14 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         }
         if (pend.on) {
             named_bar(kBarSoft, kSoftThreads);
-            if (c < N) {
+            if (orow < N) {
+                const int c = orow;
                 l_own += ((ms.red_sum[pend.par][0][c] + ms.red_sum[pend.par][1][c]) + ms.red_sum[pend.par][2][c]) +
                          ms.red_sum[pend.par][3][c];
-                l_fin = l_own;
                 const float mo = ms.st_mrun[pend.par][c], mref = ms.st_mref[pend.par][c];
-                ms.st_fin[c] = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
+                const float fin = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
+                l_fin = l_own * fin;
+                ms.st_fin[c] = fin * ms.st_sig[pend.par];
             }
             named_bar(kBarSoft, kSoftThreads);
             epilogue(pend);
