@@ -55,7 +55,8 @@ def parse():
                     help="CPU work budget of the oracle baseline")
     ap.add_argument("--case", default=None,
                     help="run one workload --reps times and exit (for profiler captures): "
-                         "tiny_decode, qsa_decode1..4, batched_decode, long_context, prompt_shaped")
+                         "tiny_decode, qsa_decode1..4, qsa_decode_sweep (T = 1, 2, 3, 4 in turn), "
+                         "batched_decode, long_context, prompt_shaped")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tcgen05"])
     return ap.parse_args()
@@ -69,13 +70,19 @@ def run_case(args):
     qsa_build.build()
     import sparse_selection_int8_gb300 as qsa
     name = args.case
-    p = wl.qsa_decode(int(name[-1])) if name.startswith("qsa_decode") else getattr(wl, name)()
+    if name == "qsa_decode_sweep":
+        problems = [wl.qsa_decode(T) for T in SWEEP]
+    elif name.startswith("qsa_decode"):
+        problems = [wl.qsa_decode(int(name[-1]))]
+    else:
+        problems = [getattr(wl, name)()]
     algo = {"auto": qsa.QSA_ALGO_AUTO, "simt": qsa.QSA_ALGO_SIMT, "tcgen05": qsa.QSA_ALGO_TCGEN05}[args.algo]
-    dp = qsa.DeviceProblem(p, algo=algo)
+    dps = [qsa.DeviceProblem(p, algo=algo) for p in problems]
     for _ in range(args.reps):
-        dp.run()
+        for dp in dps:
+            dp.run()
     torch.cuda.synchronize()
-    print(json.dumps({"case": name, "reps": args.reps, "status": int(dp.status.item())}))
+    print(json.dumps({"case": name, "reps": args.reps, "status": [int(dp.status.item()) for dp in dps]}))
     return 0
 
 
@@ -179,7 +186,16 @@ def source_digest(*names) -> str:
 
 # DRAM traffic per call of the dominant kernel from an ncu capture, valid
 # only while the kernel source hashes to the recorded digest.
-TRAFFIC = {}
+TRAFFIC = {
+    # qsa_decode T = 1..4, chunk kernel, sum of the four launches (profiles/qsa_chunk_tc_qsa_decode_sweep.md)
+    "1ce82677f82c709e": 6024960,
+}
+
+# Sources of the chunk kernel the recorded traffic belongs to.
+CHUNK_SOURCES = ("qsa_chunk_tc.cu", "qsa_sm100.cuh", "qsa_internal.cuh")
+
+# Kernels one decode-window call launches (query staging, chunk, merge).
+KERNELS_PER_DECODE_CALL = 3
 
 
 def dist_setup(args):
@@ -416,7 +432,7 @@ def run_ours(args, world, rank, local):
         cps, cores, sample = oracle_sample(problems, args.cpu_seconds)
         cpu = {"value": cps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
-    digest = source_digest("qsa_chunk_tc.cu", "qsa_merge.cu")
+    digest = source_digest(*CHUNK_SOURCES)
     traffic = TRAFFIC.get(digest)
     if rank == 0:
         line = {
@@ -431,11 +447,11 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                          "peak_source": peak_src,
-                         "timed_unit": "one library call (chunk kernel + merge kernel)"},
+                         "timed_unit": "one library call (query staging, chunk and merge kernels)"},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * len(SWEEP) * len(step_ms),
+            "gpu_launches": KERNELS_PER_DECODE_CALL * len(SWEEP) * len(step_ms),
             "cpu_baseline": cpu,
             "other_workloads": extra,
         }
