@@ -77,9 +77,12 @@ struct Cursor {
 };
 
 struct Misc {
-    float sc_ks[2][kTile];   // k_scale * softmax_scale * log2(e) per cell
-    float sc_vs[2][kTile];   // v_scale per cell
-    uint8_t sc_ok[2][kTile]; // cell holds a valid slot
+    // resolution rings (tile t in entry t % 4), filled by asynchronous copies
+    int32_t rs_sel[4][kTile]; // list entries
+    int32_t rs_pg[4][kTile];  // page-table entries (-1 masked, kBadPos out of range)
+    float rs_ks[4][kTile];    // k_scale, v_scale of the cell's slot (0 if masked)
+    float rs_vs[4][kTile];
+    uint8_t sc_ok[2][kTile];  // cell holds a valid slot
     __align__(16) float red_max[2][4][68]; // [tile parity][warp quadrant][row; 64 = |v_scale| max]
     __align__(16) float red_sum[2][4][64];
     float st_mrun[2][64];    // running max (log2 units) after the tile of that parity
@@ -101,9 +104,10 @@ struct Misc {
 template <int N>
 struct Lay {
     static constexpr int PB = N <= 48 ? 2 : 1; // P' buffers
+    static constexpr int QB = N <= 48 ? 2 : 1; // query tile buffers
     static constexpr uint32_t v = 0;
     static constexpr uint32_t q = 2 * kStageBytes;
-    static constexpr uint32_t pb = q + 2u * N * 512u;
+    static constexpr uint32_t pb = q + QB * N * 512u;
     static constexpr uint32_t misc = pb + PB * N * 256u;
     static constexpr uint32_t total = misc + (uint32_t)((sizeof(Misc) + 127) / 128 * 128);
 };
@@ -463,19 +467,26 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         const int src_k = 4 * vr; // K-mapping thread holding the V rows' slots
         const bool scl = u == 0;  // writes the scales of cells A and B, reports status
         const uint32_t t_lane = (uint32_t)R0 << 16;
-        // pipeline stage info: bg = b * G + g, mt = cells of the tile (0 = no tile)
-        int bg0 = 0, bg1 = 0, bg2 = 0, bg3 = 0, bg4 = 0;
-        int mt0 = 0, mt1 = 0, mt2 = 0, mt3 = 0, mt4 = 0;
-        int selA3 = 0, selB3 = 0, selA4 = 0, selB4 = 0;
-        int pgA2 = -1, pgB2 = -1, pgA3 = -1, pgB3 = -1;
+        // Resolution (step a1) runs ahead of the row loads through shared-memory
+        // rings filled by 4-byte asynchronous copies, so no register waits on
+        // those reads: step j copies the list entries of tile j+6, the page
+        // entries of tile j+4 (from list entries copied two steps earlier),
+        // checks the slots of tile j+2 (from page entries copied two steps
+        // earlier), prefetches that tile's rows into L2 and copies its scales;
+        // the rows of tile j+1 are loaded into registers; tile j is converted.
+        // The lane with u == 0 resolves cells A and B; the others take the
+        // slots by shuffle.
+        // tile info per stage: bg = b * G + g, mt = cells of the tile (0 = none)
+        int bg0 = 0, bg1 = 0, bg2 = 0, bg3 = 0, bg4 = 0, bg5 = 0, bg6 = 0;
+        int mt0 = 0, mt1 = 0, mt2 = 0, mt3 = 0, mt4 = 0, mt5 = 0, mt6 = 0;
         int slA0 = -1, slB0 = -1, slA1 = -1, slB1 = -1, slA2 = -1, slB2 = -1;
-        float ksA0 = 0.f, vsA0 = 0.f, ksB0 = 0.f, vsB0 = 0.f, ksA1 = 0.f, vsA1 = 0.f, ksB1 = 0.f, vsB1 = 0.f;
         uint32_t rk[32], rv[32]; // K: A p0, A p1, B p0, B p1; V: A' p0, A' p1, B' p0, B' p1
 #pragma unroll
         for (int e = 0; e < 32; ++e) rk[e] = rv[e] = 0u;
         TileIt head;
         tile_init(p, head, first);
-        for (int j = -4;; ++j) {
+        for (int j = -6;; ++j) {
+            cp_async_wait_group<1>(); // the copies of step j-2 and earlier have landed
             // ---- tile j -> tensor memory / shared memory; after each half, the
             // registers it frees take tile j+1's rows (mostly L2 hits by now)
             if (mt0) {
@@ -519,12 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             if (mt0) {
                 const int jb = j & 1;
                 if (scl) {
+                    // the scales of tile j sit in ring entry j % 4 (copied by this
+                    // thread two steps ago); the validity bits go to a 2-entry ring
                     if (j >= 2) wait(&ms.sc_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
-                    ms.sc_ks[jb][cA] = ksA0 * p.scale_log2;
-                    ms.sc_vs[jb][cA] = vsA0;
                     ms.sc_ok[jb][cA] = slA0 >= 0;
-                    ms.sc_ks[jb][cB] = ksB0 * p.scale_log2;
-                    ms.sc_vs[jb][cB] = vsB0;
                     ms.sc_ok[jb][cB] = slB0 >= 0;
                     mbar_arrive(&ms.sc_full[jb]);
                 }
@@ -566,55 +575,82 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                             }
                         }
                     }
-                    if (scl) {
-                        ksA1 = slA1 >= 0 ? __ldg(p.k_scale + kvb1 + slA1) : 0.f;
-                        vsA1 = slA1 >= 0 ? __ldg(p.v_scale + kvb1 + slA1) : 0.f;
-                        ksB1 = slB1 >= 0 ? __ldg(p.k_scale + kvb1 + slB1) : 0.f;
-                        vsB1 = slB1 >= 0 ? __ldg(p.v_scale + kvb1 + slB1) : 0.f;
+                }
+            }
+            // ---- list entries of tile j+6
+            mt6 = 0;
+            if (head.valid) {
+                const int nc = tile_cells(head);
+                bg6 = head.cur.b * p.G + head.cur.g;
+                mt6 = nc;
+                if (scl) {
+                    const int *src = p.sel + tile_base(p, head);
+                    const int e6 = (j + 6) & 3;
+                    if (cA < nc) cp_async4(smem_u32(&ms.rs_sel[e6][cA]), src + cA);
+                    if (cB < nc) cp_async4(smem_u32(&ms.rs_sel[e6][cB]), src + cB);
+                }
+                tile_next(p, head);
+            }
+            // ---- page-table entries of tile j+4 (from its list entries)
+            if (mt4 && scl) {
+                const int e4 = (j + 4) & 3;
+                const int32_t *prow = p.page_table + (size_t)(bg4 / p.G) * p.page_table_len;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int cx = x ? cB : cA;
+                    int32_t *dst = &ms.rs_pg[e4][cx];
+                    if (cx >= mt4) {
+                        *dst = -1; // past the tile's cells: masked
+                    } else {
+                        const int pos = ms.rs_sel[e4][cx];
+                        if (pos < 0 || pos >= p.page_table_len) *dst = kBadPos;
+                        else cp_async4(smem_u32(dst), prow + pos);
                     }
                 }
             }
-            // ---- list entries of tile j+4
-            mt4 = 0;
-            if (head.valid) {
-                const int nc = tile_cells(head);
-                bg4 = head.cur.b * p.G + head.cur.g;
-                mt4 = nc;
-                const int base = tile_base(p, head);
-                selA4 = cA < nc ? __ldg(p.sel + base + cA) : 0;
-                selB4 = cB < nc ? __ldg(p.sel + base + cB) : 0;
-                tile_next(p, head);
-            }
-            // ---- page-table entries of tile j+3
-            if (mt3) {
-                const int b3 = bg3 / p.G, nc = mt3;
-                pgA3 = page_entry(p, b3, selA3, cA < nc);
-                pgB3 = page_entry(p, b3, selB3, cB < nc);
-            }
-            // ---- slots of tile j+2; its rows (and scales) prefetched into L2
+            // ---- slots of tile j+2 (from its page entries): rows prefetched into
+            // L2, scales copied into the ring
             if (mt2) {
-                slA2 = slot_of(p, pgA2, scl);
-                slB2 = slot_of(p, pgB2, scl);
-                const int sa = __shfl_sync(0xffffffffu, slA2, 4 * (lane & 7));
-                const int sb = __shfl_sync(0xffffffffu, slB2, 4 * (lane & 7));
-                const int sl = (lane & 8) ? sb : sa; // slot of cell R0 + lane%16
+                int sa = -1, sb = -1;
+                if (scl) {
+                    const int e2 = (j + 2) & 3;
+                    sa = slot_of(p, ms.rs_pg[e2][cA], true);
+                    sb = slot_of(p, ms.rs_pg[e2][cB], true);
+                    const size_t kvb = (size_t)bg2 * p.pool_cells;
+                    if (sa >= 0) {
+                        cp_async4(smem_u32(&ms.rs_ks[e2][cA]), p.k_scale + kvb + sa);
+                        cp_async4(smem_u32(&ms.rs_vs[e2][cA]), p.v_scale + kvb + sa);
+                    } else {
+                        ms.rs_ks[e2][cA] = 0.f;
+                        ms.rs_vs[e2][cA] = 0.f;
+                    }
+                    if (sb >= 0) {
+                        cp_async4(smem_u32(&ms.rs_ks[e2][cB]), p.k_scale + kvb + sb);
+                        cp_async4(smem_u32(&ms.rs_vs[e2][cB]), p.v_scale + kvb + sb);
+                    } else {
+                        ms.rs_ks[e2][cB] = 0.f;
+                        ms.rs_vs[e2][cB] = 0.f;
+                    }
+                }
+                slA2 = __shfl_sync(0xffffffffu, sa, lane & ~3);
+                slB2 = __shfl_sync(0xffffffffu, sb, lane & ~3);
+                const int pa = __shfl_sync(0xffffffffu, slA2, 4 * (lane & 7));
+                const int pb = __shfl_sync(0xffffffffu, slB2, 4 * (lane & 7));
+                const int sl = (lane & 8) ? pb : pa; // slot of cell R0 + lane%16
                 if (sl >= 0) {
                     const size_t cell = (size_t)bg2 * p.pool_cells + sl;
                     prefetch_l2(p.k_pool + cell * kHeadDim + 128 * (lane >> 4));
                     prefetch_l2(p.v_pool + cell * kHeadDim + 128 * (lane >> 4));
                 }
-                if (scl) {
-                    const size_t kvb = (size_t)bg2 * p.pool_cells;
-                    if (slA2 >= 0) { prefetch_l2(p.k_scale + kvb + slA2); prefetch_l2(p.v_scale + kvb + slA2); }
-                    if (slB2 >= 0) { prefetch_l2(p.k_scale + kvb + slB2); prefetch_l2(p.v_scale + kvb + slB2); }
-                }
             }
+            cp_async_commit();
             // shift the pipeline by one tile
-            bg0 = bg1; bg1 = bg2; bg2 = bg3; bg3 = bg4;
-            mt0 = mt1; mt1 = mt2; mt2 = mt3; mt3 = mt4;
-            slA0 = slA1; slB0 = slB1; ksA0 = ksA1; vsA0 = vsA1; ksB0 = ksB1; vsB0 = vsB1;
-            slA1 = slA2; slB1 = slB2; pgA2 = pgA3; pgB2 = pgB3; selA3 = selA4; selB3 = selB4;
+            bg0 = bg1; bg1 = bg2; bg2 = bg3; bg3 = bg4; bg4 = bg5; bg5 = bg6;
+            mt0 = mt1; mt1 = mt2; mt2 = mt3; mt3 = mt4; mt4 = mt5; mt5 = mt6;
+            slA0 = slA1; slB0 = slB1;
+            slA1 = slA2; slB1 = slB2;
         }
+        cp_async_wait_group<0>();
     } else if (w < kMmaWarp) {
         // ================================================================ softmax
         const int q = w & 3, c = 32 * q + lane;
@@ -672,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             for (int ci = 0; ci < 4; ++ci) {
                 const int cc = 32 * q + 8 * ci + ra;
                 okc[ci] = ms.sc_ok[par][cc] != 0;
-                ksc[ci] = ms.sc_ks[par][cc];
-                vsc[ci] = ms.sc_vs[par][cc];
+                ksc[ci] = ms.rs_ks[i & 3][cc] * p.scale_log2;
+                vsc[ci] = ms.rs_vs[i & 3][cc];
             }
             mbar_arrive(&ms.sc_empty[par]);
             wait(&ms.s_full[par], (uint32_t)(i >> 1) & 1u);
@@ -899,21 +935,23 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             };
             TileIt it;
             tile_init(p, it, first);
-            // query tiles: one bulk copy per segment into buffer seg % 2; the
-            // first two now, segment s + 1 once segment s has started (its
-            // buffer was segment s - 1's, free after that segment's last QK)
+            // query tiles: one bulk copy per segment into buffer seg % QB.  With
+            // two buffers, the first two now and segment s + 1 once segment s
+            // has started (its buffer was segment s - 1's, free after that
+            // segment's last QK); with one, segment s + 1 after segment s ends.
+            constexpr int QB = L::QB;
             auto load_q = [&](const Cursor &sc, int seg) {
                 const uint32_t bytes = (uint32_t)N * 512u;
-                mbar_arrive_expect_tx(&ms.q_full[seg & 1], bytes);
-                bulk_g2s(smem + L::q + (size_t)(seg & 1) * N * 512,
+                mbar_arrive_expect_tx(&ms.q_full[seg % QB], bytes);
+                bulk_g2s(smem + L::q + (size_t)(seg % QB) * N * 512,
                          static_cast<const uint8_t *>(p.q_img) + ((size_t)sc.b * p.G + sc.g) * N * 512, bytes,
-                         &ms.q_full[seg & 1]);
+                         &ms.q_full[seg % QB]);
             };
             Cursor qnext = first;
             int qseg = 0; // next segment whose tile is to be loaded
             if (it.valid) {
                 cudaGridDependencySynchronize(); // the tiles come from the staging kernel
-                for (; qseg < 2 && qnext.remaining > 0; ++qseg) {
+                for (; qseg < QB && qnext.remaining > 0; ++qseg) {
                     load_q(qnext, qseg);
                     qnext = next_segment(p, qnext);
                 }
@@ -923,12 +961,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             for (; it.valid; ++i) {
                 const int seg = it.seg;
                 const bool seg_start = seg != cur_seg;
-                if (seg_start) wait(&ms.q_full[seg & 1], (uint32_t)(seg >> 1) & 1u);
+                if (seg_start) wait(&ms.q_full[seg % QB], (uint32_t)(seg / QB) & 1u);
                 cur_seg = seg;
                 wait(&ms.k_full, (uint32_t)i & 1u);
                 if (i >= 2) wait(&ms.s_empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u);
                 tc_fence_after();
-                const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg & 1) * N * 512u, 16, 1024);
+                const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg % QB) * N * 512u, 16, 1024);
                 const uint32_t sd = tmem + kColS + 64u * (i & 1);
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
@@ -942,9 +980,16 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 if (i >= 1) issue_pv(prev);
                 prev = PvT{i, cp, first_t, it.ti == it.nt - 1};
                 tile_next(p, it);
-                if (!it.valid || it.seg != seg) mma_commit(&ms.q_empty[seg & 1]);
-                if (seg_start && seg >= 1 && qnext.remaining > 0) {
+                const bool seg_end = !it.valid || it.seg != seg;
+                if (seg_end) mma_commit(&ms.q_empty[seg % QB]);
+                if (QB == 2 && seg_start && seg >= 1 && qnext.remaining > 0) {
                     wait(&ms.q_empty[(seg - 1) & 1], (uint32_t)((seg - 1) >> 1) & 1u);
+                    load_q(qnext, qseg);
+                    ++qseg;
+                    qnext = next_segment(p, qnext);
+                }
+                if (QB == 1 && seg_end && qnext.remaining > 0) {
+                    wait(&ms.q_empty[0], (uint32_t)seg & 1u);
                     load_q(qnext, qseg);
                     ++qseg;
                     qnext = next_segment(p, qnext);
@@ -971,6 +1016,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
+    static_assert(Lay<N>::total + 1024 <= 232448, "shared memory of the chunk kernel");
     const uint32_t bytes = Lay<N>::total + 1024;
     if ((int)bytes > max_smem) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
