@@ -88,7 +88,7 @@ struct Misc {
     float st_mrun[2][64];    // running max (log2 units) after the tile of that parity
     __align__(16) float st_mref[2][64]; // reference max the tile's P' were formed against
     float st_fac[64];        // O/l factor of the current tile
-    float st_fin[64];        // sigma * 2^(mref - mrun) at the end of a chunk
+    __align__(16) float st_fin[64]; // sigma * 2^(mref - mrun) at the end of a chunk
     float st_sig[2];         // sigma reference after the tile of that parity
     float st_fs[2];          // sigma factor of the tile
     int st_any[2];           // tile index whose O needs rescaling
@@ -390,7 +390,9 @@ __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
 
 // ---------------------------------------------------------------- kernel
 
-template <int N>
+// N: MMA columns (rows padded to 16); KR: 8-row score blocks that hold real
+// rows (KR * 8 >= R), the softmax skips the rest.
+template <int N, int KR>
 __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params p)
 {
     using L = Lay<N>;
@@ -676,15 +678,17 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 1
-                for (int r0 = 0; r0 < N; r0 += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + t_lane + kColO + 128u * (e.cp & 1) + 64u * hh + r0, v);
+                for (int r0 = 0; r0 < p.R; r0 += 8) { // rows R..N-1 are MMA padding
+                    float v[8];
+                    tmem_ld8(tmem + t_lane + kColO + 128u * (e.cp & 1) + 64u * hh + r0, v);
+                    const float4 f0 = *reinterpret_cast<const float4 *>(&ms.st_fin[r0]);
+                    const float4 f1 = *reinterpret_cast<const float4 *>(&ms.st_fin[r0 + 4]);
+                    const float fr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
                     tmem_wait_ld();
+                    float *dst = p.part_o + (base + r0) * kHeadDim + 128 * hh + c;
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int r = r0 + jj;
-                        if (r < p.R) p.part_o[(base + r) * kHeadDim + 128 * hh + c] = v[jj] * ms.st_fin[r];
-                    }
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (r0 + jj < p.R) dst[(size_t)jj * kHeadDim] = v[jj] * fr[jj];
                 }
             }
             tc_fence_before();
@@ -723,9 +727,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             mbar_arrive(&ms.s_empty[par]); // the scores live in registers from here on
             // ---- pass 1: tile max of every row.  The same rounded product is
             // used in pass 2 (no FMA contraction), so the max cell gets 2^0 = 1.
-            float mrow[2 * NK];
+            float mrow[2 * KR];
 #pragma unroll
-            for (int k = 0; k < NK; ++k) {
+            for (int k = 0; k < KR; ++k) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     float m = -INFINITY;
@@ -745,10 +749,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
 #pragma unroll
-                for (int jr = 0; jr < 2 * NK; ++jr) mrow[jr] = fmaxf(mrow[jr], __shfl_xor_sync(0xffffffffu, mrow[jr], o));
+                for (int jr = 0; jr < 2 * KR; ++jr)
+                    mrow[jr] = fmaxf(mrow[jr], __shfl_xor_sync(0xffffffffu, mrow[jr], o));
             }
 #pragma unroll
-            for (int k = 0; k < NK; ++k)
+            for (int k = 0; k < KR; ++k)
                 if (ra == k) *reinterpret_cast<float2 *>(&ms.red_max[par][q][8 * k + 2 * u]) = make_float2(mrow[2 * k], mrow[2 * k + 1]);
             {
                 float va = 0.f;
@@ -759,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
             named_bar(kBarSoft, kSoftThreads);
             // ---- per-row decisions (thread c owns row c)
-            if (orow < N) {
+            if (orow < p.R) {
                 const int c = orow;
                 const float mt = fmaxf(fmaxf(ms.red_max[par][0][c], ms.red_max[par][1][c]),
                                        fmaxf(ms.red_max[par][2][c], ms.red_max[par][3][c]));
@@ -820,9 +825,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             uint8_t *p_tile = smem + L::pb + (size_t)pbi * N * 256;
             // ---- pass 2: P' = f16(p * v_scale / sigma) into the B operand of
             // the P.V MMA (K-major [rows][cells]), and row sums
-            float lrow[2 * NK], mref_r[2 * NK];
+            float lrow[2 * KR], mref_r[2 * KR];
 #pragma unroll
-            for (int k = 0; k < NK; ++k) {
+            for (int k = 0; k < KR; ++k) {
                 // reference maxima of this thread's rows, read once (the P'
                 // stores below could otherwise force re-reads)
                 const float2 m2 = *reinterpret_cast<const float2 *>(&ms.st_mref[par][8 * k + 2 * u]);
@@ -841,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     const int r7 = 2 * u + e;
                     uint8_t *pe = p_tile + (cc >> 6) * N * 128 + r7 * 128 + ((((cc & 63) >> 3) ^ r7) << 4) + (cc & 7) * 2;
 #pragma unroll
-                    for (int k = 0; k < NK; ++k) {
+                    for (int k = 0; k < KR; ++k) {
                         const float pr = okc[ci] ? fast_exp2(x[L][4 * k + 2 * B + e] - mref_r[2 * k + e]) : 0.f;
                         lrow[2 * k + e] += pr;
                         *reinterpret_cast<__half *>(pe + 1024 * k) = __float2half_rn(pr * vsn);
@@ -851,10 +856,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
 #pragma unroll
-                for (int jr = 0; jr < 2 * NK; ++jr) lrow[jr] += __shfl_xor_sync(0xffffffffu, lrow[jr], o);
+                for (int jr = 0; jr < 2 * KR; ++jr)
+                    lrow[jr] += __shfl_xor_sync(0xffffffffu, lrow[jr], o);
             }
 #pragma unroll
-            for (int k = 0; k < NK; ++k)
+            for (int k = 0; k < KR; ++k)
                 if (ra == k) *reinterpret_cast<float2 *>(&ms.red_sum[par][q][8 * k + 2 * u]) = make_float2(lrow[2 * k], lrow[2 * k + 1]);
             // ---- lazy rescale of the chunk's O (rows whose max moved, or sigma)
             if (resc) {
@@ -864,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 1
-                    for (int r0 = 0; r0 < N; r0 += 16) {
+                    for (int r0 = 0; r0 < p.R; r0 += 16) {
                         const uint32_t ta = tmem + t_lane + kColO + 128u * (cp & 1) + 64u * hh + r0;
                         float v[16];
                         tmem_ld16(ta, v);
@@ -888,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         }
         if (pend.on) {
             named_bar(kBarSoft, kSoftThreads);
-            if (orow < N) {
+            if (orow < p.R) {
                 const int c = orow;
                 l_own += ((ms.red_sum[pend.par][0][c] + ms.red_sum[pend.par][1][c]) + ms.red_sum[pend.par][2][c]) +
                          ms.red_sum[pend.par][3][c];
@@ -1007,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     if (w == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int N>
+template <int N, int KR>
 cudaError_t launch_n(const Params &p, cudaStream_t stream)
 {
     int dev = 0, sms = 0, max_smem = 0;
@@ -1019,7 +1025,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     static_assert(Lay<N>::total + 1024 <= 232448, "shared memory of the chunk kernel");
     const uint32_t bytes = Lay<N>::total + 1024;
     if ((int)bytes > max_smem) return cudaErrorInvalidConfiguration;
-    if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N, KR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)bytes)) != cudaSuccess)
         return e;
     const long long pieces = (long long)p.n_seq * p.G * N * 32;
@@ -1036,7 +1042,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qsa_chunk_tc_kernel<N>, p);
+    return cudaLaunchKernelEx(&cfg, qsa_chunk_tc_kernel<N, KR>, p);
 }
 
 } // namespace
@@ -1052,12 +1058,15 @@ size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
 cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream)
 {
     if (p.n_chunks == 0) return cudaSuccess;
-    const int N = (p.R + 15) / 16 * 16;
-    switch (N) {
-    case 16: return launch_n<16>(p, stream);
-    case 32: return launch_n<32>(p, stream);
-    case 48: return launch_n<48>(p, stream);
-    case 64: return launch_n<64>(p, stream);
+    switch ((p.R + 7) / 8) { // 8-row blocks of real rows; N = that, padded to 16
+    case 1: return launch_n<16, 1>(p, stream);
+    case 2: return launch_n<16, 2>(p, stream);
+    case 3: return launch_n<32, 3>(p, stream);
+    case 4: return launch_n<32, 4>(p, stream);
+    case 5: return launch_n<48, 5>(p, stream);
+    case 6: return launch_n<48, 6>(p, stream);
+    case 7: return launch_n<64, 7>(p, stream);
+    case 8: return launch_n<64, 8>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
