@@ -177,6 +177,22 @@ def test_ragged_batch_with_empty_sequences(algo):
     assert np.array_equal(out[4], np.zeros_like(out[4]))
 
 
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+@pytest.mark.parametrize("H,T", [(12, 4), (16, 4), (5, 3), (10, 4), (1, 1)])
+def test_many_segments_per_cta(algo, H, T):
+    """Hundreds of short sequences: every CTA of the decode kernel walks
+    several (sequence, KV head) segments, so query tiles are reloaded during
+    the walk (both buffering modes: rows up to 48 and 64), with row counts
+    that are not multiples of 8 or 16 and some masked pages."""
+    rng = np.random.default_rng(7700 + 10 * H + T)
+    lens = [int(v) for v in rng.integers(1, 300, size=400)]
+    p = wl.make_problem(n_seq=len(lens), n_kv_heads=2, q_per_kv=H, n_queries=T, pool_cells=512,
+                        n_selected=lens, chunk_cells=128, mask_fraction=0.1, seed=7700 + 10 * H + T)
+    dp, out = run(p, algo, max_selected=max(lens))
+    assert_parity(out, oracle.decode_attn(p), f"many segments H={H} T={T}")
+    assert int(dp.status.item()) == 0
+
+
 @pytest.mark.parametrize("algo", ["auto", "simt"])
 def test_batch_list_above_bound_is_clamped(algo):
     import sparse_selection_int8_gb300 as qsa
