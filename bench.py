@@ -5,13 +5,19 @@ Headline workload: the pages' kernel-table shape -- 1 KV head x 12 query
 heads, head_dim 256, a 32,768-cell INT8 pool with per-cell scales, a
 permuted page table, 2,051 selected cells, chunk 128 -- with the MTP verify
 window swept over 1/2/3/4 queries.  One step = the four calls (T = 1, 2, 3,
-4), each a CUDA graph of one library call (chunk kernel + merge kernel).
+4).  As in the pages' kernel table (µs per call over a run of 200 calls),
+the calls run back to back: one CUDA graph holds 128 steps and is replayed.
+Every call of a rotation reads a different input set (its own copy of the
+pools, scales, page table, list and queries at distinct addresses), so one
+rotation touches more than 4x the L2 and every call reads its cells from HBM.
 
 Metric: selected KV cells/s (sum of selected cells over the step's calls
 divided by the step time), with the achieved HBM GB/s of the calls against
-the measured HBM peak.  L2 is flushed (a 512 MB write) before every timed
-step, so every call reads its cells from HBM.  Inputs are synthetic and
-seeded; nothing is read from disk.
+the measured HBM peak.  Also reported: µs per call of each T back to back,
+µs of an isolated call (one graph launch, L2 flushed before it), the
+headline shape replicated as 64 sequences in one batch call (bandwidth of
+the kernels on that shape), and the other workloads.  Inputs are synthetic
+and seeded; nothing is read from disk.
 
 Arms:
   default            the CUDA library (this repo), N GPUs via torchrun
@@ -20,6 +26,7 @@ Arms:
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import os
@@ -41,13 +48,15 @@ WORKLOAD = ("qsa_decode: 1 KV head x 12 query heads, head_dim 256, INT8 K/V pool
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20
+ROTATION = 128  # distinct input sets per T in the headline rotation
 SWEEP = (1, 2, 3, 4)
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
@@ -291,7 +300,6 @@ def time_graphs(torch, graphs, flush, steps, warmup, stream):
     the flush launch on the current stream, the events are recorded on it.
     Returns per-step lists of per-graph durations in ms."""
     assert torch.cuda.current_stream() == stream
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
     for _ in range(warmup):
         flush.zero_()
         for g in graphs:
@@ -315,7 +323,6 @@ def time_graphs(torch, graphs, flush, steps, warmup, stream):
     torch.cuda.synchronize()
     for e in pending:
         per_step.append([e[i].elapsed_time(e[i + 1]) for i in range(len(graphs))])
-    del ev
     return per_step
 
 
@@ -329,38 +336,169 @@ def capture(torch, dp, stream):
     return g
 
 
-def measure_extra(torch, qsa, wl, flush, stream, hbm_peak, tflops_peak, budget_s=60.0):
-    """µs per call and roofline of the other workloads (context, not the headline)."""
+def clone_set(torch, dp):
+    """The same call on copies of every input at fresh device addresses, with
+    its own output, workspace and status word (an input set of a rotation)."""
+    c = copy.copy(dp)
+    for name in ("q", "k_pool", "v_pool", "k_scale", "v_scale", "page_table", "sel", "sel_offsets"):
+        setattr(c, name, getattr(dp, name).clone())
+    c.out = torch.empty_like(dp.out)
+    c.workspace = torch.empty_like(dp.workspace)
+    c.status = torch.zeros_like(dp.status)
+    return c
+
+
+def rotation(torch, dp, n):
+    return [dp] + [clone_set(torch, dp) for _ in range(n - 1)]
+
+
+def capture_calls(torch, calls, stream):
+    """One CUDA graph holding `calls` (callables launching library calls on
+    `stream`) back to back."""
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            c()
+    return g
+
+
+def time_b2b(torch, sets, stream, rounds=4, reps=1):
+    """µs per call of back-to-back calls rotating over `sets` (graph of
+    reps x len(sets) calls, replayed `rounds` times after one warm replay)."""
+    calls = [lambda s=s: s.run(stream=stream) for _ in range(reps) for s in sets]
+    g = capture_calls(torch, calls, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(rounds):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    status = max(int(s.status.item()) for s in sets)
+    if status:
+        raise RuntimeError(f"status word {status:#x} after the timed calls")
+    return e0.elapsed_time(e1) * 1e3 / (rounds * len(calls))
+
+
+class BatchCall:
+    """The single-sequence problem of a DeviceProblem as a batch of `n_seq`
+    sequences (each with its own copy of the pools, page table and list),
+    called through qsa_decode_attn_batch."""
+
+    def __init__(self, torch, qsa, dp, n_seq):
+        p = dp.p
+        self.qsa = qsa
+        self.shape = dp.shape
+        self.n_seq = n_seq
+        self.q = dp.q.repeat(n_seq, 1, 1, 1).contiguous()
+        self.k_pool = dp.k_pool.repeat(n_seq, 1, 1, 1).contiguous()
+        self.v_pool = dp.v_pool.repeat(n_seq, 1, 1, 1).contiguous()
+        self.k_scale = dp.k_scale.repeat(n_seq, 1, 1).contiguous()
+        self.v_scale = dp.v_scale.repeat(n_seq, 1, 1).contiguous()
+        self.page_table = dp.page_table.repeat(n_seq, 1).contiguous()
+        n = int(p.sel.shape[0])
+        self.sel = dp.sel[:n].repeat(n_seq).contiguous()
+        self.sel_offsets = (torch.arange(n_seq + 1, dtype=torch.int32, device=dp.q.device) * n).contiguous()
+        self.max_selected = n
+        self.ws_bytes = qsa.qsa_workspace_bytes(dp.shape, n_seq, n)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dp.q.device)
+        self.out = torch.empty((n_seq,) + tuple(dp.out.shape[1:]), dtype=torch.float32, device=dp.q.device)
+        self.status = torch.zeros_like(dp.status)
+
+    def run(self, batch=None, stream=None, out=None):
+        self.qsa.qsa_decode_attn_batch(self.shape, self.n_seq, self.q, self.k_pool, self.v_pool,
+                                       self.k_scale, self.v_scale, self.page_table, self.sel,
+                                       self.sel_offsets, self.max_selected, self.out,
+                                       self.workspace, self.ws_bytes, self.status, stream)
+        return self.out
+
+
+def sets_for(touched_bytes, set_bytes, lo=2, hi=512, budget=12 << 30):
+    """Input sets per rotation: enough that one rotation touches >= 4x L2,
+    within a device-memory budget."""
+    n = max(lo, -(-4 * L2_BYTES // max(touched_bytes, 1)))
+    n = min(n, hi, max(lo, budget // max(set_bytes, 1)))
+    return int(n)
+
+
+def set_bytes_of(dp):
+    return sum(t.numel() * t.element_size() for t in
+               (dp.q, dp.k_pool, dp.v_pool, dp.k_scale, dp.v_scale, dp.page_table, dp.sel,
+                dp.out, dp.workspace))
+
+
+def measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush, budget_s=90.0):
+    """µs per call and roofline of the other workloads (context, not the
+    headline): back-to-back calls over rotated input sets, as the headline."""
     res = {}
     t_start = time.perf_counter()
-    specs = [("tiny_decode", wl.tiny_decode, 200), ("batched_decode", wl.batched_decode, 100),
-             ("long_context", wl.long_context, 50), ("prompt_shaped", wl.prompt_shaped, 5)]
-    for name, make, iters in specs:
+    specs = [("tiny_decode", wl.tiny_decode), ("batched_decode", wl.batched_decode),
+             ("long_context", wl.long_context), ("prompt_shaped", wl.prompt_shaped)]
+    for name, make in specs:
         if time.perf_counter() - t_start > budget_s:
             res[name] = {"skipped": "time budget"}
             continue
         p = make()
         dp = qsa.DeviceProblem(p)
-        g = capture(torch, dp, stream)
-        with torch.cuda.stream(stream):
-            per = time_graphs(torch, [g], flush, iters, 3, stream)
-        us = statistics.median([x[0] for x in per]) * 1e3
-        cells = int(p.n_selected.sum())
         ab = algorithmic_bytes(p)
+        if name == "prompt_shaped":
+            # about a millisecond per call: one graph per call, L2 flushed first
+            g = capture(torch, dp, stream)
+            with torch.cuda.stream(stream):
+                per = time_graphs(torch, [g], flush, 5, 3, stream)
+            us = statistics.median([x[0] for x in per]) * 1e3
+            how = "one call per graph, L2 flushed before each"
+            del g
+        else:
+            n = sets_for(ab, set_bytes_of(dp))
+            sets = rotation(torch, dp, n)
+            reps = max(1, 256 // n)
+            us = time_b2b(torch, sets, stream, rounds=3, reps=reps)
+            how = f"back to back, {n} rotated input sets"
+            del sets
+        cells = int(p.n_selected.sum())
         entry = {"us_per_call": round(us, 2), "cells_per_s": cells / (us * 1e-6),
-                 "algorithmic_bytes": ab, "hbm_gbs": ab / (us * 1e-6) / 1e9}
+                 "algorithmic_bytes": ab, "hbm_gbs": ab / (us * 1e-6) / 1e9, "timing": how}
         entry["hbm_frac"] = entry["hbm_gbs"] / hbm_peak
         if name == "prompt_shaped":
             entry["tflops"] = flops(p) / (us * 1e-6) / 1e12
             entry["tensor_frac_bf16"] = entry["tflops"] / tflops_peak
         res[name] = entry
-        del dp, g
+        del dp
         torch.cuda.empty_cache()
     return res
 
 
+def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64):
+    """The headline shape replicated as `n_seq` independent sequences in one
+    qsa_decode_attn_batch call (bandwidth of the kernels on that shape; a
+    labelled companion figure, not the headline)."""
+    res = {}
+    for T in (1, 4):
+        p = wl.qsa_decode(T)
+        base = qsa.DeviceProblem(p)
+        rep = BatchCall(torch, qsa, base, n_seq)
+        touched = n_seq * algorithmic_bytes(p)
+        n = sets_for(touched, set_bytes_of(rep), lo=2, hi=8, budget=8 << 30)
+        sets = rotation(torch, rep, n)
+        us = time_b2b(torch, sets, stream, rounds=4, reps=max(1, 32 // n))
+        res[f"T{T}"] = {"us_per_call": round(us, 2), "cells_per_s": n_seq * int(p.n_selected.sum()) / (us * 1e-6),
+                        "hbm_gbs": touched / (us * 1e-6) / 1e9,
+                        "hbm_frac": touched / (us * 1e-6) / 1e9 / hbm_peak, "input_sets": n}
+        del sets, rep, base
+        torch.cuda.empty_cache()
+    res["what"] = (f"qsa_decode shape replicated as {n_seq} sequences (own pools, page tables and "
+                   "lists) in one qsa_decode_attn_batch call; back to back over rotated input sets")
+    return res
+
+
 def run_ours(args, world, rank, local):
-    import numpy as np
     import torch
     if not torch.cuda.is_available():
         raise RuntimeError("the CUDA arm needs a GPU")
@@ -376,24 +514,60 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream()
     problems = [wl.qsa_decode(T) for T in SWEEP]
     dps = [qsa.DeviceProblem(p) for p in problems]
-    graphs = [capture(torch, dp, stream) for dp in dps]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
+    # Headline: the pages' method (µs per call over a run of back-to-back
+    # calls), with the inputs rotated over ROTATION distinct sets per T so
+    # that every call reads its cells from HBM: one rotation touches
+    # ROTATION x (sum over T of the calls' algorithmic bytes) > 4x L2.
+    bytes_step = sum(algorithmic_bytes(p) for p in problems)
+    cells_step = sum(int(p.n_selected.sum()) for p in problems)
+    sets = [rotation(torch, dp, ROTATION) for dp in dps]
+
+    def step_calls(s):
+        return [lambda x=sets[i][s % ROTATION]: x.run(stream=stream) for i in range(len(SWEEP))]
+
+    full_calls = [c for s in range(ROTATION) for c in step_calls(s)]
+    g_full = capture_calls(torch, full_calls, stream)
+    rem = args.steps % ROTATION
+    g_rem = capture_calls(torch, [c for s in range(rem) for c in step_calls(s)], stream) if rem else None
+    with torch.cuda.stream(stream):
+        for s in range(ROTATION - args.warmup, ROTATION):  # warm-up ends where a rotation ends
+            for c in step_calls(s):
+                c()
     dist_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk, torch.cuda.stream(stream):
-        per_step = time_graphs(torch, graphs, flush, args.steps, args.warmup, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps // ROTATION):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+        e1.synchronize()
     torch.cuda.synchronize()
     dist_barrier(world)
+    status = max(int(x.status.item()) for row in sets for x in row)
+    if status:
+        raise RuntimeError(f"status word {status:#x} after the timed calls")
+    total_ms = dist_max(e0.elapsed_time(e1), world)
+    ms_per_step = total_ms / args.steps
+    value = world * cells_step * args.steps / (total_ms * 1e-3)
+    achieved = bytes_step / (ms_per_step * 1e-3) / 1e9
+    del g_full, g_rem
 
-    step_ms = [sum(x) for x in per_step]
-    total_ms = dist_max(sum(step_ms), world)
-    ms_per_step = total_ms / len(step_ms)
-    cells_step = sum(int(p.n_selected.sum()) for p in problems)
-    value = world * cells_step * len(step_ms) / (total_ms * 1e-3)
-    call_ms = [statistics.mean([x[i] for x in per_step]) for i in range(len(SWEEP))]
-    bytes_step = sum(algorithmic_bytes(p) for p in problems)
-    achieved = bytes_step / (sum(call_ms) * 1e-3) / 1e9
+    # µs per call of each T alone (back to back over its rotation), and of an
+    # isolated call (one graph launch per call, L2 flushed before it)
+    per_T = {f"T{T}": round(time_b2b(torch, sets[i], stream, rounds=4), 3) for i, T in enumerate(SWEEP)}
+    iso_graphs = [capture(torch, dp, stream) for dp in dps]
+    with torch.cuda.stream(stream):
+        per_step = time_graphs(torch, iso_graphs, flush, 200, 5, stream)
+    isolated = {f"T{T}": round(statistics.median([x[i] for x in per_step]) * 1e3, 3)
+                for i, T in enumerate(SWEEP)}
+    del iso_graphs, sets
+    torch.cuda.empty_cache()
 
     # end to end through the public API with host buffers: per step, the
     # queries and selection lists go host->device from pinned memory and the
@@ -408,24 +582,25 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         for s in range(e2e_steps + 5):
             flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             for i, dp in enumerate(dps):
                 dp.q.copy_(h_q[i], non_blocking=True)
                 dp.sel.copy_(h_sel[i], non_blocking=True)
                 dp.run(stream=stream)
                 h_out[i].copy_(dp.out, non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
+            b.record(stream)
+            b.synchronize()
             if s >= 5:
-                e2e_times.append(e0.elapsed_time(e1))
+                e2e_times.append(a.elapsed_time(b))
     e2e_ms = dist_max(statistics.mean(e2e_times), world)
     e2e_value = world * cells_step / (e2e_ms * 1e-3)
 
-    extra = {}
+    extra, steady = {}, {}
     if rank == 0 and not args.no_extra:
-        extra = measure_extra(torch, qsa, wl, flush, stream, hbm_peak, tflops_peak)
+        steady = measure_steady(torch, qsa, wl, stream, hbm_peak)
+        extra = measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush)
 
     cpu = None
     if rank == 0 and world == 1:
@@ -437,22 +612,29 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": len(step_ms), "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16 (int8 codes exact) x f16 -> f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "l2": "flushed (512 MB write) before every timed step",
-                       "launch": "one CUDA graph per call, replayed", "parallelism":
-                       f"replica per GPU x{world}" if world > 1 else "1 GPU"},
-            "us_per_call": {f"T{T}": round(ms * 1e3, 3) for T, ms in zip(SWEEP, call_ms)},
+            "config": {"workload": WORKLOAD,
+                       "l2": (f"inputs larger than L2: calls rotate over {ROTATION} distinct input sets "
+                              f"per T ({ROTATION * bytes_step / L2_BYTES:.1f}x L2 of algorithmic bytes "
+                              "touched per rotation)"),
+                       "launch": (f"back to back: one CUDA graph of {ROTATION} steps (4 calls each), "
+                                  "replayed; the pages' method (µs per call over a run of calls)"),
+                       "parallelism": f"replica per GPU x{world}" if world > 1 else "1 GPU"},
+            "us_per_call": per_T,
+            "isolated_call_us": isolated,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                          "peak_source": peak_src,
-                         "timed_unit": "one library call (query staging, chunk and merge kernels)"},
+                         "timed_unit": "one library call (query staging, chunk and merge kernels)",
+                         "note": "latency-bound shape: about 1.1 MB per call"},
             "clocks": clk.summary(),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": KERNELS_PER_DECODE_CALL * len(SWEEP) * len(step_ms),
+            "gpu_launches": KERNELS_PER_DECODE_CALL * len(SWEEP) * args.steps,
             "cpu_baseline": cpu,
+            "steady_state": steady,
             "other_workloads": extra,
         }
         print(json.dumps(line), flush=True)
