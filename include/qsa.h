@@ -28,6 +28,14 @@
  *     nothing.  A failed launch returns QSA_ERR_CUDA.
  *   - Device-side input errors never trap: an out-of-range list entry or page
  *     slot is treated as masked and raises a bit in the optional status word.
+ *   - Kernels are launched with programmatic dependent launch: a call's first
+ *     kernel may start while the previous kernel on the stream finishes (it
+ *     waits for that kernel before reading anything), and the next kernel on
+ *     the stream may start early too.  A kernel launched after a call with
+ *     the programmatic-serialization attribute must call
+ *     cudaGridDependencySynchronize() before it reads the call's outputs (the
+ *     CUDA contract for such launches); ordinary launches, copies and events
+ *     see the call complete.
  *
  * Dequantised values: k_hat = k_scale[cell] * K[cell][d] (same for V), a
  * symmetric per-cell fp32 scale with no zero point.  Scores

@@ -37,9 +37,10 @@
 //            P' written to shared memory as the second MMA's B operand and
 //            row sums by a reduce-scatter butterfly.  At the end of a chunk
 //            they read O from tensor memory and write the partials.
-//   MMA warp 12 (one thread) issues S = K.Q^T for tile i+1 before
-//            O += V^T.P'^T for tile i; completion is signalled by
-//            tcgen05.commit on the rings' "empty" and "full" barriers.
+//   S warp 12 (one thread) issues S = K.Q^T of each tile, and P.V warp 13
+//            (one thread) O += V^T.P'^T, side by side; completion is
+//            signalled by tcgen05.commit on the rings' "empty" and "full"
+//            barriers.
 //
 // Every wait is bounded; a wait that runs out raises QSA_STATUS_TIMEOUT and
 // makes all later waits of the CTA return at once, so the kernel always ends.
@@ -56,8 +57,9 @@ using namespace sm100;
 constexpr int kTile = 128;                        // cells per tile (MMA M)
 constexpr int kLoadWarps = 8;
 constexpr int kSoftWarps = 4;
-constexpr int kMmaWarp = kLoadWarps + kSoftWarps; // 12
-constexpr int kThreads = (kMmaWarp + 1) * 32;     // 416
+constexpr int kMmaWarp = kLoadWarps + kSoftWarps; // 12: issues S = K.Q^T
+constexpr int kPvWarp = kMmaWarp + 1;             // 13: issues O += V^T.P'^T
+constexpr int kThreads = (kPvWarp + 1) * 32;      // 448
 constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kScaleThreads = kLoadThreads / 4;   // loader threads that write the scales
@@ -170,23 +172,57 @@ __device__ inline int seq_chunks(const Params &p, int b, int *start, int *n)
     return *n > 0 ? (*n + p.chunk_cells - 1) / p.chunk_cells : 0;
 }
 
+// Quotient and remainder of non-negative a / b (b > 0): 32-bit division
+// (a few instructions) whenever both fit, 64-bit otherwise.
+__device__ __forceinline__ void divmod_nn(long long a, long long b, long long &q, long long &r)
+{
+    if (a < 0x7fffffffll && b < 0x7fffffffll) {
+        const unsigned ua = (unsigned)a, ub = (unsigned)b;
+        q = ua / ub;
+        r = ua - (unsigned)q * ub;
+    } else {
+        q = a / b;
+        r = a - q * b;
+    }
+}
+
 // Position of this CTA's first item, computed by one full warp: lanes read
 // the sequences' list offsets in parallel, a warp scan finds the sequence
 // that holds item `lo`.  Items are (sequence, KV head, chunk) in that order;
 // each CTA takes a contiguous range (consecutive chunks share their queries).
 __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
 {
+    cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
+    cur.remaining = 0;
+    long long per, rem, q, r;
+    if (p.sel_offsets == nullptr) {
+        // one sequence (the step entry): closed form, no scan
+        int s, n;
+        const int nch = seq_chunks(p, 0, &s, &n);
+        const long long total = (long long)p.G * nch;
+        divmod_nn(total + gridDim.x - 1, gridDim.x, per, rem);
+        const long long lo = per * blockIdx.x;
+        const long long hi = min(lo + per, total);
+        if (lo >= hi) return;
+        cur.remaining = (int)(hi - lo);
+        cur.nch = nch;
+        cur.start = s;
+        cur.n = n;
+        divmod_nn(lo, nch, q, r);
+        cur.g = (int)q;
+        cur.c = (int)r;
+        return;
+    }
     long long total = 0;
     int s, n;
     for (int b = lane; b < p.n_seq; b += 32) total += (long long)p.G * seq_chunks(p, b, &s, &n);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-    const long long per = (total + gridDim.x - 1) / gridDim.x;
+    divmod_nn(total + gridDim.x - 1, gridDim.x, per, rem);
     const long long lo = per * blockIdx.x;
     const long long hi = min(lo + per, total);
-    cur.remaining = lo < hi ? (int)(hi - lo) : 0;
-    cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
-    if (cur.remaining == 0) return;
+    if (lo >= hi) return;
+    cur.remaining = (int)(hi - lo);
     long long before = 0;
     for (int b0 = 0; b0 < p.n_seq; b0 += 32) {
         const int b = b0 + lane;
@@ -208,8 +244,9 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
             cur.nch = __shfl_sync(0xffffffffu, nch, src);
             cur.start = __shfl_sync(0xffffffffu, st, src);
             cur.n = __shfl_sync(0xffffffffu, len, src);
-            cur.g = (int)(off / cur.nch);
-            cur.c = (int)(off % cur.nch);
+            divmod_nn(off, cur.nch, q, r);
+            cur.g = (int)q;
+            cur.c = (int)r;
             return;
         }
         before += __shfl_sync(0xffffffffu, incl, 31);
@@ -373,7 +410,12 @@ __device__ __forceinline__ uint4 q_piece_f16(const Params &p, const uint8_t *row
 template <int N>
 __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
 {
-    // the chunk kernel may launch now; it waits for this grid before reading
+    // Launched as a programmatic dependent of the kernel before the call on
+    // the stream (if any): its launch overlaps that kernel's tail, and it
+    // waits for that kernel to finish before it reads anything.  The chunk
+    // kernel may launch from then on (it reads the list, page table and
+    // pools before it waits for this grid, so it must not start earlier).
+    cudaGridDependencySynchronize();
     cudaTriggerProgrammaticLaunchCompletion();
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long pieces = (long long)p.n_seq * p.G * N * 32;
@@ -411,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     if (tid == 0) {
         mbar_init(&ms.k_full, kLoadThreads);
         mbar_init(&ms.k_empty, 1);
-        mbar_init(&ms.done, 1);
+        mbar_init(&ms.done, 2);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.v_full[i], kLoadThreads);
             mbar_init(&ms.v_empty[i], 1);
@@ -677,18 +719,24 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll 1
-                for (int r0 = 0; r0 < p.R; r0 += 8) { // rows R..N-1 are MMA padding
-                    float v[8];
-                    tmem_ld8(tmem + t_lane + kColO + 128u * (e.cp & 1) + 64u * hh + r0, v);
-                    const float4 f0 = *reinterpret_cast<const float4 *>(&ms.st_fin[r0]);
-                    const float4 f1 = *reinterpret_cast<const float4 *>(&ms.st_fin[r0 + 4]);
-                    const float fr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-                    tmem_wait_ld();
-                    float *dst = p.part_o + (base + r0) * kHeadDim + 128 * hh + c;
+                // all 8-row blocks that hold real rows in flight together, one wait
+                float v[8 * KR];
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        if (r0 + jj < p.R) dst[(size_t)jj * kHeadDim] = v[jj] * fr[jj];
+                for (int k = 0; k < KR; ++k)
+                    tmem_ld8(tmem + t_lane + kColO + 128u * (e.cp & 1) + 64u * hh + 8u * k, v + 8 * k);
+                tmem_wait_ld();
+                regs_after_wait<8 * KR>(v);
+                float *dst = p.part_o + base * kHeadDim + 128 * hh + c;
+#pragma unroll
+                for (int k = 0; k < KR; ++k) {
+                    const float4 f0 = *reinterpret_cast<const float4 *>(&ms.st_fin[8 * k]);
+                    const float4 f1 = *reinterpret_cast<const float4 *>(&ms.st_fin[8 * k + 4]);
+                    const float fr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int r = 8 * k + jj; // rows R..N-1 are MMA padding
+                        if (r < p.R) dst[(size_t)r * kHeadDim] = v[r] * fr[jj];
+                    }
                 }
             }
             tc_fence_before();
@@ -906,39 +954,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             named_bar(kBarSoft, kSoftThreads);
             epilogue(pend);
         }
-    } else {
-        // ================================================================ MMA warp
+    } else if (w == kMmaWarp) {
+        // ================================================================ S warp
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
-            const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
-            struct PvT {
-                int i, cp;
-                bool first, last;
-            };
-            auto issue_pv = [&](const PvT &t) {
-                wait(&ms.p_full[t.i % PB], (uint32_t)(t.i / PB) & 1u);
-                wait(&ms.v_full[t.i & 1], (uint32_t)(t.i >> 1) & 1u);
-                if (t.first && t.cp >= 2) wait(&ms.o_empty[t.cp & 1], (uint32_t)((t.cp - 2) >> 1) & 1u);
-                tc_fence_after();
-                // descriptors built once; a K step only moves the start address
-                // (field [0,14) in 16-byte units, no carry for shared addresses)
-                const uint64_t ad0 = smem_desc(s_v + (uint32_t)(t.i & 1) * kStageBytes, 16384, 1024);
-                const uint64_t bd0 = smem_desc(s_p + (uint32_t)(t.i % PB) * N * 256u, 16, 1024);
-                const uint32_t d0 = tmem + kColO + 128u * (t.cp & 1);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    // the two d halves interleaved: independent accumulators
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint64_t ad = ad0 + (uint64_t)(((uint32_t)(2 * hh) * 16384u + (uint32_t)kk * 2048u) >> 4);
-                        const uint64_t bd = bd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
-                        mma_f16_ss(d0 + 64u * hh, ad, bd, idesc_o, (t.first && kk == 0) ? 0u : 1u);
-                    }
-                }
-                mma_commit(&ms.v_empty[t.i & 1]);
-                mma_commit(&ms.p_empty[t.i % PB]);
-                if (t.last) mma_commit(&ms.o_full[t.cp & 1]);
-            };
             TileIt it;
             tile_init(p, it, first);
             // query tiles: one bulk copy per segment into buffer seg % QB.  With
@@ -962,9 +981,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     qnext = next_segment(p, qnext);
                 }
             }
-            int cp = -1, i = 0, cur_seg = -1;
-            PvT prev{0, 0, false, false};
-            for (; it.valid; ++i) {
+            int cur_seg = -1;
+            for (int i = 0; it.valid; ++i) {
                 const int seg = it.seg;
                 const bool seg_start = seg != cur_seg;
                 if (seg_start) wait(&ms.q_full[seg % QB], (uint32_t)(seg / QB) & 1u);
@@ -981,10 +999,6 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 }
                 mma_commit(&ms.k_empty);
                 mma_commit(&ms.s_full[i & 1]);
-                const bool first_t = it.ti == 0;
-                if (first_t) ++cp;
-                if (i >= 1) issue_pv(prev);
-                prev = PvT{i, cp, first_t, it.ti == it.nt - 1};
                 tile_next(p, it);
                 const bool seg_end = !it.valid || it.seg != seg;
                 if (seg_end) mma_commit(&ms.q_empty[seg % QB]);
@@ -1001,7 +1015,47 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     qnext = next_segment(p, qnext);
                 }
             }
-            if (i >= 1) issue_pv(prev);
+            mma_commit(&ms.done);
+            wait(&ms.done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ P.V warp
+        // A second issuing thread: one thread issues a tcgen05.mma every ~50-70
+        // cycles on this GPU, so S of the next tile and P.V of the current one
+        // go out from two warps side by side.
+        if (lane == 0) {
+            const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
+            TileIt it;
+            tile_init(p, it, first);
+            int cp = -1;
+            for (int i = 0; it.valid; ++i) {
+                const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
+                if (first_t) ++cp;
+                wait(&ms.p_full[i % PB], (uint32_t)(i / PB) & 1u);
+                wait(&ms.v_full[i & 1], (uint32_t)(i >> 1) & 1u);
+                if (first_t && cp >= 2) wait(&ms.o_empty[cp & 1], (uint32_t)((cp - 2) >> 1) & 1u);
+                tc_fence_after();
+                // descriptors built once; a K step only moves the start address
+                // (field [0,14) in 16-byte units, no carry for shared addresses)
+                const uint64_t ad0 = smem_desc(s_v + (uint32_t)(i & 1) * kStageBytes, 16384, 1024);
+                const uint64_t bd0 = smem_desc(s_p + (uint32_t)(i % PB) * N * 256u, 16, 1024);
+                const uint32_t d0 = tmem + kColO + 128u * (cp & 1);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    // the two d halves interleaved: independent accumulators
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint64_t ad = ad0 + (uint64_t)(((uint32_t)(2 * hh) * 16384u + (uint32_t)kk * 2048u) >> 4);
+                        const uint64_t bd = bd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
+                        mma_f16_ss(d0 + 64u * hh, ad, bd, idesc_o, (first_t && kk == 0) ? 0u : 1u);
+                    }
+                }
+                mma_commit(&ms.v_empty[i & 1]);
+                mma_commit(&ms.p_empty[i % PB]);
+                if (last_t) mma_commit(&ms.o_full[cp & 1]);
+                tile_next(p, it);
+            }
             mma_commit(&ms.done);
             wait(&ms.done, 0);
         }
@@ -1029,17 +1083,22 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
                                   (int)bytes)) != cudaSuccess)
         return e;
     const long long pieces = (long long)p.n_seq * p.G * N * 32;
-    qsa_query_stage_kernel<N><<<(unsigned)((pieces + 255) / 256), 256, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t scfg = {};
+    scfg.gridDim = dim3((unsigned)((pieces + 255) / 256));
+    scfg.blockDim = dim3(256);
+    scfg.stream = stream;
+    scfg.attrs = attr;
+    scfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&scfg, qsa_query_stage_kernel<N>, p)) != cudaSuccess) return e;
     const long long items = (long long)p.n_seq * p.G * p.n_chunks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, qsa_chunk_tc_kernel<N, KR>, p);

@@ -6,47 +6,55 @@
 //   M = max_{c: l_c > 0} m_c,  L = sum_c l_c e^{m_c - M},
 //   out = sum_c o_c e^{m_c - M} / L   (zeros when no chunk holds a cell).
 // A CTA of four warps covers four query rows with one warp each when a row
-// has at most four chunks, or one row with all four warps otherwise (warp w
-// takes chunks w, w+4, ...).  Lane k owns output dimensions 8k..8k+7.  Each
-// warp forms its own (M_w, L_w, acc_w), four chunks at a time with all their
-// loads in flight together and a running maximum; with four warps per row
-// their results are then combined in shared memory.  Every sum runs in a
-// fixed order, so the output is bit-identical from run to run.
+// has at most four chunks; otherwise a CTA of 4 (up to 16 chunks) or 16
+// warps takes one row (warp w takes chunks w, w + WPR, ...), so one round of
+// loads covers up to 64 chunks.  Lane k owns output dimensions 8k..8k+7.
+// Each warp forms its own (M_w, L_w, acc_w), four chunks at a time with all
+// their loads in flight together and a running maximum; the warps' results
+// are then combined in shared memory.  Every sum runs in a fixed order, so
+// the output is bit-identical from run to run.
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kMergeWarps = 4;
+constexpr int kHeadDimMerge = 256;
 
-template <int WPR> // warps per row: 1 or kMergeWarps
-__global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Params p)
+// WPR warps per row: 1 (a CTA of four warps takes four rows, a warp per
+// row), or 4 / 16 (a CTA per row; warp w takes chunks w, w + WPR, ...).
+template <int WPR>
+__global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(const Params p)
 {
-    __shared__ float s_acc[kMergeWarps][kHeadDim];
-    __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
+    constexpr int kWarps = WPR == 1 ? 4 : WPR;
+    constexpr int kRound = 4; // chunks per warp with all loads in flight together
+    __shared__ float s_acc[WPR == 1 ? 1 : WPR][kHeadDimMerge];
+    __shared__ float s_m[kWarps], s_l[kWarps];
     const int lane = threadIdx.x & 31;
     const int w = WPR == 1 ? 0 : threadIdx.x >> 5; // this warp's first chunk
-    const int r = WPR == 1 ? blockIdx.x * kMergeWarps + (threadIdx.x >> 5) : blockIdx.x;
+    const int r = WPR == 1 ? blockIdx.x * 4 + (threadIdx.x >> 5) : blockIdx.x;
     const int g = blockIdx.y;
     const int b = blockIdx.z;
+    // the next call's first kernel may launch now (it waits for this grid
+    // before it reads or writes anything)
+    cudaTriggerProgrammaticLaunchCompletion();
     // launched as a programmatic dependent of the chunk kernel: wait until
     // that grid has finished and its partials are visible
     cudaGridDependencySynchronize();
     if (r >= p.R) return;
     const size_t base = ((size_t)b * p.G + g) * p.n_chunks * p.R + r;
     const size_t stride = (size_t)p.R; // chunk stride of m and l
-    // chunks are taken four at a time with every load of a group issued
-    // together (the list length is only needed to mask the group, so its
-    // read overlaps the first group's), combined with a running maximum
+    // a round: kRound chunks per warp, every load issued together (the list
+    // length is only needed to mask them, so its read overlaps the loads),
+    // then folded in with a running maximum
     int start, n;
     seq_range(p, b, &start, &n);
     float M = -INFINITY, Lpart = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c0 = w; c0 < p.n_chunks; c0 += 4 * WPR) {
-        float mu[4], lu[4];
-        float4 ou[4][2];
+    for (int c0 = w; c0 < p.n_chunks; c0 += kRound * WPR) {
+        float mu[kRound], lu[kRound];
+        float4 ou[kRound][2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kRound; ++u) {
             const int c = c0 + u * WPR;
             mu[u] = -INFINITY;
             lu[u] = 0.f;
@@ -60,10 +68,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Param
             }
         }
         const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
-        bool ok[4];
+        bool ok[kRound];
         float gm = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kRound; ++u) {
             ok[u] = c0 + u * WPR < n_chunks && lu[u] > 0.f;
             if (ok[u]) gm = fmaxf(gm, mu[u]);
         }
@@ -75,7 +83,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Param
             M = gm;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kRound; ++u) {
             if (!ok[u]) continue;
             const float wu = mu[u] == M ? 1.f : expf(mu[u] - M);
             Lpart = fmaf(lu[u], wu, Lpart);
@@ -88,7 +96,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Param
             acc[6] = fmaf(ou[u][1].z, wu, acc[6]);
             acc[7] = fmaf(ou[u][1].w, wu, acc[7]);
         }
-        if (c0 + 4 * WPR >= n_chunks) break;
+        if (c0 + kRound * WPR >= n_chunks) break;
     }
     const int t = r / p.H, j = r % p.H;
     float *orow = p.out + (((size_t)b * p.T + t) * p.G * p.H + (size_t)g * p.H + j) * kHeadDim;
@@ -104,43 +112,55 @@ __global__ void __launch_bounds__(kMergeWarps * 32) qsa_merge_kernel(const Param
         }
         return;
     }
-    *reinterpret_cast<float4 *>(&s_acc[w][lane * 8]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4 *>(&s_acc[w][lane * 8 + 4]) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    const int wi = WPR == 1 ? 0 : w;
+    *reinterpret_cast<float4 *>(&s_acc[wi][lane * 8]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(&s_acc[wi][lane * 8 + 4]) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     if (lane == 0) {
-        s_m[w] = M;
-        s_l[w] = Lpart;
+        s_m[wi] = M;
+        s_l[wi] = Lpart;
     }
     __syncthreads();
 
-    // combine the warps' results (fixed order); thread t owns dimensions 2t, 2t+1
+    // combine the warps' results in a fixed order; each thread owns
+    // dimensions threadIdx.x, threadIdx.x + blockDim.x, ...
     float Mt = -INFINITY;
 #pragma unroll
-    for (int x = 0; x < kMergeWarps; ++x)
+    for (int x = 0; x < kWarps; ++x)
         if (s_l[x] > 0.f) Mt = fmaxf(Mt, s_m[x]);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-    if (Mt > -INFINITY) {
+    float fx[kWarps];
+    float L = 0.f;
 #pragma unroll
-        for (int x = 0; x < kMergeWarps; ++x) {
-            if (!(s_l[x] > 0.f)) continue;
-            const float f = s_m[x] == Mt ? 1.f : expf(s_m[x] - Mt);
-            L = fmaf(s_l[x], f, L);
-            o0 = fmaf(s_acc[x][2 * threadIdx.x], f, o0);
-            o1 = fmaf(s_acc[x][2 * threadIdx.x + 1], f, o1);
+    for (int x = 0; x < kWarps; ++x) {
+        fx[x] = 0.f;
+        if (Mt > -INFINITY && s_l[x] > 0.f) {
+            fx[x] = s_m[x] == Mt ? 1.f : expf(s_m[x] - Mt);
+            L = fmaf(s_l[x], fx[x], L);
         }
     }
-    float2 *dst = reinterpret_cast<float2 *>(orow + 2 * threadIdx.x);
-    *dst = L > 0.f ? make_float2(o0 / L, o1 / L) : make_float2(0.f, 0.f);
+    for (int d = threadIdx.x; d < kHeadDimMerge; d += WPR * 32) {
+        float o = 0.f;
+#pragma unroll
+        for (int x = 0; x < kWarps; ++x)
+            if (fx[x] != 0.f) o = fmaf(s_acc[x][d], fx[x], o);
+        orow[d] = L > 0.f ? o / L : 0.f;
+    }
 }
 
 } // namespace
 
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
-    // one warp per row when rows have few chunks, four otherwise
-    const bool wide = p.n_chunks > kMergeWarps;
+    // a warp per row when rows have few chunks; otherwise a CTA per row with
+    // enough warps that one round of loads covers every chunk when possible
+    // (16 warps per row only while the whole grid stays within about 48
+    // warps per SM; more rows take 4 warps each)
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long rows = (long long)p.R * p.G * p.n_seq;
+    const int wpr = p.n_chunks <= 4 ? 1 : (p.n_chunks > 16 && rows * 16 <= 48ll * sms) ? 16 : 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(wide ? p.R : (p.R + kMergeWarps - 1) / kMergeWarps), (unsigned)p.G, (unsigned)p.n_seq);
-    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.gridDim = dim3((unsigned)(wpr == 1 ? (p.R + 3) / 4 : p.R), (unsigned)p.G, (unsigned)p.n_seq);
+    cfg.blockDim = dim3(wpr == 1 ? 128 : wpr * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -148,8 +168,9 @@ cudaError_t launch_merge(const Params &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return wide ? cudaLaunchKernelEx(&cfg, qsa_merge_kernel<kMergeWarps>, p)
-                : cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1>, p);
+    if (wpr == 1) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1>, p);
+    if (wpr == 4) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<4>, p);
+    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<16>, p);
 }
 
 } // namespace qsa

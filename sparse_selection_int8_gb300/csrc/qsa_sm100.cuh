@@ -247,6 +247,15 @@ __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, float *v)
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// After tmem_wait_ld(): mark registers filled by tcgen05.ld as written here,
+// so no use of them can be scheduled before the wait.
+template <int K>
+__device__ __forceinline__ void regs_after_wait(float *v)
+{
+#pragma unroll
+    for (int i = 0; i < K; ++i) asm volatile("" : "+f"(v[i]));
+}
+
 // registers -> 32 lanes x 32-bit, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v)
 {
