@@ -754,12 +754,13 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             wait(&ms.sc_full[par], (uint32_t)(i >> 1) & 1u);
             // this thread's four cells (16x256b layout): cell(i) = 32q + 8i + t/4,
             // i = 2L + B for lane group L (lanes +16) and row half B (+8)
-            float ksc[4], vsc[4];
-            bool okc[4];
+            // per cell: K scale (x softmax scale x log2 e), V scale (0 when the
+            // cell is masked), and a bias of -inf that masks the cell's scores
+            float ksc[4], vsc[4], kbias[4];
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int cc = 32 * q + 8 * ci + ra;
-                okc[ci] = ms.sc_ok[par][cc] != 0;
+                kbias[ci] = ms.sc_ok[par][cc] != 0 ? 0.f : -INFINITY;
                 ksc[ci] = ms.rs_ks[i & 3][cc] * p.scale_log2;
                 vsc[ci] = ms.rs_vs[i & 3][cc];
             }
@@ -787,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                         for (int B = 0; B < 2; ++B) {
                             const int ci = 2 * L + B;
                             float &xv = x[L][4 * k + 2 * B + e];
-                            xv = okc[ci] ? __fmul_rn(xv, ksc[ci]) : -INFINITY;
+                            xv = __fmaf_rn(xv, ksc[ci], kbias[ci]); // = the rounded product, or -inf
                             m = fmaxf(m, xv);
                         }
                     }
@@ -806,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             {
                 float va = 0.f;
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci) va = fmaxf(va, okc[ci] ? fabsf(vsc[ci]) : 0.f);
+                for (int ci = 0; ci < 4; ++ci) va = fmaxf(va, fabsf(vsc[ci])); // (0 if masked)
                 const unsigned uu = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
                 if (lane == 0) ms.red_max[par][q][64] = __uint_as_float(uu);
             }
@@ -879,14 +880,16 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 // reference maxima of this thread's rows, read once (the P'
                 // stores below could otherwise force re-reads)
                 const float2 m2 = *reinterpret_cast<const float2 *>(&ms.st_mref[par][8 * k + 2 * u]);
-                mref_r[2 * k] = m2.x;
-                mref_r[2 * k + 1] = m2.y;
+                // (a row with no valid cell yet has mref = -inf: use 0, so its
+                // masked scores give 2^-inf = 0 rather than NaN)
+                mref_r[2 * k] = m2.x == -INFINITY ? 0.f : m2.x;
+                mref_r[2 * k + 1] = m2.y == -INFINITY ? 0.f : m2.y;
                 lrow[2 * k] = lrow[2 * k + 1] = 0.f;
             }
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int cc = 32 * q + 8 * ci + ra;
-                const float vsn = okc[ci] ? vsc[ci] * inv_sig : 0.f;
+                const float vsn = vsc[ci] * inv_sig; // 0 for a masked cell
                 const int L = ci >> 1, B = ci & 1;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -895,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     uint8_t *pe = p_tile + (cc >> 6) * N * 128 + r7 * 128 + ((((cc & 63) >> 3) ^ r7) << 4) + (cc & 7) * 2;
 #pragma unroll
                     for (int k = 0; k < KR; ++k) {
-                        const float pr = okc[ci] ? fast_exp2(x[L][4 * k + 2 * B + e] - mref_r[2 * k + e]) : 0.f;
+                        const float pr = fast_exp2(x[L][4 * k + 2 * B + e] - mref_r[2 * k + e]); // 0 if masked
                         lrow[2 * k + e] += pr;
                         *reinterpret_cast<__half *>(pe + 1024 * k) = __float2half_rn(pr * vsn);
                     }
