@@ -14,11 +14,13 @@
 //             bias, and the queries, each 128-row or 128-cell tile a
 //             contiguous 64 KB block in the 128-byte-swizzled layout;
 //   main      one CTA per (128-row query tile, chunk) loads image tiles with
-//             bulk async copies and runs, per 128-cell tile,
+//             bulk async copies (a copy warp) and runs, per 128-cell tile,
 //               S = Q . K_code^T        (M=128 rows, N=128 cells, K=256)
 //               P = 2^(S*ksc + bias - m_ref)      (online softmax)
 //               O += P . V_hat          (M=128 rows, N=256 d, K=128 cells)
-//             with S and O in tensor memory.  O is rescaled only when a
+//             with two S buffers and O in tensor memory, so the MMA warp
+//             runs S of the next tile while the softmax warps work on this
+//             one.  O is rescaled only when a
 //             row's max grows by more than 2^8 over its reference, so P
 //             stays below 256 and f16 holds it; the partial is brought to
 //             the true running max at the end.
@@ -160,16 +162,23 @@ __global__ void __launch_bounds__(256) qsa_prompt_stage_q(const Params p, const 
 
 // ---------------------------------------------------------------- main
 
-constexpr int kThreads = 2 * kTile; // two threads per query row (column halves)
+constexpr int kSoftThreads = 2 * kTile;       // two threads per query row (column halves)
+constexpr int kMmaWarp = kSoftThreads / 32;   // 8: issues the MMAs (one thread)
+constexpr int kLoadWarp = kMmaWarp + 1;       // 9: issues the bulk copies (one thread)
+constexpr int kThreads = kSoftThreads + 64;   // 320
+constexpr uint32_t kBarSoft = 1;              // named barrier of the softmax warps
 
+// (With the Q, K, V and P tiles, shared memory has 3 KB left for this.)
 struct PromptSmem {
-    float ksc[kTile];
-    float bias[kTile];
-    float rowmax[2][kTile]; // row maxima of the two column halves (rows' sums at the end)
-    uint64_t bar_q, bar_k, bar_v, bar_mma;
+    float ksc[kTile];           // per-cell score factors of the current tile
+    float bias[kTile];          // 0 or -inf (masked cell)
+    float rowmax[2][kTile];     // [column half][row]; the rows' sums at the end
+    uint64_t bar_q, k_full, k_empty, v_full, o_done, p_full, c_full;
+    uint64_t s_full[2], s_empty[2];
     uint32_t tmem;
     int32_t abort;
 };
+static_assert(sizeof(PromptSmem) <= 3072, "shared memory of the prompt kernel");
 
 __device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64_t *bar, uint32_t parity)
 {
@@ -182,8 +191,15 @@ __device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64
     return true;
 }
 
-// 256 threads: warp w owns query rows 32*(w%4)..+31 (its TMEM lanes) and
-// column half w/4 of S (cells) and of O (dimensions).
+// Warp roles: softmax warps 0-7 (warp w owns query rows 32*(w%4)..+31, its
+// TMEM lanes, and column half w/4 of S (cells) and of O (dimensions)); MMA
+// warp 8; bulk-copy warp 9.  Two S buffers in tensor memory let S of tile
+// j+1 run on the tensor cores while the softmax works on tile j; the
+// tensor pipe then takes O += P.V of tile j.  K, V and P have one shared-
+// memory buffer each (with Q resident, shared memory holds no more): K of
+// tile j+1 is copied as soon as S of tile j is done (during P.V of tile
+// j-1), V of tile j+1 as soon as P.V of tile j is done (during S of tile
+// j+2), the score factors once the softmax has read the previous ones.
 template <bool QBF16>
 __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params p, const PromptImages im)
 {
@@ -198,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     const uint32_t s_q = smem_u32(smem), s_k = s_q + kTileBytes, s_v = s_k + kTileBytes;
     const uint32_t s_p = s_v + kTileBytes;
     PromptSmem &ms = *reinterpret_cast<PromptSmem *>(smem + 3 * kTileBytes + kPBytes);
-    const int tid = threadIdx.x, w = tid >> 5;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x / p.n_chunks, c = blockIdx.x % p.n_chunks;
     const int g = blockIdx.y, b = blockIdx.z;
     int start, n;
@@ -212,14 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     const uint8_t *vimg = static_cast<const uint8_t *>(im.v) + tile0 * kTileBytes;
     const uint8_t *qimg = static_cast<const uint8_t *>(im.q) + (((size_t)b * p.G + g) * im.row_tiles + mt) * kTileBytes;
     const float *kscg = im.ksc + tile0 * kTile, *biasg = im.bias + tile0 * kTile;
-    const uint32_t idesc_s = idesc_f16(kTile, kTile, QBF16, QBF16, false, false);
-    const uint32_t idesc_o = idesc_f16(kTile, kHeadDim, false, false, false, true);
 
     if (tid == 0) {
         mbar_init(&ms.bar_q, 1);
-        mbar_init(&ms.bar_k, 1);
-        mbar_init(&ms.bar_v, 1);
-        mbar_init(&ms.bar_mma, 1);
+        mbar_init(&ms.k_full, 1);
+        mbar_init(&ms.k_empty, 1);
+        mbar_init(&ms.v_full, 1);
+        mbar_init(&ms.o_done, 1);
+        mbar_init(&ms.p_full, kSoftThreads);
+        mbar_init(&ms.c_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.s_empty[i], kSoftThreads);
+        }
         ms.abort = 0;
         fence_mbar_init();
     }
@@ -230,151 +251,214 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = ms.tmem, t_s = tmem, t_o = tmem + kTile;
-    const int row = 32 * (w & 3) + (tid & 31), hc = w >> 2;
-    const uint32_t t_lane = (uint32_t)(32 * (w & 3)) << 16;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&ms.bar_q, kTileBytes);
-        bulk_g2s(smem, qimg, kTileBytes, &ms.bar_q);
-        mbar_arrive_expect_tx(&ms.bar_k, kTileBytes + 2 * kTile * 4);
-        bulk_g2s(smem + kTileBytes, kimg, kTileBytes, &ms.bar_k);
-        bulk_g2s(ms.ksc, kscg, kTile * 4, &ms.bar_k);
-        bulk_g2s(ms.bias, biasg, kTile * 4, &ms.bar_k);
-        mbar_arrive_expect_tx(&ms.bar_v, kTileBytes);
-        bulk_g2s(smem + 2 * kTileBytes, vimg, kTileBytes, &ms.bar_v);
-    }
-    wait_bar(p, ms, &ms.bar_q, 0);
+    const uint32_t tmem = ms.tmem, t_o = tmem + 2 * kTile; // S buffers at columns 0 and 128
 
-    float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
-    uint32_t mma_phase = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-        wait_bar(p, ms, &ms.bar_k, j & 1);
-        if (tid == 0) {
+    if (w == kLoadWarp) {
+        // ================================================================ bulk copies
+        if (lane == 0) {
+            auto load_k = [&](int j) {
+                mbar_arrive_expect_tx(&ms.k_full, kTileBytes);
+                bulk_g2s(smem + kTileBytes, kimg + (size_t)j * kTileBytes, kTileBytes, &ms.k_full);
+            };
+            auto load_c = [&](int j) {
+                mbar_arrive_expect_tx(&ms.c_full, 2 * kTile * 4);
+                bulk_g2s(ms.ksc, kscg + (size_t)j * kTile, kTile * 4, &ms.c_full);
+                bulk_g2s(ms.bias, biasg + (size_t)j * kTile, kTile * 4, &ms.c_full);
+            };
+            auto load_v = [&](int j) {
+                mbar_arrive_expect_tx(&ms.v_full, kTileBytes);
+                bulk_g2s(smem + 2 * kTileBytes, vimg + (size_t)j * kTileBytes, kTileBytes, &ms.v_full);
+            };
+            mbar_arrive_expect_tx(&ms.bar_q, kTileBytes);
+            bulk_g2s(smem, qimg, kTileBytes, &ms.bar_q);
+            load_k(0);
+            load_c(0);
+            load_v(0);
+            int nk = 1, nc = 1, nv = 1; // copies issued
+            for (int j = 0; j + 1 < n_tiles && !ms.abort; ++j) {
+                // K of tile j+1 once S of tile j is done
+                if (!wait_bar(p, ms, &ms.k_empty, (uint32_t)j & 1u)) break;
+                load_k(j + 1);
+                ++nk;
+                // score factors of tile j+1 once the softmax of tile j has read its own
+                if (!wait_bar(p, ms, &ms.s_empty[j & 1], (uint32_t)(j >> 1) & 1u)) break;
+                load_c(j + 1);
+                ++nc;
+                // V of tile j+1 once P.V of tile j is done
+                if (!wait_bar(p, ms, &ms.o_done, (uint32_t)j & 1u)) break;
+                load_v(j + 1);
+                ++nv;
+            }
+            if (ms.abort) {
+                // copies still in flight after a timeout must land before exit
+                mbar_wait(&ms.k_full, (uint32_t)(nk - 1) & 1u, 1ll << 26);
+                mbar_wait(&ms.c_full, (uint32_t)(nc - 1) & 1u, 1ll << 26);
+                mbar_wait(&ms.v_full, (uint32_t)(nv - 1) & 1u, 1ll << 26);
+            }
+        }
+        __syncwarp();
+    } else if (w == kMmaWarp) {
+        // ================================================================ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(kTile, kTile, QBF16, QBF16, false, false);
+            const uint32_t idesc_o = idesc_f16(kTile, kHeadDim, false, false, false, true);
+            auto issue_s = [&](int j) {
+                const uint32_t t_s = tmem + (uint32_t)(j & 1) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint64_t ad = smem_desc(s_q + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc(s_k + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_f16_ss(t_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&ms.k_empty);
+                mma_commit(&ms.s_full[j & 1]);
+            };
+            wait_bar(p, ms, &ms.bar_q, 0);
+            wait_bar(p, ms, &ms.k_full, 0);
             tc_fence_after();
+            issue_s(0);
+            for (int j = 0; j < n_tiles && !ms.abort; ++j) {
+                if (j + 1 < n_tiles) {
+                    wait_bar(p, ms, &ms.k_full, (uint32_t)(j + 1) & 1u);
+                    if (j >= 1) wait_bar(p, ms, &ms.s_empty[(j + 1) & 1], (uint32_t)((j - 1) >> 1) & 1u);
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                wait_bar(p, ms, &ms.p_full, (uint32_t)j & 1u);
+                wait_bar(p, ms, &ms.v_full, (uint32_t)j & 1u);
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                const uint64_t ad = smem_desc(s_q + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
-                const uint64_t bd = smem_desc(s_k + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
-                mma_f16_ss(t_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint64_t ad = smem_desc(s_p + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc(s_v + kk * 2048, kTile * 128, 1024);
+                    mma_f16_ss(t_o, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&ms.o_done);
             }
-            mma_commit(&ms.bar_mma);
         }
-        wait_bar(p, ms, &ms.bar_mma, mma_phase);
-        mma_phase ^= 1;
-        tc_fence_after();
-        // ---- this thread's 64 scaled, masked scores, the row max, then P
-        float sv[64];
+        __syncwarp();
+    } else {
+        // ================================================================ softmax
+        const int row = 32 * (w & 3) + lane, hc = w >> 2;
+        const uint32_t t_lane = (uint32_t)(32 * (w & 3)) << 16;
+        float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int par = j & 1;
+            wait_bar(p, ms, &ms.c_full, (uint32_t)j & 1u);
+            wait_bar(p, ms, &ms.s_full[par], (uint32_t)(j >> 1) & 1u);
+            tc_fence_after();
+            // ---- this thread's 64 scaled, masked scores and the row max
+            float sv[64];
 #pragma unroll
-        for (int c16 = 0; c16 < 4; ++c16) tmem_ld16(t_s + t_lane + hc * 64 + c16 * 16, sv + c16 * 16);
-        tmem_wait_ld();
-        float mx = -INFINITY;
+            for (int c16 = 0; c16 < 4; ++c16)
+                tmem_ld16(tmem + (uint32_t)par * kTile + t_lane + hc * 64 + c16 * 16, sv + c16 * 16);
+            tmem_wait_ld();
+            regs_after_wait<64>(sv);
+            float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            sv[i] = fmaf(sv[i], ms.ksc[hc * 64 + i], ms.bias[hc * 64 + i]);
-            mx = fmaxf(mx, sv[i]);
-        }
-        ms.rowmax[hc][row] = mx;
-        __syncthreads();
-        mx = fmaxf(ms.rowmax[0][row], ms.rowmax[1][row]);
-        // rescale O (and l) when this row's max outgrows its reference by 2^8
-        bool rescale = false;
-        float factor = 1.f;
-        if (mx > -INFINITY) {
-            if (m_ref == -INFINITY) {
-                m_ref = mx;
-            } else if (mx > m_ref + 8.f) {
-                factor = fast_exp2(m_ref - mx);
-                l *= factor;
-                m_ref = mx;
-                rescale = true;
+            for (int i4 = 0; i4 < 16; ++i4) { // the factors by 16-byte broadcast loads
+                const float4 kf = *reinterpret_cast<const float4 *>(&ms.ksc[hc * 64 + 4 * i4]);
+                const float4 bf = *reinterpret_cast<const float4 *>(&ms.bias[hc * 64 + 4 * i4]);
+                sv[4 * i4] = fmaf(sv[4 * i4], kf.x, bf.x);
+                sv[4 * i4 + 1] = fmaf(sv[4 * i4 + 1], kf.y, bf.y);
+                sv[4 * i4 + 2] = fmaf(sv[4 * i4 + 2], kf.z, bf.z);
+                sv[4 * i4 + 3] = fmaf(sv[4 * i4 + 3], kf.w, bf.w);
+                mx = fmaxf(mx, fmaxf(fmaxf(sv[4 * i4], sv[4 * i4 + 1]), fmaxf(sv[4 * i4 + 2], sv[4 * i4 + 3])));
             }
-            m_run = fmaxf(m_run, mx);
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
+            tc_fence_before();
+            mbar_arrive(&ms.s_empty[par]); // S buffer of this parity and the score factors free
+            // every softmax thread has read the previous tile's row maxima
+            // once P of that tile is complete
+            if (j >= 1) wait_bar(p, ms, &ms.p_full, (uint32_t)(j - 1) & 1u);
+            ms.rowmax[hc][row] = mx;
+            named_bar(kBarSoft, kSoftThreads);
+            mx = fmaxf(ms.rowmax[0][row], ms.rowmax[1][row]);
+            // rescale O (and l) when this row's max outgrows its reference by 2^8
+            bool rescale = false;
+            float factor = 1.f;
+            if (mx > -INFINITY) {
+                if (m_ref == -INFINITY) {
+                    m_ref = mx;
+                } else if (mx > m_ref + 8.f) {
+                    factor = fast_exp2(m_ref - mx);
+                    l *= factor;
+                    m_ref = mx;
+                    rescale = true;
+                }
+                m_run = fmaxf(m_run, mx);
+            }
+            // P of this tile into registers first (the exponentials overlap P.V
+            // of tile j-1 on the tensor cores); a row with no valid cell yet
+            // keeps m_ref = -inf and only -inf scores: subtract 0 instead, so
+            // they give 2^-inf = 0, not NaN
+            const float m_sub = m_ref > -INFINITY ? m_ref : 0.f;
+            float lp[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t hw[32];
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                const float p0 = fast_exp2(sv[i] - m_sub);
+                const float p1 = fast_exp2(sv[i + 1] - m_sub);
+                lp[(i >> 1) & 3] += p0 + p1;
+                hw[i >> 1] = pack2<false>(p0, p1);
+            }
+            // P.V of tile j-1 must be done: it reads the P buffer, and O is
+            // rescaled in place
+            if (j >= 1) wait_bar(p, ms, &ms.o_done, (uint32_t)(j - 1) & 1u);
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-            for (int c16 = 0; c16 < 8; ++c16) {
-                float ov[16];
-                tmem_ld16(t_o + t_lane + hc * 128 + c16 * 16, ov);
-                tmem_wait_ld();
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    float ov[16];
+                    tmem_ld16(t_o + t_lane + hc * 128 + c16 * 16, ov);
+                    tmem_wait_ld();
+                    regs_after_wait<16>(ov);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) ov[i] *= factor;
-                tmem_st16(t_o + t_lane + hc * 128 + c16 * 16, ov);
+                    for (int i = 0; i < 16; ++i) ov[i] *= factor;
+                    tmem_st16(t_o + t_lane + hc * 128 + c16 * 16, ov);
+                }
+                tmem_wait_st();
             }
-            tmem_wait_st();
-        }
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t hw[4];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const float p0 = m_ref > -INFINITY ? fast_exp2(sv[c8 * 8 + i] - m_ref) : 0.f;
-                const float p1 = m_ref > -INFINITY ? fast_exp2(sv[c8 * 8 + i + 1] - m_ref) : 0.f;
-                l += p0 + p1;
-                hw[i / 2] = pack2<false>(p0, p1);
-            }
-            sts128(s_p + kmajor_sw128_off(row, hc * 64 + c8 * 8, kTile), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+            for (int c8 = 0; c8 < 8; ++c8)
+                sts128(s_p + kmajor_sw128_off(row, hc * 64 + c8 * 8, kTile),
+                       make_uint4(hw[4 * c8], hw[4 * c8 + 1], hw[4 * c8 + 2], hw[4 * c8 + 3]));
+            l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&ms.p_full);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads(); // P written, S and the scale vectors read, O rescaled
-        tc_fence_after();
-        if (tid == 0 && j + 1 < n_tiles && !ms.abort) {
-            mbar_arrive_expect_tx(&ms.bar_k, kTileBytes + 2 * kTile * 4);
-            bulk_g2s(smem + kTileBytes, kimg + (size_t)(j + 1) * kTileBytes, kTileBytes, &ms.bar_k);
-            bulk_g2s(ms.ksc, kscg + (size_t)(j + 1) * kTile, kTile * 4, &ms.bar_k);
-            bulk_g2s(ms.bias, biasg + (size_t)(j + 1) * kTile, kTile * 4, &ms.bar_k);
-        }
-        wait_bar(p, ms, &ms.bar_v, j & 1);
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-                const uint64_t ad = smem_desc(s_p + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
-                const uint64_t bd = smem_desc(s_v + kk * 2048, kTile * 128, 1024);
-                mma_f16_ss(t_o, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&ms.bar_mma);
-        }
-        wait_bar(p, ms, &ms.bar_mma, mma_phase);
-        mma_phase ^= 1;
-        tc_fence_after();
-        if (tid == 0 && j + 1 < n_tiles && !ms.abort) {
-            mbar_arrive_expect_tx(&ms.bar_v, kTileBytes);
-            bulk_g2s(smem + 2 * kTileBytes, vimg + (size_t)(j + 1) * kTileBytes, kTileBytes, &ms.bar_v);
-        }
-    }
 
-    // ---- the partial relative to the row's true maximum
-    ms.rowmax[hc][row] = l; // reused for the two halves' sums
-    __syncthreads();
-    const int r = mt * kTile + row;
-    const size_t base = (((size_t)b * p.G + g) * p.n_chunks + c) * p.R;
-    const float fin = (m_run > -INFINITY && m_ref < m_run) ? fast_exp2(m_ref - m_run) : 1.f;
-    if (r < p.R && hc == 0) {
-        p.part_m[base + r] = m_run > -INFINITY ? m_run * kLn2 : -INFINITY;
-        p.part_l[base + r] = m_run > -INFINITY ? (ms.rowmax[0][row] + ms.rowmax[1][row]) * fin : 0.f;
-    }
+        // ---- the partial relative to the row's true maximum
+        wait_bar(p, ms, &ms.o_done, (uint32_t)(n_tiles - 1) & 1u); // last P.V done
+        tc_fence_after();
+        wait_bar(p, ms, &ms.p_full, (uint32_t)(n_tiles - 1) & 1u); // (row maxima read)
+        ms.rowmax[hc][row] = l; // reused for the two halves' sums
+        named_bar(kBarSoft, kSoftThreads);
+        const int r = mt * kTile + row;
+        const size_t base = (((size_t)b * p.G + g) * p.n_chunks + c) * p.R;
+        const float fin = (m_run > -INFINITY && m_ref < m_run) ? fast_exp2(m_ref - m_run) : 1.f;
+        if (r < p.R && hc == 0) {
+            p.part_m[base + r] = m_run > -INFINITY ? m_run * kLn2 : -INFINITY;
+            p.part_l[base + r] = m_run > -INFINITY ? (ms.rowmax[0][row] + ms.rowmax[1][row]) * fin : 0.f;
+        }
 #pragma unroll 1
-    for (int c16 = 0; c16 < 8; ++c16) {
-        float ov[16];
-        tmem_ld16(t_o + t_lane + hc * 128 + c16 * 16, ov);
-        tmem_wait_ld();
-        if (r < p.R) {
-            float4 *dst = reinterpret_cast<float4 *>(p.part_o + (base + r) * kHeadDim + hc * 128 + c16 * 16);
+        for (int c16 = 0; c16 < 8; ++c16) {
+            float ov[16];
+            tmem_ld16(t_o + t_lane + hc * 128 + c16 * 16, ov);
+            tmem_wait_ld();
+            regs_after_wait<16>(ov);
+            if (r < p.R) {
+                float4 *dst = reinterpret_cast<float4 *>(p.part_o + (base + r) * kHeadDim + hc * 128 + c16 * 16);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float a0 = m_run > -INFINITY ? ov[4 * i] * fin : 0.f;
-                const float a1 = m_run > -INFINITY ? ov[4 * i + 1] * fin : 0.f;
-                const float a2 = m_run > -INFINITY ? ov[4 * i + 2] * fin : 0.f;
-                const float a3 = m_run > -INFINITY ? ov[4 * i + 3] * fin : 0.f;
-                dst[i] = make_float4(a0, a1, a2, a3);
+                for (int i = 0; i < 4; ++i) {
+                    const float a0 = m_run > -INFINITY ? ov[4 * i] * fin : 0.f;
+                    const float a1 = m_run > -INFINITY ? ov[4 * i + 1] * fin : 0.f;
+                    const float a2 = m_run > -INFINITY ? ov[4 * i + 2] * fin : 0.f;
+                    const float a3 = m_run > -INFINITY ? ov[4 * i + 3] * fin : 0.f;
+                    dst[i] = make_float4(a0, a1, a2, a3);
+                }
             }
         }
-    }
-    // bulk copies still in flight after a timeout must land before exit
-    if (tid == 0 && ms.abort) {
-        mbar_wait(&ms.bar_k, n_tiles & 1, 1ll << 26);
-        mbar_wait(&ms.bar_v, n_tiles & 1, 1ll << 26);
     }
     tc_fence_before();
     __syncthreads();
