@@ -20,7 +20,8 @@
 //               O += P . V_hat          (M=128 rows, N=256 d, K=128 cells)
 //             with two S buffers and O in tensor memory, so the MMA warp
 //             runs S of the next tile while the softmax warps work on this
-//             one.  O is rescaled only when a
+//             one; P (f16) overwrites its own S in tensor memory and is the
+//             A operand of P . V_hat there.  O is rescaled only when a
 //             row's max grows by more than 2^8 over its reference, so P
 //             stays below 256 and f16 holds it; the partial is brought to
 //             the true running max at the end.
@@ -43,14 +44,11 @@ using namespace sm100;
 
 constexpr int kTile = 128;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2; // 64 KB image tile
-constexpr uint32_t kPBytes = kTile * kTile * 2;       // 32 KB P tile
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
+// Tensor-memory column of P's packed f16 pair k (cells 2k, 2k+1) inside its
+// S buffer: the softmax thread of column half h holds S columns 64h..64h+63
+// and writes its 32 pairs over the first half of them.
+__device__ __forceinline__ uint32_t p_col(int k) { return (uint32_t)(k < 32 ? k : 32 + k); }
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b)
@@ -168,7 +166,7 @@ constexpr int kLoadWarp = kMmaWarp + 1;       // 9: issues the bulk copies (one 
 constexpr int kThreads = kSoftThreads + 64;   // 320
 constexpr uint32_t kBarSoft = 1;              // named barrier of the softmax warps
 
-// (With the Q, K, V and P tiles, shared memory has 3 KB left for this.)
+// (Shared memory holds the Q, K and V tiles and this.)
 struct PromptSmem {
     float ksc[kTile];           // per-cell score factors of the current tile
     float bias[kTile];          // 0 or -inf (masked cell)
@@ -195,11 +193,14 @@ __device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64
 // TMEM lanes, and column half w/4 of S (cells) and of O (dimensions)); MMA
 // warp 8; bulk-copy warp 9.  Two S buffers in tensor memory let S of tile
 // j+1 run on the tensor cores while the softmax works on tile j; the
-// tensor pipe then takes O += P.V of tile j.  K, V and P have one shared-
-// memory buffer each (with Q resident, shared memory holds no more): K of
-// tile j+1 is copied as soon as S of tile j is done (during P.V of tile
-// j-1), V of tile j+1 as soon as P.V of tile j is done (during S of tile
-// j+2), the score factors once the softmax has read the previous ones.
+// tensor pipe then takes O += P.V of tile j, with P of tile j in tensor
+// memory where S of tile j was.  S of tile j+2 reuses that buffer; it is
+// issued after P.V of tile j by the same thread, and the tensor pipe runs
+// one thread's MMAs in order.  K and V have one shared-memory buffer each
+// (with Q resident, shared memory holds no more): K of tile j+1 is copied
+// as soon as S of tile j is done (during P.V of tile j-1), V of tile j+1 as
+// soon as P.V of tile j is done (during S of tile j+2), the score factors
+// once the softmax has read the previous ones.
 template <bool QBF16>
 __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params p, const PromptImages im)
 {
@@ -212,8 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
         return;
     }
     const uint32_t s_q = smem_u32(smem), s_k = s_q + kTileBytes, s_v = s_k + kTileBytes;
-    const uint32_t s_p = s_v + kTileBytes;
-    PromptSmem &ms = *reinterpret_cast<PromptSmem *>(smem + 3 * kTileBytes + kPBytes);
+    PromptSmem &ms = *reinterpret_cast<PromptSmem *>(smem + 3 * kTileBytes);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.x / p.n_chunks, c = blockIdx.x % p.n_chunks;
     const int g = blockIdx.y, b = blockIdx.z;
@@ -327,11 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 wait_bar(p, ms, &ms.p_full, (uint32_t)j & 1u);
                 wait_bar(p, ms, &ms.v_full, (uint32_t)j & 1u);
                 tc_fence_after();
+                const uint32_t t_p = tmem + (uint32_t)(j & 1) * kTile; // P of tile j
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t ad = smem_desc(s_p + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc(s_v + kk * 2048, kTile * 128, 1024);
-                    mma_f16_ss(t_o, ad, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_ts(t_o, t_p + p_col(8 * kk), bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&ms.o_done);
             }
@@ -401,11 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 lp[(i >> 1) & 3] += p0 + p1;
                 hw[i >> 1] = pack2<false>(p0, p1);
             }
-            // P.V of tile j-1 must be done: it reads the P buffer, and O is
-            // rescaled in place
-            if (j >= 1) wait_bar(p, ms, &ms.o_done, (uint32_t)(j - 1) & 1u);
-            tc_fence_after();
+            // P over this thread's half of S (already in registers)
+            const uint32_t t_p = tmem + (uint32_t)par * kTile + t_lane + hc * 64;
+            tmem_st16u(t_p, hw);
+            tmem_st16u(t_p + 16, hw + 16);
             if (__any_sync(0xffffffffu, rescale)) {
+                // O is rescaled in place once P.V of tile j-1 is done
+                if (j >= 1) wait_bar(p, ms, &ms.o_done, (uint32_t)(j - 1) & 1u);
+                tc_fence_after();
 #pragma unroll 1
                 for (int c16 = 0; c16 < 8; ++c16) {
                     float ov[16];
@@ -418,12 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 }
                 tmem_wait_st();
             }
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                sts128(s_p + kmajor_sw128_off(row, hc * 64 + c8 * 8, kTile),
-                       make_uint4(hw[4 * c8], hw[4 * c8 + 1], hw[4 * c8 + 2], hw[4 * c8 + 3]));
             l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&ms.p_full);
         }
@@ -476,7 +475,7 @@ cudaError_t launch_prompt(const Params &p, const PromptImages &im, cudaStream_t 
     dim3 gq((unsigned)im.row_tiles, (unsigned)p.G, (unsigned)p.n_seq);
     qsa_prompt_stage_q<QBF16><<<gq, 256, 0, stream>>>(p, im);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int bytes = (int)(3 * kTileBytes + kPBytes + sizeof(PromptSmem));
+    const int bytes = (int)(3 * kTileBytes + sizeof(PromptSmem));
     if ((e = cudaFuncSetAttribute(qsa_prompt_tc_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   bytes)) != cudaSuccess)
         return e;
