@@ -162,8 +162,9 @@ __global__ void __launch_bounds__(256) qsa_prompt_stage_q(const Params p, const 
 
 constexpr int kSoftThreads = 2 * kTile;       // two threads per query row (column halves)
 constexpr int kMmaWarp = kSoftThreads / 32;   // 8: issues the MMAs (one thread)
-constexpr int kLoadWarp = kMmaWarp + 1;       // 9: issues the bulk copies (one thread)
-constexpr int kThreads = kSoftThreads + 64;   // 320
+constexpr int kLoadWarp = kMmaWarp + 1;       // 9: bulk copies of Q, K and the score factors (one thread)
+constexpr int kVLoadWarp = kLoadWarp + 1;     // 10: bulk copies of V (one thread)
+constexpr int kThreads = kSoftThreads + 96;   // 352
 constexpr uint32_t kBarSoft = 1;              // named barrier of the softmax warps
 
 // (Shared memory holds the Q, K and V tiles and this.)
@@ -254,7 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     const uint32_t tmem = ms.tmem, t_o = tmem + 2 * kTile; // S buffers at columns 0 and 128
 
     if (w == kLoadWarp) {
-        // ================================================================ bulk copies
+        // ================================================================ bulk copies (Q, K, factors)
+        // K and V have their own copy threads: the tensor pipe frees the K
+        // buffer (S of a tile) before the V buffer (P.V of the previous
+        // tile), and neither copy waits for the other's buffer.
         if (lane == 0) {
             auto load_k = [&](int j) {
                 mbar_arrive_expect_tx(&ms.k_full, kTileBytes);
@@ -265,16 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 bulk_g2s(ms.ksc, kscg + (size_t)j * kTile, kTile * 4, &ms.c_full);
                 bulk_g2s(ms.bias, biasg + (size_t)j * kTile, kTile * 4, &ms.c_full);
             };
-            auto load_v = [&](int j) {
-                mbar_arrive_expect_tx(&ms.v_full, kTileBytes);
-                bulk_g2s(smem + 2 * kTileBytes, vimg + (size_t)j * kTileBytes, kTileBytes, &ms.v_full);
-            };
             mbar_arrive_expect_tx(&ms.bar_q, kTileBytes);
             bulk_g2s(smem, qimg, kTileBytes, &ms.bar_q);
             load_k(0);
             load_c(0);
-            load_v(0);
-            int nk = 1, nc = 1, nv = 1; // copies issued
+            int nk = 1, nc = 1; // copies issued
             for (int j = 0; j + 1 < n_tiles && !ms.abort; ++j) {
                 // K of tile j+1 once S of tile j is done
                 if (!wait_bar(p, ms, &ms.k_empty, (uint32_t)j & 1u)) break;
@@ -284,17 +283,30 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 if (!wait_bar(p, ms, &ms.s_empty[j & 1], (uint32_t)(j >> 1) & 1u)) break;
                 load_c(j + 1);
                 ++nc;
-                // V of tile j+1 once P.V of tile j is done
-                if (!wait_bar(p, ms, &ms.o_done, (uint32_t)j & 1u)) break;
-                load_v(j + 1);
-                ++nv;
             }
             if (ms.abort) {
                 // copies still in flight after a timeout must land before exit
                 mbar_wait(&ms.k_full, (uint32_t)(nk - 1) & 1u, 1ll << 26);
                 mbar_wait(&ms.c_full, (uint32_t)(nc - 1) & 1u, 1ll << 26);
-                mbar_wait(&ms.v_full, (uint32_t)(nv - 1) & 1u, 1ll << 26);
             }
+        }
+        __syncwarp();
+    } else if (w == kVLoadWarp) {
+        // ================================================================ bulk copies (V)
+        if (lane == 0) {
+            auto load_v = [&](int j) {
+                mbar_arrive_expect_tx(&ms.v_full, kTileBytes);
+                bulk_g2s(smem + 2 * kTileBytes, vimg + (size_t)j * kTileBytes, kTileBytes, &ms.v_full);
+            };
+            load_v(0);
+            int nv = 1;
+            for (int j = 0; j + 1 < n_tiles && !ms.abort; ++j) {
+                // V of tile j+1 once P.V of tile j is done
+                if (!wait_bar(p, ms, &ms.o_done, (uint32_t)j & 1u)) break;
+                load_v(j + 1);
+                ++nv;
+            }
+            if (ms.abort) mbar_wait(&ms.v_full, (uint32_t)(nv - 1) & 1u, 1ll << 26);
         }
         __syncwarp();
     } else if (w == kMmaWarp) {
