@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
             tmem_st16u(t_p, hw);
             tmem_st16u(t_p + 16, hw + 16);
             if (__any_sync(0xffffffffu, rescale)) {
-                // O is rescaled in place once P.V of tile j-1 is done
+                // O is rescaled in place once P.V of tile j-1 is done (S of
+                // tile j, done, was issued after P.V of tile j-2, so the
+                // barrier is at most one phase behind)
                 if (j >= 1) wait_bar(p, ms, &ms.o_done, (uint32_t)(j - 1) & 1u);
                 tc_fence_after();
 #pragma unroll 1
@@ -439,7 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
             mbar_arrive(&ms.p_full);
         }
 
-        // ---- the partial relative to the row's true maximum
+        // ---- the partial relative to the row's true maximum.  The waits
+        // test phase parity, so they go one phase at a time: S of the last
+        // tile was issued after P.V of the tile three back, so the barrier
+        // is at most two phases behind here.
+        if (n_tiles >= 2) wait_bar(p, ms, &ms.o_done, (uint32_t)(n_tiles - 2) & 1u);
         wait_bar(p, ms, &ms.o_done, (uint32_t)(n_tiles - 1) & 1u); // last P.V done
         tc_fence_after();
         wait_bar(p, ms, &ms.p_full, (uint32_t)(n_tiles - 1) & 1u); // (row maxima read)

@@ -374,3 +374,24 @@ def test_prompt_path_growing_scores():
     ks = np.linspace(0.005, 0.1, p.pool_cells, dtype=np.float32)
     p.k_scale[0, 0] = ks[p.page_table[0].argsort()]  # cell at list position i gets ks[i]
     check_full(p, "auto", "prompt growing scores")
+
+
+@pytest.mark.parametrize("cells", [256, 512, 1536])
+def test_prompt_path_multi_tile_repeatable(cells):
+    """Chunks of two or more 128-cell tiles on the rows-on-M path: every row
+    against the oracle, and the output bit-identical over repeated calls (the
+    last tiles' P.V must be complete before the partials are read)."""
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.prompt_shaped(n_queries=11, pool_cells=cells, chunk_cells=cells)
+    ref = oracle.decode_attn(p)
+    first = None
+    for _ in range(5):
+        dp = qsa.DeviceProblem(p, algo=algo_code("tcgen05"))
+        dp.out.fill_(float("nan"))
+        dp.run()
+        torch.cuda.synchronize()
+        out = dp.out.cpu().numpy()
+        assert_parity(out, ref, f"prompt {cells} cells")
+        if first is None:
+            first = out
+        assert out.tobytes() == first.tobytes()
