@@ -197,7 +197,7 @@ def source_digest(*names) -> str:
 # only while the kernel source hashes to the recorded digest.
 TRAFFIC = {
     # qsa_decode T = 1..4, chunk kernel, sum of the four launches (profiles/qsa_chunk_tc_qsa_decode_sweep.md)
-    "1ce82677f82c709e": 6024960,
+    "3a44965674c11597": 6039552,
 }
 
 # Sources of the chunk kernel the recorded traffic belongs to.
