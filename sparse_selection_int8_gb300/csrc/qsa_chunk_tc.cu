@@ -380,26 +380,51 @@ __device__ __forceinline__ int q_piece_source(int pc)
     return (k < 8 ? 4 * k : 128 + 4 * (k - 8)) + 32 * u0;
 }
 
-// Query piece pc of the row at `row` (f32 or bf16 elements) -> f16x8.
-__device__ __forceinline__ uint4 q_piece_f16(const Params &p, const uint8_t *row, int pc)
+// The raw elements of query piece pc of the row at `row`: four at s0 and
+// four at s0 + 32 (f32: a and b whole; bf16: a.x, a.y and b.x, b.y).
+struct QRaw {
+    uint4 a, b;
+};
+
+__device__ __forceinline__ QRaw q_piece_load(const Params &p, const uint8_t *row, int pc)
 {
     const int s0 = q_piece_source(pc);
-    float f[8];
+    QRaw q;
     if (p.q_bf16) {
         const uint2 a = *reinterpret_cast<const uint2 *>(row + 2 * s0);
         const uint2 b = *reinterpret_cast<const uint2 *>(row + 2 * (s0 + 32));
-        f[0] = bf16_bits_to_f32(a.x & 0xffff); f[1] = bf16_bits_to_f32(a.x >> 16);
-        f[2] = bf16_bits_to_f32(a.y & 0xffff); f[3] = bf16_bits_to_f32(a.y >> 16);
-        f[4] = bf16_bits_to_f32(b.x & 0xffff); f[5] = bf16_bits_to_f32(b.x >> 16);
-        f[6] = bf16_bits_to_f32(b.y & 0xffff); f[7] = bf16_bits_to_f32(b.y >> 16);
+        q.a = make_uint4(a.x, a.y, 0u, 0u);
+        q.b = make_uint4(b.x, b.y, 0u, 0u);
     } else {
-        const float4 a = *reinterpret_cast<const float4 *>(row + 4 * s0);
-        const float4 b = *reinterpret_cast<const float4 *>(row + 4 * (s0 + 32));
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        q.a = *reinterpret_cast<const uint4 *>(row + 4 * s0);
+        q.b = *reinterpret_cast<const uint4 *>(row + 4 * (s0 + 32));
+    }
+    return q;
+}
+
+// Raw query piece -> f16x8.
+__device__ __forceinline__ uint4 q_piece_cvt(const Params &p, const QRaw &q)
+{
+    float f[8];
+    if (p.q_bf16) {
+        f[0] = bf16_bits_to_f32(q.a.x & 0xffff); f[1] = bf16_bits_to_f32(q.a.x >> 16);
+        f[2] = bf16_bits_to_f32(q.a.y & 0xffff); f[3] = bf16_bits_to_f32(q.a.y >> 16);
+        f[4] = bf16_bits_to_f32(q.b.x & 0xffff); f[5] = bf16_bits_to_f32(q.b.x >> 16);
+        f[6] = bf16_bits_to_f32(q.b.y & 0xffff); f[7] = bf16_bits_to_f32(q.b.y >> 16);
+    } else {
+        f[0] = __uint_as_float(q.a.x); f[1] = __uint_as_float(q.a.y);
+        f[2] = __uint_as_float(q.a.z); f[3] = __uint_as_float(q.a.w);
+        f[4] = __uint_as_float(q.b.x); f[5] = __uint_as_float(q.b.y);
+        f[6] = __uint_as_float(q.b.z); f[7] = __uint_as_float(q.b.w);
     }
     return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
                       pack_f16x2(f[6], f[7]));
+}
+
+// Query piece pc of the row at `row` (f32 or bf16 elements) -> f16x8.
+__device__ __forceinline__ uint4 q_piece_f16(const Params &p, const uint8_t *row, int pc)
+{
+    return q_piece_cvt(p, q_piece_load(p, row, pc));
 }
 
 // Query tiles of every (sequence, KV head) pair, written once per call into
@@ -465,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             mbar_init(&ms.p_empty[i], 1);
             mbar_init(&ms.o_full[i], 1);
             mbar_init(&ms.o_empty[i], kSoftThreads);
-            mbar_init(&ms.q_full[i], 1);
+            // bulk copy (one arrival + bytes), or the softmax threads' stores
+            mbar_init(&ms.q_full[i], p.q_inline ? kSoftThreads : 1);
             mbar_init(&ms.q_empty[i], 1);
             ms.st_any[i] = -1;
             ms.st_sig[i] = 1.f;
@@ -747,6 +773,25 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
         };
 
+        if (p.q_inline && it.valid) {
+            // One (sequence, KV head) in the whole call: this CTA converts its
+            // query tile itself into buffer 0, in the layout of the staged
+            // images (f16, K-major, 128-byte swizzle, permuted contraction
+            // index, rows >= R zero), while the loaders resolve the first
+            // tiles.  Nothing of the previous call is read or written here.
+            const int esz = p.q_bf16 ? 2 : 4;
+            for (int e = c; e < N * 32; e += kSoftThreads) {
+                const int r = e >> 5, pc = e & 31;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (r < p.R) v = q_piece_f16(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, first.b, first.g, r) * esz, pc);
+                *reinterpret_cast<uint4 *>(smem + L::q + kmajor_sw128_off(r, pc * 8, N)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&ms.q_full[0]);
+            // the call before may still be reading the workspace (partials) or
+            // writing the output: wait for it before this CTA writes anything
+            cudaGridDependencySynchronize();
+        }
         for (int i = 0; it.valid; ++i) {
             const int par = i & 1;
             const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
@@ -977,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             };
             Cursor qnext = first;
             int qseg = 0; // next segment whose tile is to be loaded
-            if (it.valid) {
+            if (it.valid && !p.q_inline) {
                 cudaGridDependencySynchronize(); // the tiles come from the staging kernel
                 for (; qseg < QB && qnext.remaining > 0; ++qseg) {
                     load_q(qnext, qseg);
@@ -1089,13 +1134,15 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t scfg = {};
-    scfg.gridDim = dim3((unsigned)((pieces + 255) / 256));
-    scfg.blockDim = dim3(256);
-    scfg.stream = stream;
-    scfg.attrs = attr;
-    scfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&scfg, qsa_query_stage_kernel<N>, p)) != cudaSuccess) return e;
+    if (!p.q_inline) {
+        cudaLaunchConfig_t scfg = {};
+        scfg.gridDim = dim3((unsigned)((pieces + 255) / 256));
+        scfg.blockDim = dim3(256);
+        scfg.stream = stream;
+        scfg.attrs = attr;
+        scfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&scfg, qsa_query_stage_kernel<N>, p)) != cudaSuccess) return e;
+    }
     const long long items = (long long)p.n_seq * p.G * p.n_chunks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
@@ -1117,9 +1164,13 @@ size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
     return (size_t)n_seq * G * N * 512;
 }
 
-cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream)
+cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
 {
-    if (p.n_chunks == 0) return cudaSuccess;
+    if (p_in.n_chunks == 0) return cudaSuccess;
+    // one (sequence, KV head): every CTA works on the same query tile and
+    // converts it itself, so the call is two kernels (chunk, merge)
+    Params p = p_in;
+    p.q_inline = p.n_seq * p.G == 1 ? 1 : 0;
     switch ((p.R + 7) / 8) { // 8-row blocks of real rows; N = that, padded to 16
     case 1: return launch_n<16, 1>(p, stream);
     case 2: return launch_n<16, 2>(p, stream);
