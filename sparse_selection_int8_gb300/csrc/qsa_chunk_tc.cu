@@ -436,12 +436,15 @@ template <int N>
 __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
 {
     // Launched as a programmatic dependent of the kernel before the call on
-    // the stream (if any): its launch overlaps that kernel's tail, and it
-    // waits for that kernel to finish before it reads anything.  The chunk
-    // kernel may launch from then on (it reads the list, page table and
-    // pools before it waits for this grid, so it must not start earlier).
-    cudaGridDependencySynchronize();
+    // the stream (if any, the previous call's merge).  The chunk kernel may
+    // launch at once: before it waits for this grid it only reads the
+    // caller's inputs (list, page table, pools).  This kernel then waits for
+    // the kernel before it, whose chunk kernel may still be reading the query
+    // images, before it rewrites them; so once this grid is complete the call
+    // before is too, and the chunk kernel's wait for it covers its partial
+    // writes as well.
     cudaTriggerProgrammaticLaunchCompletion();
+    cudaGridDependencySynchronize();
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long pieces = (long long)p.n_seq * p.G * N * 32;
     if (e >= pieces) return;
