@@ -114,13 +114,6 @@ struct Lay {
     static constexpr uint32_t total = misc + (uint32_t)((sizeof(Misc) + 127) / 128 * 128);
 };
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 // Four int8 codes -> four f16 values (exact): bias the bytes to u = code+128,
 // place them as the low mantissa bits of 1024 (0x6400), subtract 1152.
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
@@ -131,17 +124,6 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     const uint32_t bias = 0x64806480u;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
-}
-
-__device__ __forceinline__ int ordered_key(float f)
-{
-    const int i = __float_as_int(f);
-    return i >= 0 ? i : i ^ 0x7fffffff;
-}
-
-__device__ __forceinline__ float from_ordered_key(int k)
-{
-    return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b)
@@ -335,16 +317,8 @@ __device__ __forceinline__ int tile_base(const Params &p, const TileIt &t)
 
 constexpr int kBadPos = INT_MIN;
 
-// Page-table entry of list entry `pos` (has = the tile holds this cell).
-__device__ __forceinline__ int page_entry(const Params &p, int b, int pos, bool has)
-{
-    if (!has) return -1;
-    if (pos < 0 || pos >= p.page_table_len) return kBadPos;
-    return __ldg(p.page_table + (size_t)b * p.page_table_len + pos);
-}
-
 // Checked pool slot, -1 when masked or out of range; `report` raises the
-// status bits (one of the two threads of a cell reports).
+// status bits (the one thread that resolves the cell reports).
 __device__ __forceinline__ int slot_of(const Params &p, int raw, bool report)
 {
     if (raw == kBadPos) {
