@@ -29,9 +29,15 @@
  *   - Device-side input errors never trap: an out-of-range list entry or page
  *     slot is treated as masked and raises a bit in the optional status word.
  *   - Kernels are launched with programmatic dependent launch: a call's first
- *     kernel may start while the previous kernel on the stream finishes (it
- *     waits for that kernel before reading anything), and the next kernel on
- *     the stream may start early too.  A kernel launched after a call with
+ *     kernel may start while the previous kernel on the stream is still
+ *     running, if that kernel allows it (a kernel that calls
+ *     cudaTriggerProgrammaticLaunchCompletion, as this library's do).  Until
+ *     it has waited for that kernel, a call only reads its own inputs
+ *     (queries, pools, scales, page table, list, offsets) and writes nothing
+ *     but status bits; so a kernel that triggers early must not write the
+ *     next call's inputs after its trigger.  Copies, events and ordinary
+ *     launches before a call are complete before it starts.  The next kernel
+ *     on the stream may start early too: a kernel launched after a call with
  *     the programmatic-serialization attribute must call
  *     cudaGridDependencySynchronize() before it reads the call's outputs (the
  *     CUDA contract for such launches); ordinary launches, copies and events
