@@ -74,7 +74,8 @@ typedef enum qsa_dtype {
 
 /* Which kernel family runs the chunk step.  AUTO picks by shape: the
  * cells-on-M tensor-core kernel for decode windows (q_per_kv * n_queries
- * <= 64 rows), the rows-on-M tensor-core kernel for prompt-shaped calls.
+ * <= 80 rows: up to six queries of 12 heads), the rows-on-M tensor-core
+ * kernel for wider calls (prompt-shaped; chunk_cells >= 128).
  * SIMT forces the CUDA-core kernel (kept as an independent second path). */
 typedef enum qsa_algo {
     QSA_ALGO_AUTO = 0,

@@ -41,7 +41,7 @@ Path select_path(const qsa_shape *s)
 {
     const long long R = (long long)s->q_per_kv * s->n_queries;
     if (s->algo == QSA_ALGO_SIMT) return kPathSimt;
-    if (R <= 64) return kPathDecodeTc;
+    if (R <= kDecodeTcMaxRows) return kPathDecodeTc;
     if (s->chunk_cells >= 128) return kPathPromptTc;
     return s->algo == QSA_ALGO_TCGEN05 ? kPathNone : kPathSimt;
 }

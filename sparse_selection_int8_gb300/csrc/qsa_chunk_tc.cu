@@ -65,8 +65,8 @@ constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kScaleThreads = kLoadThreads / 4;   // loader threads that write the scales
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColK = 0;   // K codes, 128 columns (two f16 per column)
-constexpr uint32_t kColS = 128; // scores, two buffers of 64 columns
-constexpr uint32_t kColO = 256; // O^T, two chunk buffers x two d halves x 64 columns
+constexpr uint32_t kColS = 128; // scores, two buffers (see Lay)
+constexpr int kMaxRows = kDecodeTcMaxRows;
 constexpr uint32_t kStageBytes = kTile * kHeadDim * 2; // one f16 V tile, 64 KB
 constexpr uint32_t kBarSoft = 1;                       // named barrier of the softmax warps
 constexpr float kRescaleLog2 = 8.f; // O is rescaled when a row max grows past 2^8
@@ -85,12 +85,13 @@ struct Misc {
     float rs_ks[4][kTile];    // k_scale, v_scale of the cell's slot (0 if masked)
     float rs_vs[4][kTile];
     uint8_t sc_ok[2][kTile];  // cell holds a valid slot
-    __align__(16) float red_max[2][4][68]; // [tile parity][warp quadrant][row; 64 = |v_scale| max]
-    __align__(16) float red_sum[2][4][64];
-    float st_mrun[2][64];    // running max (log2 units) after the tile of that parity
-    __align__(16) float st_mref[2][64]; // reference max the tile's P' were formed against
-    float st_fac[64];        // O/l factor of the current tile
-    __align__(16) float st_fin[64]; // sigma * 2^(mref - mrun) at the end of a chunk
+    // [tile parity][warp quadrant][row; kMaxRows = |v_scale| max]
+    __align__(16) float red_max[2][4][kMaxRows + 4];
+    __align__(16) float red_sum[2][4][kMaxRows];
+    float st_mrun[2][kMaxRows];    // running max (log2 units) after the tile of that parity
+    __align__(16) float st_mref[2][kMaxRows]; // reference max the tile's P' were formed against
+    float st_fac[kMaxRows];        // O/l factor of the current tile
+    __align__(16) float st_fin[kMaxRows]; // sigma * 2^(mref - mrun) at the end of a chunk
     float st_sig[2];         // sigma reference after the tile of that parity
     float st_fs[2];          // sigma factor of the tile
     int st_any[2];           // tile index whose O needs rescaling
@@ -107,6 +108,20 @@ template <int N>
 struct Lay {
     static constexpr int PB = N <= 48 ? 2 : 1; // P' buffers
     static constexpr int QB = N <= 48 ? 2 : 1; // query tile buffers
+    // tensor memory: K codes (128 columns), two score buffers of SW columns,
+    // then O^T in OB chunk buffers x two d halves x SW columns.  Up to 64
+    // rows two chunks' O alternate (a chunk's epilogue overlaps the next
+    // chunk's first P.V); wider windows keep one.
+    static constexpr uint32_t SW = N <= 64 ? 64u : (uint32_t)N;
+    static constexpr int OB = N <= 64 ? 2 : 1;
+    static constexpr uint32_t colO = kColS + 2 * SW;
+    static __device__ __forceinline__ uint32_t col_s(int par) { return kColS + SW * (uint32_t)par; }
+    static __device__ __forceinline__ uint32_t col_o(int cp, int hh)
+    {
+        return colO + 2 * SW * (uint32_t)(cp % OB) + SW * (uint32_t)hh;
+    }
+    static_assert(N % 16 == 0 && N <= kMaxRows, "MMA N");
+    static_assert(colO + OB * 2 * SW <= kTmemCols, "tensor memory columns");
     static constexpr uint32_t v = 0;
     static constexpr uint32_t q = 2 * kStageBytes;
     static constexpr uint32_t pb = q + QB * N * 512u;
@@ -717,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 
         // partials of the chunk that ended at the previous tile
         auto epilogue = [&](const Pend &e) {
-            wait(&ms.o_full[e.cp & 1], (uint32_t)(e.cp >> 1) & 1u);
+            wait(&ms.o_full[e.cp % L::OB], (uint32_t)(e.cp / L::OB) & 1u);
             tc_fence_after();
             const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R;
 #pragma unroll 1
@@ -726,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 float v[8 * KR];
 #pragma unroll
                 for (int k = 0; k < KR; ++k)
-                    tmem_ld8(tmem + t_lane + kColO + 128u * (e.cp & 1) + 64u * hh + 8u * k, v + 8 * k);
+                    tmem_ld8(tmem + t_lane + L::col_o(e.cp, hh) + 8u * k, v + 8 * k);
                 tmem_wait_ld();
                 regs_after_wait<8 * KR>(v);
                 float *dst = p.part_o + base * kHeadDim + 128 * hh + c;
@@ -743,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 }
             }
             tc_fence_before();
-            mbar_arrive(&ms.o_empty[e.cp & 1]);
+            mbar_arrive(&ms.o_empty[e.cp % L::OB]);
             if (orow < p.R) {
                 p.part_m[base + orow] = ms.st_mrun[e.par][orow] * kLn2;
                 p.part_l[base + orow] = l_fin;
@@ -791,8 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             tc_fence_after();
             // scores: x[L][4k + 2B + e] = cell 2L+B, row 8k + 2u + e (log2 units)
             float x[2][4 * NK];
-            tmem_ld_16x256b<NK>(tmem + ((uint32_t)(32 * q) << 16) + kColS + 64u * par, x[0]);
-            tmem_ld_16x256b<NK>(tmem + ((uint32_t)(32 * q + 16) << 16) + kColS + 64u * par, x[1]);
+            tmem_ld_16x256b<NK>(tmem + ((uint32_t)(32 * q) << 16) + L::col_s(par), x[0]);
+            tmem_ld_16x256b<NK>(tmem + ((uint32_t)(32 * q + 16) << 16) + L::col_s(par), x[1]);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&ms.s_empty[par]); // the scores live in registers from here on
@@ -825,13 +840,13 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
 #pragma unroll
             for (int k = 0; k < KR; ++k)
-                if (ra == k) *reinterpret_cast<float2 *>(&ms.red_max[par][q][8 * k + 2 * u]) = make_float2(mrow[2 * k], mrow[2 * k + 1]);
+                if (ra == (k & 7)) *reinterpret_cast<float2 *>(&ms.red_max[par][q][8 * k + 2 * u]) = make_float2(mrow[2 * k], mrow[2 * k + 1]);
             {
                 float va = 0.f;
 #pragma unroll
                 for (int ci = 0; ci < 4; ++ci) va = fmaxf(va, fabsf(vsc[ci])); // (0 if masked)
                 const unsigned uu = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
-                if (lane == 0) ms.red_max[par][q][64] = __uint_as_float(uu);
+                if (lane == 0) ms.red_max[par][q][kMaxRows] = __uint_as_float(uu);
             }
             named_bar(kBarSoft, kSoftThreads);
             // ---- per-row decisions (thread c owns row c)
@@ -873,9 +888,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 ms.st_mref[par][c] = mref_n;
                 ms.st_fac[c] = fac;
             }
-            if (c == kSoftThreads - 1) { // owns no row (N <= 64)
-                const float st = fmaxf(fmaxf(ms.red_max[par][0][64], ms.red_max[par][1][64]),
-                                       fmaxf(ms.red_max[par][2][64], ms.red_max[par][3][64]));
+            if (c == kSoftThreads - 1) { // owns no row (at most kMaxRows < 127 rows)
+                const float st = fmaxf(fmaxf(ms.red_max[par][0][kMaxRows], ms.red_max[par][1][kMaxRows]),
+                                       fmaxf(ms.red_max[par][2][kMaxRows], ms.red_max[par][3][kMaxRows]));
                 const float so = ms.st_sig[par ^ 1];
                 float sn = so, fs = 1.f;
                 if (first_t) {
@@ -934,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
 #pragma unroll
             for (int k = 0; k < KR; ++k)
-                if (ra == k) *reinterpret_cast<float2 *>(&ms.red_sum[par][q][8 * k + 2 * u]) = make_float2(lrow[2 * k], lrow[2 * k + 1]);
+                if (ra == (k & 7)) *reinterpret_cast<float2 *>(&ms.red_sum[par][q][8 * k + 2 * u]) = make_float2(lrow[2 * k], lrow[2 * k + 1]);
             // ---- lazy rescale of the chunk's O (rows whose max moved, or sigma)
             if (resc) {
                 if (PB == 2) wait(&ms.p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u); // P.V of tile i-1 done
@@ -944,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 1
                     for (int r0 = 0; r0 < p.R; r0 += 16) {
-                        const uint32_t ta = tmem + t_lane + kColO + 128u * (cp & 1) + 64u * hh + r0;
+                        const uint32_t ta = tmem + t_lane + L::col_o(cp, hh) + r0;
                         float v[16];
                         tmem_ld16(ta, v);
                         tmem_wait_ld();
@@ -1016,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 if (i >= 2) wait(&ms.s_empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u);
                 tc_fence_after();
                 const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg % QB) * N * 512u, 16, 1024);
-                const uint32_t sd = tmem + kColS + 64u * (i & 1);
+                const uint32_t sd = tmem + L::col_s(i & 1);
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint64_t bd = qd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
@@ -1059,13 +1074,13 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 if (first_t) ++cp;
                 wait(&ms.p_full[i % PB], (uint32_t)(i / PB) & 1u);
                 wait(&ms.v_full[i & 1], (uint32_t)(i >> 1) & 1u);
-                if (first_t && cp >= 2) wait(&ms.o_empty[cp & 1], (uint32_t)((cp - 2) >> 1) & 1u);
+                if (first_t && cp >= L::OB) wait(&ms.o_empty[cp % L::OB], (uint32_t)((cp - L::OB) / L::OB) & 1u);
                 tc_fence_after();
                 // descriptors built once; a K step only moves the start address
                 // (field [0,14) in 16-byte units, no carry for shared addresses)
                 const uint64_t ad0 = smem_desc(s_v + (uint32_t)(i & 1) * kStageBytes, 16384, 1024);
                 const uint64_t bd0 = smem_desc(s_p + (uint32_t)(i % PB) * N * 256u, 16, 1024);
-                const uint32_t d0 = tmem + kColO + 128u * (cp & 1);
+                const uint32_t d0 = tmem + L::col_o(cp, 0);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     // the two d halves interleaved: independent accumulators
@@ -1073,12 +1088,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint64_t ad = ad0 + (uint64_t)(((uint32_t)(2 * hh) * 16384u + (uint32_t)kk * 2048u) >> 4);
                         const uint64_t bd = bd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
-                        mma_f16_ss(d0 + 64u * hh, ad, bd, idesc_o, (first_t && kk == 0) ? 0u : 1u);
+                        mma_f16_ss(d0 + L::SW * hh, ad, bd, idesc_o, (first_t && kk == 0) ? 0u : 1u);
                     }
                 }
                 mma_commit(&ms.v_empty[i & 1]);
                 mma_commit(&ms.p_empty[i % PB]);
-                if (last_t) mma_commit(&ms.o_full[cp & 1]);
+                if (last_t) mma_commit(&ms.o_full[cp % L::OB]);
                 tile_next(p, it);
             }
             mma_commit(&ms.done);
@@ -1133,7 +1148,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
 
 } // namespace
 
-bool chunk_tc_supports(const Params &p) { return p.R <= 64; }
+bool chunk_tc_supports(const Params &p) { return p.R <= kDecodeTcMaxRows; }
 
 size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
 {
@@ -1157,6 +1172,8 @@ cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
     case 6: return launch_n<48, 6>(p, stream);
     case 7: return launch_n<64, 7>(p, stream);
     case 8: return launch_n<64, 8>(p, stream);
+    case 9: return launch_n<80, 9>(p, stream);
+    case 10: return launch_n<80, 10>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

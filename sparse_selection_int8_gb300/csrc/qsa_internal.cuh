@@ -17,6 +17,9 @@
 namespace qsa {
 
 constexpr int kHeadDim = 256;
+// Query rows (T x H of one KV head) the cells-on-M decode kernel takes; wider
+// windows go to the rows-on-M kernel.
+constexpr int kDecodeTcMaxRows = 80;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

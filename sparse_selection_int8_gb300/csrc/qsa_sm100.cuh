@@ -232,14 +232,14 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, float *v)
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// NK repetitions (NK in {2, 4, 6, 8}) starting at taddr's column.
+// NK repetitions (NK even, >= 2) starting at taddr's column.
 template <int NK>
 __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, float *v)
 {
+    static_assert(NK >= 2 && NK % 2 == 0, "16x256b repetitions");
     if constexpr (NK >= 4) {
         tmem_ld_16x256b_x4(taddr, v);
-        if constexpr (NK >= 8) tmem_ld_16x256b_x4(taddr + 32, v + 16);
-        else if constexpr (NK == 6) tmem_ld_16x256b_x2(taddr + 32, v + 16);
+        if constexpr (NK > 4) tmem_ld_16x256b<NK - 4>(taddr + 32, v + 16);
     } else {
         tmem_ld_16x256b_x2(taddr, v);
     }

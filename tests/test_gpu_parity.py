@@ -124,7 +124,7 @@ def test_chunk_sizes(algo, C):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("T", [1, 3, 5])
+@pytest.mark.parametrize("T", [1, 3, 5, 6, 8])
 def test_query_counts_and_heads(algo, T):
     p = wl.make_problem(n_queries=T, q_per_kv=12, n_kv_heads=3, pool_cells=2048,
                         n_selected=700, chunk_cells=128, seed=7200 + T)
@@ -191,6 +191,38 @@ def test_many_segments_per_cta(algo, H, T):
     dp, out = run(p, algo, max_selected=max(lens))
     assert_parity(out, oracle.decode_attn(p), f"many segments H={H} T={T}")
     assert int(dp.status.item()) == 0
+
+
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+@pytest.mark.parametrize("H,T,G", [(12, 6, 1), (12, 6, 2), (16, 5, 1), (10, 7, 2)])
+def test_wide_windows(algo, H, T, G):
+    """Windows of 65-80 query rows (five to seven queries) on the cells-on-M
+    decode kernel: one O buffer in tensor memory, 8-row score blocks past 64,
+    the query tile converted in the kernel (one KV head) or staged (two), and
+    chunks of one tile, two tiles and a partial second tile."""
+    for C in (128, 256, 200):
+        p = wl.make_problem(n_kv_heads=G, q_per_kv=H, n_queries=T, pool_cells=8192,
+                            n_selected=2051, chunk_cells=C, mask_fraction=0.05,
+                            seed=9100 + 100 * H + 10 * T + G + C)
+        check_full(p, algo, f"wide window H={H} T={T} G={G} C={C}")
+
+
+@pytest.mark.parametrize("H,T", [(12, 1), (12, 4), (12, 6), (16, 5)])
+@pytest.mark.parametrize("G", [1, 2])
+def test_decode_path_rescaling(H, T, G):
+    """K scales that grow along the list make each row's running max climb by
+    tens of log2 units (O is rescaled in tensor memory whenever the reference
+    max moves by more than 2^8), and V scales that grow 100x make the chunk's
+    V reference move (a tile's largest V scale above 16x the reference), in
+    one chunk of 16 tiles.  bf16 queries convert to f16 exactly."""
+    p = wl.make_problem(n_kv_heads=G, q_per_kv=H, n_queries=T, pool_cells=4096,
+                        n_selected=2048, chunk_cells=2048, q_dtype="bf16",
+                        seed=9300 + 10 * H + T + 1000 * G)
+    pos = np.argsort(p.page_table[0]).astype(np.float64)  # list position order of each slot
+    frac = pos / p.page_table_len
+    p.k_scale[0, :] = (0.005 + 0.055 * frac).astype(np.float32)
+    p.v_scale[0, :] = (0.0002 * 100.0 ** frac).astype(np.float32)
+    check_full(p, "auto", f"decode rescaling H={H} T={T} G={G}")
 
 
 @pytest.mark.parametrize("algo", ["auto", "simt"])
