@@ -197,7 +197,7 @@ def source_digest(*names) -> str:
 # only while the kernel source hashes to the recorded digest.
 TRAFFIC = {
     # qsa_decode T = 1..4, chunk kernel, sum of the four launches (profiles/qsa_chunk_tc_qsa_decode_sweep.md)
-    "3609a5db0a0c8e15": 6096640,
+    "8eefbd587c7d7fc2": 6096128,
 }
 
 # Sources of the chunk kernel the recorded traffic belongs to.
@@ -477,7 +477,28 @@ def measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush, budget_s
     return res
 
 
-def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64):
+def measure_windows(torch, qsa, wl, stream, hbm_peak):
+    """Verify windows of five and six queries (60 and 72 query rows) on the
+    qsa_decode shape, back to back over rotated input sets as the headline
+    (a labelled companion figure, not the headline)."""
+    res = {}
+    for T in (5, 6):
+        p = wl.qsa_decode(T)
+        dp = qsa.DeviceProblem(p)
+        ab = algorithmic_bytes(p)
+        n = sets_for(ab, set_bytes_of(dp))
+        sets = rotation(torch, dp, n)
+        us = time_b2b(torch, sets, stream, rounds=3, reps=max(1, 256 // n))
+        res[f"T{T}"] = {"us_per_call": round(us, 2), "cells_per_s": int(p.n_selected.sum()) / (us * 1e-6),
+                        "hbm_gbs": ab / (us * 1e-6) / 1e9, "hbm_frac": ab / (us * 1e-6) / 1e9 / hbm_peak,
+                        "input_sets": n}
+        del sets, dp
+        torch.cuda.empty_cache()
+    res["what"] = "qsa_decode shape (2,051 of 32,768 cells, chunk 128) with 5 and 6 queries per call"
+    return res
+
+
+def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64, what=None):
     """The headline shape replicated as `n_seq` independent sequences in one
     qsa_decode_attn_batch call (bandwidth of the kernels on that shape; a
     labelled companion figure, not the headline)."""
@@ -487,7 +508,7 @@ def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64):
         base = qsa.DeviceProblem(p)
         rep = BatchCall(torch, qsa, base, n_seq)
         touched = n_seq * algorithmic_bytes(p)
-        n = sets_for(touched, set_bytes_of(rep), lo=2, hi=8, budget=8 << 30)
+        n = sets_for(touched, set_bytes_of(rep), lo=2, hi=64, budget=8 << 30)
         sets = rotation(torch, rep, n)
         us = time_b2b(torch, sets, stream, rounds=4, reps=max(1, 32 // n))
         res[f"T{T}"] = {"us_per_call": round(us, 2), "cells_per_s": n_seq * int(p.n_selected.sum()) / (us * 1e-6),
@@ -495,8 +516,8 @@ def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64):
                         "hbm_frac": touched / (us * 1e-6) / 1e9 / hbm_peak, "input_sets": n}
         del sets, rep, base
         torch.cuda.empty_cache()
-    res["what"] = (f"qsa_decode shape replicated as {n_seq} sequences (own pools, page tables and "
-                   "lists) in one qsa_decode_attn_batch call; back to back over rotated input sets")
+    res["what"] = what or (f"qsa_decode shape replicated as {n_seq} sequences (own pools, page tables and "
+                           "lists) in one qsa_decode_attn_batch call; back to back over rotated input sets")
     return res
 
 
@@ -599,9 +620,13 @@ def run_ours(args, world, rank, local):
     e2e_ms = dist_max(statistics.mean(e2e_times), world)
     e2e_value = world * cells_step / (e2e_ms * 1e-3)
 
-    extra, steady = {}, {}
+    extra, steady, layers, windows = {}, {}, {}, {}
     if rank == 0 and not args.no_extra:
         steady = measure_steady(torch, qsa, wl, stream, hbm_peak)
+        layers = measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=12, what=(
+            "one verify window of 12 QSA layers (the qsa_decode shape per layer: own pools, page "
+            "tables and lists) in one qsa_decode_attn_batch call; back to back over rotated input sets"))
+        windows = measure_windows(torch, qsa, wl, stream, hbm_peak)
         extra = measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush)
 
     cpu = None
@@ -637,6 +662,8 @@ def run_ours(args, world, rank, local):
             "gpu_launches": KERNELS_PER_DECODE_CALL * len(SWEEP) * args.steps,
             "cpu_baseline": cpu,
             "steady_state": steady,
+            "layers_in_one_call": layers,
+            "wide_windows": windows,
             "other_workloads": extra,
         }
         print(json.dumps(line), flush=True)
