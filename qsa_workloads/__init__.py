@@ -241,9 +241,10 @@ def long_context(seed_offset: int = 0) -> Problem:
 
 
 def prompt_shaped(seed_offset: int = 0, n_queries: int = 2048,
-                  pool_cells: int = 32768, chunk_cells: int = 16384) -> Problem:
+                  pool_cells: int = 32768, chunk_cells: int = 11008) -> Problem:
     """1 KV head x 12 query heads, 2,048 bf16 queries against all 32,768 cells
-    in page-table order, no causal mask."""
+    in page-table order, no causal mask.  Chunk 11,008 cells: three split-K
+    chunks (86, 86 and 84 tiles of 128 cells)."""
     return make_problem(n_seq=1, n_kv_heads=1, n_queries=n_queries,
                         pool_cells=pool_cells, n_selected=pool_cells,
                         chunk_cells=chunk_cells, q_dtype="bf16", selection="full",
