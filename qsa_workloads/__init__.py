@@ -258,3 +258,89 @@ CONFIGS = {
     "long_context": long_context,
     "prompt_shaped": prompt_shaped,
 }
+
+
+# ---------------------------------------------------------------------------
+# K/V append calls: new rows quantised into the INT8 pools.
+# ---------------------------------------------------------------------------
+
+@dataclass
+class AppendProblem:
+    """One K/V append call plus the pools it writes into.
+
+    ``k_new``/``v_new`` ``[B][n_new][G][D]`` f32 (or bf16 bit patterns as
+    uint16); ``positions`` int32 ``[B][n_new]`` logical positions; pools,
+    scales and page table laid out as in :class:`Problem`."""
+
+    n_seq: int
+    n_kv_heads: int
+    head_dim: int
+    n_new: int
+    pool_cells: int
+    page_table_len: int
+    dtype: str  # "f32" or "bf16"
+    k_new: np.ndarray
+    v_new: np.ndarray
+    positions: np.ndarray
+    page_table: np.ndarray
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    k_scale: np.ndarray
+    v_scale: np.ndarray
+    name: str = ""
+
+
+def make_append(*, n_seq: int = 1, n_kv_heads: int = 1, head_dim: int = 256, n_new: int = 4,
+                pool_cells: int = 4096, page_table_len: Optional[int] = None,
+                dtype: str = "f32", mask_fraction: float = 0.0, seed: int = SEED_BASE,
+                name: str = "") -> AppendProblem:
+    """Draw one seeded append call.
+
+    New rows are N(0,1) values times a per-row magnitude log-uniform in
+    [0.05, 20] (projection outputs of varied size), rounded to bf16 when
+    ``dtype == "bf16"``.  Each sequence appends ``n_new`` distinct logical
+    positions whose pages are resident, drawn without replacement.  The pools
+    start as in :func:`make_problem` (random codes and scales), so a slot the
+    call must not touch keeps visibly different contents."""
+    if page_table_len is None:
+        page_table_len = pool_cells
+    rng = np.random.Generator(np.random.PCG64(seed))
+    G, D = n_kv_heads, head_dim
+    k_pool = _codes(rng, (n_seq, G, pool_cells, D))
+    v_pool = _codes(rng, (n_seq, G, pool_cells, D))
+    k_scale = _scales(rng, (n_seq, G, pool_cells))
+    v_scale = _scales(rng, (n_seq, G, pool_cells))
+    pts, poss = [], []
+    for b in range(n_seq):
+        pt = _page_table(rng, pool_cells, page_table_len, mask_fraction)
+        resident = np.flatnonzero(pt >= 0)
+        assert resident.size >= n_new, "not enough resident positions"
+        poss.append(rng.choice(resident, size=n_new, replace=False).astype(np.int32))
+        pts.append(pt)
+
+    def rows():
+        mag = np.exp(rng.uniform(np.log(0.05), np.log(20.0), size=(n_seq, n_new, G, 1)))
+        x = (rng.standard_normal((n_seq, n_new, G, D)) * mag).astype(np.float32)
+        return bf16_bits_from_f32(x) if dtype == "bf16" else x
+
+    k_new, v_new = rows(), rows()
+    return AppendProblem(n_seq=n_seq, n_kv_heads=G, head_dim=D, n_new=n_new,
+                         pool_cells=pool_cells, page_table_len=page_table_len, dtype=dtype,
+                         k_new=k_new, v_new=v_new,
+                         positions=np.stack(poss).reshape(n_seq, n_new).astype(np.int32),
+                         page_table=np.stack(pts).astype(np.int32), k_pool=k_pool,
+                         v_pool=v_pool, k_scale=k_scale, v_scale=v_scale, name=name)
+
+
+def decode_step_append(seed_offset: int = 0) -> AppendProblem:
+    """A verify window's append for the batched shape: 16 sequences x 2 KV
+    heads, 4 new cells each, into 32,768-cell pools."""
+    return make_append(n_seq=16, n_kv_heads=2, n_new=4, pool_cells=32768,
+                       seed=SEED_BASE + 16 + seed_offset, name="append_decode_step")
+
+
+def prompt_append(seed_offset: int = 0) -> AppendProblem:
+    """The prompt-shaped pool written in one call: 32,768 new cells of one
+    sequence with 2 KV heads (the rows of a 32,768-token prefill)."""
+    return make_append(n_seq=1, n_kv_heads=2, n_new=32768, pool_cells=32768,
+                       seed=SEED_BASE + 17 + seed_offset, name="append_prompt")
