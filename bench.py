@@ -67,7 +67,8 @@ def parse():
     ap.add_argument("--case", default=None,
                     help="run one workload --reps times and exit (for profiler captures): "
                          "tiny_decode, qsa_decode1..4, qsa_decode_sweep (T = 1, 2, 3, 4 in turn), "
-                         "batched_decode, long_context, prompt_shaped")
+                         "batched_decode, long_context, prompt_shaped, prompt_append, "
+                         "decode_step_append")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tcgen05"])
     return ap.parse_args()
@@ -81,6 +82,13 @@ def run_case(args):
     qsa_build.build()
     import sparse_selection_int8_gb300 as qsa
     name = args.case
+    if name.endswith("_append"):
+        d = qsa.DeviceAppend(getattr(wl, name)())
+        for _ in range(args.reps):
+            d.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"case": name, "reps": args.reps, "status": [int(d.status.item())]}))
+        return 0
     if name == "qsa_decode_sweep":
         problems = [wl.qsa_decode(T) for T in SWEEP]
     elif name.startswith("qsa_decode"):
@@ -297,6 +305,21 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+class L2Flush:
+    """Evicts the L2 between timed steps: writes a buffer larger than L2, then
+    reads it back, so the L2 holds clean lines (a write-only flush would leave
+    129 MB of dirty lines whose write-back lands inside the next timed call)."""
+
+    def __init__(self, torch, nbytes=None):
+        self.buf = torch.empty((nbytes or L2_FLUSH_BYTES) // 4, dtype=torch.float32, device="cuda")
+        self.acc = torch.empty((), dtype=torch.float32, device="cuda")
+        self.torch = torch
+
+    def zero_(self):
+        self.buf.zero_()
+        self.torch.sum(self.buf, dim=0, out=self.acc)
+
 
 def time_graphs(torch, graphs, flush, steps, warmup, stream):
     """Replay each graph in order per step; L2 flushed before each step.
@@ -529,6 +552,41 @@ def measure_windows(torch, qsa, wl, stream, hbm_peak):
     return res
 
 
+def append_bytes(a) -> int:
+    """Algorithmic bytes of one K/V append call: per new cell its position and
+    page entry; per (cell, KV head) the K and V rows read and their codes and
+    scales written."""
+    esz = 2 if a.dtype == "bf16" else 4
+    return a.n_seq * a.n_new * (8 + a.n_kv_heads * 2 * (a.head_dim * esz + a.head_dim + 4))
+
+
+def measure_append(torch, qsa, wl, stream, hbm_peak, flush):
+    """The K/V append (new rows quantised into the pools): one call per graph,
+    L2 flushed before each (a labelled companion figure, not the headline)."""
+    res = {}
+    cases = [("prompt_f32", wl.prompt_append()),
+             ("prompt_bf16", wl.make_append(n_seq=1, n_kv_heads=2, n_new=32768, pool_cells=32768,
+                                            dtype="bf16", seed=wl.SEED_BASE + 18)),
+             ("decode_step", wl.decode_step_append())]
+    for name, a in cases:
+        d = qsa.DeviceAppend(a)
+        g = capture(torch, d, stream)
+        with torch.cuda.stream(stream):
+            per = time_graphs(torch, [g], flush, 20, 3, stream)
+        if int(d.status.item()):
+            raise RuntimeError(f"append status {int(d.status.item()):#x}")
+        us = statistics.median([x[0] for x in per]) * 1e3
+        ab = append_bytes(a)
+        res[name] = {"us_per_call": round(us, 2), "cells": a.n_seq * a.n_new, "kv_heads": a.n_kv_heads,
+                     "dtype": a.dtype, "algorithmic_bytes": ab, "hbm_gbs": ab / (us * 1e-6) / 1e9,
+                     "hbm_frac": ab / (us * 1e-6) / 1e9 / hbm_peak}
+        del g, d
+        torch.cuda.empty_cache()
+    res["what"] = ("qsa_kv_append: new K/V rows quantised (scale = max|x|/127, round half to even) "
+                   "into the pools at their page-table slots; one call per graph, L2 flushed before each")
+    return res
+
+
 def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64, what=None):
     """The headline shape replicated as `n_seq` independent sequences in one
     qsa_decode_attn_batch call (bandwidth of the kernels on that shape; a
@@ -568,7 +626,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream()
     problems = [wl.qsa_decode(T) for T in SWEEP]
     dps = [qsa.DeviceProblem(p) for p in problems]
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(torch)
 
     # Headline: the pages' method (µs per call over a run of back-to-back
     # calls), with the inputs rotated over ROTATION distinct sets per T so
@@ -667,13 +725,14 @@ def run_ours(args, world, rank, local):
     e2e_ms = dist_max(statistics.mean(e2e_times), world)
     e2e_value = world * cells_step / (e2e_ms * 1e-3)
 
-    extra, steady, layers, windows = {}, {}, {}, {}
+    extra, steady, layers, windows, append = {}, {}, {}, {}, {}
     if rank == 0 and not args.no_extra:
         steady = measure_steady(torch, qsa, wl, stream, hbm_peak)
         layers = measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=12, what=(
             "one verify window of 12 QSA layers (the qsa_decode shape per layer: own pools, page "
             "tables and lists) in one qsa_decode_attn_batch call; back to back over rotated input sets"))
         windows = measure_windows(torch, qsa, wl, stream, hbm_peak)
+        append = measure_append(torch, qsa, wl, stream, hbm_peak, flush)
         extra = measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush)
 
     cpu = None
@@ -714,6 +773,7 @@ def run_ours(args, world, rank, local):
             "steady_state": steady,
             "layers_in_one_call": layers,
             "wide_windows": windows,
+            "kv_append": append,
             "other_workloads": extra,
         }
         print(json.dumps(line), flush=True)

@@ -89,6 +89,7 @@ typedef enum qsa_algo {
 #define QSA_STATUS_BAD_SLOT 0x2u     /* a page entry outside [0, pool_cells) and not -1 */
 #define QSA_STATUS_BAD_OFFSETS 0x4u  /* batch offsets decreasing or a list above max_selected */
 #define QSA_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait ran out: outputs invalid */
+#define QSA_STATUS_NOT_RESIDENT 0x10u /* qsa_kv_append: a position whose page entry is -1 */
 
 typedef struct qsa_shape {
     int32_t n_kv_heads;     /* G: KV heads per sequence (>= 1) */
@@ -200,6 +201,43 @@ qsa_status qsa_decode_attn_step_noalloc(const qsa_shape *shape, const void *q,
                                         const int32_t *page_table, const int32_t *sel,
                                         int32_t n_sel, float *out, uint32_t *status,
                                         void *stream);
+
+/*
+ * INT8 K/V append: quantise new K and V rows and write them into the pools
+ * the attention calls read.  The step is the KV append that follows a QSA
+ * layer's K/V projections ("Strata PR #2220, R9-gpu-8: one exact launch for
+ * QSA K and V", implementation handoff); the format is the pools' of
+ * "attn_chunk_q8_v3_kernel" (INT8 codes, one fp32 scale per cell).  The
+ * pages print no quantiser; this library's reading, per (cell, KV head) and
+ * separately for K and V: scale = max|x| / 127 (fp32, correctly rounded),
+ * code = x / scale (fp32, correctly rounded) rounded to nearest, ties to
+ * even; a row of zeros gets scale 0 and zero codes.
+ *   shape      the attention calls' shape; n_kv_heads, head_dim (256),
+ *              pool_cells and page_table_len are read, the rest ignored.
+ *   n_seq, n_new  sequences and new cells per sequence (either 0: no work).
+ *   kv_dtype   QSA_F32 or QSA_BF16: the element type of k_new and v_new.
+ *   k_new      [n_seq][n_new][G][D] finite values, 16-byte aligned; v_new
+ *              the same.  Row i of sequence b is that sequence's new cell i.
+ *   positions  [n_seq][n_new] int32: logical position of each new cell.
+ *   page_table [n_seq][page_table_len] int32: pool slot of each position.
+ *   k_pool     [n_seq][G][pool_cells][D] int8, 16-byte aligned; written at
+ *              the new cells' slots only; v_pool the same.
+ *   k_scale    [n_seq][G][pool_cells] fp32; written at those slots; v_scale
+ *              the same.
+ *   status     optional device word: QSA_STATUS_BAD_POSITION (a position
+ *              outside the page table), QSA_STATUS_NOT_RESIDENT (its page
+ *              entry is -1), QSA_STATUS_BAD_SLOT (an entry outside the pool):
+ *              such a cell is skipped and nothing is written for it.
+ * Two new cells of one call that resolve to the same slot leave either row
+ * there.  Asynchronous on `stream`, graph-capturable, allocates nothing.
+ * Errors: QSA_ERR_INVALID_ARG (null or misaligned pointer, negative count,
+ * bad kv_dtype, new rows or scales aliasing the pools); QSA_ERR_UNSUPPORTED
+ * (head_dim != 256); QSA_ERR_CUDA (launch failed).
+ */
+qsa_status qsa_kv_append(const qsa_shape *shape, int32_t n_seq, int32_t n_new, int32_t kv_dtype,
+                         const void *k_new, const void *v_new, const int32_t *positions,
+                         const int32_t *page_table, int8_t *k_pool, int8_t *v_pool,
+                         float *k_scale, float *v_scale, uint32_t *status, void *stream);
 
 /* Static description of a status code. */
 const char *qsa_status_string(int32_t status);

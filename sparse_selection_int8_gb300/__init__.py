@@ -33,6 +33,7 @@ QSA_STATUS_BAD_POSITION = 0x1
 QSA_STATUS_BAD_SLOT = 0x2
 QSA_STATUS_BAD_OFFSETS = 0x4
 QSA_STATUS_TIMEOUT = 0x8
+QSA_STATUS_NOT_RESIDENT = 0x10
 
 HEAD_DIM = 256
 
@@ -84,6 +85,8 @@ _SIG = {
     "qsa_status_string": ([ctypes.c_int32], ctypes.c_char_p),
     "qsa_decode_attn_step_noalloc": ([ctypes.POINTER(qsa_shape), _VP, _VP, _VP, _VP, _VP, _VP,
                                       _VP, ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int32),
+    "qsa_kv_append": ([ctypes.POINTER(qsa_shape), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                       _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int32),
 }
 
 
@@ -190,4 +193,16 @@ def qsa_partials_view(shape: qsa_shape, n_seq: int, max_selected: int, workspace
     return m.value, l.value, o.value, int(nch.value)
 
 
-from .device import DeviceProblem, run_problem, partials_of  # noqa: E402,F401
+
+
+def qsa_kv_append(shape: qsa_shape, n_seq: int, n_new: int, kv_dtype: int, k_new, v_new,
+                  positions, page_table, k_pool, v_pool, k_scale, v_scale, status=None,
+                  stream=None) -> None:
+    """Quantise new K/V rows into the INT8 pools (see include/qsa.h)."""
+    _check(load_library().qsa_kv_append(
+        ctypes.byref(shape), int(n_seq), int(n_new), int(kv_dtype), _ptr(k_new), _ptr(v_new),
+        _ptr(positions), _ptr(page_table), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(status), _stream(stream)), "qsa_kv_append")
+
+
+from .device import DeviceAppend, DeviceProblem, run_problem, partials_of  # noqa: E402,F401

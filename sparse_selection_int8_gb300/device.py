@@ -11,7 +11,7 @@ from typing import Optional
 import numpy as np
 
 from . import (QSA_ALGO_AUTO, QSA_BF16, QSA_F32, make_shape, qsa_decode_attn_batch,
-               qsa_decode_attn_step, qsa_partials_view, qsa_workspace_bytes)
+               qsa_decode_attn_step, qsa_kv_append, qsa_partials_view, qsa_workspace_bytes)
 
 
 def _to_dev(torch, a: np.ndarray, device, pin: bool = False):
@@ -76,6 +76,38 @@ class DeviceProblem:
                                  int(self.p.sel.shape[0]), out, self.workspace, self.ws_bytes,
                                  self.status, stream)
         return out
+
+
+class DeviceAppend:
+    """An append call (as drawn by the input generator) resident in device
+    memory: new rows, positions, page table, and the pools it writes."""
+
+    def __init__(self, a, device: str = "cuda"):
+        import torch
+        self.a = a
+        if a.dtype == "bf16":
+            self.k_new = _to_dev(torch, np.asarray(a.k_new).view(np.int16), device).view(torch.bfloat16)
+            self.v_new = _to_dev(torch, np.asarray(a.v_new).view(np.int16), device).view(torch.bfloat16)
+        else:
+            self.k_new = _to_dev(torch, a.k_new.astype(np.float32), device)
+            self.v_new = _to_dev(torch, a.v_new.astype(np.float32), device)
+        self.positions = _to_dev(torch, a.positions, device)
+        self.page_table = _to_dev(torch, a.page_table, device)
+        self.k_pool = _to_dev(torch, a.k_pool, device)
+        self.v_pool = _to_dev(torch, a.v_pool, device)
+        self.k_scale = _to_dev(torch, a.k_scale, device)
+        self.v_scale = _to_dev(torch, a.v_scale, device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.kv_dtype = QSA_BF16 if a.dtype == "bf16" else QSA_F32
+        self.shape = make_shape(n_kv_heads=a.n_kv_heads, q_per_kv=1, n_queries=1,
+                                pool_cells=a.pool_cells, page_table_len=a.page_table_len,
+                                chunk_cells=1, softmax_scale=1.0, head_dim=a.head_dim)
+
+    def run(self, stream=None):
+        a = self.a
+        qsa_kv_append(self.shape, a.n_seq, a.n_new, self.kv_dtype, self.k_new, self.v_new,
+                      self.positions, self.page_table, self.k_pool, self.v_pool, self.k_scale,
+                      self.v_scale, self.status, stream)
 
 
 def run_problem(p, algo: int = QSA_ALGO_AUTO, batch: Optional[bool] = None) -> np.ndarray:

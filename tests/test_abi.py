@@ -137,6 +137,49 @@ def test_batch_rejects_before_launch(lib):
                                      None) == qsa.QSA_ERR_INVALID_ARG
 
 
+def append_args(**over):
+    mb = 1 << 20
+    a = dict(n_seq=2, n_new=4, kv_dtype=qsa.QSA_F32, k_new=FAKE, v_new=FAKE + mb, positions=FAKE + 2 * mb,
+             page_table=FAKE + 3 * mb, k_pool=FAKE + 4 * mb, v_pool=FAKE + 5 * mb,
+             k_scale=FAKE + 6 * mb, v_scale=FAKE + 7 * mb)
+    a.update(over)
+    return a
+
+
+def call_append(lib, s, a):
+    return lib.qsa_kv_append(ctypes.byref(s), a["n_seq"], a["n_new"], a["kv_dtype"], a["k_new"],
+                             a["v_new"], a["positions"], a["page_table"], a["k_pool"], a["v_pool"],
+                             a["k_scale"], a["v_scale"], None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(k_new=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(positions=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(v_scale=None), qsa.QSA_ERR_INVALID_ARG),
+    (dict(n_new=-1), qsa.QSA_ERR_INVALID_ARG),
+    (dict(n_seq=-1), qsa.QSA_ERR_INVALID_ARG),
+    (dict(kv_dtype=7), qsa.QSA_ERR_INVALID_ARG),
+    (dict(k_new=FAKE + 8), qsa.QSA_ERR_INVALID_ARG),      # misaligned rows
+    (dict(v_pool=FAKE + (5 << 20) + 4), qsa.QSA_ERR_INVALID_ARG),
+    (dict(k_pool=FAKE), qsa.QSA_ERR_INVALID_ARG),         # pool aliases the new K rows
+    (dict(v_scale=FAKE + (6 << 20)), qsa.QSA_ERR_INVALID_ARG),  # one scale array for K and V
+])
+def test_append_rejects_before_launch(lib, over, code):
+    assert call_append(lib, shape(), append_args(**over)) == code
+
+
+def test_append_checks_shape_and_skips_empty_calls(lib):
+    s = shape()
+    s.head_dim = 128
+    assert call_append(lib, s, append_args()) == qsa.QSA_ERR_UNSUPPORTED
+    s = shape()
+    s.pool_cells = 0
+    assert call_append(lib, s, append_args()) == qsa.QSA_ERR_INVALID_ARG
+    # nothing to append: success without touching the device (none here)
+    assert call_append(lib, shape(), append_args(n_new=0)) == qsa.QSA_OK
+    assert call_append(lib, shape(), append_args(n_seq=0)) == qsa.QSA_OK
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4):
         assert qsa.qsa_status_string(code)
