@@ -13,8 +13,8 @@
 //
 // HBM-bound: per new cell and KV head it reads the K and V rows (2 x 1 KB of
 // fp32, or 2 x 512 B of bf16) and writes 2 x 256 code bytes and two scales.
-// One warp per (sequence, new cell, KV head): lane l holds elements
-// 8l..8l+7 of both rows (each warp load is 1 KB or 512 B of contiguous
+// One warp per new cell (sequence, cell) with all its KV heads: lane l holds
+// elements 8l..8l+7 of a row (each warp load is 1 KB or 512 B of contiguous
 // memory), the row maximum is one warp reduction, and lane l stores its 8
 // codes as one 8-byte word (256 contiguous bytes per warp store).  The row
 // loads do not depend on the page-table lookup, so they are issued first and
@@ -88,7 +88,8 @@ __device__ __forceinline__ void widen8(const Raw8 &r, float *x)
 // division by Newton-Raphson iteration with FMA): q + (a - q b) yb equals
 // a/b + (1 - b yb)(q - a/b), so the first correction brings RN(a yb) within
 // one ulp of a/b, where the remainder a - q b is exact in one FMA and the
-// second correction rounds correctly.  Five instructions.
+// second correction rounds correctly.  Five instructions.  (Here a quotient
+// below the normal range is a code of 0 whichever way its last bits fall.)
 __device__ __forceinline__ float div_rn_by(float a, float b, float yb)
 {
     float q = a * yb;
@@ -98,8 +99,10 @@ __device__ __forceinline__ float div_rn_by(float a, float b, float yb)
     return fmaf(r, yb, q);
 }
 
-// q rounded to the nearest integer, ties to even, for |q| <= 2^22, as the low
-// byte of the fp32 sum q + 1.5 * 2^23 (whose unit in the last place is 1).
+// For |q| <= 127.5: the int8 code of q rounded to the nearest integer, ties
+// to even, in the low byte.  The fp32 sum q + 1.5 * 2^23 lies in [2^23, 2^24),
+// where the unit in the last place is 1, so the addition rounds q half to
+// even and the low mantissa bits hold 0x400000 + rint(q).
 __device__ __forceinline__ uint32_t rint_low_byte(float q)
 {
     return __float_as_uint(__fadd_rn(q, 12582912.f));
