@@ -63,15 +63,15 @@ def build() -> str:
 def _bind(lib):
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
-    lib.qsa_oracle_attend_row.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, i32, dbl, P]
+    lib.qsa_oracle_attend_row.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32, dbl, P]
     lib.qsa_oracle_attend_row.restype = i32
-    lib.qsa_oracle_chunk_partial.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
+    lib.qsa_oracle_chunk_partial.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
                                              dbl, P, P, P]
     lib.qsa_oracle_chunk_partial.restype = i32
     lib.qsa_oracle_merge.argtypes = [i32, i32, P, P, P, P]
     lib.qsa_oracle_merge.restype = None
-    lib.qsa_oracle_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, dbl, P, P, P,
-                                           P, P, P, P, P, P, i64, P]
+    lib.qsa_oracle_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, dbl, P, P,
+                                           P, P, P, P, P, P, P, i64, P]
     lib.qsa_oracle_decode_attn.restype = i32
     lib.qsa_oracle_threads.argtypes = []
     lib.qsa_oracle_threads.restype = i32
@@ -121,11 +121,12 @@ def set_threads(n: int) -> None:
 
 
 def attend_row(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel,
-               softmax_scale: float, lib=None) -> np.ndarray:
+               softmax_scale: float, lib=None, page_cells: int = 1) -> np.ndarray:
     """One query row against one (sequence, KV head): the unchunked definition.
 
     q_row [D] (any float dtype, used as double), k/v codes int8 [pool][D],
-    scales fp32 [pool], page_table int32 [N_log], sel int32 [n].
+    scales fp32 [pool], page_table int32 [pages] (pages of page_cells cells),
+    sel int32 [n] logical positions.
     """
     lib = lib or load()
     q = _c(q_row, np.float64)
@@ -137,14 +138,14 @@ def attend_row(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel,
     sl = _c(sel, np.int32)
     D = q.shape[0]
     out = np.zeros(D, dtype=np.float64)
-    _check(lib.qsa_oracle_attend_row(D, k.shape[0], pt.shape[0], _ptr(q), _ptr(k), _ptr(v),
+    _check(lib.qsa_oracle_attend_row(D, k.shape[0], pt.shape[0], int(page_cells), _ptr(q), _ptr(k), _ptr(v),
                                      _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl), sl.shape[0],
                                      float(softmax_scale), _ptr(out)))
     return out
 
 
 def chunk_partial(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel, start: int,
-                  count: int, softmax_scale: float, lib=None):
+                  count: int, softmax_scale: float, lib=None, page_cells: int = 1):
     """(m, l, o) of list positions [start, start+count) for one query row."""
     lib = lib or load()
     q = _c(q_row, np.float64)
@@ -160,7 +161,7 @@ def chunk_partial(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel, st
     m = np.zeros(1, np.float64)
     l = np.zeros(1, np.float64)
     o = np.zeros(D, np.float64)
-    _check(lib.qsa_oracle_chunk_partial(D, k.shape[0], pt.shape[0], _ptr(q), _ptr(k), _ptr(v),
+    _check(lib.qsa_oracle_chunk_partial(D, k.shape[0], pt.shape[0], int(page_cells), _ptr(q), _ptr(k), _ptr(v),
                                         _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl), int(start),
                                         int(count), float(softmax_scale), _ptr(m), _ptr(l),
                                         _ptr(o)))
@@ -180,7 +181,7 @@ def merge(m, l, o, lib=None) -> np.ndarray:
 
 
 def row_partials(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel,
-                 chunk_cells: int, softmax_scale: float, lib=None):
+                 chunk_cells: int, softmax_scale: float, lib=None, page_cells: int = 1):
     """Partials of every chunk of the list for one row: arrays m, l, o."""
     n = int(np.asarray(sel).shape[0])
     n_chunks = (n + chunk_cells - 1) // chunk_cells
@@ -192,7 +193,8 @@ def row_partials(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel,
         start = c * chunk_cells
         cnt = min(chunk_cells, n - start)
         ms[c], ls[c], os_[c] = chunk_partial(q_row, k_codes, v_codes, k_scale, v_scale,
-                                             page_table, sel, start, cnt, softmax_scale, lib)
+                                             page_table, sel, start, cnt, softmax_scale, lib,
+                                             page_cells)
     return ms, ls, os_
 
 
@@ -222,7 +224,7 @@ def decode_attn(p, rows: Optional[Sequence[int]] = None, lib=None) -> np.ndarray
         out = np.zeros((n_rows, p.head_dim), np.float64)
     _check(lib.qsa_oracle_decode_attn(
         p.n_seq, p.n_kv_heads, p.q_per_kv, p.head_dim, p.n_queries, p.pool_cells,
-        p.page_table_len, float(p.softmax_scale), _ptr(q), _ptr(k), _ptr(v), _ptr(ks),
+        p.page_table_len, int(getattr(p, "page_cells", 1)), float(p.softmax_scale), _ptr(q), _ptr(k), _ptr(v), _ptr(ks),
         _ptr(vs), _ptr(pt), _ptr(sl), _ptr(offs),
         _ptr(rows_arr) if rows_arr is not None else None, n_rows, _ptr(out)))
     if rows is None:

@@ -15,10 +15,11 @@ is the plainest symmetric one:
 * ``code = x / scale`` (fp32 division) rounded to the nearest integer, ties
   to even, kept in [-127, 127];
 * a row of zeros gets scale 0 and zero codes;
-* new cell i of sequence b goes to pool slot ``page_table[b][pos]`` with
-  ``pos = positions[b][i]``; a position outside the page table, a page entry
-  of -1 (the cell is not resident) or a page entry outside the pool writes
-  nothing and raises a status bit.
+* new cell i of sequence b goes to the pool slot of ``pos = positions[b][i]``:
+  with pages of P cells (``page_cells``, 1 by default) that is
+  ``page_table[b][pos // P] * P + pos % P``; a position outside the page
+  table, a page entry of -1 (the cell is not resident) or a page entry
+  outside the pool writes nothing and raises a status bit.
 
 All arithmetic is float32, element by element, so a device kernel that makes
 the same float32 operations reaches the same codes and scales bit for bit.
@@ -69,20 +70,22 @@ def kv_append(a, k_pool: np.ndarray, v_pool: np.ndarray, k_scale: np.ndarray,
     Returns the status bits the call raises."""
     k_new = widen(a.k_new, a.dtype)
     v_new = widen(a.v_new, a.dtype)
+    P = int(getattr(a, "page_cells", 1))
     status = 0
     for b in range(a.n_seq):
         for i in range(a.n_new):
             pos = int(a.positions[b, i])
-            if pos < 0 or pos >= a.page_table_len:
+            if pos < 0 or pos >= a.page_table_len * P:
                 status |= STATUS_BAD_POSITION
                 continue
-            slot = int(a.page_table[b, pos])
-            if slot == -1:
+            page = int(a.page_table[b, pos // P])
+            if page == -1:
                 status |= STATUS_NOT_RESIDENT
                 continue
-            if slot < 0 or slot >= a.pool_cells:
+            if page < 0 or page >= a.pool_cells // P:
                 status |= STATUS_BAD_SLOT
                 continue
+            slot = page * P + pos % P
             for g in range(a.n_kv_heads):
                 k_pool[b, g, slot], k_scale[b, g, slot] = quantize_row(k_new[b, i, g])
                 v_pool[b, g, slot], v_scale[b, g, slot] = quantize_row(v_new[b, i, g])

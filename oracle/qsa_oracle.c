@@ -22,7 +22,11 @@
  *   - a masked cell is left out of the softmax, exactly as if it were not in
  *     the list; no valid cell gives an all-zero output;
  *   - an out-of-range list entry or page slot is an error here (the CUDA
- *     path masks it and raises a status bit instead).
+ *     path masks it and raises a status bit instead);
+ *   - pages of page_cells cells (1 by default: one entry per cell): logical
+ *     position pos lies on page pos / page_cells at offset pos % page_cells,
+ *     and a page entry e, a page of the pool, puts it in pool slot
+ *     e * page_cells + offset (the pages leave the page size open).
  *
  * The chunked form (partials m, l, o per chunk and their merge) is here only
  * so the merge identity can be checked; the reference result is the plain
@@ -48,15 +52,16 @@ enum {
     ORACLE_ERR_NOMEM = 4
 };
 
-/* Step a1 (gather): logical position -> pool slot.  *slot = -1 means masked. */
-static int resolve_cell(const int32_t *page_table, int page_table_len, int pool_cells,
-                        int32_t pos, int32_t *slot)
+/* Step a1 (gather): logical position -> pool slot.  *slot = -1 means masked.
+ * The page table has page_table_len entries of page_cells cells each. */
+static int resolve_cell(const int32_t *page_table, int page_table_len, int page_cells,
+                        int pool_cells, int32_t pos, int32_t *slot)
 {
-    if (pos < 0 || pos >= page_table_len) return ORACLE_ERR_POSITION;
-    int32_t s = page_table[pos];
+    if (pos < 0 || (int64_t)pos >= (int64_t)page_table_len * page_cells) return ORACLE_ERR_POSITION;
+    int32_t s = page_table[pos / page_cells];
     if (s == -1) { *slot = -1; return ORACLE_OK; }
-    if (s < 0 || s >= pool_cells) return ORACLE_ERR_SLOT;
-    *slot = s;
+    if (s < 0 || s >= pool_cells / page_cells) return ORACLE_ERR_SLOT;
+    *slot = s * page_cells + pos % page_cells;
     return ORACLE_OK;
 }
 
@@ -76,14 +81,16 @@ static double cell_score(int D, const double *q, const int8_t *k_row, float k_sc
  * Score list positions [start, start+count) of one (sequence, KV head) for one
  * query row.  slots[i] = pool slot or -1 (masked); s[i] = score (valid cells).
  */
-static int score_range(int D, int pool_cells, int page_table_len, const double *q,
-                       const int8_t *k_codes, const float *k_scale,
+static int score_range(int D, int pool_cells, int page_table_len, int page_cells,
+                       const double *q, const int8_t *k_codes, const float *k_scale,
                        const int32_t *page_table, const int32_t *sel, int start, int count,
                        double softmax_scale, int32_t *slots, double *s)
 {
+    if (page_cells < 1 || pool_cells % page_cells != 0) return ORACLE_ERR_ARG;
     for (int i = 0; i < count; ++i) {
         int32_t slot;
-        int err = resolve_cell(page_table, page_table_len, pool_cells, sel[start + i], &slot);
+        int err = resolve_cell(page_table, page_table_len, page_cells, pool_cells,
+                               sel[start + i], &slot);
         if (err) return err;
         slots[i] = slot;
         if (slot >= 0)
@@ -97,8 +104,8 @@ static int score_range(int D, int pool_cells, int page_table_len, const double *
  *   m = max_i s_i,  w_i = exp(s_i - m),  out = sum_i w_i v_hat_i / sum_i w_i.
  * Subtracting m does not change the ratio; it only keeps exp finite.
  */
-int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, const double *q,
-                          const int8_t *k_codes, const int8_t *v_codes,
+int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, int page_cells,
+                          const double *q, const int8_t *k_codes, const int8_t *v_codes,
                           const float *k_scale, const float *v_scale,
                           const int32_t *page_table, const int32_t *sel, int n_sel,
                           double softmax_scale, double *out)
@@ -109,8 +116,8 @@ int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, const doubl
     int32_t *slots = (int32_t *)malloc((size_t)n_sel * sizeof(int32_t));
     double *s = (double *)malloc((size_t)n_sel * sizeof(double));
     if (!slots || !s) { free(slots); free(s); return ORACLE_ERR_NOMEM; }
-    int err = score_range(D, pool_cells, page_table_len, q, k_codes, k_scale, page_table,
-                          sel, 0, n_sel, softmax_scale, slots, s);
+    int err = score_range(D, pool_cells, page_table_len, page_cells, q, k_codes, k_scale,
+                          page_table, sel, 0, n_sel, softmax_scale, slots, s);
     if (err) { free(slots); free(s); return err; }
 
     double m = -INFINITY;
@@ -140,8 +147,8 @@ int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, const doubl
  *   m = max s_i (-inf if no valid cell), l = sum exp(s_i - m),
  *   o = sum exp(s_i - m) v_hat_i (not normalised).
  */
-int qsa_oracle_chunk_partial(int D, int pool_cells, int page_table_len, const double *q,
-                             const int8_t *k_codes, const int8_t *v_codes,
+int qsa_oracle_chunk_partial(int D, int pool_cells, int page_table_len, int page_cells,
+                             const double *q, const int8_t *k_codes, const int8_t *v_codes,
                              const float *k_scale, const float *v_scale,
                              const int32_t *page_table, const int32_t *sel, int start,
                              int count, double softmax_scale, double *m_out, double *l_out,
@@ -155,8 +162,8 @@ int qsa_oracle_chunk_partial(int D, int pool_cells, int page_table_len, const do
     int32_t *slots = (int32_t *)malloc((size_t)count * sizeof(int32_t));
     double *s = (double *)malloc((size_t)count * sizeof(double));
     if (!slots || !s) { free(slots); free(s); return ORACLE_ERR_NOMEM; }
-    int err = score_range(D, pool_cells, page_table_len, q, k_codes, k_scale, page_table,
-                          sel, start, count, softmax_scale, slots, s);
+    int err = score_range(D, pool_cells, page_table_len, page_cells, q, k_codes, k_scale,
+                          page_table, sel, start, count, softmax_scale, slots, s);
     if (err) { free(slots); free(s); return err; }
     double m = -INFINITY;
     for (int i = 0; i < count; ++i)
@@ -208,7 +215,7 @@ void qsa_oracle_merge(int D, int n_chunks, const double *m, const double *l, con
  *   q        [B][T][G*H][D]        (double, widened exactly by the caller)
  *   k/v      [B][G][pool][D]       int8 codes
  *   scales   [B][G][pool]          fp32
- *   pages    [B][page_table_len]   int32
+ *   pages    [B][page_table_len]   int32, pages of page_cells cells
  *   sel      CSR by sel_offsets[B+1]; the list and the page table belong to
  *            the sequence and are shared by its KV heads.
  * rows: NULL for every output row, else n_rows flat row ids
@@ -217,7 +224,7 @@ void qsa_oracle_merge(int D, int n_chunks, const double *m, const double *l, con
  * with -fopenmp.
  */
 int qsa_oracle_decode_attn(int n_seq, int n_kv_heads, int q_per_kv, int head_dim,
-                           int n_queries, int pool_cells, int page_table_len,
+                           int n_queries, int pool_cells, int page_table_len, int page_cells,
                            double softmax_scale, const double *q, const int8_t *k_pool,
                            const int8_t *v_pool, const float *k_scale, const float *v_scale,
                            const int32_t *page_table, const int32_t *sel,
@@ -244,7 +251,7 @@ int qsa_oracle_decode_attn(int n_seq, int n_kv_heads, int q_per_kv, int head_dim
         int g = h / H;
         size_t kv_off = ((size_t)b * G + g) * (size_t)pool_cells;
         int err = qsa_oracle_attend_row(
-            D, pool_cells, page_table_len, q + (size_t)flat * D, k_pool + kv_off * D,
+            D, pool_cells, page_table_len, page_cells, q + (size_t)flat * D, k_pool + kv_off * D,
             v_pool + kv_off * D, k_scale + kv_off, v_scale + kv_off,
             page_table + (size_t)b * page_table_len, sel + sel_offsets[b],
             (int)(sel_offsets[b + 1] - sel_offsets[b]), softmax_scale, o);

@@ -58,6 +58,12 @@ class Problem:
     sel_offsets: np.ndarray
     name: str = ""
     notes: dict = field(default_factory=dict)
+    page_cells: int = 1  # cells per page: the page table has one entry per page
+
+    @property
+    def n_positions(self) -> int:
+        """Logical positions the page table covers."""
+        return self.page_table_len * self.page_cells
 
     @property
     def rows_per_kv(self) -> int:
@@ -153,15 +159,20 @@ def make_problem(*, n_seq: int = 1, n_kv_heads: int = 1, q_per_kv: int = 12,
                  n_selected: Sequence[int] | int = 600, chunk_cells: int = 64,
                  softmax_scale: float = 1.0 / 16.0, q_dtype: str = "f32",
                  selection: str = "sorted", mask_fraction: float = 0.0,
-                 seed: int = SEED_BASE, name: str = "") -> Problem:
+                 seed: int = SEED_BASE, name: str = "", page_cells: int = 1) -> Problem:
     """Draw one seeded problem.
 
     ``selection`` is ``"sorted"`` (without replacement, ascending),
     ``"clustered"`` (30% of cells in runs of 8-64) or ``"full"`` (every
-    logical position 0..N_log-1 in page-table order).
+    logical position 0..N_log-1 in page-table order).  With ``page_cells``
+    P > 1 the page table maps pages of P cells: ``page_table_len`` entries
+    (default pool_cells / P), each a page of the pool or -1, covering
+    ``page_table_len * P`` logical positions.
     """
+    assert pool_cells % page_cells == 0
     if page_table_len is None:
-        page_table_len = pool_cells
+        page_table_len = pool_cells // page_cells
+    n_pos = page_table_len * page_cells
     if isinstance(n_selected, (int, np.integer)):
         n_list: List[int] = [int(n_selected)] * n_seq
     else:
@@ -176,15 +187,15 @@ def make_problem(*, n_seq: int = 1, n_kv_heads: int = 1, q_per_kv: int = 12,
     v_scale = _scales(rng, (n_seq, G, pool_cells))
     pts, sels = [], []
     for b in range(n_seq):
-        pts.append(_page_table(rng, pool_cells, page_table_len, mask_fraction))
+        pts.append(_page_table(rng, pool_cells // page_cells, page_table_len, mask_fraction))
         n = n_list[b]
         if selection == "sorted":
-            sels.append(_select_sorted(rng, page_table_len, n))
+            sels.append(_select_sorted(rng, n_pos, n))
         elif selection == "clustered":
-            sels.append(_select_clustered(rng, page_table_len, n))
+            sels.append(_select_clustered(rng, n_pos, n))
         elif selection == "full":
-            assert n == page_table_len
-            sels.append(np.arange(page_table_len, dtype=np.int32))
+            assert n == n_pos
+            sels.append(np.arange(n_pos, dtype=np.int32))
         else:
             raise ValueError(selection)
     q32 = rng.standard_normal((n_seq, T, G * H, D), dtype=np.float64).astype(np.float32)
@@ -198,7 +209,7 @@ def make_problem(*, n_seq: int = 1, n_kv_heads: int = 1, q_per_kv: int = 12,
                    q_dtype=q_dtype, q=np.ascontiguousarray(q), k_pool=k_pool,
                    v_pool=v_pool, k_scale=k_scale, v_scale=v_scale,
                    page_table=np.stack(pts).astype(np.int32), sel=sel,
-                   sel_offsets=offsets, name=name)
+                   sel_offsets=offsets, name=name, page_cells=page_cells)
 
 
 # ---------------------------------------------------------------------------
@@ -288,12 +299,13 @@ class AppendProblem:
     k_scale: np.ndarray
     v_scale: np.ndarray
     name: str = ""
+    page_cells: int = 1  # cells per page: the page table has one entry per page
 
 
 def make_append(*, n_seq: int = 1, n_kv_heads: int = 1, head_dim: int = 256, n_new: int = 4,
                 pool_cells: int = 4096, page_table_len: Optional[int] = None,
                 dtype: str = "f32", mask_fraction: float = 0.0, seed: int = SEED_BASE,
-                name: str = "") -> AppendProblem:
+                name: str = "", page_cells: int = 1) -> AppendProblem:
     """Draw one seeded append call.
 
     New rows are N(0,1) values times a per-row magnitude log-uniform in
@@ -301,9 +313,11 @@ def make_append(*, n_seq: int = 1, n_kv_heads: int = 1, head_dim: int = 256, n_n
     ``dtype == "bf16"``.  Each sequence appends ``n_new`` distinct logical
     positions whose pages are resident, drawn without replacement.  The pools
     start as in :func:`make_problem` (random codes and scales), so a slot the
-    call must not touch keeps visibly different contents."""
+    call must not touch keeps visibly different contents.  ``page_cells`` as
+    in :func:`make_problem`."""
+    assert pool_cells % page_cells == 0
     if page_table_len is None:
-        page_table_len = pool_cells
+        page_table_len = pool_cells // page_cells
     rng = np.random.Generator(np.random.PCG64(seed))
     G, D = n_kv_heads, head_dim
     k_pool = _codes(rng, (n_seq, G, pool_cells, D))
@@ -312,8 +326,8 @@ def make_append(*, n_seq: int = 1, n_kv_heads: int = 1, head_dim: int = 256, n_n
     v_scale = _scales(rng, (n_seq, G, pool_cells))
     pts, poss = [], []
     for b in range(n_seq):
-        pt = _page_table(rng, pool_cells, page_table_len, mask_fraction)
-        resident = np.flatnonzero(pt >= 0)
+        pt = _page_table(rng, pool_cells // page_cells, page_table_len, mask_fraction)
+        resident = np.flatnonzero(np.repeat(pt, page_cells) >= 0)  # resident positions
         assert resident.size >= n_new, "not enough resident positions"
         poss.append(rng.choice(resident, size=n_new, replace=False).astype(np.int32))
         pts.append(pt)
@@ -329,7 +343,8 @@ def make_append(*, n_seq: int = 1, n_kv_heads: int = 1, head_dim: int = 256, n_n
                          k_new=k_new, v_new=v_new,
                          positions=np.stack(poss).reshape(n_seq, n_new).astype(np.int32),
                          page_table=np.stack(pts).astype(np.int32), k_pool=k_pool,
-                         v_pool=v_pool, k_scale=k_scale, v_scale=v_scale, name=name)
+                         v_pool=v_pool, k_scale=k_scale, v_scale=v_scale, name=name,
+                         page_cells=page_cells)
 
 
 def decode_step_append(seed_offset: int = 0) -> AppendProblem:

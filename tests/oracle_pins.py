@@ -59,6 +59,7 @@ def load_golden(name):
         "v_scale": np.array(nums(fields["v_scale"]), dtype=np.float32),
         "expected": np.array([float(Fraction(x)) for x in fields["expected"].split()]),
         "tol": float(fields["tolerance"]),
+        "page_cells": int(fields.get("page_cells", "1")),
     }
 
 
@@ -128,6 +129,48 @@ def pin_golden_dominant_cell(lib):
     out = oracle.attend_row(g["q"], g["k_codes"], g["v_codes"], g["k_scale"], g["v_scale"],
                             g["page_table"], g["sel"], g["scale"], lib=lib)
     assert np.array_equal(out, g["expected"]), (out, g["expected"])
+
+
+def pin_golden_paged_mean(lib):
+    g = load_golden("paged_mean.txt")
+    out = oracle.attend_row(g["q"], g["k_codes"], g["v_codes"], g["k_scale"], g["v_scale"],
+                            g["page_table"], g["sel"], g["scale"], lib=lib, page_cells=g["page_cells"])
+    assert np.abs(out - g["expected"]).max() <= g["tol"] + 1e-15, (out, g["expected"])
+
+
+def pin_page_relabelling(lib):
+    """Moving whole pages of the pool (rows and scales) and rewriting the page
+    table to match changes no output: bit for bit in fp64."""
+    P, n_pages, D = 4, 8, 8
+    rng = np.random.Generator(np.random.PCG64(1300))
+    k = rng.integers(-127, 128, (P * n_pages, D), dtype=np.int8)
+    v = rng.integers(-127, 128, (P * n_pages, D), dtype=np.int8)
+    ks = rng.uniform(0.005, 0.02, P * n_pages).astype(np.float32)
+    vs = rng.uniform(0.005, 0.02, P * n_pages).astype(np.float32)
+    pt = rng.permutation(n_pages).astype(np.int32)
+    pt[3] = -1
+    sel = np.sort(rng.choice(P * n_pages, 20, replace=False)).astype(np.int32)
+    q = rng.standard_normal(D)
+    ref = oracle.attend_row(q, k, v, ks, vs, pt, sel, 0.4, lib=lib, page_cells=P)
+    perm = rng.permutation(n_pages)  # new page of old page i: perm[i]
+    rows = np.empty(P * n_pages, np.int64)
+    for i in range(n_pages):
+        rows[perm[i] * P:(perm[i] + 1) * P] = np.arange(i * P, (i + 1) * P)
+    pt2 = np.where(pt >= 0, perm[np.maximum(pt, 0)], -1).astype(np.int32)
+    out = oracle.attend_row(q, k[rows], v[rows], ks[rows], vs[rows], pt2, sel, 0.4, lib=lib,
+                            page_cells=P)
+    assert np.array_equal(out, ref)
+    assert not np.array_equal(out, oracle.attend_row(q, k[rows], v[rows], ks[rows], vs[rows], pt,
+                                                     sel, 0.4, lib=lib, page_cells=P))
+
+
+def pin_one_page_is_the_pool(lib):
+    """A single page holding the whole pool: the offset alone places each
+    position, so the result is that of one-cell pages in pool order."""
+    q, k, v, ks, vs, _, sel = small_case(1400, n_pool=16, n_sel=7)
+    one = oracle.attend_row(q, k, v, ks, vs, np.array([0], np.int32), sel, 0.3, lib=lib, page_cells=16)
+    ident = oracle.attend_row(q, k, v, ks, vs, np.arange(16, dtype=np.int32), sel, 0.3, lib=lib)
+    assert np.array_equal(one, ident)
 
 
 def pin_single_cell_is_its_v(lib):
@@ -391,6 +434,9 @@ def pin_rejects_bad_indices(lib):
 PINS = [
     pin_golden_masked_mean,
     pin_golden_dominant_cell,
+    pin_golden_paged_mean,
+    pin_page_relabelling,
+    pin_one_page_is_the_pool,
     pin_single_cell_is_its_v,
     pin_equal_scores_give_mean,
     pin_two_cells_sigmoid,

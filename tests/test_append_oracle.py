@@ -133,6 +133,27 @@ def pin_routing(m):
     assert kp[2].tolist() == [99] * 8 and vp[2].tolist() == [99] * 8 and vs[2] == -1.0
 
 
+def pin_paged_routing(m):
+    """Pages of two cells, page table [1, -1, 0] over a 4-cell pool: new rows
+    at positions [0, 5, 2, 4, 6] go to slots 2 (page 1, offset 0), 1 (page 0,
+    offset 1), nowhere (page -1), 0 (page 0, offset 0), nowhere (position 6
+    is past the 3 pages x 2 cells); slot 3 keeps its contents."""
+    x = np.array([[127.0] * 8, [63.5] * 8, [1.0] * 8, [254.0] * 8, [2.0] * 8], np.float32)
+    a = wl.AppendProblem(n_seq=1, n_kv_heads=1, head_dim=8, n_new=5, pool_cells=4, page_table_len=3,
+                         dtype="f32", k_new=x.reshape(1, 5, 1, 8), v_new=(-x).reshape(1, 5, 1, 8),
+                         positions=np.array([[0, 5, 2, 4, 6]], np.int32),
+                         page_table=np.array([[1, -1, 0]], np.int32), k_pool=None, v_pool=None,
+                         k_scale=None, v_scale=None, page_cells=2)
+    kp = np.full((1, 1, 4, 8), 99, np.int8)
+    vp = np.full((1, 1, 4, 8), 99, np.int8)
+    ks = np.full((1, 1, 4), -1.0, np.float32)
+    vs = np.full((1, 1, 4), -1.0, np.float32)
+    st = m.kv_append(a, kp, vp, ks, vs)
+    assert st == ka.STATUS_NOT_RESIDENT | ka.STATUS_BAD_POSITION, st
+    assert ks[0, 0].tolist() == [2.0, 0.5, 1.0, -1.0], ks
+    assert kp[0, 0, 3].tolist() == [99] * 8 and vp[0, 0, 2].tolist() == [-127] * 8
+
+
 def pin_kv_heads_and_sequences(m):
     """Every (sequence, KV head) row goes to its own pool at the slot of its
     own sequence's page table; the other slots keep their contents."""
@@ -155,7 +176,8 @@ def pin_kv_heads_and_sequences(m):
 
 
 PINS = [pin_golden_rows, pin_golden_through_append, pin_round_trip_bound, pin_max_element,
-        pin_zero_row, pin_pow2_scaling, pin_bf16_rows, pin_routing, pin_kv_heads_and_sequences]
+        pin_zero_row, pin_pow2_scaling, pin_bf16_rows, pin_routing, pin_paged_routing,
+        pin_kv_heads_and_sequences]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -173,9 +195,10 @@ MUTANTS = [
     ("signed_max", "amax = np.float32(np.max(np.abs(x)))", "amax = np.float32(np.max(x))"),
     ("v_from_k_rows", "v_scale[b, g, slot] = quantize_row(v_new[b, i, g])",
      "v_scale[b, g, slot] = quantize_row(k_new[b, i, g])"),
-    ("slot_is_position", "slot = int(a.page_table[b, pos])", "slot = pos"),
-    ("not_resident_to_slot0", "if slot == -1:\n                status |= STATUS_NOT_RESIDENT\n                continue",
-     "if slot == -1:\n                slot = 0"),
+    ("slot_is_position", "slot = page * P + pos % P", "slot = pos"),
+    ("page_offset_dropped", "slot = page * P + pos % P", "slot = page * P"),
+    ("not_resident_to_page0", "if page == -1:\n                status |= STATUS_NOT_RESIDENT\n                continue",
+     "if page == -1:\n                page = 0"),
     ("bf16_high_bits_dropped", "np.asarray(rows).astype(np.uint32) << np.uint32(16)",
      "np.asarray(rows).astype(np.uint32) << np.uint32(15)"),
     ("wrong_kv_head", "k_pool[b, g, slot], k_scale[b, g, slot] = quantize_row(k_new[b, i, g])",

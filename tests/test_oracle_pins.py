@@ -40,12 +40,16 @@ MUTANTS = [
      "double w = exp(s[i]);\n            L += w;"),
     ("position_not_slot", "cell_score(D, q, k_codes + (size_t)slot * D",
      "cell_score(D, q, k_codes + (size_t)(sel[start + i] % pool_cells) * D"),
-    ("k_from_v_pool", "int err = score_range(D, pool_cells, page_table_len, q, k_codes, k_scale, page_table,\n                          sel, 0, n_sel",
-     "int err = score_range(D, pool_cells, page_table_len, q, v_codes, k_scale, page_table,\n                          sel, 0, n_sel"),
+    ("k_from_v_pool", "int err = score_range(D, pool_cells, page_table_len, page_cells, q, k_codes, k_scale,\n                          page_table, sel, 0, n_sel",
+     "int err = score_range(D, pool_cells, page_table_len, page_cells, q, v_codes, k_scale,\n                          page_table, sel, 0, n_sel"),
     ("masked_as_slot0", "if (s == -1) { *slot = -1; return ORACLE_OK; }",
      "if (s == -1) { *slot = 0; return ORACLE_OK; }"),
     ("chunk_ignores_start", "sel[start + i], &slot", "sel[i], &slot"),
     ("merge_no_rescale", "double f = exp(m[c] - M);", "double f = 1.0;"),
+    ("page_offset_dropped", "*slot = s * page_cells + pos % page_cells;", "*slot = s * page_cells;"),
+    ("page_entry_as_cell", "*slot = s * page_cells + pos % page_cells;", "*slot = s + pos % page_cells;"),
+    ("page_index_is_position", "int32_t s = page_table[pos / page_cells];",
+     "int32_t s = page_table[pos % page_table_len];"),
     ("kv_head_by_modulo", "int g = h / H;", "int g = h % G;"),
     ("normaliser_dropped", "for (int d = 0; d < D; ++d) out[d] /= L;\n    }\n    free(slots);",
      "\n    }\n    free(slots);"),
