@@ -85,8 +85,8 @@ typedef enum qsa_algo {
 
 /* Bits of the optional device status word (OR-ed in by the kernels; the
  * library never clears it -- the caller zeroes it when it wants a fresh read). */
-#define QSA_STATUS_BAD_POSITION 0x1u /* a selected position outside [0, page_table_len) */
-#define QSA_STATUS_BAD_SLOT 0x2u     /* a page entry outside [0, pool_cells) and not -1 */
+#define QSA_STATUS_BAD_POSITION 0x1u /* a position outside [0, page_table_len * P) */
+#define QSA_STATUS_BAD_SLOT 0x2u     /* a page entry outside [0, pool_cells / P) and not -1 */
 #define QSA_STATUS_BAD_OFFSETS 0x4u  /* batch offsets decreasing or a list above max_selected */
 #define QSA_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait ran out: outputs invalid */
 #define QSA_STATUS_NOT_RESIDENT 0x10u /* qsa_kv_append: a position whose page entry is -1 */
@@ -96,12 +96,20 @@ typedef struct qsa_shape {
     int32_t q_per_kv;       /* H: query heads per KV head (1..64; 12 on the pages) */
     int32_t head_dim;       /* D: must be 256 */
     int32_t n_queries;      /* T: queries per sequence (1-4 decode; up to 65536) */
-    int32_t pool_cells;     /* N_pool: pool rows per (sequence, KV head) (>= 1) */
-    int32_t page_table_len; /* N_log: page-table entries per sequence (>= 1) */
+    int32_t pool_cells;     /* N_pool: pool rows per (sequence, KV head) (>= 1),
+                               a multiple of the page size P */
+    int32_t page_table_len; /* page-table entries (pages) per sequence (>= 1); the
+                               logical positions are 0 .. page_table_len * P - 1 */
     int32_t chunk_cells;    /* C: selected-list positions per chunk (>= 1) */
     float softmax_scale;    /* multiplies q . k_hat (1/16 on the pages' shapes) */
     int32_t q_dtype;        /* qsa_dtype */
     int32_t algo;           /* qsa_algo */
+    int32_t page_cells;     /* P: cells per page; 0 means 1 (one entry per cell).
+                               Position pos lies on page pos / P at offset pos % P;
+                               a page entry e (a page of the pool, or -1: masked)
+                               puts it in pool slot e * P + pos % P.  The pages
+                               leave the page size open; P = 1 is the configs'
+                               permuted per-cell table. */
 } qsa_shape;
 
 /*
@@ -122,8 +130,9 @@ qsa_status qsa_workspace_bytes(const qsa_shape *shape, int32_t n_seq, int32_t ma
  *              of KV head g is head index g*H + j.  16-byte aligned.
  *   k_pool     [G][pool_cells][D] int8 codes; v_pool the same.  16-byte aligned.
  *   k_scale    [G][pool_cells] fp32 per-cell scales; v_scale the same.
- *   page_table [page_table_len] int32: pool slot of each logical position,
- *              or -1 (masked).
+ *   page_table [page_table_len] int32: pool page of each page of logical
+ *              positions (with P = 1: pool slot of each position), or -1
+ *              (masked).
  *   sel        [n_sel] int32 logical positions (the QSA selection), in list
  *              order; chunk c covers list positions [c*C, min((c+1)*C, n_sel)).
  *   out        [T][G*H][D] fp32, fully written (zeros for rows with no valid
@@ -213,13 +222,15 @@ qsa_status qsa_decode_attn_step_noalloc(const qsa_shape *shape, const void *q,
  * code = x / scale (fp32, correctly rounded) rounded to nearest, ties to
  * even; a row of zeros gets scale 0 and zero codes.
  *   shape      the attention calls' shape; n_kv_heads, head_dim (256),
- *              pool_cells and page_table_len are read, the rest ignored.
+ *              pool_cells, page_table_len and page_cells are read, the rest
+ *              ignored.
  *   n_seq, n_new  sequences and new cells per sequence (either 0: no work).
  *   kv_dtype   QSA_F32 or QSA_BF16: the element type of k_new and v_new.
  *   k_new      [n_seq][n_new][G][D] finite values, 16-byte aligned; v_new
  *              the same.  Row i of sequence b is that sequence's new cell i.
  *   positions  [n_seq][n_new] int32: logical position of each new cell.
- *   page_table [n_seq][page_table_len] int32: pool slot of each position.
+ *   page_table [n_seq][page_table_len] int32: pool page of each page of
+ *              positions (pages of shape->page_cells cells).
  *   k_pool     [n_seq][G][pool_cells][D] int8, 16-byte aligned; written at
  *              the new cells' slots only; v_pool the same.
  *   k_scale    [n_seq][G][pool_cells] fp32; written at those slots; v_scale

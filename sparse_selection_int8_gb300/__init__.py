@@ -56,15 +56,16 @@ class qsa_shape(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("q_dtype", ctypes.c_int32),
         ("algo", ctypes.c_int32),
+        ("page_cells", ctypes.c_int32),
     ]
 
 
 def make_shape(*, n_kv_heads: int, q_per_kv: int, n_queries: int, pool_cells: int,
                page_table_len: int, chunk_cells: int, softmax_scale: float,
                q_dtype: int = QSA_F32, algo: int = QSA_ALGO_AUTO,
-               head_dim: int = HEAD_DIM) -> qsa_shape:
+               head_dim: int = HEAD_DIM, page_cells: int = 1) -> qsa_shape:
     return qsa_shape(n_kv_heads, q_per_kv, head_dim, n_queries, pool_cells, page_table_len,
-                     chunk_cells, softmax_scale, q_dtype, algo)
+                     chunk_cells, softmax_scale, q_dtype, algo, page_cells)
 
 
 _lib = None

@@ -24,6 +24,10 @@ qsa_status check_shape(const qsa_shape *s)
     if (s->q_dtype != QSA_F32 && s->q_dtype != QSA_BF16) return QSA_ERR_INVALID_ARG;
     if (s->algo != QSA_ALGO_AUTO && s->algo != QSA_ALGO_SIMT && s->algo != QSA_ALGO_TCGEN05)
         return QSA_ERR_INVALID_ARG;
+    if (s->page_cells < 0) return QSA_ERR_INVALID_ARG;
+    const int P = s->page_cells > 0 ? s->page_cells : 1;
+    if (s->pool_cells % P != 0 || (long long)s->page_table_len * P > 0x7fffffffll)
+        return QSA_ERR_INVALID_ARG;
     if (s->head_dim != kHeadDim) return QSA_ERR_UNSUPPORTED;
     if (s->q_per_kv > 64 || s->n_queries > 65536 || s->n_kv_heads > 65535)
         return QSA_ERR_UNSUPPORTED;
@@ -137,6 +141,8 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.R = s->q_per_kv * s->n_queries;
     p.pool_cells = s->pool_cells;
     p.page_table_len = s->page_table_len;
+    p.page_cells = s->page_cells > 0 ? s->page_cells : 1;
+    p.pool_pages = s->pool_cells / p.page_cells;
     p.chunk_cells = s->chunk_cells;
     p.max_selected = max_selected;
     p.n_chunks = max_selected > 0 ? (max_selected + s->chunk_cells - 1) / s->chunk_cells : 0;

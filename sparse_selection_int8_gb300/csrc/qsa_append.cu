@@ -41,6 +41,7 @@ struct AppendParams {
     uint32_t pairs;            // n_seq * n_new (new cells); pairs * G < 2^31
     uint32_t n_new, G;
     int pool_cells, page_table_len;
+    int page_cells, pool_pages; // P cells per page; valid page entries 0 .. pool_pages - 1
     int bf16;
 };
 
@@ -173,14 +174,18 @@ __global__ void __launch_bounds__(kAppendThreads, 4) qsa_kv_append_kernel(const 
         }
         const int pos = __ldg(p.positions + bi);
         const uint32_t b = bi / p.n_new;
+        // position pos: page pos / P at offset pos % P; the entry is a page of the pool
+        const int P = p.page_cells;
         int slot = -1;
         uint32_t bad = 0;
-        if (pos < 0 || pos >= p.page_table_len) {
+        if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
             bad = QSA_STATUS_BAD_POSITION;
         } else {
-            slot = __ldg(p.page_table + (size_t)b * p.page_table_len + pos);
-            if (slot == -1) bad = QSA_STATUS_NOT_RESIDENT;
-            else if (slot < 0 || slot >= p.pool_cells) bad = QSA_STATUS_BAD_SLOT;
+            const int page = P == 1 ? pos : pos / P;
+            const int e = __ldg(p.page_table + (size_t)b * p.page_table_len + page);
+            if (e == -1) bad = QSA_STATUS_NOT_RESIDENT;
+            else if (e < 0 || e >= p.pool_pages) bad = QSA_STATUS_BAD_SLOT;
+            else slot = P == 1 ? e : e * P + (pos - page * P);
         }
         if (bad) { // the whole warp agrees
             if (lane == 0 && p.status) atomicOr(p.status, bad);
@@ -218,6 +223,10 @@ extern "C" qsa_status qsa_kv_append(const qsa_shape *shape, int32_t n_seq, int32
     if (shape->n_kv_heads < 1 || shape->pool_cells < 1 || shape->page_table_len < 1)
         return QSA_ERR_INVALID_ARG;
     if (shape->head_dim != qsa::kHeadDim) return QSA_ERR_UNSUPPORTED;
+    if (shape->page_cells < 0) return QSA_ERR_INVALID_ARG;
+    const int P = shape->page_cells > 0 ? shape->page_cells : 1;
+    if (shape->pool_cells % P != 0 || (long long)shape->page_table_len * P > 0x7fffffffll)
+        return QSA_ERR_INVALID_ARG;
     if (n_seq < 0 || n_new < 0) return QSA_ERR_INVALID_ARG;
     if (kv_dtype != QSA_F32 && kv_dtype != QSA_BF16) return QSA_ERR_INVALID_ARG;
     if (!k_new || !v_new || !positions || !page_table || !k_pool || !v_pool || !k_scale || !v_scale)
@@ -252,6 +261,8 @@ extern "C" qsa_status qsa_kv_append(const qsa_shape *shape, int32_t n_seq, int32
     p.G = (uint32_t)shape->n_kv_heads;
     p.pool_cells = shape->pool_cells;
     p.page_table_len = shape->page_table_len;
+    p.page_cells = P;
+    p.pool_pages = shape->pool_cells / P;
     p.bf16 = kv_dtype == QSA_BF16;
     // as many blocks as are resident at once (every warp strides over items)
     auto kernel = p.bf16 ? qsa::qsa_kv_append_kernel<true> : qsa::qsa_kv_append_kernel<false>;

@@ -82,6 +82,7 @@ struct Misc {
     // resolution rings (tile t in entry t % 4), filled by asynchronous copies
     int32_t rs_sel[4][kTile]; // list entries
     int32_t rs_pg[4][kTile];  // page-table entries (-1 masked, kBadPos out of range)
+    int32_t rs_off[4][kTile]; // offset of the position in its page (pages of P > 1 cells)
     float rs_ks[4][kTile];    // k_scale, v_scale of the cell's slot (0 if masked)
     float rs_vs[4][kTile];
     uint8_t sc_ok[2][kTile];  // cell holds a valid slot
@@ -332,20 +333,21 @@ __device__ __forceinline__ int tile_base(const Params &p, const TileIt &t)
 
 constexpr int kBadPos = INT_MIN;
 
-// Checked pool slot, -1 when masked or out of range; `report` raises the
-// status bits (the one thread that resolves the cell reports).
-__device__ __forceinline__ int slot_of(const Params &p, int raw, bool report)
+// Checked pool slot of a page entry `raw` and the position's offset in its
+// page, -1 when masked or out of range; `report` raises the status bits (the
+// one thread that resolves the cell reports).
+__device__ __forceinline__ int slot_of(const Params &p, int raw, int off, bool report)
 {
     if (raw == kBadPos) {
         if (report) raise_status(p, QSA_STATUS_BAD_POSITION);
         return -1;
     }
     if (raw == -1) return -1;
-    if (raw < 0 || raw >= p.pool_cells) {
+    if (raw < 0 || raw >= p.pool_pages) {
         if (report) raise_status(p, QSA_STATUS_BAD_SLOT);
         return -1;
     }
-    return raw;
+    return p.page_cells == 1 ? raw : raw * p.page_cells + off;
 }
 
 // ---------------------------------------------------------------- queries
@@ -664,9 +666,17 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     if (cx >= mt4) {
                         *dst = -1; // past the tile's cells: masked
                     } else {
-                        const int pos = ms.rs_sel[e4][cx];
-                        if (pos < 0 || pos >= p.page_table_len) *dst = kBadPos;
-                        else cp_async4(smem_u32(dst), prow + pos);
+                        // position pos: page pos / P, offset pos % P (P = 1: the entry is the slot)
+                        const int pos = ms.rs_sel[e4][cx], P = p.page_cells;
+                        if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
+                            *dst = kBadPos;
+                        } else if (P == 1) {
+                            cp_async4(smem_u32(dst), prow + pos);
+                        } else {
+                            const int page = pos / P;
+                            ms.rs_off[e4][cx] = pos - page * P;
+                            cp_async4(smem_u32(dst), prow + page);
+                        }
                     }
                 }
             }
@@ -676,8 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 int sa = -1, sb = -1;
                 if (scl) {
                     const int e2 = (j + 2) & 3;
-                    sa = slot_of(p, ms.rs_pg[e2][cA], true);
-                    sb = slot_of(p, ms.rs_pg[e2][cB], true);
+                    sa = slot_of(p, ms.rs_pg[e2][cA], ms.rs_off[e2][cA], true);
+                    sb = slot_of(p, ms.rs_pg[e2][cB], ms.rs_off[e2][cB], true);
                     const size_t kvb = (size_t)bg2 * p.pool_cells;
                     if (sa >= 0) {
                         cp_async4(smem_u32(&ms.rs_ks[e2][cA]), p.k_scale + kvb + sa);

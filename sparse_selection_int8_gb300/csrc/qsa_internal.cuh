@@ -44,6 +44,8 @@ struct Params {
     int32_t n_sel_single;      // list length when sel_offsets == nullptr
     int32_t n_seq, G, H, T, R; // R = T*H rows per KV head
     int32_t pool_cells, page_table_len, chunk_cells, n_chunks, max_selected;
+    int32_t page_cells;        // P >= 1: cells per page (positions: page_table_len * P)
+    int32_t pool_pages;        // pool_cells / P: valid page entries are 0 .. pool_pages - 1
     int32_t q_bf16;
     float scale_log2;          // softmax_scale * log2(e)
 };
@@ -98,20 +100,24 @@ __device__ __forceinline__ void seq_range(const Params &p, int b, int *start, in
 }
 
 // Step a1: logical position -> pool slot of sequence b; -1 when masked or
-// out of range (out-of-range entries also raise a status bit).
+// out of range (out-of-range entries also raise a status bit).  Position pos
+// lies on page pos / P at offset pos % P; the page entry (a page of the pool)
+// places it at slot entry * P + offset.
 __device__ __forceinline__ int resolve_slot(const Params &p, int b, int pos)
 {
-    if (pos < 0 || pos >= p.page_table_len) {
+    const int P = p.page_cells;
+    if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
         raise_status(p, QSA_STATUS_BAD_POSITION);
         return -1;
     }
-    int slot = __ldg(p.page_table + (size_t)b * p.page_table_len + pos);
-    if (slot == -1) return -1;
-    if (slot < 0 || slot >= p.pool_cells) {
+    const int page = P == 1 ? pos : pos / P;
+    const int e = __ldg(p.page_table + (size_t)b * p.page_table_len + page);
+    if (e == -1) return -1;
+    if (e < 0 || e >= p.pool_pages) {
         raise_status(p, QSA_STATUS_BAD_SLOT);
         return -1;
     }
-    return slot;
+    return P == 1 ? e : e * P + (pos - page * P);
 }
 
 __device__ __forceinline__ float fast_exp2(float x)

@@ -51,7 +51,8 @@ class DeviceProblem:
                                 page_table_len=p.page_table_len, chunk_cells=p.chunk_cells,
                                 softmax_scale=p.softmax_scale,
                                 q_dtype=QSA_BF16 if p.q_dtype == "bf16" else QSA_F32,
-                                algo=algo, head_dim=p.head_dim)
+                                algo=algo, head_dim=p.head_dim,
+                                page_cells=getattr(p, "page_cells", 1))
         self.ws_bytes = qsa_workspace_bytes(self.shape, self.n_seq, self.max_selected)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty((p.n_seq, p.n_queries, p.n_kv_heads * p.q_per_kv, p.head_dim),
@@ -101,7 +102,8 @@ class DeviceAppend:
         self.kv_dtype = QSA_BF16 if a.dtype == "bf16" else QSA_F32
         self.shape = make_shape(n_kv_heads=a.n_kv_heads, q_per_kv=1, n_queries=1,
                                 pool_cells=a.pool_cells, page_table_len=a.page_table_len,
-                                chunk_cells=1, softmax_scale=1.0, head_dim=a.head_dim)
+                                chunk_cells=1, softmax_scale=1.0, head_dim=a.head_dim,
+                                page_cells=getattr(a, "page_cells", 1))
 
     def run(self, stream=None):
         a = self.a

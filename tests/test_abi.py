@@ -168,6 +168,21 @@ def test_append_rejects_before_launch(lib, over, code):
     assert call_append(lib, shape(), append_args(**over)) == code
 
 
+@pytest.mark.parametrize("page_cells,pool_cells,code", [
+    (-1, 4096, qsa.QSA_ERR_INVALID_ARG),
+    (3, 4096, qsa.QSA_ERR_INVALID_ARG),   # the pool is not a whole number of pages
+    (16, 4096, qsa.QSA_OK),
+    (0, 4096, qsa.QSA_OK),                # 0 means one cell per page
+])
+def test_page_size_checked(lib, page_cells, pool_cells, code):
+    s = shape(pool_cells=pool_cells, page_table_len=256)
+    s.page_cells = page_cells
+    out = ctypes.c_size_t(0)
+    assert lib.qsa_workspace_bytes(ctypes.byref(s), 1, 100, ctypes.byref(out)) == code
+    if code != qsa.QSA_OK:
+        assert call_append(lib, s, append_args()) == code
+
+
 def test_append_checks_shape_and_skips_empty_calls(lib):
     s = shape()
     s.head_dim = 128

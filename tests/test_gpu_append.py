@@ -67,6 +67,17 @@ def test_append_shapes(dtype, n_seq, G, n_new):
     assert_same(a, f"append B={n_seq} G={G} n_new={n_new} {dtype}")
 
 
+@pytest.mark.parametrize("P", [2, 16])
+def test_paged_append(P):
+    a = wl.make_append(n_seq=3, n_kv_heads=2, n_new=300, pool_cells=4096, mask_fraction=0.2,
+                       page_cells=P, seed=6700 + P)
+    a.positions[1, 7] = a.page_table_len * P          # past the last position
+    bad = np.flatnonzero(a.page_table[2] >= 0)[0]
+    a.page_table[2, bad] = 4096 // P                   # past the last pool page
+    a.positions[2, 3] = bad * P + P - 1
+    assert_same(a, f"paged append P={P}")
+
+
 def test_prompt_sized_append():
     """A whole 32,768-cell pool of two KV heads written in one call (more
     warps than the grid, so the grid-stride loop runs several rounds)."""

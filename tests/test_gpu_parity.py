@@ -225,6 +225,72 @@ def test_decode_path_rescaling(H, T, G):
     check_full(p, "auto", f"decode rescaling H={H} T={T} G={G}")
 
 
+def expanded_table(p):
+    """The same problem with its page table written out per cell (P = 1)."""
+    import copy
+    P = p.page_cells
+    e = copy.copy(p)
+    pt = np.repeat(p.page_table, P, axis=1).astype(np.int64)
+    off = np.tile(np.arange(P), p.page_table_len)[None, :]
+    e.page_table = np.where(pt >= 0, pt * P + off, -1).astype(np.int32)
+    e.page_table_len = p.page_table_len * P
+    e.page_cells = 1
+    return e
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("P", [2, 16, 64])
+def test_paged_tables(algo, P):
+    """Page tables of P-cell pages with masked pages, on a ragged batch and on
+    one sequence: against the oracle, and bit-identical to the same calls with
+    the table written out per cell (every cell must resolve to the same slot)."""
+    for n_seq, lens in ((3, [700, 1500, 37]), (1, [2051])):
+        p = wl.make_problem(n_seq=n_seq, n_kv_heads=2, n_queries=2, pool_cells=8192,
+                            n_selected=lens, chunk_cells=128, mask_fraction=0.1,
+                            page_cells=P, seed=9500 + P + n_seq)
+        dp, out = run(p, algo)
+        assert_parity(out, oracle.decode_attn(p), f"paged P={P} B={n_seq}")
+        assert int(dp.status.item()) == 0
+        _, out1 = run(expanded_table(p), algo)
+        assert np.array_equal(out.view(np.uint32), out1.view(np.uint32)), f"P={P} B={n_seq}"
+
+
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+def test_paged_prompt_path(algo):
+    p = wl.make_problem(n_queries=64, pool_cells=2048, n_selected=2048, chunk_cells=1024,
+                        q_dtype="bf16", selection="full", page_cells=16, seed=9600)
+    dp, out = run(p, algo)
+    assert_parity(out, oracle.decode_attn(p), "paged prompt path")
+    _, out1 = run(expanded_table(p), algo)
+    assert np.array_equal(out.view(np.uint32), out1.view(np.uint32))
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_paged_bad_entries_are_masked_and_reported(algo):
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_kv_heads=1, n_queries=1, pool_cells=1024, n_selected=300,
+                        chunk_cells=64, page_cells=8, seed=9700)
+    p.sel[5] = p.page_table_len * 8           # one past the last position
+    p.page_table[0, p.sel[40] // 8] = 1024 // 8  # one past the last pool page
+    dp, out = run(p, algo)
+    assert int(dp.status.item()) == qsa.QSA_STATUS_BAD_POSITION | qsa.QSA_STATUS_BAD_SLOT
+    q = copy_problem_masking(p)
+    assert_parity(out, oracle.decode_attn(q), "paged bad entries")
+
+
+def copy_problem_masking(p):
+    """The oracle's view of a call with bad entries: they count as masked."""
+    import copy
+    q = copy.copy(p)
+    q.page_table = p.page_table.copy()
+    bad_page = p.page_table[0] >= p.pool_cells // p.page_cells
+    q.page_table[0, bad_page] = -1
+    keep = (p.sel >= 0) & (p.sel < p.page_table_len * p.page_cells)
+    q.sel = p.sel[keep]
+    q.sel_offsets = np.array([0, q.sel.shape[0]], np.int32)
+    return q
+
+
 @pytest.mark.parametrize("algo", ["auto", "simt"])
 def test_batch_list_above_bound_is_clamped(algo):
     import sparse_selection_int8_gb300 as qsa
