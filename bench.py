@@ -207,7 +207,7 @@ def source_digest(*names) -> str:
 # only while the kernel source hashes to the recorded digest.
 TRAFFIC = {
     # qsa_decode T = 1..4, chunk kernel, sum of the four launches (profiles/qsa_chunk_tc_qsa_decode_sweep.md)
-    "8eefbd587c7d7fc2": 6096128,
+    "a14981ef6c8371e5": 6097152,
 }
 
 # Sources of the chunk kernel the recorded traffic belongs to.
@@ -495,7 +495,8 @@ def measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush, budget_s
     res = {}
     t_start = time.perf_counter()
     specs = [("tiny_decode", wl.tiny_decode), ("batched_decode", wl.batched_decode),
-             ("long_context", wl.long_context), ("prompt_shaped", wl.prompt_shaped)]
+             ("long_context", wl.long_context), ("long_context_pages16", wl.long_context_paged),
+             ("prompt_shaped", wl.prompt_shaped)]
     for name, make in specs:
         if time.perf_counter() - t_start > budget_s:
             res[name] = {"skipped": "time budget"}

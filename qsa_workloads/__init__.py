@@ -251,6 +251,16 @@ def long_context(seed_offset: int = 0) -> Problem:
                         seed=SEED_BASE + 4 + seed_offset, name="long_context")
 
 
+def long_context_paged(page_cells: int = 16, seed_offset: int = 0) -> Problem:
+    """long_context with a page table of ``page_cells``-cell pages (a
+    companion case: the clustered runs then sit on physically contiguous
+    slots)."""
+    return make_problem(n_seq=8, n_kv_heads=2, n_queries=2, pool_cells=131072,
+                        n_selected=16384, chunk_cells=256, selection="clustered",
+                        page_cells=page_cells, seed=SEED_BASE + 4 + seed_offset,
+                        name=f"long_context_pages{page_cells}")
+
+
 def prompt_shaped(seed_offset: int = 0, n_queries: int = 2048,
                   pool_cells: int = 32768, chunk_cells: int = 11008) -> Problem:
     """1 KV head x 12 query heads, 2,048 bf16 queries against all 32,768 cells
