@@ -38,7 +38,7 @@ qsa_status check_shape(const qsa_shape *s)
 enum Path { kPathSimt = 0, kPathDecodeTc = 1, kPathPromptTc = 2, kPathNone = -1 };
 
 // Kernel family by shape: the cells-on-M tensor-core kernel for decode
-// windows (at most 64 query rows per KV head), the rows-on-M tensor-core
+// windows (at most 80 query rows per KV head), the rows-on-M tensor-core
 // kernel for prompt-shaped calls (chunks of at least one 128-cell tile), the
 // CUDA-core kernel otherwise or when asked for.
 Path select_path(const qsa_shape *s)

@@ -6,7 +6,7 @@
 // (T queries x H heads of one KV head).  The pages' Turing kernel reads each
 // cell once for all 12 heads and does the dot products with warp shuffles;
 // here both contractions run on the 5th-generation tensor cores with the
-// cells on the MMA's M dimension, because a decode window has only 12-64
+// cells on the MMA's M dimension, because a decode window has only 12-80
 // query rows:
 //
 //   S^T[cell][row] = K_code[cell][:] . Q[row][:]      M=128 cells, N=rows, K=256
