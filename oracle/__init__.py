@@ -63,15 +63,15 @@ def build() -> str:
 def _bind(lib):
     P = ctypes.c_void_p
     i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
-    lib.qsa_oracle_attend_row.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32, dbl, P]
+    lib.qsa_oracle_attend_row.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, dbl, P]
     lib.qsa_oracle_attend_row.restype = i32
-    lib.qsa_oracle_chunk_partial.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
-                                             dbl, P, P, P]
+    lib.qsa_oracle_chunk_partial.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32,
+                                             i32, dbl, P, P, P]
     lib.qsa_oracle_chunk_partial.restype = i32
     lib.qsa_oracle_merge.argtypes = [i32, i32, P, P, P, P]
     lib.qsa_oracle_merge.restype = None
     lib.qsa_oracle_decode_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, dbl, P, P,
-                                           P, P, P, P, P, P, P, i64, P]
+                                           P, P, P, P, P, P, P, P, i64, P]
     lib.qsa_oracle_decode_attn.restype = i32
     lib.qsa_oracle_threads.argtypes = []
     lib.qsa_oracle_threads.restype = i32
@@ -107,6 +107,10 @@ def widen_queries(q: np.ndarray, q_dtype: str) -> np.ndarray:
     return np.asarray(q, dtype=np.float32).astype(np.float64)
 
 
+def _limit(limit) -> int:
+    return 0x7FFFFFFF if limit is None else int(limit)
+
+
 def _check(err: int):
     if err:
         raise OracleError(ERRORS.get(err, f"oracle error {err}"))
@@ -121,12 +125,14 @@ def set_threads(n: int) -> None:
 
 
 def attend_row(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel,
-               softmax_scale: float, lib=None, page_cells: int = 1) -> np.ndarray:
+               softmax_scale: float, lib=None, page_cells: int = 1,
+               limit: Optional[int] = None) -> np.ndarray:
     """One query row against one (sequence, KV head): the unchunked definition.
 
     q_row [D] (any float dtype, used as double), k/v codes int8 [pool][D],
     scales fp32 [pool], page_table int32 [pages] (pages of page_cells cells),
-    sel int32 [n] logical positions.
+    sel int32 [n] logical positions; ``limit``: the row sees only positions
+    below it (None: no limit).
     """
     lib = lib or load()
     q = _c(q_row, np.float64)
@@ -138,14 +144,16 @@ def attend_row(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel,
     sl = _c(sel, np.int32)
     D = q.shape[0]
     out = np.zeros(D, dtype=np.float64)
-    _check(lib.qsa_oracle_attend_row(D, k.shape[0], pt.shape[0], int(page_cells), _ptr(q), _ptr(k), _ptr(v),
+    _check(lib.qsa_oracle_attend_row(D, k.shape[0], pt.shape[0], int(page_cells), _limit(limit),
+                                     _ptr(q), _ptr(k), _ptr(v),
                                      _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl), sl.shape[0],
                                      float(softmax_scale), _ptr(out)))
     return out
 
 
 def chunk_partial(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel, start: int,
-                  count: int, softmax_scale: float, lib=None, page_cells: int = 1):
+                  count: int, softmax_scale: float, lib=None, page_cells: int = 1,
+                  limit: Optional[int] = None):
     """(m, l, o) of list positions [start, start+count) for one query row."""
     lib = lib or load()
     q = _c(q_row, np.float64)
@@ -161,7 +169,8 @@ def chunk_partial(q_row, k_codes, v_codes, k_scale, v_scale, page_table, sel, st
     m = np.zeros(1, np.float64)
     l = np.zeros(1, np.float64)
     o = np.zeros(D, np.float64)
-    _check(lib.qsa_oracle_chunk_partial(D, k.shape[0], pt.shape[0], int(page_cells), _ptr(q), _ptr(k), _ptr(v),
+    _check(lib.qsa_oracle_chunk_partial(D, k.shape[0], pt.shape[0], int(page_cells), _limit(limit),
+                                        _ptr(q), _ptr(k), _ptr(v),
                                         _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl), int(start),
                                         int(count), float(softmax_scale), _ptr(m), _ptr(l),
                                         _ptr(o)))
@@ -212,6 +221,8 @@ def decode_attn(p, rows: Optional[Sequence[int]] = None, lib=None) -> np.ndarray
     pt = _c(p.page_table, np.int32)
     sl = _c(p.sel, np.int32)
     offs = _c(p.sel_offsets, np.int64)
+    lim = getattr(p, "q_limit", None)
+    lim = None if lim is None else _c(lim, np.int32).reshape(p.n_seq, p.n_queries)
     GH = p.n_kv_heads * p.q_per_kv
     total = p.n_seq * p.n_queries * GH
     if rows is None:
@@ -225,7 +236,7 @@ def decode_attn(p, rows: Optional[Sequence[int]] = None, lib=None) -> np.ndarray
     _check(lib.qsa_oracle_decode_attn(
         p.n_seq, p.n_kv_heads, p.q_per_kv, p.head_dim, p.n_queries, p.pool_cells,
         p.page_table_len, int(getattr(p, "page_cells", 1)), float(p.softmax_scale), _ptr(q), _ptr(k), _ptr(v), _ptr(ks),
-        _ptr(vs), _ptr(pt), _ptr(sl), _ptr(offs),
+        _ptr(vs), _ptr(pt), _ptr(sl), _ptr(offs), _ptr(lim) if lim is not None else None,
         _ptr(rows_arr) if rows_arr is not None else None, n_rows, _ptr(out)))
     if rows is None:
         return out.reshape(p.n_seq, p.n_queries, GH, p.head_dim)

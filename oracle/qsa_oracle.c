@@ -26,7 +26,10 @@
  *   - pages of page_cells cells (1 by default: one entry per cell): logical
  *     position pos lies on page pos / page_cells at offset pos % page_cells,
  *     and a page entry e, a page of the pool, puts it in pool slot
- *     e * page_cells + offset (the pages leave the page size open).
+ *     e * page_cells + offset (the pages leave the page size open);
+ *   - an optional causal limit per query of the window: query t sees only
+ *     the selected cells whose logical position is below limit[t] (a cell
+ *     it does not see is left out of its softmax, as if masked).
  *
  * The chunked form (partials m, l, o per chunk and their merge) is here only
  * so the merge identity can be checked; the reference result is the plain
@@ -82,9 +85,9 @@ static double cell_score(int D, const double *q, const int8_t *k_row, float k_sc
  * query row.  slots[i] = pool slot or -1 (masked); s[i] = score (valid cells).
  */
 static int score_range(int D, int pool_cells, int page_table_len, int page_cells,
-                       const double *q, const int8_t *k_codes, const float *k_scale,
-                       const int32_t *page_table, const int32_t *sel, int start, int count,
-                       double softmax_scale, int32_t *slots, double *s)
+                       int32_t limit, const double *q, const int8_t *k_codes,
+                       const float *k_scale, const int32_t *page_table, const int32_t *sel,
+                       int start, int count, double softmax_scale, int32_t *slots, double *s)
 {
     if (page_cells < 1 || pool_cells % page_cells != 0) return ORACLE_ERR_ARG;
     for (int i = 0; i < count; ++i) {
@@ -92,6 +95,7 @@ static int score_range(int D, int pool_cells, int page_table_len, int page_cells
         int err = resolve_cell(page_table, page_table_len, page_cells, pool_cells,
                                sel[start + i], &slot);
         if (err) return err;
+        if (sel[start + i] >= limit) slot = -1; /* beyond this query's causal limit */
         slots[i] = slot;
         if (slot >= 0)
             s[i] = cell_score(D, q, k_codes + (size_t)slot * D, k_scale[slot], softmax_scale);
@@ -105,7 +109,8 @@ static int score_range(int D, int pool_cells, int page_table_len, int page_cells
  * Subtracting m does not change the ratio; it only keeps exp finite.
  */
 int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, int page_cells,
-                          const double *q, const int8_t *k_codes, const int8_t *v_codes,
+                          int32_t limit, const double *q, const int8_t *k_codes,
+                          const int8_t *v_codes,
                           const float *k_scale, const float *v_scale,
                           const int32_t *page_table, const int32_t *sel, int n_sel,
                           double softmax_scale, double *out)
@@ -116,8 +121,8 @@ int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, int page_ce
     int32_t *slots = (int32_t *)malloc((size_t)n_sel * sizeof(int32_t));
     double *s = (double *)malloc((size_t)n_sel * sizeof(double));
     if (!slots || !s) { free(slots); free(s); return ORACLE_ERR_NOMEM; }
-    int err = score_range(D, pool_cells, page_table_len, page_cells, q, k_codes, k_scale,
-                          page_table, sel, 0, n_sel, softmax_scale, slots, s);
+    int err = score_range(D, pool_cells, page_table_len, page_cells, limit, q, k_codes,
+                          k_scale, page_table, sel, 0, n_sel, softmax_scale, slots, s);
     if (err) { free(slots); free(s); return err; }
 
     double m = -INFINITY;
@@ -148,7 +153,8 @@ int qsa_oracle_attend_row(int D, int pool_cells, int page_table_len, int page_ce
  *   o = sum exp(s_i - m) v_hat_i (not normalised).
  */
 int qsa_oracle_chunk_partial(int D, int pool_cells, int page_table_len, int page_cells,
-                             const double *q, const int8_t *k_codes, const int8_t *v_codes,
+                             int32_t limit, const double *q, const int8_t *k_codes,
+                             const int8_t *v_codes,
                              const float *k_scale, const float *v_scale,
                              const int32_t *page_table, const int32_t *sel, int start,
                              int count, double softmax_scale, double *m_out, double *l_out,
@@ -162,8 +168,8 @@ int qsa_oracle_chunk_partial(int D, int pool_cells, int page_table_len, int page
     int32_t *slots = (int32_t *)malloc((size_t)count * sizeof(int32_t));
     double *s = (double *)malloc((size_t)count * sizeof(double));
     if (!slots || !s) { free(slots); free(s); return ORACLE_ERR_NOMEM; }
-    int err = score_range(D, pool_cells, page_table_len, page_cells, q, k_codes, k_scale,
-                          page_table, sel, start, count, softmax_scale, slots, s);
+    int err = score_range(D, pool_cells, page_table_len, page_cells, limit, q, k_codes,
+                          k_scale, page_table, sel, start, count, softmax_scale, slots, s);
     if (err) { free(slots); free(s); return err; }
     double m = -INFINITY;
     for (int i = 0; i < count; ++i)
@@ -218,6 +224,7 @@ void qsa_oracle_merge(int D, int n_chunks, const double *m, const double *l, con
  *   pages    [B][page_table_len]   int32, pages of page_cells cells
  *   sel      CSR by sel_offsets[B+1]; the list and the page table belong to
  *            the sequence and are shared by its KV heads.
+ *   limits   NULL, or [B][T]: query t of sequence b sees positions < limits[b][t].
  * rows: NULL for every output row, else n_rows flat row ids
  *   ((b*T + t)*G*H + h); out is [rows][D].
  * Rows are independent; OpenMP spreads them over the host cores when built
@@ -228,8 +235,8 @@ int qsa_oracle_decode_attn(int n_seq, int n_kv_heads, int q_per_kv, int head_dim
                            double softmax_scale, const double *q, const int8_t *k_pool,
                            const int8_t *v_pool, const float *k_scale, const float *v_scale,
                            const int32_t *page_table, const int32_t *sel,
-                           const int64_t *sel_offsets, const int64_t *rows, int64_t n_rows,
-                           double *out)
+                           const int64_t *sel_offsets, const int32_t *limits,
+                           const int64_t *rows, int64_t n_rows, double *out)
 {
     const int B = n_seq, G = n_kv_heads, H = q_per_kv, D = head_dim, T = n_queries;
     if (B < 0 || G <= 0 || H <= 0 || D <= 0 || T <= 0) return ORACLE_ERR_ARG;
@@ -251,11 +258,11 @@ int qsa_oracle_decode_attn(int n_seq, int n_kv_heads, int q_per_kv, int head_dim
         int g = h / H;
         size_t kv_off = ((size_t)b * G + g) * (size_t)pool_cells;
         int err = qsa_oracle_attend_row(
-            D, pool_cells, page_table_len, page_cells, q + (size_t)flat * D, k_pool + kv_off * D,
+            D, pool_cells, page_table_len, page_cells,
+            limits ? limits[(size_t)b * T + t] : INT32_MAX, q + (size_t)flat * D, k_pool + kv_off * D,
             v_pool + kv_off * D, k_scale + kv_off, v_scale + kv_off,
             page_table + (size_t)b * page_table_len, sel + sel_offsets[b],
             (int)(sel_offsets[b + 1] - sel_offsets[b]), softmax_scale, o);
-        (void)t;
         if (err) {
 #pragma omp critical
             err_all = err;

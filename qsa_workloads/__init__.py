@@ -59,6 +59,8 @@ class Problem:
     name: str = ""
     notes: dict = field(default_factory=dict)
     page_cells: int = 1  # cells per page: the page table has one entry per page
+    # optional causal limits [B][T]: query t of sequence b sees positions < q_limit[b][t]
+    q_limit: Optional[np.ndarray] = None
 
     @property
     def n_positions(self) -> int:

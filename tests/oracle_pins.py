@@ -60,6 +60,7 @@ def load_golden(name):
         "expected": np.array([float(Fraction(x)) for x in fields["expected"].split()]),
         "tol": float(fields["tolerance"]),
         "page_cells": int(fields.get("page_cells", "1")),
+        "fields": fields,
     }
 
 
@@ -171,6 +172,50 @@ def pin_one_page_is_the_pool(lib):
     one = oracle.attend_row(q, k, v, ks, vs, np.array([0], np.int32), sel, 0.3, lib=lib, page_cells=16)
     ident = oracle.attend_row(q, k, v, ks, vs, np.arange(16, dtype=np.int32), sel, 0.3, lib=lib)
     assert np.array_equal(one, ident)
+
+
+def pin_golden_causal_window(lib):
+    g = load_golden("causal_window.txt")
+    for t in (0, 1):
+        limit = int(g["fields"][f"limit_{t}"])
+        expected = np.array([float(Fraction(x)) for x in g["fields"][f"expected_{t}"].split()])
+        out = oracle.attend_row(g["q"], g["k_codes"], g["v_codes"], g["k_scale"], g["v_scale"],
+                                g["page_table"], g["sel"], g["scale"], lib=lib, limit=limit)
+        assert np.abs(out - expected).max() <= g["tol"] + 1e-15, (t, out, expected)
+
+
+def pin_limit_equals_removal(lib):
+    """A causal limit L gives, bit for bit, the result of the list without its
+    positions >= L (in list order), for partials as well."""
+    q, k, v, ks, vs, pt, sel = small_case(1500, n_pool=64, n_sel=30, mask=5)
+    rng = np.random.default_rng(1501)
+    sel = rng.permutation(sel).astype(np.int32)
+    for L in (0, 1, 17, 40, 64, 1000):
+        kept = sel[sel < L]
+        a = oracle.attend_row(q, k, v, ks, vs, pt, sel, 0.5, lib=lib, limit=L)
+        b = oracle.attend_row(q, k, v, ks, vs, pt, kept, 0.5, lib=lib)
+        assert np.array_equal(a, b), L
+        m, l, o = oracle.chunk_partial(q, k, v, ks, vs, pt, sel, 0, 30, 0.5, lib=lib, limit=L)
+        m2, l2, o2 = oracle.chunk_partial(q, k, v, ks, vs, pt, kept, 0, len(kept), 0.5, lib=lib)
+        assert (m, l) == (m2, l2) and np.array_equal(o, o2), L
+
+
+def pin_limits_in_whole_call(lib):
+    """The whole-call driver applies limits[b][t] to query t of sequence b."""
+    import qsa_workloads as wl
+    p = wl.make_problem(n_seq=2, n_kv_heads=2, q_per_kv=3, n_queries=3, head_dim=16,
+                        pool_cells=256, n_selected=[40, 25], chunk_cells=8, seed=1600)
+    p.q_limit = np.array([[60, 120, 200], [30, 31, 256]], np.int32)
+    out = oracle.decode_attn(p, lib=lib)
+    q = oracle.widen_queries(p.q, p.q_dtype)
+    for b in range(2):
+        for t in range(3):
+            for h in range(6):
+                g = h // 3
+                ref = oracle.attend_row(q[b, t, h], p.k_pool[b, g], p.v_pool[b, g], p.k_scale[b, g],
+                                        p.v_scale[b, g], p.page_table[b], p.sel_of(b), p.softmax_scale,
+                                        lib=lib, limit=int(p.q_limit[b, t]))
+                assert np.array_equal(out[b, t, h], ref), (b, t, h)
 
 
 def pin_single_cell_is_its_v(lib):
@@ -437,6 +482,9 @@ PINS = [
     pin_golden_paged_mean,
     pin_page_relabelling,
     pin_one_page_is_the_pool,
+    pin_golden_causal_window,
+    pin_limit_equals_removal,
+    pin_limits_in_whole_call,
     pin_single_cell_is_its_v,
     pin_equal_scores_give_mean,
     pin_two_cells_sigmoid,

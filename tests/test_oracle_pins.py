@@ -40,8 +40,8 @@ MUTANTS = [
      "double w = exp(s[i]);\n            L += w;"),
     ("position_not_slot", "cell_score(D, q, k_codes + (size_t)slot * D",
      "cell_score(D, q, k_codes + (size_t)(sel[start + i] % pool_cells) * D"),
-    ("k_from_v_pool", "int err = score_range(D, pool_cells, page_table_len, page_cells, q, k_codes, k_scale,\n                          page_table, sel, 0, n_sel",
-     "int err = score_range(D, pool_cells, page_table_len, page_cells, q, v_codes, k_scale,\n                          page_table, sel, 0, n_sel"),
+    ("k_from_v_pool", "int err = score_range(D, pool_cells, page_table_len, page_cells, limit, q, k_codes,\n                          k_scale, page_table, sel, 0, n_sel",
+     "int err = score_range(D, pool_cells, page_table_len, page_cells, limit, q, v_codes,\n                          k_scale, page_table, sel, 0, n_sel"),
     ("masked_as_slot0", "if (s == -1) { *slot = -1; return ORACLE_OK; }",
      "if (s == -1) { *slot = 0; return ORACLE_OK; }"),
     ("chunk_ignores_start", "sel[start + i], &slot", "sel[i], &slot"),
@@ -50,6 +50,10 @@ MUTANTS = [
     ("page_entry_as_cell", "*slot = s * page_cells + pos % page_cells;", "*slot = s + pos % page_cells;"),
     ("page_index_is_position", "int32_t s = page_table[pos / page_cells];",
      "int32_t s = page_table[pos % page_table_len];"),
+    ("limit_ignored", "if (sel[start + i] >= limit) slot = -1;", ""),
+    ("limit_off_by_one", "if (sel[start + i] >= limit) slot = -1;", "if (sel[start + i] > limit) slot = -1;"),
+    ("limit_of_first_query", "limits ? limits[(size_t)b * T + t] : INT32_MAX",
+     "limits ? limits[(size_t)b * T] : INT32_MAX"),
     ("kv_head_by_modulo", "int g = h / H;", "int g = h % G;"),
     ("normaliser_dropped", "for (int d = 0; d < D; ++d) out[d] /= L;\n    }\n    free(slots);",
      "\n    }\n    free(slots);"),
