@@ -90,6 +90,7 @@ typedef enum qsa_algo {
 #define QSA_STATUS_BAD_OFFSETS 0x4u  /* batch offsets decreasing or a list above max_selected */
 #define QSA_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait ran out: outputs invalid */
 #define QSA_STATUS_NOT_RESIDENT 0x10u /* qsa_kv_append: a position whose page entry is -1 */
+#define QSA_STATUS_BAD_LIMITS 0x20u  /* causal limits that decrease along a window */
 
 typedef struct qsa_shape {
     int32_t n_kv_heads;     /* G: KV heads per sequence (>= 1) */
@@ -171,6 +172,28 @@ qsa_status qsa_decode_attn_batch(const qsa_shape *shape, int32_t n_seq, const vo
                                  const int32_t *sel_offsets, int32_t max_selected, float *out,
                                  void *workspace, size_t workspace_bytes, uint32_t *status,
                                  void *stream);
+
+/*
+ * qsa_decode_attn_batch with a causal limit per query of the window: query t
+ * of sequence b sees only the selected cells whose logical position is below
+ * q_limit[b][t]; a cell beyond it is left out of that query's softmax, as a
+ * masked cell is.  The pages leave a causal order inside a verify window open;
+ * this is the library's reading (the window's queries are consecutive tokens,
+ * each seeing the positions before its own).
+ *   q_limit    [n_seq][T] int32, device, non-decreasing in t within each
+ *              sequence (a decreasing pair raises QSA_STATUS_BAD_LIMITS and
+ *              leaves that sequence's outputs unspecified).
+ * Other arguments and the workspace are those of qsa_decode_attn_batch.
+ * Windows of more than 80 query rows run on the CUDA-core kernel
+ * (QSA_ALGO_TCGEN05 then returns QSA_ERR_UNSUPPORTED).
+ */
+qsa_status qsa_decode_attn_batch_limited(const qsa_shape *shape, int32_t n_seq, const void *q,
+                                         const int8_t *k_pool, const int8_t *v_pool,
+                                         const float *k_scale, const float *v_scale,
+                                         const int32_t *page_table, const int32_t *sel,
+                                         const int32_t *sel_offsets, int32_t max_selected,
+                                         const int32_t *q_limit, float *out, void *workspace,
+                                         size_t workspace_bytes, uint32_t *status, void *stream);
 
 /*
  * Where the chunk partials of the last call with this (shape, n_seq,

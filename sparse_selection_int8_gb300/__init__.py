@@ -34,6 +34,7 @@ QSA_STATUS_BAD_SLOT = 0x2
 QSA_STATUS_BAD_OFFSETS = 0x4
 QSA_STATUS_TIMEOUT = 0x8
 QSA_STATUS_NOT_RESIDENT = 0x10
+QSA_STATUS_BAD_LIMITS = 0x20
 
 HEAD_DIM = 256
 
@@ -86,6 +87,9 @@ _SIG = {
     "qsa_status_string": ([ctypes.c_int32], ctypes.c_char_p),
     "qsa_decode_attn_step_noalloc": ([ctypes.POINTER(qsa_shape), _VP, _VP, _VP, _VP, _VP, _VP,
                                       _VP, ctypes.c_int32, _VP, _VP, _VP], ctypes.c_int32),
+    "qsa_decode_attn_batch_limited": ([ctypes.POINTER(qsa_shape), ctypes.c_int32, _VP, _VP, _VP,
+                                       _VP, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
+                                       ctypes.c_size_t, _VP, _VP], ctypes.c_int32),
     "qsa_kv_append": ([ctypes.POINTER(qsa_shape), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                        _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int32),
 }
@@ -170,6 +174,17 @@ def qsa_decode_attn_batch(shape: qsa_shape, n_seq: int, q, k_pool, v_pool, k_sca
         _ptr(v_scale), _ptr(page_table), _ptr(sel), _ptr(sel_offsets), int(max_selected),
         _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
         "qsa_decode_attn_batch")
+
+
+def qsa_decode_attn_batch_limited(shape: qsa_shape, n_seq: int, q, k_pool, v_pool, k_scale,
+                                  v_scale, page_table, sel, sel_offsets, max_selected: int,
+                                  q_limit, out, workspace, workspace_bytes: int, status=None,
+                                  stream=None) -> None:
+    _check(load_library().qsa_decode_attn_batch_limited(
+        ctypes.byref(shape), int(n_seq), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+        _ptr(v_scale), _ptr(page_table), _ptr(sel), _ptr(sel_offsets), int(max_selected),
+        _ptr(q_limit), _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(status),
+        _stream(stream)), "qsa_decode_attn_batch_limited")
 
 
 def qsa_decode_attn_step_noalloc(shape: qsa_shape, q, k_pool, v_pool, k_scale, v_scale,

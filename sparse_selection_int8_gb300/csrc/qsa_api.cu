@@ -97,7 +97,8 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
                const int8_t *v_pool, const float *k_scale, const float *v_scale,
                const int32_t *page_table, const int32_t *sel, const int32_t *sel_offsets,
                int n_sel_single, int max_selected, float *out, void *workspace,
-               size_t workspace_bytes, uint32_t *status, void *stream)
+               size_t workspace_bytes, uint32_t *status, void *stream,
+               const int32_t *q_limit = nullptr)
 {
     qsa_status st = check_shape(s);
     if (st != QSA_OK) return st;
@@ -107,7 +108,8 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     if (max_selected > 0 && !sel) return QSA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
         !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(page_table, 4) ||
-        (sel && !aligned(sel, 4)) || (status && !aligned(status, 4)))
+        (sel && !aligned(sel, 4)) || (status && !aligned(status, 4)) ||
+        (q_limit && !aligned(q_limit, 4)))
         return QSA_ERR_INVALID_ARG;
     if ((const void *)out == q || (const void *)out == (const void *)k_pool ||
         (const void *)out == (const void *)v_pool)
@@ -126,6 +128,7 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.page_table = page_table;
     p.sel = sel;
     p.sel_offsets = sel_offsets;
+    p.q_limit = q_limit;
     p.out = out;
     char *ws = static_cast<char *>(workspace);
     p.part_m = reinterpret_cast<float *>(ws + w.off_m);
@@ -150,7 +153,10 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.scale_log2 = s->softmax_scale * kLog2e;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const Path path = select_path(s);
+    Path path = select_path(s);
+    // the rows-on-M kernel has no per-query limits: wide limited windows run
+    // on the CUDA-core kernel (the workspace it needs is no larger)
+    if (q_limit && path == kPathPromptTc) path = s->algo == QSA_ALGO_TCGEN05 ? kPathNone : kPathSimt;
     if (path == kPathNone) return QSA_ERR_UNSUPPORTED;
     cudaError_t e;
     if (path == kPathDecodeTc)
@@ -203,6 +209,20 @@ qsa_status qsa_decode_attn_batch(const qsa_shape *shape, int32_t n_seq, const vo
     return qsa::run(shape, n_seq, q, k_pool, v_pool, k_scale, v_scale, page_table, sel,
                     sel_offsets, 0, max_selected, out, workspace, workspace_bytes, status,
                     stream);
+}
+
+qsa_status qsa_decode_attn_batch_limited(const qsa_shape *shape, int32_t n_seq, const void *q,
+                                         const int8_t *k_pool, const int8_t *v_pool,
+                                         const float *k_scale, const float *v_scale,
+                                         const int32_t *page_table, const int32_t *sel,
+                                         const int32_t *sel_offsets, int32_t max_selected,
+                                         const int32_t *q_limit, float *out, void *workspace,
+                                         size_t workspace_bytes, uint32_t *status, void *stream)
+{
+    if (!sel_offsets || !qsa::aligned(sel_offsets, 4) || !q_limit) return QSA_ERR_INVALID_ARG;
+    return qsa::run(shape, n_seq, q, k_pool, v_pool, k_scale, v_scale, page_table, sel,
+                    sel_offsets, 0, max_selected, out, workspace, workspace_bytes, status,
+                    stream, q_limit);
 }
 
 qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_selected,

@@ -34,6 +34,7 @@ qsa_chunk_simt_kernel(const Params p, int n_row_blocks)
     __shared__ __align__(16) int8_t s_k[kStage][kHeadDim];
     __shared__ __align__(16) int8_t s_v[kStage][kHeadDim];
     __shared__ int s_slot[kStage];
+    __shared__ int s_pos[kStage];
     __shared__ float s_ks[kStage];
     __shared__ float s_vs[kStage];
 
@@ -54,11 +55,13 @@ qsa_chunk_simt_kernel(const Params p, int n_row_blocks)
 
     float qv[RPW][8];
     bool rvalid[RPW];
+    int rlim[RPW]; // causal limit of the row's query (positions below it are seen)
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
         const int r = rb * kSimtWarps * RPW + warp + kSimtWarps * i;
         rvalid[i] = r < p.R;
         const int t = rvalid[i] ? r / p.H : 0, j = rvalid[i] ? r % p.H : 0;
+        rlim[i] = p.q_limit ? __ldg(p.q_limit + (size_t)b * p.T + t) : INT_MAX;
         const size_t qoff = (((size_t)b * p.T + t) * GH + (size_t)g * p.H + j) * kHeadDim + lane * 8;
         if (!rvalid[i]) {
 #pragma unroll
@@ -93,9 +96,13 @@ qsa_chunk_simt_kernel(const Params p, int n_row_blocks)
         __syncthreads(); // previous stage fully consumed
         if (threadIdx.x < kStage) {
             const int i = threadIdx.x;
-            int slot = -1;
-            if (i < nt) slot = resolve_slot(p, b, __ldg(p.sel + start + tile + i));
+            int slot = -1, pos = 0;
+            if (i < nt) {
+                pos = __ldg(p.sel + start + tile + i);
+                slot = resolve_slot(p, b, pos);
+            }
             s_slot[i] = slot;
+            s_pos[i] = pos;
             s_ks[i] = slot >= 0 ? __ldg(p.k_scale + kv_base + slot) : 0.f;
             s_vs[i] = slot >= 0 ? __ldg(p.v_scale + kv_base + slot) : 0.f;
         }
@@ -125,7 +132,7 @@ qsa_chunk_simt_kernel(const Params p, int n_row_blocks)
             for (int e = 0; e < 8; ++e) vf[e] *= vsc;
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
-                if (!rvalid[i]) continue;
+                if (!rvalid[i] || s_pos[c] >= rlim[i]) continue; // uniform across the warp
                 float dot = 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) dot = fmaf(qv[i][e], kf[e], dot);

@@ -83,9 +83,11 @@ struct Misc {
     int32_t rs_sel[4][kTile]; // list entries
     int32_t rs_pg[4][kTile];  // page-table entries (-1 masked, kBadPos out of range)
     int32_t rs_off[4][kTile]; // offset of the position in its page (pages of P > 1 cells)
+    int32_t rs_r0[4][kTile];  // causal limits: the first query row that sees the cell
     float rs_ks[4][kTile];    // k_scale, v_scale of the cell's slot (0 if masked)
     float rs_vs[4][kTile];
     uint8_t sc_ok[2][kTile];  // cell holds a valid slot
+    int32_t sc_r0[2][kTile];  // causal limits: first query row that sees the cell
     // [tile parity][warp quadrant][row; kMaxRows = |v_scale| max]
     __align__(16) float red_max[2][4][kMaxRows + 4];
     __align__(16) float red_sum[2][4][kMaxRows];
@@ -452,8 +454,10 @@ __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
 // ---------------------------------------------------------------- kernel
 
 // N: MMA columns (rows padded to 16); KR: 8-row score blocks that hold real
-// rows (KR * 8 >= R), the softmax skips the rest.
-template <int N, int KR>
+// rows (KR * 8 >= R), the softmax skips the rest; LIM: the call carries
+// causal limits per query (a separate instantiation, so calls without them
+// run exactly the code they ran before limits existed).
+template <int N, int KR, bool LIM>
 __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params p)
 {
     using L = Lay<N>;
@@ -599,6 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     if (j >= 2) wait(&ms.sc_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
                     ms.sc_ok[jb][cA] = slA0 >= 0;
                     ms.sc_ok[jb][cB] = slB0 >= 0;
+                    if (LIM) { // written by this thread at tile j's page stage
+                        ms.sc_r0[jb][cA] = ms.rs_r0[j & 3][cA];
+                        ms.sc_r0[jb][cB] = ms.rs_r0[j & 3][cB];
+                    }
                     mbar_arrive(&ms.sc_full[jb]);
                 }
                 if (j >= 2) wait(&ms.v_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
@@ -668,6 +676,15 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     } else {
                         // position pos: page pos / P, offset pos % P (P = 1: the entry is the slot)
                         const int pos = ms.rs_sel[e4][cx], P = p.page_cells;
+                        if (LIM && pos >= 0) {
+                            // rows t*H.. of the queries whose limit is above pos see the
+                            // cell: with limits non-decreasing in t, those are the rows
+                            // from H * #{t : limit[t] <= pos} on
+                            const int32_t *lim = p.q_limit + (size_t)(bg4 / p.G) * p.T;
+                            int below = 0;
+                            for (int t = 0; t < p.T; ++t) below += __ldg(lim + t) <= pos;
+                            ms.rs_r0[e4][cx] = below * p.H;
+                        }
                         if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
                             *dst = kBadPos;
                         } else if (P == 1) {
@@ -804,12 +821,14 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             // per cell: K scale (x softmax scale x log2 e), V scale (0 when the
             // cell is masked), and a bias of -inf that masks the cell's scores
             float ksc[4], vsc[4], kbias[4];
+            int r0[4]; // causal limits: the cell's first visible query row
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int cc = 32 * q + 8 * ci + ra;
                 kbias[ci] = ms.sc_ok[par][cc] != 0 ? 0.f : -INFINITY;
                 ksc[ci] = ms.rs_ks[i & 3][cc] * p.scale_log2;
                 vsc[ci] = ms.rs_vs[i & 3][cc];
+                r0[ci] = LIM ? ms.sc_r0[par][cc] : 0;
             }
             mbar_arrive(&ms.sc_empty[par]);
             wait(&ms.s_full[par], (uint32_t)(i >> 1) & 1u);
@@ -836,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                             const int ci = 2 * L + B;
                             float &xv = x[L][4 * k + 2 * B + e];
                             xv = __fmaf_rn(xv, ksc[ci], kbias[ci]); // = the rounded product, or -inf
+                            if (LIM && 8 * k + 2 * u + e < r0[ci]) xv = -INFINITY; // beyond its query's limit
                             m = fmaxf(m, xv);
                         }
                     }
@@ -1117,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     if (w == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int N, int KR>
+template <int N, int KR, bool LIM = false>
 cudaError_t launch_n(const Params &p, cudaStream_t stream)
 {
     int dev = 0, sms = 0, max_smem = 0;
@@ -1129,7 +1149,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     static_assert(Lay<N>::total + 1024 <= 232448, "shared memory of the chunk kernel");
     const uint32_t bytes = Lay<N>::total + 1024;
     if ((int)bytes > max_smem) return cudaErrorInvalidConfiguration;
-    if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N, KR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N, KR, LIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)bytes)) != cudaSuccess)
         return e;
     const long long pieces = (long long)p.n_seq * p.G * N * 32;
@@ -1153,7 +1173,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qsa_chunk_tc_kernel<N, KR>, p);
+    return cudaLaunchKernelEx(&cfg, qsa_chunk_tc_kernel<N, KR, LIM>, p);
 }
 
 } // namespace
@@ -1173,6 +1193,16 @@ cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
     // converts it itself, so the call is two kernels (chunk, merge)
     Params p = p_in;
     p.q_inline = p.n_seq * p.G == 1 ? 1 : 0;
+    if (p.q_limit) { // causal limits: one instantiation per N (padding rows cost a little)
+        switch ((p.R + 15) / 16) {
+        case 1: return launch_n<16, 2, true>(p, stream);
+        case 2: return launch_n<32, 4, true>(p, stream);
+        case 3: return launch_n<48, 6, true>(p, stream);
+        case 4: return launch_n<64, 8, true>(p, stream);
+        case 5: return launch_n<80, 10, true>(p, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch ((p.R + 7) / 8) { // 8-row blocks of real rows; N = that, padded to 16
     case 1: return launch_n<16, 1>(p, stream);
     case 2: return launch_n<16, 2>(p, stream);

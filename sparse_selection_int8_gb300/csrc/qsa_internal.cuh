@@ -33,6 +33,7 @@ struct Params {
     const int32_t *page_table; // [n_seq][N_log]
     const int32_t *sel;        // concatenated lists
     const int32_t *sel_offsets; // [n_seq+1] or nullptr (single sequence)
+    const int32_t *q_limit;    // [n_seq][T] causal limits or nullptr: query t sees positions < limit
     float *out;                // [n_seq][T][G*H][D]
     float *part_m;             // [n_seq][G][n_chunks][R]
     float *part_l;

@@ -41,6 +41,12 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
     // that grid has finished and its partials are visible
     cudaGridDependencySynchronize();
     if (r >= p.R) return;
+    if (p.q_limit && g == 0 && threadIdx.x % (32 * (WPR == 1 ? 1 : WPR)) == 0 && r % p.H == 0) {
+        // causal limits must not decrease along the window
+        const int t = r / p.H;
+        if (t + 1 < p.T && __ldg(p.q_limit + (size_t)b * p.T + t) > __ldg(p.q_limit + (size_t)b * p.T + t + 1))
+            raise_status(p, QSA_STATUS_BAD_LIMITS);
+    }
     const size_t base = ((size_t)b * p.G + g) * p.n_chunks * p.R + r;
     const size_t stride = (size_t)p.R; // chunk stride of m and l
     // a round: kRound chunks per warp, every load issued together (the list

@@ -11,7 +11,8 @@ from typing import Optional
 import numpy as np
 
 from . import (QSA_ALGO_AUTO, QSA_BF16, QSA_F32, make_shape, qsa_decode_attn_batch,
-               qsa_decode_attn_step, qsa_kv_append, qsa_partials_view, qsa_workspace_bytes)
+               qsa_decode_attn_batch_limited, qsa_decode_attn_step, qsa_kv_append,
+               qsa_partials_view, qsa_workspace_bytes)
 
 
 def _to_dev(torch, a: np.ndarray, device, pin: bool = False):
@@ -44,6 +45,8 @@ class DeviceProblem:
         self.page_table = _to_dev(torch, p.page_table, device)
         self.sel = _to_dev(torch, p.sel if p.sel.size else np.zeros(1, np.int32), device)
         self.sel_offsets = _to_dev(torch, p.sel_offsets, device)
+        lim = getattr(p, "q_limit", None)
+        self.q_limit = None if lim is None else _to_dev(torch, np.asarray(lim, np.int32), device)
         self.n_seq = p.n_seq
         self.max_selected = p.max_selected if max_selected is None else max_selected
         self.shape = make_shape(n_kv_heads=p.n_kv_heads, q_per_kv=p.q_per_kv,
@@ -63,6 +66,12 @@ class DeviceProblem:
         """One call.  ``batch=None`` uses the step entry for one sequence and
         the batch entry otherwise."""
         out = self.out if out is None else out
+        if self.q_limit is not None:  # causal limits: the batch entry that takes them
+            qsa_decode_attn_batch_limited(self.shape, self.n_seq, self.q, self.k_pool, self.v_pool,
+                                          self.k_scale, self.v_scale, self.page_table, self.sel,
+                                          self.sel_offsets, self.max_selected, self.q_limit, out,
+                                          self.workspace, self.ws_bytes, self.status, stream)
+            return out
         if batch is None:
             batch = self.n_seq != 1
         if batch:

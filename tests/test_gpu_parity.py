@@ -291,6 +291,69 @@ def copy_problem_masking(p):
     return q
 
 
+def window_limits(p, rng, step=1):
+    """Causal limits of a verify window per sequence: query t sees positions
+    below base + step * t, with base around the middle of the sequence's
+    selected positions (so some selected cells lie beyond every limit)."""
+    lim = np.zeros((p.n_seq, p.n_queries), np.int32)
+    for b in range(p.n_seq):
+        s = np.sort(p.sel_of(b))
+        base = int(s[len(s) // 2]) if len(s) else 0
+        lim[b] = base + step * np.arange(p.n_queries) + int(rng.integers(0, 3))
+    return lim
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("T,H,G", [(1, 12, 1), (4, 12, 1), (6, 12, 2), (3, 5, 3)])
+def test_causal_limits(algo, T, H, G):
+    """Per-query causal limits inside the window, on ragged batches (chunks of
+    one and two tiles) and with the limits spread far apart (step 97) or
+    consecutive (step 1): against the oracle."""
+    rng = np.random.default_rng(9800 + 10 * T + H + G)
+    for C, step in ((128, 1), (256, 97)):
+        p = wl.make_problem(n_seq=3, n_kv_heads=G, q_per_kv=H, n_queries=T, pool_cells=4096,
+                            n_selected=[600, 1300, 37], chunk_cells=C, mask_fraction=0.05,
+                            seed=int(rng.integers(1 << 30)))
+        p.q_limit = window_limits(p, rng, step)
+        dp, out = run(p, algo)
+        assert_parity(out, oracle.decode_attn(p), f"limits T={T} H={H} G={G} C={C}")
+        assert int(dp.status.item()) == 0
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_limits_beyond_every_position_change_nothing(algo):
+    """Limits at or above every position: bit for bit the unlimited call."""
+    p = wl.make_problem(n_seq=2, n_kv_heads=2, n_queries=4, pool_cells=4096,
+                        n_selected=[900, 2051], chunk_cells=128, seed=9900)
+    _, ref = run(p, algo)
+    p.q_limit = np.full((2, 4), p.n_positions, np.int32)
+    _, out = run(p, algo)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
+def test_limits_on_a_wide_window():
+    """More than 80 query rows with limits: the CUDA-core kernel (the
+    rows-on-M kernel takes no limits), a causal prefill over 64 queries."""
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_queries=64, pool_cells=2048, n_selected=2048, chunk_cells=1024,
+                        q_dtype="bf16", selection="full", seed=9950)
+    p.q_limit = (1984 + np.arange(64, dtype=np.int32))[None, :]
+    dp, out = run(p, "auto")
+    assert_parity(out, oracle.decode_attn(p), "limits on a wide window")
+    dp2 = qsa.DeviceProblem(p, algo=qsa.QSA_ALGO_TCGEN05)
+    with pytest.raises(qsa.QsaError):
+        dp2.run()
+
+
+def test_decreasing_limits_are_reported():
+    import sparse_selection_int8_gb300 as qsa
+    p = wl.make_problem(n_seq=2, n_queries=3, pool_cells=1024, n_selected=200, chunk_cells=64,
+                        seed=9960)
+    p.q_limit = np.array([[100, 200, 300], [500, 400, 600]], np.int32)
+    dp, _ = run(p, "auto")
+    assert int(dp.status.item()) == qsa.QSA_STATUS_BAD_LIMITS
+
+
 @pytest.mark.parametrize("algo", ["auto", "simt"])
 def test_batch_list_above_bound_is_clamped(algo):
     import sparse_selection_int8_gb300 as qsa
