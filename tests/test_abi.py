@@ -195,6 +195,16 @@ def test_append_checks_shape_and_skips_empty_calls(lib):
     assert call_append(lib, shape(), append_args(n_seq=0)) == qsa.QSA_OK
 
 
+def test_limited_batch_rejects_before_launch(lib):
+    s = shape()
+    base = [ctypes.byref(s), 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 100]
+    tail = [FAKE + 4096, FAKE, 1 << 30, None, None]
+    assert lib.qsa_decode_attn_batch_limited(*base, None, *tail) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_decode_attn_batch_limited(*base, FAKE + 2, *tail) == qsa.QSA_ERR_INVALID_ARG
+    base_no_offsets = base[:9] + [None, 100]
+    assert lib.qsa_decode_attn_batch_limited(*base_no_offsets, FAKE, *tail) == qsa.QSA_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4):
         assert qsa.qsa_status_string(code)
