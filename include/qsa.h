@@ -184,8 +184,8 @@ qsa_status qsa_decode_attn_batch(const qsa_shape *shape, int32_t n_seq, const vo
  *              sequence (a decreasing pair raises QSA_STATUS_BAD_LIMITS and
  *              leaves that sequence's outputs unspecified).
  * Other arguments and the workspace are those of qsa_decode_attn_batch.
- * Windows of more than 80 query rows run on the CUDA-core kernel
- * (QSA_ALGO_TCGEN05 then returns QSA_ERR_UNSUPPORTED).
+ * Every kernel family takes limits (a causal prefill is a wide window whose
+ * limits are its own positions plus one).
  */
 qsa_status qsa_decode_attn_batch_limited(const qsa_shape *shape, int32_t n_seq, const void *q,
                                          const int8_t *k_pool, const int8_t *v_pool,

@@ -66,7 +66,7 @@ Workspace carve(const qsa_shape *s, int n_seq, int max_selected)
     if (select_path(s) == kPathPromptTc && n_chunks > 0) {
         size_t kb, qb, cb;
         prompt_image_bytes(n_seq, s->n_kv_heads, (int)R, s->chunk_cells, (int)n_chunks, &kb, &qb, &cb);
-        w.total = w.off_extra + 2 * align_up(kb, 1024) + align_up(qb, 1024) + 2 * align_up(cb, 1024);
+        w.total = w.off_extra + 2 * align_up(kb, 1024) + align_up(qb, 1024) + 3 * align_up(cb, 1024);
     }
     return w;
 }
@@ -88,6 +88,8 @@ PromptImages prompt_images(const qsa_shape *s, int n_seq, int max_selected, char
     im.ksc = reinterpret_cast<float *>(ws + off);
     off += align_up(cb, 1024);
     im.bias = reinterpret_cast<float *>(ws + off);
+    off += align_up(cb, 1024);
+    im.pos = reinterpret_cast<int32_t *>(ws + off);
     im.tiles_per_chunk = (s->chunk_cells + 127) / 128;
     im.row_tiles = (R + 127) / 128;
     return im;
@@ -153,10 +155,7 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.scale_log2 = s->softmax_scale * kLog2e;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    Path path = select_path(s);
-    // the rows-on-M kernel has no per-query limits: wide limited windows run
-    // on the CUDA-core kernel (the workspace it needs is no larger)
-    if (q_limit && path == kPathPromptTc) path = s->algo == QSA_ALGO_TCGEN05 ? kPathNone : kPathSimt;
+    const Path path = select_path(s);
     if (path == kPathNone) return QSA_ERR_UNSUPPORTED;
     cudaError_t e;
     if (path == kPathDecodeTc)

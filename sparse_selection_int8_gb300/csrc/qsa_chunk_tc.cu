@@ -1178,8 +1178,6 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
 
 } // namespace
 
-bool chunk_tc_supports(const Params &p) { return p.R <= kDecodeTcMaxRows; }
-
 size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
 {
     const size_t N = (size_t)(R + 15) / 16 * 16;

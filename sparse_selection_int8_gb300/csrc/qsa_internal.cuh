@@ -58,6 +58,7 @@ struct PromptImages {
     void *q;     // [n_seq][G][row_tiles] 64 KB tiles: queries (bf16|f16)
     float *ksc;  // [..][tiles_per_chunk][128]: k_scale * softmax_scale * log2(e), 0 if masked
     float *bias; // same: 0, or -inf for a masked cell
+    int32_t *pos; // same: the cell's logical position (for causal limits)
     int tiles_per_chunk;
     int row_tiles;
 };
@@ -144,10 +145,8 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
 
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_chunk_simt(const Params &p, cudaStream_t stream);
-bool chunk_tc_supports(const Params &p);
 size_t chunk_tc_query_image_bytes(int n_seq, int G, int R);
 cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream);
-bool prompt_tc_supports(const Params &p);
 size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks, size_t *k_bytes,
                           size_t *q_bytes, size_t *cell_bytes);
 cudaError_t launch_prompt_tc(const Params &p, const PromptImages &im, cudaStream_t stream);

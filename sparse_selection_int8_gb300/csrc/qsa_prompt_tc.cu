@@ -82,8 +82,12 @@ __global__ void __launch_bounds__(256) qsa_prompt_stage_kv(const Params p, const
     const long long hi = min(min(c0 + p.chunk_cells, (long long)n), lo + kTile);
     const int tid = threadIdx.x;
     if (tid < kTile) {
-        int slot = -1;
-        if (lo + tid < hi) slot = resolve_slot(p, b, __ldg(p.sel + start + lo + tid));
+        int slot = -1, pos = INT_MAX;
+        if (lo + tid < hi) {
+            pos = __ldg(p.sel + start + lo + tid);
+            slot = resolve_slot(p, b, pos);
+        }
+        im.pos[tile_id * kTile + tid] = pos;
         s_slot[tid] = slot;
         s_vs[tid] = slot >= 0 ? __ldg(p.v_scale + kv_base + slot) : 0.f;
         im.ksc[tile_id * kTile + tid] = slot >= 0 ? __ldg(p.k_scale + kv_base + slot) * p.scale_log2 : 0.f;
@@ -171,6 +175,7 @@ constexpr uint32_t kBarSoft = 1;              // named barrier of the softmax wa
 struct PromptSmem {
     float ksc[kTile];           // per-cell score factors of the current tile
     float bias[kTile];          // 0 or -inf (masked cell)
+    int32_t pos[kTile];         // the cells' logical positions (calls with causal limits)
     float rowmax[2][kTile];     // [column half][row]; the rows' sums at the end
     uint64_t bar_q, k_full, k_empty, v_full, o_done, p_full, c_full;
     uint64_t s_full[2], s_empty[2];
@@ -202,7 +207,7 @@ __device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64
 // as soon as S of tile j is done (during P.V of tile j-1), V of tile j+1 as
 // soon as P.V of tile j is done (during S of tile j+2), the score factors
 // once the softmax has read the previous ones.
-template <bool QBF16>
+template <bool QBF16, bool LIM>
 __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params p, const PromptImages im)
 {
     // The operand tiles need 1024-byte alignment (128-byte swizzle atoms);
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     const uint8_t *vimg = static_cast<const uint8_t *>(im.v) + tile0 * kTileBytes;
     const uint8_t *qimg = static_cast<const uint8_t *>(im.q) + (((size_t)b * p.G + g) * im.row_tiles + mt) * kTileBytes;
     const float *kscg = im.ksc + tile0 * kTile, *biasg = im.bias + tile0 * kTile;
+    const int32_t *posg = im.pos + tile0 * kTile;
 
     if (tid == 0) {
         mbar_init(&ms.bar_q, 1);
@@ -265,9 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 bulk_g2s(smem + kTileBytes, kimg + (size_t)j * kTileBytes, kTileBytes, &ms.k_full);
             };
             auto load_c = [&](int j) {
-                mbar_arrive_expect_tx(&ms.c_full, 2 * kTile * 4);
+                mbar_arrive_expect_tx(&ms.c_full, (LIM ? 3 : 2) * kTile * 4);
                 bulk_g2s(ms.ksc, kscg + (size_t)j * kTile, kTile * 4, &ms.c_full);
                 bulk_g2s(ms.bias, biasg + (size_t)j * kTile, kTile * 4, &ms.c_full);
+                if (LIM) bulk_g2s(ms.pos, posg + (size_t)j * kTile, kTile * 4, &ms.c_full);
             };
             mbar_arrive_expect_tx(&ms.bar_q, kTileBytes);
             bulk_g2s(smem, qimg, kTileBytes, &ms.bar_q);
@@ -354,6 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
         const int row = 32 * (w & 3) + lane, hc = w >> 2;
         const uint32_t t_lane = (uint32_t)(32 * (w & 3)) << 16;
         float m_run = -INFINITY, m_ref = -INFINITY, l = 0.f;
+        int lim = INT_MAX; // causal limit of this row's query: it sees positions below it
+        if (LIM && mt * kTile + row < p.R)
+            lim = __ldg(p.q_limit + (size_t)b * p.T + (mt * kTile + row) / p.H);
         for (int j = 0; j < n_tiles; ++j) {
             const int par = j & 1;
             wait_bar(p, ms, &ms.c_full, (uint32_t)j & 1u);
@@ -375,6 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 sv[4 * i4 + 1] = fmaf(sv[4 * i4 + 1], kf.y, bf.y);
                 sv[4 * i4 + 2] = fmaf(sv[4 * i4 + 2], kf.z, bf.z);
                 sv[4 * i4 + 3] = fmaf(sv[4 * i4 + 3], kf.w, bf.w);
+                if (LIM) {
+                    const int4 pf = *reinterpret_cast<const int4 *>(&ms.pos[hc * 64 + 4 * i4]);
+                    if (pf.x >= lim) sv[4 * i4] = -INFINITY;
+                    if (pf.y >= lim) sv[4 * i4 + 1] = -INFINITY;
+                    if (pf.z >= lim) sv[4 * i4 + 2] = -INFINITY;
+                    if (pf.w >= lim) sv[4 * i4 + 3] = -INFINITY;
+                }
                 mx = fmaxf(mx, fmaxf(fmaxf(sv[4 * i4], sv[4 * i4 + 1]), fmaxf(sv[4 * i4 + 2], sv[4 * i4 + 3])));
             }
             tc_fence_before();
@@ -483,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     if (w == 0) tmem_dealloc(tmem, 512);
 }
 
-template <bool QBF16>
+template <bool QBF16, bool LIM>
 cudaError_t launch_prompt(const Params &p, const PromptImages &im, cudaStream_t stream)
 {
     dim3 gkv((unsigned)(p.n_chunks * im.tiles_per_chunk), (unsigned)p.G, (unsigned)p.n_seq);
@@ -494,17 +511,15 @@ cudaError_t launch_prompt(const Params &p, const PromptImages &im, cudaStream_t 
     qsa_prompt_stage_q<QBF16><<<gq, 256, 0, stream>>>(p, im);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int bytes = (int)(3 * kTileBytes + sizeof(PromptSmem));
-    if ((e = cudaFuncSetAttribute(qsa_prompt_tc_kernel<QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(qsa_prompt_tc_kernel<QBF16, LIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   bytes)) != cudaSuccess)
         return e;
     dim3 gm((unsigned)(im.row_tiles * p.n_chunks), (unsigned)p.G, (unsigned)p.n_seq);
-    qsa_prompt_tc_kernel<QBF16><<<gm, kThreads, bytes, stream>>>(p, im);
+    qsa_prompt_tc_kernel<QBF16, LIM><<<gm, kThreads, bytes, stream>>>(p, im);
     return cudaGetLastError();
 }
 
 } // namespace
-
-bool prompt_tc_supports(const Params &p) { return p.R > 64 && p.chunk_cells >= kTile; }
 
 size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks, size_t *k_bytes,
                           size_t *q_bytes, size_t *cell_bytes)
@@ -514,13 +529,15 @@ size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks
     *k_bytes = (size_t)n_seq * G * n_chunks * tpc * kTileBytes;
     *q_bytes = (size_t)n_seq * G * row_tiles * kTileBytes;
     *cell_bytes = (size_t)n_seq * G * n_chunks * tpc * kTile * sizeof(float);
-    return 2 * *k_bytes + *q_bytes + 2 * *cell_bytes;
+    return 2 * *k_bytes + *q_bytes + 3 * *cell_bytes;
 }
 
 cudaError_t launch_prompt_tc(const Params &p, const PromptImages &im, cudaStream_t stream)
 {
     if (p.n_chunks == 0) return cudaSuccess;
-    return p.q_bf16 ? launch_prompt<true>(p, im, stream) : launch_prompt<false>(p, im, stream);
+    if (p.q_limit)
+        return p.q_bf16 ? launch_prompt<true, true>(p, im, stream) : launch_prompt<false, true>(p, im, stream);
+    return p.q_bf16 ? launch_prompt<true, false>(p, im, stream) : launch_prompt<false, false>(p, im, stream);
 }
 
 } // namespace qsa

@@ -331,18 +331,20 @@ def test_limits_beyond_every_position_change_nothing(algo):
     assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
 
 
-def test_limits_on_a_wide_window():
-    """More than 80 query rows with limits: the CUDA-core kernel (the
-    rows-on-M kernel takes no limits), a causal prefill over 64 queries."""
-    import sparse_selection_int8_gb300 as qsa
-    p = wl.make_problem(n_queries=64, pool_cells=2048, n_selected=2048, chunk_cells=1024,
-                        q_dtype="bf16", selection="full", seed=9950)
-    p.q_limit = (1984 + np.arange(64, dtype=np.int32))[None, :]
-    dp, out = run(p, "auto")
-    assert_parity(out, oracle.decode_attn(p), "limits on a wide window")
-    dp2 = qsa.DeviceProblem(p, algo=qsa.QSA_ALGO_TCGEN05)
-    with pytest.raises(qsa.QsaError):
-        dp2.run()
+@pytest.mark.parametrize("algo", ALGOS)
+def test_limits_on_a_wide_window(algo):
+    """More than 80 query rows with limits (the rows-on-M kernel under auto):
+    a causal prefill of 64 queries over 2,048 cells in 128-cell tiles, each
+    query seeing the positions up to its own, and the same window with limits
+    cutting tiles at ragged places."""
+    ref = None
+    for lim0, step in ((1984, 1), (700, 23)):
+        p = wl.make_problem(n_queries=64, pool_cells=2048, n_selected=2048, chunk_cells=1024,
+                            q_dtype="bf16", selection="full", seed=9950)
+        p.q_limit = (lim0 + step * np.arange(64, dtype=np.int32))[None, :]
+        dp, out = run(p, algo)
+        assert_parity(out, oracle.decode_attn(p), f"limits on a wide window {lim0}+{step}t")
+        assert int(dp.status.item()) == 0
 
 
 def test_decreasing_limits_are_reported():
