@@ -496,7 +496,7 @@ def measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush, budget_s
     t_start = time.perf_counter()
     specs = [("tiny_decode", wl.tiny_decode), ("batched_decode", wl.batched_decode),
              ("long_context", wl.long_context), ("long_context_pages16", wl.long_context_paged),
-             ("prompt_shaped", wl.prompt_shaped)]
+             ("prompt_shaped", wl.prompt_shaped), ("prompt_shaped_causal", wl.prompt_causal)]
     for name, make in specs:
         if time.perf_counter() - t_start > budget_s:
             res[name] = {"skipped": "time budget"}
@@ -504,7 +504,7 @@ def measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush, budget_s
         p = make()
         dp = qsa.DeviceProblem(p)
         ab = algorithmic_bytes(p)
-        if name == "prompt_shaped":
+        if name.startswith("prompt_shaped"):
             # about a millisecond per call: one graph per call, L2 flushed first
             g = capture(torch, dp, stream)
             with torch.cuda.stream(stream):
@@ -523,7 +523,7 @@ def measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush, budget_s
         entry = {"us_per_call": round(us, 2), "cells_per_s": cells / (us * 1e-6),
                  "algorithmic_bytes": ab, "hbm_gbs": ab / (us * 1e-6) / 1e9, "timing": how}
         entry["hbm_frac"] = entry["hbm_gbs"] / hbm_peak
-        if name == "prompt_shaped":
+        if name.startswith("prompt_shaped"):
             entry["tflops"] = flops(p) / (us * 1e-6) / 1e12
             entry["tensor_frac_bf16"] = entry["tflops"] / tflops_peak
         res[name] = entry

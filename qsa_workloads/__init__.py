@@ -274,6 +274,17 @@ def prompt_shaped(seed_offset: int = 0, n_queries: int = 2048,
                         seed=SEED_BASE + 5 + seed_offset, name="prompt_shaped")
 
 
+def prompt_causal(seed_offset: int = 0) -> Problem:
+    """The prompt-shaped call as a causal prefill: the 2,048 queries are the
+    tokens at the pool's last 2,048 positions, each seeing the positions up
+    to its own (limit 30,721 + t).  A companion case; the configuration
+    itself has the causal mask off."""
+    p = prompt_shaped(seed_offset)
+    p.q_limit = (p.n_positions - p.n_queries + 1 + np.arange(p.n_queries, dtype=np.int32))[None, :]
+    p.name = "prompt_causal"
+    return p
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "qsa_decode": qsa_decode,
