@@ -83,11 +83,11 @@ struct Misc {
     int32_t rs_sel[4][kTile]; // list entries
     int32_t rs_pg[4][kTile];  // page-table entries (-1 masked, kBadPos out of range)
     int32_t rs_off[4][kTile]; // offset of the position in its page (pages of P > 1 cells)
-    int32_t rs_r0[4][kTile];  // causal limits: the first query row that sees the cell
+    uint8_t rs_r0[4][kTile];  // causal limits: the first query row that sees the cell (<= 80)
     float rs_ks[4][kTile];    // k_scale, v_scale of the cell's slot (0 if masked)
     float rs_vs[4][kTile];
     uint8_t sc_ok[2][kTile];  // cell holds a valid slot
-    int32_t sc_r0[2][kTile];  // causal limits: first query row that sees the cell
+    uint8_t sc_r0[2][kTile];  // causal limits: first query row that sees the cell
     // [tile parity][warp quadrant][row; kMaxRows = |v_scale| max]
     __align__(16) float red_max[2][4][kMaxRows + 4];
     __align__(16) float red_sum[2][4][kMaxRows];
@@ -462,9 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 {
     using L = Lay<N>;
     constexpr int PB = L::PB;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + pad;
+    // The operand tiles need 1024-byte alignment (128-byte swizzle atoms); the
+    // dynamic shared memory of a kernel without static shared memory starts
+    // there, so no padding is reserved (it would cost the 196 KB shared-memory
+    // carve-out at 32 and 64 query columns).  The check keeps a misplaced
+    // window from being used.
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) raise_status(p, QSA_STATUS_TIMEOUT);
+        return;
+    }
     Misc &ms = *reinterpret_cast<Misc *>(smem + L::misc);
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
@@ -683,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                             const int32_t *lim = p.q_limit + (size_t)(bg4 / p.G) * p.T;
                             int below = 0;
                             for (int t = 0; t < p.T; ++t) below += __ldg(lim + t) <= pos;
-                            ms.rs_r0[e4][cx] = below * p.H;
+                            ms.rs_r0[e4][cx] = (uint8_t)(below * p.H); // <= T * H <= 80
                         }
                         if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
                             *dst = kBadPos;
@@ -1146,8 +1153,8 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return e;
-    static_assert(Lay<N>::total + 1024 <= 232448, "shared memory of the chunk kernel");
-    const uint32_t bytes = Lay<N>::total + 1024;
+    static_assert(Lay<N>::total <= 232448, "shared memory of the chunk kernel");
+    const uint32_t bytes = Lay<N>::total;
     if ((int)bytes > max_smem) return cudaErrorInvalidConfiguration;
     if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N, KR, LIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)bytes)) != cudaSuccess)
