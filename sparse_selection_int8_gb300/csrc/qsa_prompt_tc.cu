@@ -10,9 +10,10 @@
 //   staging   one pass resolves every listed cell through the page table
 //             (a1) and writes tensor-core-ready images to the workspace:
 //             K codes as 16-bit floats (exact), V as f16(code x v_scale),
-//             per-cell k_scale*softmax_scale*log2(e) and a 0/-inf mask
-//             bias, and the queries, each 128-row or 128-cell tile a
-//             contiguous 64 KB block in the 128-byte-swizzled layout;
+//             per-cell k_scale*softmax_scale*log2(e), a 0/-inf mask bias and
+//             the cell's logical position (read only by calls with causal
+//             limits per query), and the queries, each 128-row or 128-cell
+//             tile a contiguous 64 KB block in the 128-byte-swizzled layout;
 //   main      one CTA per (128-row query tile, chunk) loads image tiles with
 //             bulk async copies (a copy warp) and runs, per 128-cell tile,
 //               S = Q . K_code^T        (M=128 rows, N=128 cells, K=256)
@@ -26,6 +27,8 @@
 //             stays below 256 and f16 holds it; the partial is brought to
 //             the true running max at the end.
 // The partials have the decode path's layout and go to the same merge.
+// Calls with causal limits run a separate instantiation whose softmax also
+// sets the scores of cells at or past the row's limit to -inf.
 //
 // Queries keep their own 16-bit type (bf16 queries with bf16 K codes; f32
 // queries are rounded to f16 and use f16 K codes), since one tcgen05.mma
