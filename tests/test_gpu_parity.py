@@ -321,6 +321,20 @@ def test_causal_limits(algo, T, H, G):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
+def test_paged_tables_with_causal_limits(algo):
+    """Pages of 16 cells and causal limits in one call (the decode kernel's
+    page stage resolves both from the same position)."""
+    rng = np.random.default_rng(9870)
+    p = wl.make_problem(n_seq=3, n_kv_heads=2, n_queries=4, pool_cells=8192,
+                        n_selected=[900, 2051, 300], chunk_cells=128, mask_fraction=0.1,
+                        page_cells=16, seed=9871)
+    p.q_limit = window_limits(p, rng, 37)
+    dp, out = run(p, algo)
+    assert_parity(out, oracle.decode_attn(p), "paged with limits")
+    assert int(dp.status.item()) == 0
+
+
+@pytest.mark.parametrize("algo", ALGOS)
 def test_limits_beyond_every_position_change_nothing(algo):
     """Limits at or above every position: bit for bit the unlimited call."""
     p = wl.make_problem(n_seq=2, n_kv_heads=2, n_queries=4, pool_cells=4096,
