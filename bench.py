@@ -206,7 +206,7 @@ def source_digest(*names) -> str:
 # DRAM traffic per call of the dominant kernel from an ncu capture, valid
 # only while the kernel source hashes to the recorded digest.
 TRAFFIC = {
-    # qsa_decode T = 1..4, chunk kernel, sum of the four launches (profiles/qsa_chunk_tc_qsa_decode_sweep.md)
+    # qsa_decode T = 1..4, chunk kernel, sum of the four launches (ncu dram__bytes_read + write)
     "91369a909f44003b": 6110720,
 }
 

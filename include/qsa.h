@@ -91,6 +91,7 @@ typedef enum qsa_algo {
 #define QSA_STATUS_TIMEOUT 0x8u      /* a bounded device-side wait ran out: outputs invalid */
 #define QSA_STATUS_NOT_RESIDENT 0x10u /* qsa_kv_append: a position whose page entry is -1 */
 #define QSA_STATUS_BAD_LIMITS 0x20u  /* causal limits that decrease along a window */
+#define QSA_STATUS_LAUNCH 0x40u      /* a kernel's shared-memory window was misplaced: outputs invalid */
 
 typedef struct qsa_shape {
     int32_t n_kv_heads;     /* G: KV heads per sequence (>= 1) */
@@ -221,8 +222,12 @@ qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_
  *   A call whose qsa_workspace_bytes(shape, 1, n_sel) exceeds 8 MiB returns
  *   QSA_ERR_WORKSPACE and launches nothing (e.g. 48 query rows at chunk 128
  *   fit about 21,000 selected cells).
- *   The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
+ *   Each call on a stream that is not being captured looks up the array's
+ *   device address in the current context (no allocation); a call made
+ *   during stream capture reuses the last address found on that device.  So
+ *   make the first call on each device, and the first after a
+ *   cudaDeviceReset or a change of the current context, outside capture (a
+ *   captured first call returns QSA_ERR_CUDA).
  *   All calls share the array: calls whose kernels may overlap on the GPU
  *   (different streams) race and must be ordered by the caller.
  *   It allocates nothing and calls no allocating routine.
@@ -237,8 +242,8 @@ qsa_status qsa_decode_attn_step_noalloc(const qsa_shape *shape, const void *q,
 /*
  * INT8 K/V append: quantise new K and V rows and write them into the pools
  * the attention calls read.  The step is the KV append that follows a QSA
- * layer's K/V projections ("Strata PR #2220, R9-gpu-8: one exact launch for
- * QSA K and V", implementation handoff); the format is the pools' of
+ * layer's K/V projections ("Strata issue #8, round 9: performance candidate
+ * set on v0.2.9", R9-gpu-8, implementation handoff); the format is the pools' of
  * "attn_chunk_q8_v3_kernel" (INT8 codes, one fp32 scale per cell).  The
  * pages print no quantiser; this library's reading, per (cell, KV head) and
  * separately for K and V: scale = max|x| / 127 (fp32, correctly rounded),
@@ -272,6 +277,19 @@ qsa_status qsa_kv_append(const qsa_shape *shape, int32_t n_seq, int32_t n_new, i
                          const void *k_new, const void *v_new, const int32_t *positions,
                          const int32_t *page_table, int8_t *k_pool, int8_t *v_pool,
                          float *k_scale, float *v_scale, uint32_t *status, void *stream);
+
+/*
+ * Testing aid: the bound, in SM clock cycles, of every device-side wait of the
+ * tensor-core kernels in calls launched after this one, process-wide (0
+ * restores the default of 2^32 cycles, about two seconds).  A wait that runs
+ * out sets QSA_STATUS_TIMEOUT, the kernel stops waiting, drains its own
+ * tensor-core operations and copies (each with a bound of its own), frees its
+ * tensor memory and returns; that call's outputs are invalid.  A bound of a
+ * few cycles makes a correct call's waits run out, which is how the time-out
+ * path is tested.  Not for production use: it affects calls from every
+ * thread.
+ */
+void qsa_set_wait_limit(int64_t cycles);
 
 /* Static description of a status code. */
 const char *qsa_status_string(int32_t status);

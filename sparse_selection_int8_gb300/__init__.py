@@ -35,6 +35,7 @@ QSA_STATUS_BAD_OFFSETS = 0x4
 QSA_STATUS_TIMEOUT = 0x8
 QSA_STATUS_NOT_RESIDENT = 0x10
 QSA_STATUS_BAD_LIMITS = 0x20
+QSA_STATUS_LAUNCH = 0x40
 
 HEAD_DIM = 256
 
@@ -92,6 +93,7 @@ _SIG = {
                                        ctypes.c_size_t, _VP, _VP], ctypes.c_int32),
     "qsa_kv_append": ([ctypes.POINTER(qsa_shape), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                        _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int32),
+    "qsa_set_wait_limit": ([ctypes.c_int64], None),
 }
 
 
@@ -143,6 +145,12 @@ def _stream(stream) -> Optional[int]:
 def _check(code: int, where: str):
     if code != QSA_OK:
         raise QsaError(code, where)
+
+
+def qsa_set_wait_limit(cycles: int) -> None:
+    """Testing aid: bound of the kernels' device-side waits in SM clock
+    cycles for later calls (0 restores the default)."""
+    load_library().qsa_set_wait_limit(int(cycles))
 
 
 def qsa_status_string(code: int) -> str:

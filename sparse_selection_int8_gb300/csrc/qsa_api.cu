@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -11,6 +13,10 @@ namespace {
 
 constexpr int kMaxRowsPerKv = 64 * 65536; // q_per_kv <= 64, n_queries <= 65536
 constexpr size_t kWorkspaceAlign = 256;
+constexpr long long kDefaultWaitCycles = 1ll << 32; // about two seconds of SM clock
+
+// Bound of the kernels' device-side waits (qsa_set_wait_limit; 0 = default).
+std::atomic<long long> g_wait_cycles{0};
 
 bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
@@ -153,6 +159,8 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.n_chunks = max_selected > 0 ? (max_selected + s->chunk_cells - 1) / s->chunk_cells : 0;
     p.q_bf16 = s->q_dtype == QSA_BF16;
     p.scale_log2 = s->softmax_scale * kLog2e;
+    const long long wl = g_wait_cycles.load(std::memory_order_relaxed);
+    p.wait_cycles = wl > 0 ? wl : kDefaultWaitCycles;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const Path path = select_path(s);
@@ -239,6 +247,11 @@ qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_
     if (n_chunks)
         *n_chunks = max_selected > 0 ? (max_selected + shape->chunk_cells - 1) / shape->chunk_cells : 0;
     return QSA_OK;
+}
+
+void qsa_set_wait_limit(int64_t cycles)
+{
+    qsa::g_wait_cycles.store(cycles > 0 ? (long long)cycles : 0, std::memory_order_relaxed);
 }
 
 const char *qsa_status_string(int32_t status)

@@ -3,8 +3,8 @@
 // slots the page table gives for the cells' logical positions.
 //
 // The step is the KV append that follows the K/V projections of a QSA layer
-// ("Strata PR #2220, R9-gpu-8: one exact launch for QSA K and V",
-// implementation handoff); what it writes is the format the decode-attention
+// ("Strata issue #8, round 9: performance candidate set on v0.2.9",
+// R9-gpu-8, implementation handoff); what it writes is the format the decode-attention
 // step reads ("attn_chunk_q8_v3_kernel": INT8 K/V pools with per-cell fp32
 // scales).  The pages print no quantiser; the reading here is the plainest
 // symmetric one: scale = max|x| / 127, code = x / scale rounded to nearest,

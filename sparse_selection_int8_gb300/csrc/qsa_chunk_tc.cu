@@ -14,37 +14,48 @@
 //
 // INT8 codes convert exactly to f16 (|code| <= 127).  The K scale (times the
 // softmax scale and log2 e) multiplies the fp32 score after the MMA; the V
-// scale, divided by a per-chunk reference sigma, multiplies the probability
-// before it is rounded to f16 (P' = p * v_scale / sigma), and sigma
-// multiplies the fp32 result.  Queries are rounded to f16.
+// scale, divided by a reference sigma, multiplies the probability before it
+// is rounded to f16 (P' = p * v_scale / sigma), and sigma multiplies the fp32
+// result.  Queries are rounded to f16.
+//
+// Probabilities are formed against a reference maximum per row (mref) that
+// moves only when a score exceeds it by more than 2^8, so P' <= 2^8 * 16 stays
+// far inside f16.  The reference lives from the first cell of a (sequence, KV
+// head) pair that a CTA meets to its last one, across chunks.  Each tile the
+// softmax threads vote, in one barrier-reduction, whether any score or V scale
+// leaves the reference's range; only then (the first tile of a pair, or a
+// score that jumps by 2^8) do they reduce the tile's true row maxima and move
+// the reference, rescaling l and O.  Row sums and row maxima are kept per
+// thread and reduced across the CTA once per chunk, where the partials are
+// brought to the chunk's true maximum: m = max score, l = sum 2^(s - m),
+// o = sum 2^(s - m) v_hat.
 //
 // One persistent CTA per SM walks a contiguous range of non-empty (sequence,
 // KV head, chunk) items as a stream of 128-cell tiles, with warp roles that
 // run concurrently and hand tiles over through mbarrier rings:
 //
-//   loader warps 0-7  (warp w: cells 32(w%4)..+31, row half w/4).  A software
-//            pipeline, one tile per step: list entries four tiles ahead,
-//            page-table entries three ahead, slot checks and L2 prefetch of
-//            the K/V rows two ahead, 32-byte register loads of the rows one
-//            ahead; the current tile's K codes go to tensor memory as the
-//            MMA's A operand (tcgen05.st), its V codes to a double-buffered
-//            shared-memory tile in the MN-major 128-byte-swizzled layout, its
-//            scales and validity bits to a small double-buffered ring.
-//   softmax warps 8-11 (thread = cell).  Per tile: max of every row over the
-//            128 cells (redux), per-row decisions by the row's own thread
-//            (running max; the reference max moves, and O is rescaled in
-//            tensor memory, only when the max grows by more than 2^8), then
-//            P' written to shared memory as the second MMA's B operand and
-//            row sums by a reduce-scatter butterfly.  At the end of a chunk
-//            they read O from tensor memory and write the partials.
+//   loader warps 0-7  (warp w: cells 32(w%4)+16(w/4)..+15).  A software
+//            pipeline, one tile per step: list entries six tiles ahead,
+//            page-table entries four ahead, slot checks, scale copies and L2
+//            prefetch of the K/V rows two ahead (lanes 0-15 resolve one cell
+//            each), 32-byte register loads of the rows one ahead; the current
+//            tile's K codes go to tensor memory as the MMA's A operand
+//            (tcgen05.st), its V codes to a double-buffered shared-memory
+//            tile in the MN-major 128-byte-swizzled layout.
+//   softmax warps 8-11 (warp q: tensor-memory lanes 32q..32q+31).  Per tile:
+//            scores from tensor memory, the vote, P' as the second MMA's B
+//            operand; at a chunk's end the partials.
 //   S warp 12 (one thread) issues S = K.Q^T of each tile, and P.V warp 13
 //            (one thread) O += V^T.P'^T, side by side; completion is
-//            signalled by tcgen05.commit on the rings' "empty" and "full"
-//            barriers.
+//            signalled by tcgen05.commit on the rings' barriers.
 //
 // Every wait is bounded; a wait that runs out raises QSA_STATUS_TIMEOUT and
-// makes all later waits of the CTA return at once, so the kernel always ends.
+// makes all later waits of the CTA return at once, so the kernel always
+// ends.  Before the CTA leaves, each issuing thread waits (with a bound of its
+// own) for its tensor-core operations and bulk copies, and each loader for its
+// asynchronous copies, so nothing is in flight when tensor memory is freed.
 #include <cuda_fp16.h>
+#include <float.h>
 
 #include "qsa_internal.cuh"
 #include "qsa_sm100.cuh"
@@ -62,15 +73,14 @@ constexpr int kPvWarp = kMmaWarp + 1;             // 13: issues O += V^T.P'^T
 constexpr int kThreads = (kPvWarp + 1) * 32;      // 448
 constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kScaleThreads = kLoadThreads / 4;   // loader threads that write the scales
+constexpr int kResolveThreads = kLoadWarps * 16;  // loader lanes 0-15: one cell each
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColK = 0;   // K codes, 128 columns (two f16 per column)
-constexpr uint32_t kColS = 128; // scores, two buffers (see Lay)
 constexpr int kMaxRows = kDecodeTcMaxRows;
 constexpr uint32_t kStageBytes = kTile * kHeadDim * 2; // one f16 V tile, 64 KB
 constexpr uint32_t kBarSoft = 1;                       // named barrier of the softmax warps
-constexpr float kRescaleLog2 = 8.f; // O is rescaled when a row max grows past 2^8
-constexpr float kSigmaGrow = 16.f;  // ... or a V scale exceeds 16 x the reference
+constexpr float kRescaleLog2 = 8.f; // the reference moves when a score exceeds it by 2^8
+constexpr float kSigmaGrow = 16.f;  // ... sigma when a V scale exceeds 16 x sigma
+constexpr long long kDrainCycles = 1ll << 30; // bound of the waits before the CTA leaves
 
 // Position in the work list (see cursor_init_warp / cursor_next).
 struct Cursor {
@@ -83,25 +93,26 @@ struct Misc {
     int32_t rs_sel[4][kTile]; // list entries
     int32_t rs_pg[4][kTile];  // page-table entries (-1 masked, kBadPos out of range)
     int32_t rs_off[4][kTile]; // offset of the position in its page (pages of P > 1 cells)
-    uint8_t rs_r0[4][kTile];  // causal limits: the first query row that sees the cell (<= 80)
     float rs_ks[4][kTile];    // k_scale, v_scale of the cell's slot (0 if masked)
     float rs_vs[4][kTile];
-    uint8_t sc_ok[2][kTile];  // cell holds a valid slot
-    uint8_t sc_r0[2][kTile];  // causal limits: first query row that sees the cell
-    // [tile parity][warp quadrant][row; kMaxRows = |v_scale| max]
-    __align__(16) float red_max[2][4][kMaxRows + 4];
-    __align__(16) float red_sum[2][4][kMaxRows];
-    float st_mrun[2][kMaxRows];    // running max (log2 units) after the tile of that parity
-    __align__(16) float st_mref[2][kMaxRows]; // reference max the tile's P' were formed against
-    float st_fac[kMaxRows];        // O/l factor of the current tile
-    __align__(16) float st_fin[kMaxRows]; // sigma * 2^(mref - mrun) at the end of a chunk
-    float st_sig[2];         // sigma reference after the tile of that parity
-    float st_fs[2];          // sigma factor of the tile
-    int st_any[2];           // tile index whose O needs rescaling
+    uint8_t rs_ok[4][kTile];  // cell holds a valid slot
+    uint8_t rs_r0[4][kTile];  // causal limits: the first query row that sees the cell (<= 80)
+    uint8_t sc_r0[2][kTile];  // the same, handed to the softmax (two-entry ring)
+    // softmax, after a vote: [warp][row] tile maxima, with the largest
+    // |v_scale| at [kMaxRows]; the O factors of a moved reference.  (One
+    // buffer: the next writer passes at least one barrier after the readers.)
+    __align__(16) float red_max[4][kMaxRows + 4];
+    __align__(16) float red_fac[kMaxRows + 4];
+    // chunk ends: [warp][row] maxima and sums, the reference; and, per chunk
+    // parity, the factor sigma * 2^(mref - m) the chunk's O is read out with
+    __align__(16) float ch_max[4][kMaxRows];
+    __align__(16) float ch_sum[4][kMaxRows];
+    __align__(16) float ch_ref[kMaxRows];
+    __align__(16) float st_fin[2][kMaxRows];
     Cursor first;
     uint32_t tmem;
     int abort;
-    uint64_t k_full, k_empty, done;
+    uint64_t k_full[2], k_empty[2], s_done, pv_done;
     uint64_t q_full[2], q_empty[2];
     uint64_t v_full[2], v_empty[2], sc_full[2], sc_empty[2];
     uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
@@ -111,14 +122,20 @@ template <int N>
 struct Lay {
     static constexpr int PB = N <= 48 ? 2 : 1; // P' buffers
     static constexpr int QB = N <= 48 ? 2 : 1; // query tile buffers
-    // tensor memory: K codes (128 columns), two score buffers of SW columns,
-    // then O^T in OB chunk buffers x two d halves x SW columns.  Up to 64
-    // rows two chunks' O alternate (a chunk's epilogue overlaps the next
-    // chunk's first P.V); wider windows keep one.
-    static constexpr uint32_t SW = N <= 64 ? 64u : (uint32_t)N;
-    static constexpr int OB = N <= 64 ? 2 : 1;
-    static constexpr uint32_t colO = kColS + 2 * SW;
-    static __device__ __forceinline__ uint32_t col_s(int par) { return kColS + SW * (uint32_t)par; }
+    // Tensor memory (512 columns): KB buffers of K codes (128 columns each),
+    // two score buffers of N columns, then O^T in OB chunk buffers x two d
+    // halves x N columns.  Two K buffers let the loaders write the K codes of
+    // tile i+1 while the MMAs of tile i read tile i's; two O buffers let a
+    // chunk's epilogue overlap the next chunk's first P.V.  Up to 32 rows
+    // both fit; 48 and 64 rows keep two K buffers and one O; 80 rows one K
+    // and one O.
+    static constexpr int KB = N <= 64 ? 2 : 1;
+    static constexpr int OB = N <= 32 ? 2 : 1;
+    static constexpr uint32_t SW = (uint32_t)N;
+    static constexpr uint32_t colS = 128u * KB;
+    static constexpr uint32_t colO = colS + 2 * SW;
+    static __device__ __forceinline__ uint32_t col_k(int kb) { return 128u * (uint32_t)kb; }
+    static __device__ __forceinline__ uint32_t col_s(int par) { return colS + SW * (uint32_t)par; }
     static __device__ __forceinline__ uint32_t col_o(int cp, int hh)
     {
         return colO + 2 * SW * (uint32_t)(cp % OB) + SW * (uint32_t)hh;
@@ -148,20 +165,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b)
 {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// One stage of a reduce-scatter over the warp: values [0, 2*HALF) -> [0, HALF);
-// a lane keeps the half selected by its bit `o` and adds the partner's.
-template <int HALF>
-__device__ __forceinline__ void rs_stage(float *e, int lane, int o)
-{
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int x = 0; x < HALF; ++x) {
-        const float send = up ? e[x] : e[x + HALF];
-        const float keep = up ? e[x + HALF] : e[x];
-        e[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
 }
 
 // ---------------------------------------------------------------- work list
@@ -254,20 +257,22 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
     cur.remaining = 0;
 }
 
-__device__ inline void cursor_next(const Params &p, Cursor &cur)
+__device__ __forceinline__ void cursor_next(const Params &p, Cursor &cur)
 {
     if (--cur.remaining <= 0) return;
     if (++cur.c < cur.nch) return;
     cur.c = 0;
     if (++cur.g < p.G) return;
     cur.g = 0;
-    int s, n;
+    // the next sequence with a non-empty list (the offsets were checked, and
+    // any bad ones reported, when the CTA's first item was found)
     for (int b = cur.b + 1; b < p.n_seq; ++b) {
-        const int nch = seq_chunks(p, b, &s, &n);
-        if (nch > 0) {
+        const int o0 = __ldg(p.sel_offsets + b);
+        const int n = min(__ldg(p.sel_offsets + b + 1) - o0, p.max_selected);
+        if (o0 >= 0 && n > 0) {
             cur.b = b;
-            cur.nch = nch;
-            cur.start = s;
+            cur.nch = (n + p.chunk_cells - 1) / p.chunk_cells;
+            cur.start = o0;
             cur.n = n;
             return;
         }
@@ -462,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 {
     using L = Lay<N>;
     constexpr int PB = L::PB;
+    constexpr int NR = 2 * KR; // score rows a softmax thread holds: 8k + 2u + e
     // The operand tiles need 1024-byte alignment (128-byte swizzle atoms); the
     // dynamic shared memory of a kernel without static shared memory starts
     // there, so no padding is reserved (it would cost the 196 KB shared-memory
@@ -469,25 +475,29 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     // window from being used.
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {
-        if (threadIdx.x == 0) raise_status(p, QSA_STATUS_TIMEOUT);
+        if (threadIdx.x == 0) raise_status(p, QSA_STATUS_LAUNCH);
         return;
     }
     Misc &ms = *reinterpret_cast<Misc *>(smem + L::misc);
     const int tid = threadIdx.x;
-    const int w = tid >> 5, lane = tid & 31;
+    // the warp index read through a shuffle: provably the same in every
+    // lane, so values derived from it (tensor-memory addresses, roles) stay
+    // in uniform registers and warp-wide tcgen05 operations need no per-lane
+    // fallback
+    const int w = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
     const uint32_t s_v = smem_u32(smem + L::v);
     const uint32_t s_q = smem_u32(smem + L::q);
     const uint32_t s_p = smem_u32(smem + L::pb);
-    volatile int *abort_flag = &ms.abort;
 
     if (tid == 0) {
-        mbar_init(&ms.k_full, kLoadThreads);
-        mbar_init(&ms.k_empty, 1);
-        mbar_init(&ms.done, 2);
+        mbar_init(&ms.s_done, 1);
+        mbar_init(&ms.pv_done, 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.k_full[i], kLoadThreads);
+            mbar_init(&ms.k_empty[i], 1);
             mbar_init(&ms.v_full[i], kLoadThreads);
             mbar_init(&ms.v_empty[i], 1);
-            mbar_init(&ms.sc_full[i], kScaleThreads);
+            mbar_init(&ms.sc_full[i], kResolveThreads);
             mbar_init(&ms.sc_empty[i], kSoftThreads);
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.s_empty[i], kSoftThreads);
@@ -498,10 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             // bulk copy (one arrival + bytes), or the softmax threads' stores
             mbar_init(&ms.q_full[i], p.q_inline ? kSoftThreads : 1);
             mbar_init(&ms.q_empty[i], 1);
-            ms.st_any[i] = -1;
-            ms.st_sig[i] = 1.f;
-            ms.st_fs[i] = 1.f;
         }
+        for (int r = 0; r < kMaxRows + 4; ++r) ms.red_fac[r] = 1.f;
         ms.abort = 0;
         fence_mbar_init();
     }
@@ -515,14 +523,33 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     tc_fence_after();
     // the merge kernel may be scheduled now; it waits for this grid's results
     cudaTriggerProgrammaticLaunchCompletion();
-    const uint32_t tmem = ms.tmem;
-    const Cursor first = ms.first;
+    // (shuffled from lane 0 for the same reason as the warp index)
+    const uint32_t tmem = __shfl_sync(0xffffffffu, ms.tmem, 0);
+    Cursor first;
+    first.b = __shfl_sync(0xffffffffu, ms.first.b, 0);
+    first.g = __shfl_sync(0xffffffffu, ms.first.g, 0);
+    first.c = __shfl_sync(0xffffffffu, ms.first.c, 0);
+    first.nch = __shfl_sync(0xffffffffu, ms.first.nch, 0);
+    first.start = __shfl_sync(0xffffffffu, ms.first.start, 0);
+    first.n = __shfl_sync(0xffffffffu, ms.first.n, 0);
+    first.remaining = __shfl_sync(0xffffffffu, ms.first.remaining, 0);
 
+    // Waits: a completed phase costs one test.  Otherwise the thread
+    // suspends between tests (for short bounds, used to exercise the
+    // time-out path, it polls); a wait that runs out raises
+    // QSA_STATUS_TIMEOUT and sets the CTA's abort flag, after which waits
+    // return at once and the roles run to the end of their loops.
+    volatile int *abort_flag = &ms.abort;
+    const uint32_t suspend_ns = p.wait_cycles >= (1ll << 24) ? 200000u : 0u;
     auto wait = [&](uint64_t *bar, uint32_t parity) {
-        if (*abort_flag) return;
-        if (!mbar_wait(bar, parity)) {
-            *abort_flag = 1;
-            raise_status(p, QSA_STATUS_TIMEOUT);
+        if (mbar_test_wait(bar, parity) || *abort_flag) return;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, parity, suspend_ns)) {
+            if (clock64() - t0 > p.wait_cycles) {
+                *abort_flag = 1;
+                raise_status(p, QSA_STATUS_TIMEOUT);
+                return;
+            }
         }
     };
 
@@ -537,11 +564,19 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         // 32v and 128 + 32v (v = t/8), so the 16-byte swizzled shared-memory
         // stores of 8 consecutive threads hit 8 different bank groups.
         const int R0 = 32 * (w & 3) + 16 * (w >> 2);
-        const int u = lane & 3, cA = R0 + (lane >> 2), cB = cA + 8;
-        const int vr = lane & 7, vu = lane >> 3, vA = R0 + vr, vB = vA + 8;
-        const int src_k = 4 * vr; // K-mapping thread holding the V rows' slots
-        const bool scl = u == 0;  // writes the scales of cells A and B, reports status
+        const int u = lane & 3;
+        const int vr = lane & 7, vu = lane >> 3, vA = R0 + vr; // and B' = A' + 8
+        const bool res = lane < 16; // resolves cell R0 + lane, reports its status
+        const int cr = R0 + (lane & 15);
         const uint32_t t_lane = (uint32_t)R0 << 16;
+        // V stores: piece i of (cell A' + 8rr, 32 dims at byte 128pc + 32vu) goes
+        // to d-block 2pc + vu/2, row group (A' + 8rr)/8, row A' % 8, 16-byte
+        // chunk (4(vu&1) + i) ^ (A' % 8): a base plus rr * 1024 + pc * 32768
+        // plus one of four swizzled chunk offsets
+        const uint32_t vbase = (uint32_t)((vu >> 1) * 16384 + (vA >> 3) * 1024 + vr * 128);
+        uint32_t vchunk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vchunk[i] = (uint32_t)(((4 * (vu & 1) + i) ^ vr) << 4);
         // Resolution (step a1) runs ahead of the row loads through shared-memory
         // rings filled by 4-byte asynchronous copies, so no register waits on
         // those reads: step j copies the list entries of tile j+6, the page
@@ -549,12 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         // checks the slots of tile j+2 (from page entries copied two steps
         // earlier), prefetches that tile's rows into L2 and copies its scales;
         // the rows of tile j+1 are loaded into registers; tile j is converted.
-        // The lane with u == 0 resolves cells A and B; the others take the
-        // slots by shuffle.
         // tile info per stage: bg = b * G + g, mt = cells of the tile (0 = none)
-        int bg0 = 0, bg1 = 0, bg2 = 0, bg3 = 0, bg4 = 0, bg5 = 0, bg6 = 0;
+        int bg1 = 0, bg2 = 0, bg3 = 0, bg4 = 0, bg5 = 0, bg6 = 0;
         int mt0 = 0, mt1 = 0, mt2 = 0, mt3 = 0, mt4 = 0, mt5 = 0, mt6 = 0;
-        int slA0 = -1, slB0 = -1, slA1 = -1, slB1 = -1, slA2 = -1, slB2 = -1;
+        // slots (-1: masked) of the K cells A, B and the V cells A', B' at stages 1 and 2
+        int kA1 = -1, kB1 = -1, vA1 = -1, vB1 = -1, kA2 = -1, kB2 = -1, vA2 = -1, vB2 = -1;
         uint32_t rk[32], rv[32]; // K: A p0, A p1, B p0, B p1; V: A' p0, A' p1, B' p0, B' p1
 #pragma unroll
         for (int e = 0; e < 32; ++e) rk[e] = rv[e] = 0u;
@@ -562,10 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         tile_init(p, head, first);
         for (int j = -6;; ++j) {
             cp_async_wait_group<1>(); // the copies of step j-2 and earlier have landed
-            // ---- tile j -> tensor memory / shared memory; after each half, the
-            // registers it frees take tile j+1's rows (mostly L2 hits by now)
+            // ---- tile j: K codes -> tensor memory
             if (mt0) {
-                if (j >= 1) wait(&ms.k_empty, (uint32_t)(j - 1) & 1u);
+                const int kb = j % L::KB;
+                if (j >= L::KB) wait(&ms.k_empty[kb], (uint32_t)((j - L::KB) / L::KB) & 1u);
                 tc_fence_after();
 #pragma unroll
                 for (int pc = 0; pc < 2; ++pc) {
@@ -577,84 +611,63 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                             i8x4_to_f16x4(rk[8 * pc + 4 * hq + k], f[4 * k], f[4 * k + 1]);
                             i8x4_to_f16x4(rk[16 + 8 * pc + 4 * hq + k], f[4 * k + 2], f[4 * k + 3]);
                         }
-                        tmem_st_16x256b_x4(tmem + t_lane + kColK + 64u * pc + 32u * hq, f);
+                        tmem_st_16x256b_x4(tmem + t_lane + L::col_k(kb) + 64u * pc + 32u * hq, f);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&ms.k_full);
+                mbar_arrive(&ms.k_full[kb]);
             } else if (j >= 0) {
                 break;
             }
+            // ---- rows of tile j+1 (K); a masked cell loads nothing (its score
+            // is -inf and its probability 0 whatever the registers hold)
             const size_t kvb1 = (size_t)bg1 * p.pool_cells;
             if (mt1) {
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int sk = rr ? slB1 : slA1;
-#pragma unroll
-                    for (int pc = 0; pc < 2; ++pc) {
-                        if (sk >= 0) {
-                            ldg256_stream(p.k_pool + (kvb1 + sk) * kHeadDim + 128 * pc + 32 * u, rk + 16 * rr + 8 * pc);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) rk[16 * rr + 8 * pc + e] = 0u;
-                        }
-                    }
-                }
+                const int8_t *ka = p.k_pool + (kvb1 + (size_t)max(kA1, 0)) * kHeadDim + 32 * u;
+                const int8_t *kb = p.k_pool + (kvb1 + (size_t)max(kB1, 0)) * kHeadDim + 32 * u;
+                ldg256_stream_if(ka, rk, kA1 >= 0);
+                ldg256_stream_if(ka + 128, rk + 8, kA1 >= 0);
+                ldg256_stream_if(kb, rk + 16, kB1 >= 0);
+                ldg256_stream_if(kb + 128, rk + 24, kB1 >= 0);
             }
             if (mt0) {
                 const int jb = j & 1;
-                if (scl) {
-                    // the scales of tile j sit in ring entry j % 4 (copied by this
-                    // thread two steps ago); the validity bits go to a 2-entry ring
+                if (res) {
+                    // the scales and validity of tile j sit in ring entry j % 4
+                    // (copied by this thread two steps ago); the softmax frees
+                    // the entry of tile j-2, which the slot stage below reuses
                     if (j >= 2) wait(&ms.sc_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
-                    ms.sc_ok[jb][cA] = slA0 >= 0;
-                    ms.sc_ok[jb][cB] = slB0 >= 0;
-                    if (LIM) { // written by this thread at tile j's page stage
-                        ms.sc_r0[jb][cA] = ms.rs_r0[j & 3][cA];
-                        ms.sc_r0[jb][cB] = ms.rs_r0[j & 3][cB];
-                    }
+                    if (LIM) ms.sc_r0[jb][cr] = ms.rs_r0[j & 3][cr];
                     mbar_arrive(&ms.sc_full[jb]);
                 }
+                // ---- tile j: V codes -> shared memory
                 if (j >= 2) wait(&ms.v_empty[jb], (uint32_t)((j - 2) >> 1) & 1u);
                 uint8_t *sv = smem + L::v + (size_t)jb * kStageBytes;
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    const int c = rr ? vB : vA;
 #pragma unroll
                     for (int pc = 0; pc < 2; ++pc) {
-                        // 32 dims at byte 128pc + 32vu: d-block 2pc + vu/2, chunks 4(vu&1)..+3
-                        uint8_t *line = sv + (size_t)(2 * pc + (vu >> 1)) * 16384 + (c >> 3) * 1024 + (c & 7) * 128;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             uint4 v;
                             i8x4_to_f16x4(rv[16 * rr + 8 * pc + 2 * i], v.x, v.y);
                             i8x4_to_f16x4(rv[16 * rr + 8 * pc + 2 * i + 1], v.z, v.w);
-                            *reinterpret_cast<uint4 *>(line + (((4 * (vu & 1) + i) ^ (c & 7)) << 4)) = v;
+                            *reinterpret_cast<uint4 *>(sv + vbase + (uint32_t)(rr * 1024 + pc * 32768) + vchunk[i]) = v;
                         }
                     }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&ms.v_full[jb]);
             }
-            {
-                const int va = __shfl_sync(0xffffffffu, slA1, src_k);
-                const int vb = __shfl_sync(0xffffffffu, slB1, src_k);
-                if (mt1) {
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int sv2 = rr ? vb : va;
-#pragma unroll
-                        for (int pc = 0; pc < 2; ++pc) {
-                            if (sv2 >= 0) {
-                                ldg256_stream(p.v_pool + (kvb1 + sv2) * kHeadDim + 128 * pc + 32 * vu, rv + 16 * rr + 8 * pc);
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) rv[16 * rr + 8 * pc + e] = 0u;
-                            }
-                        }
-                    }
-                }
+            // ---- rows of tile j+1 (V)
+            if (mt1) {
+                const int8_t *va = p.v_pool + (kvb1 + (size_t)max(vA1, 0)) * kHeadDim + 32 * vu;
+                const int8_t *vb = p.v_pool + (kvb1 + (size_t)max(vB1, 0)) * kHeadDim + 32 * vu;
+                ldg256_stream_if(va, rv, vA1 >= 0);
+                ldg256_stream_if(va + 128, rv + 8, vA1 >= 0);
+                ldg256_stream_if(vb, rv + 16, vB1 >= 0);
+                ldg256_stream_if(vb + 128, rv + 24, vB1 >= 0);
             }
             // ---- list entries of tile j+6
             mt6 = 0;
@@ -662,113 +675,108 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 const int nc = tile_cells(head);
                 bg6 = head.cur.b * p.G + head.cur.g;
                 mt6 = nc;
-                if (scl) {
-                    const int *src = p.sel + tile_base(p, head);
-                    const int e6 = (j + 6) & 3;
-                    if (cA < nc) cp_async4(smem_u32(&ms.rs_sel[e6][cA]), src + cA);
-                    if (cB < nc) cp_async4(smem_u32(&ms.rs_sel[e6][cB]), src + cB);
-                }
+                if (res && cr < nc) cp_async4(smem_u32(&ms.rs_sel[(j + 6) & 3][cr]), p.sel + tile_base(p, head) + cr);
                 tile_next(p, head);
             }
             // ---- page-table entries of tile j+4 (from its list entries)
-            if (mt4 && scl) {
+            if (mt4 && res) {
                 const int e4 = (j + 4) & 3;
-                const int32_t *prow = p.page_table + (size_t)(bg4 / p.G) * p.page_table_len;
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int cx = x ? cB : cA;
-                    int32_t *dst = &ms.rs_pg[e4][cx];
-                    if (cx >= mt4) {
-                        *dst = -1; // past the tile's cells: masked
+                int32_t *dst = &ms.rs_pg[e4][cr];
+                if (cr >= mt4) {
+                    *dst = -1; // past the tile's cells: masked
+                } else {
+                    // position pos: page pos / P, offset pos % P (P = 1: the entry is the slot)
+                    const int pos = ms.rs_sel[e4][cr], P = p.page_cells;
+                    const int32_t *prow = p.page_table + (size_t)(bg4 / p.G) * p.page_table_len;
+                    if (LIM && pos >= 0) {
+                        // rows t*H.. of the queries whose limit is above pos see the
+                        // cell: with limits non-decreasing in t, those are the rows
+                        // from H * #{t : limit[t] <= pos} on
+                        const int32_t *lim = p.q_limit + (size_t)(bg4 / p.G) * p.T;
+                        int below = 0;
+                        for (int t = 0; t < p.T; ++t) below += __ldg(lim + t) <= pos;
+                        ms.rs_r0[e4][cr] = (uint8_t)(below * p.H); // <= T * H <= 80
+                    }
+                    if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
+                        *dst = kBadPos;
+                    } else if (P == 1) {
+                        cp_async4(smem_u32(dst), prow + pos);
                     } else {
-                        // position pos: page pos / P, offset pos % P (P = 1: the entry is the slot)
-                        const int pos = ms.rs_sel[e4][cx], P = p.page_cells;
-                        if (LIM && pos >= 0) {
-                            // rows t*H.. of the queries whose limit is above pos see the
-                            // cell: with limits non-decreasing in t, those are the rows
-                            // from H * #{t : limit[t] <= pos} on
-                            const int32_t *lim = p.q_limit + (size_t)(bg4 / p.G) * p.T;
-                            int below = 0;
-                            for (int t = 0; t < p.T; ++t) below += __ldg(lim + t) <= pos;
-                            ms.rs_r0[e4][cx] = (uint8_t)(below * p.H); // <= T * H <= 80
-                        }
-                        if (pos < 0 || (long long)pos >= (long long)p.page_table_len * P) {
-                            *dst = kBadPos;
-                        } else if (P == 1) {
-                            cp_async4(smem_u32(dst), prow + pos);
-                        } else {
-                            const int page = pos / P;
-                            ms.rs_off[e4][cx] = pos - page * P;
-                            cp_async4(smem_u32(dst), prow + page);
-                        }
+                        const int page = pos / P;
+                        ms.rs_off[e4][cr] = pos - page * P;
+                        cp_async4(smem_u32(dst), prow + page);
                     }
                 }
             }
-            // ---- slots of tile j+2 (from its page entries): rows prefetched into
-            // L2, scales copied into the ring
+            // ---- slots of tile j+2 (from its page entries): scales copied into
+            // the ring, rows prefetched into L2
             if (mt2) {
-                int sa = -1, sb = -1;
-                if (scl) {
+                int sl = -1;
+                if (res) {
                     const int e2 = (j + 2) & 3;
-                    sa = slot_of(p, ms.rs_pg[e2][cA], ms.rs_off[e2][cA], true);
-                    sb = slot_of(p, ms.rs_pg[e2][cB], ms.rs_off[e2][cB], true);
+                    sl = slot_of(p, ms.rs_pg[e2][cr], ms.rs_off[e2][cr], true);
                     const size_t kvb = (size_t)bg2 * p.pool_cells;
-                    if (sa >= 0) {
-                        cp_async4(smem_u32(&ms.rs_ks[e2][cA]), p.k_scale + kvb + sa);
-                        cp_async4(smem_u32(&ms.rs_vs[e2][cA]), p.v_scale + kvb + sa);
+                    if (sl >= 0) {
+                        cp_async4(smem_u32(&ms.rs_ks[e2][cr]), p.k_scale + kvb + sl);
+                        cp_async4(smem_u32(&ms.rs_vs[e2][cr]), p.v_scale + kvb + sl);
                     } else {
-                        ms.rs_ks[e2][cA] = 0.f;
-                        ms.rs_vs[e2][cA] = 0.f;
+                        ms.rs_ks[e2][cr] = 0.f;
+                        ms.rs_vs[e2][cr] = 0.f;
                     }
-                    if (sb >= 0) {
-                        cp_async4(smem_u32(&ms.rs_ks[e2][cB]), p.k_scale + kvb + sb);
-                        cp_async4(smem_u32(&ms.rs_vs[e2][cB]), p.v_scale + kvb + sb);
-                    } else {
-                        ms.rs_ks[e2][cB] = 0.f;
-                        ms.rs_vs[e2][cB] = 0.f;
-                    }
+                    ms.rs_ok[e2][cr] = sl >= 0;
                 }
-                slA2 = __shfl_sync(0xffffffffu, sa, lane & ~3);
-                slB2 = __shfl_sync(0xffffffffu, sb, lane & ~3);
-                const int pa = __shfl_sync(0xffffffffu, slA2, 4 * (lane & 7));
-                const int pb = __shfl_sync(0xffffffffu, slB2, 4 * (lane & 7));
-                const int sl = (lane & 8) ? pb : pa; // slot of cell R0 + lane%16
-                if (sl >= 0) {
-                    const size_t cell = (size_t)bg2 * p.pool_cells + sl;
+                kA2 = __shfl_sync(0xffffffffu, sl, lane >> 2);
+                kB2 = __shfl_sync(0xffffffffu, sl, (lane >> 2) + 8);
+                vA2 = __shfl_sync(0xffffffffu, sl, vr);
+                vB2 = __shfl_sync(0xffffffffu, sl, vr + 8);
+                const int pf = __shfl_sync(0xffffffffu, sl, lane & 15); // cell R0 + lane%16, half lane/16
+                if (pf >= 0) {
+                    const size_t cell = (size_t)bg2 * p.pool_cells + pf;
                     prefetch_l2(p.k_pool + cell * kHeadDim + 128 * (lane >> 4));
                     prefetch_l2(p.v_pool + cell * kHeadDim + 128 * (lane >> 4));
                 }
             }
             cp_async_commit();
             // shift the pipeline by one tile
-            bg0 = bg1; bg1 = bg2; bg2 = bg3; bg3 = bg4; bg4 = bg5; bg5 = bg6;
+            bg1 = bg2; bg2 = bg3; bg3 = bg4; bg4 = bg5; bg5 = bg6;
             mt0 = mt1; mt1 = mt2; mt2 = mt3; mt3 = mt4; mt4 = mt5; mt5 = mt6;
-            slA0 = slA1; slB0 = slB1;
-            slA1 = slA2; slB1 = slB2;
+            kA1 = kA2; kB1 = kB2; vA1 = vA2; vB1 = vB2;
         }
         cp_async_wait_group<0>();
     } else if (w < kMmaWarp) {
         // ================================================================ softmax
         const int q = w & 3, c = 32 * q + lane;
         const int u = lane & 3, ra = lane >> 2; // 16x256b: rows 8k + 2u + e, cells 32q + 8i + ra
-        const int orow = 4 * lane + q;          // the row this thread owns (running values, decisions)
+        const int orow = 4 * lane + q;          // the row this thread writes at a chunk's end
         constexpr int NK = N / 8;               // 16x256b repetitions over the score columns
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
         struct Pend {
-            int b, g, c, cp, par;
+            int b, g, c, cp;
             bool on;
         };
-        Pend pend{0, 0, 0, 0, 0, false};
-        float l_own = 0.f, l_fin = 0.f;
-        int cp = -1;
+        Pend pend{0, 0, 0, 0, false};
+        // per row (index 2k + e = row 8k + 2u + e): the reference maximum (log2
+        // units, the same in every thread that holds the row; -FLT_MAX until
+        // the row's first valid score, when all its scores are -inf), and this
+        // thread's share of the chunk's sum of probabilities and of its maximum
+        float mref[NR], lsum[NR], cmax[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            mref[r] = -FLT_MAX;
+            lsum[r] = 0.f;
+            cmax[r] = -INFINITY;
+        }
+        float sig = 0.f, inv_sig = 0.f; // the V-scale reference of the pair, 0 before its first cell
+        int cp = -1, cur_seg = -1;
         TileIt it;
         tile_init(p, it, first);
 
-        // partials of the chunk that ended at the previous tile
+        // partials of chunk e.cp: O read out of tensor memory, times sigma * 2^(mref - m)
         auto epilogue = [&](const Pend &e) {
             wait(&ms.o_full[e.cp % L::OB], (uint32_t)(e.cp / L::OB) & 1u);
             tc_fence_after();
             const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R;
+            const float *fin = ms.st_fin[e.cp & 1];
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 // all 8-row blocks that hold real rows in flight together, one wait
@@ -781,8 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 float *dst = p.part_o + base * kHeadDim + 128 * hh + c;
 #pragma unroll
                 for (int k = 0; k < KR; ++k) {
-                    const float4 f0 = *reinterpret_cast<const float4 *>(&ms.st_fin[8 * k]);
-                    const float4 f1 = *reinterpret_cast<const float4 *>(&ms.st_fin[8 * k + 4]);
+                    const float4 f0 = *reinterpret_cast<const float4 *>(fin + 8 * k);
+                    const float4 f1 = *reinterpret_cast<const float4 *>(fin + 8 * k + 4);
                     const float fr[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
@@ -793,9 +801,47 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
             tc_fence_before();
             mbar_arrive(&ms.o_empty[e.cp % L::OB]);
+        };
+
+        // end of chunk cp: the rows' true maxima and sums across the CTA; the
+        // row's owner writes m and l and the factor its O is read out with
+        auto chunk_end = [&](int chunk, int b, int g, int cc) {
+            const int cpar = chunk & 1;
+            float cm[NR], cs[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                cm[r] = cmax[r];
+                cs[r] = lsum[r];
+            }
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    cm[r] = fmaxf(cm[r], __shfl_xor_sync(0xffffffffu, cm[r], o));
+                    cs[r] += __shfl_xor_sync(0xffffffffu, cs[r], o);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < KR; ++k) {
+                if (ra == (k & 7)) {
+                    *reinterpret_cast<float2 *>(&ms.ch_max[q][8 * k + 2 * u]) = make_float2(cm[2 * k], cm[2 * k + 1]);
+                    *reinterpret_cast<float2 *>(&ms.ch_sum[q][8 * k + 2 * u]) = make_float2(cs[2 * k], cs[2 * k + 1]);
+                    if (q == 0)
+                        *reinterpret_cast<float2 *>(&ms.ch_ref[8 * k + 2 * u]) = make_float2(mref[2 * k], mref[2 * k + 1]);
+                }
+            }
+            named_bar(kBarSoft, kSoftThreads);
             if (orow < p.R) {
-                p.part_m[base + orow] = ms.st_mrun[e.par][orow] * kLn2;
-                p.part_l[base + orow] = l_fin;
+                const float m = fmaxf(fmaxf(ms.ch_max[0][orow], ms.ch_max[1][orow]),
+                                      fmaxf(ms.ch_max[2][orow], ms.ch_max[3][orow]));
+                const float l = ((ms.ch_sum[0][orow] + ms.ch_sum[1][orow]) + ms.ch_sum[2][orow]) +
+                                ms.ch_sum[3][orow];
+                // (a row with a valid score has a finite reference)
+                const float fin = m > -INFINITY ? fast_exp2(ms.ch_ref[orow] - m) : 0.f;
+                ms.st_fin[cpar][orow] = fin * sig;
+                const size_t base = (((size_t)b * p.G + g) * p.n_chunks + cc) * p.R;
+                p.part_m[base + orow] = m > -INFINITY ? m * kLn2 : -INFINITY;
+                p.part_l[base + orow] = l * fin;
             }
         };
 
@@ -821,10 +867,23 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         for (int i = 0; it.valid; ++i) {
             const int par = i & 1;
             const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
-            if (first_t) ++cp;
+            if (it.seg != cur_seg) { // new (sequence, KV head): new rows, no reference yet
+                cur_seg = it.seg;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) mref[r] = -FLT_MAX;
+                sig = inv_sig = 0.f;
+            }
+            if (first_t) {
+                ++cp;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    lsum[r] = 0.f;
+                    cmax[r] = -INFINITY;
+                }
+            }
             wait(&ms.sc_full[par], (uint32_t)(i >> 1) & 1u);
-            // this thread's four cells (16x256b layout): cell(i) = 32q + 8i + t/4,
-            // i = 2L + B for lane group L (lanes +16) and row half B (+8)
+            // this thread's four cells (16x256b layout): cell(ci) = 32q + 8ci + t/4,
+            // ci = 2L + B for lane group L (lanes +16) and row half B (+8)
             // per cell: K scale (x softmax scale x log2 e), V scale (0 when the
             // cell is masked), and a bias of -inf that masks the cell's scores
             float ksc[4], vsc[4], kbias[4];
@@ -832,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int cc = 32 * q + 8 * ci + ra;
-                kbias[ci] = ms.sc_ok[par][cc] != 0 ? 0.f : -INFINITY;
+                kbias[ci] = ms.rs_ok[i & 3][cc] != 0 ? 0.f : -INFINITY;
                 ksc[ci] = ms.rs_ks[i & 3][cc] * p.scale_log2;
                 vsc[ci] = ms.rs_vs[i & 3][cc];
                 r0[ci] = LIM ? ms.sc_r0[par][cc] : 0;
@@ -847,124 +906,128 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&ms.s_empty[par]); // the scores live in registers from here on
-            // ---- pass 1: tile max of every row.  The same rounded product is
-            // used in pass 2 (no FMA contraction), so the max cell gets 2^0 = 1.
-            float mrow[2 * KR];
+            // ---- scale and mask; the vote: does a score pass its row's
+            // reference by more than 2^8, or a V scale sigma by 16x (the first
+            // valid cell of a pair passes both)?  The same rounded product is
+            // used for the probabilities, so the max cell gets exactly 2^0.
+            bool need = false;
 #pragma unroll
             for (int k = 0; k < KR; ++k) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     float m = -INFINITY;
 #pragma unroll
-                    for (int L = 0; L < 2; ++L) {
+                    for (int L2 = 0; L2 < 2; ++L2) {
 #pragma unroll
                         for (int B = 0; B < 2; ++B) {
-                            const int ci = 2 * L + B;
-                            float &xv = x[L][4 * k + 2 * B + e];
+                            const int ci = 2 * L2 + B;
+                            float &xv = x[L2][4 * k + 2 * B + e];
                             xv = __fmaf_rn(xv, ksc[ci], kbias[ci]); // = the rounded product, or -inf
                             if (LIM && 8 * k + 2 * u + e < r0[ci]) xv = -INFINITY; // beyond its query's limit
                             m = fmaxf(m, xv);
                         }
                     }
-                    mrow[2 * k + e] = m;
+                    cmax[2 * k + e] = fmaxf(cmax[2 * k + e], m);
+                    need |= m > mref[2 * k + e] + kRescaleLog2;
                 }
             }
 #pragma unroll
-            for (int o = 4; o <= 16; o <<= 1) {
+            for (int ci = 0; ci < 4; ++ci) need |= fabsf(vsc[ci]) > sig * kSigmaGrow;
+            if (named_bar_or(kBarSoft, kSoftThreads, need)) {
+                // ---- the tile's true row maxima and largest V scale (rare: the
+                // first tile of a pair, or a jump of 2^8)
+                float tm[NR];
 #pragma unroll
-                for (int jr = 0; jr < 2 * KR; ++jr)
-                    mrow[jr] = fmaxf(mrow[jr], __shfl_xor_sync(0xffffffffu, mrow[jr], o));
-            }
+                for (int k = 0; k < KR; ++k)
 #pragma unroll
-            for (int k = 0; k < KR; ++k)
-                if (ra == (k & 7)) *reinterpret_cast<float2 *>(&ms.red_max[par][q][8 * k + 2 * u]) = make_float2(mrow[2 * k], mrow[2 * k + 1]);
-            {
-                float va = 0.f;
+                    for (int e = 0; e < 2; ++e)
+                        tm[2 * k + e] = fmaxf(fmaxf(x[0][4 * k + e], x[0][4 * k + 2 + e]),
+                                              fmaxf(x[1][4 * k + e], x[1][4 * k + 2 + e]));
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci) va = fmaxf(va, fabsf(vsc[ci])); // (0 if masked)
-                const unsigned uu = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
-                if (lane == 0) ms.red_max[par][q][kMaxRows] = __uint_as_float(uu);
-            }
-            named_bar(kBarSoft, kSoftThreads);
-            // ---- per-row decisions (thread c owns row c)
-            if (orow < p.R) {
-                const int c = orow;
-                const float mt = fmaxf(fmaxf(ms.red_max[par][0][c], ms.red_max[par][1][c]),
-                                       fmaxf(ms.red_max[par][2][c], ms.red_max[par][3][c]));
-                const float mo = ms.st_mrun[par ^ 1][c], mref = ms.st_mref[par ^ 1][c];
-                if (i >= 1)
-                    l_own += ((ms.red_sum[par ^ 1][0][c] + ms.red_sum[par ^ 1][1][c]) + ms.red_sum[par ^ 1][2][c]) +
-                             ms.red_sum[par ^ 1][3][c];
-                if (pend.on) {
-                    // the chunk that ended at the previous tile: its partials are
-                    // o * sigma * 2^(mref - mrun), l * 2^(mref - mrun)
-                    const float fin = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
-                    l_fin = l_own * fin;
-                    ms.st_fin[c] = fin * ms.st_sig[par ^ 1];
+                for (int o = 4; o <= 16; o <<= 1)
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) tm[r] = fmaxf(tm[r], __shfl_xor_sync(0xffffffffu, tm[r], o));
+#pragma unroll
+                for (int k = 0; k < KR; ++k)
+                    if (ra == (k & 7))
+                        *reinterpret_cast<float2 *>(&ms.red_max[q][8 * k + 2 * u]) = make_float2(tm[2 * k], tm[2 * k + 1]);
+                {
+                    float va = 0.f;
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) va = fmaxf(va, fabsf(vsc[ci])); // (0 if masked)
+                    const unsigned uu = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
+                    if (lane == 0) ms.red_max[q][kMaxRows] = __uint_as_float(uu);
                 }
-                float mrun_n, mref_n, fac;
-                if (first_t) {
-                    mrun_n = mref_n = mt;
-                    fac = 0.f;
-                } else {
-                    mrun_n = fmaxf(mo, mt);
-                    if (mref == -INFINITY) {
-                        mref_n = mrun_n; // nothing accumulated yet
-                        fac = 0.f;
-                    } else if (mrun_n > mref + kRescaleLog2) {
-                        mref_n = mrun_n;
-                        fac = fast_exp2(mref - mref_n);
-                        ms.st_any[par] = i;
-                    } else {
-                        mref_n = mref;
-                        fac = 1.f;
+                named_bar(kBarSoft, kSoftThreads);
+                // every thread takes the same decisions for the rows it holds;
+                // O of this chunk (if any is accumulated) is rescaled by rows
+                bool resc = false;
+#pragma unroll
+                for (int k = 0; k < KR; ++k) {
+                    float2 t2 = *reinterpret_cast<const float2 *>(&ms.red_max[0][8 * k + 2 * u]);
+#pragma unroll
+                    for (int ww = 1; ww < 4; ++ww) {
+                        const float2 o2 = *reinterpret_cast<const float2 *>(&ms.red_max[ww][8 * k + 2 * u]);
+                        t2.x = fmaxf(t2.x, o2.x);
+                        t2.y = fmaxf(t2.y, o2.y);
                     }
+                    float fac[2] = {1.f, 1.f};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int r = 2 * k + e;
+                        const float t = e ? t2.y : t2.x;
+                        if (t > mref[r] + kRescaleLog2) {
+                            if (mref[r] > -FLT_MAX) fac[e] = fast_exp2(mref[r] - t);
+                            lsum[r] *= fac[e];
+                            mref[r] = t;
+                        }
+                    }
+                    if (!first_t && (fac[0] != 1.f || fac[1] != 1.f)) resc = true;
+                    if (q == 0 && ra == (k & 7))
+                        *reinterpret_cast<float2 *>(&ms.red_fac[8 * k + 2 * u]) = make_float2(fac[0], fac[1]);
                 }
-                l_own *= fac;
-                ms.st_mrun[par][c] = mrun_n;
-                ms.st_mref[par][c] = mref_n;
-                ms.st_fac[c] = fac;
-            }
-            if (c == kSoftThreads - 1) { // owns no row (at most kMaxRows < 127 rows)
-                const float st = fmaxf(fmaxf(ms.red_max[par][0][kMaxRows], ms.red_max[par][1][kMaxRows]),
-                                       fmaxf(ms.red_max[par][2][kMaxRows], ms.red_max[par][3][kMaxRows]));
-                const float so = ms.st_sig[par ^ 1];
-                float sn = so, fs = 1.f;
-                if (first_t) {
-                    sn = st > 0.f ? st : 1.f;
-                } else if (st > so * kSigmaGrow) {
-                    sn = st;
-                    fs = so / st;
-                    ms.st_any[par] = i;
+                const float st = fmaxf(fmaxf(ms.red_max[0][kMaxRows], ms.red_max[1][kMaxRows]),
+                                       fmaxf(ms.red_max[2][kMaxRows], ms.red_max[3][kMaxRows]));
+                float fs = 1.f;
+                if (st > sig * kSigmaGrow) {
+                    if (sig > 0.f && !first_t) {
+                        fs = sig / st;
+                        resc = true;
+                    }
+                    sig = st;
+                    inv_sig = 1.f / st;
                 }
-                ms.st_sig[par] = sn;
-                ms.st_fs[par] = fs;
+                if (named_bar_or(kBarSoft, kSoftThreads, resc)) {
+                    // P.V of the previous tile (same chunk) must be done
+                    if (PB == 2) wait(&ms.p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u);
+                    else wait(&ms.p_empty[0], (uint32_t)(i - 1) & 1u);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
+                        for (int rb = 0; rb < p.R; rb += 16) {
+                            const uint32_t ta = tmem + t_lane + L::col_o(cp, hh) + rb;
+                            float v[16];
+                            tmem_ld16(ta, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) v[jj] *= ms.red_fac[rb + jj] * fs;
+                            tmem_st16(ta, v);
+                        }
+                    }
+                    tmem_wait_st();
+                }
             }
-            named_bar(kBarSoft, kSoftThreads);
-            const float inv_sig = 1.f / ms.st_sig[par];
-            const bool resc = ms.st_any[par] == i;
             const int pbi = i % PB;
             if (i >= PB) wait(&ms.p_empty[pbi], (uint32_t)((i - PB) / PB) & 1u);
             uint8_t *p_tile = smem + L::pb + (size_t)pbi * N * 256;
-            // ---- pass 2: P' = f16(p * v_scale / sigma) into the B operand of
-            // the P.V MMA (K-major [rows][cells]), and row sums
-            float lrow[2 * KR], mref_r[2 * KR];
-#pragma unroll
-            for (int k = 0; k < KR; ++k) {
-                // reference maxima of this thread's rows, read once (the P'
-                // stores below could otherwise force re-reads)
-                const float2 m2 = *reinterpret_cast<const float2 *>(&ms.st_mref[par][8 * k + 2 * u]);
-                // (a row with no valid cell yet has mref = -inf: use 0, so its
-                // masked scores give 2^-inf = 0 rather than NaN)
-                mref_r[2 * k] = m2.x == -INFINITY ? 0.f : m2.x;
-                mref_r[2 * k + 1] = m2.y == -INFINITY ? 0.f : m2.y;
-                lrow[2 * k] = lrow[2 * k + 1] = 0.f;
-            }
+            // ---- P' = f16(p * v_scale / sigma) into the B operand of the P.V
+            // MMA (K-major [rows][cells]); this thread's share of the row sums
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int cc = 32 * q + 8 * ci + ra;
                 const float vsn = vsc[ci] * inv_sig; // 0 for a masked cell
-                const int L = ci >> 1, B = ci & 1;
+                const int L2 = ci >> 1, B = ci & 1;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     // element (row 8k + 2u + e, cell cc) at pe + 1024k
@@ -972,40 +1035,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     uint8_t *pe = p_tile + (cc >> 6) * N * 128 + r7 * 128 + ((((cc & 63) >> 3) ^ r7) << 4) + (cc & 7) * 2;
 #pragma unroll
                     for (int k = 0; k < KR; ++k) {
-                        const float pr = fast_exp2(x[L][4 * k + 2 * B + e] - mref_r[2 * k + e]); // 0 if masked
-                        lrow[2 * k + e] += pr;
+                        const float pr = fast_exp2(x[L2][4 * k + 2 * B + e] - mref[2 * k + e]); // 0 if masked
+                        lsum[2 * k + e] += pr;
                         *reinterpret_cast<__half *>(pe + 1024 * k) = __float2half_rn(pr * vsn);
                     }
                 }
-            }
-#pragma unroll
-            for (int o = 4; o <= 16; o <<= 1) {
-#pragma unroll
-                for (int jr = 0; jr < 2 * KR; ++jr)
-                    lrow[jr] += __shfl_xor_sync(0xffffffffu, lrow[jr], o);
-            }
-#pragma unroll
-            for (int k = 0; k < KR; ++k)
-                if (ra == (k & 7)) *reinterpret_cast<float2 *>(&ms.red_sum[par][q][8 * k + 2 * u]) = make_float2(lrow[2 * k], lrow[2 * k + 1]);
-            // ---- lazy rescale of the chunk's O (rows whose max moved, or sigma)
-            if (resc) {
-                if (PB == 2) wait(&ms.p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u); // P.V of tile i-1 done
-                tc_fence_after();
-                const float fs = ms.st_fs[par];
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll 1
-                    for (int r0 = 0; r0 < p.R; r0 += 16) {
-                        const uint32_t ta = tmem + t_lane + L::col_o(cp, hh) + r0;
-                        float v[16];
-                        tmem_ld16(ta, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) v[jj] *= ms.st_fac[r0 + jj] * fs;
-                        tmem_st16(ta, v);
-                    }
-                }
-                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1014,110 +1048,121 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 epilogue(pend);
                 pend.on = false;
             }
-            if (last_t) pend = Pend{it.cur.b, it.cur.g, it.cur.c, cp, par, true};
+            if (last_t) {
+                chunk_end(cp, it.cur.b, it.cur.g, it.cur.c);
+                pend = Pend{it.cur.b, it.cur.g, it.cur.c, cp, true};
+            }
             tile_next(p, it);
         }
         if (pend.on) {
-            named_bar(kBarSoft, kSoftThreads);
-            if (orow < p.R) {
-                const int c = orow;
-                l_own += ((ms.red_sum[pend.par][0][c] + ms.red_sum[pend.par][1][c]) + ms.red_sum[pend.par][2][c]) +
-                         ms.red_sum[pend.par][3][c];
-                const float mo = ms.st_mrun[pend.par][c], mref = ms.st_mref[pend.par][c];
-                const float fin = mo > -INFINITY ? fast_exp2(mref - mo) : 0.f;
-                l_fin = l_own * fin;
-                ms.st_fin[c] = fin * ms.st_sig[pend.par];
-            }
-            named_bar(kBarSoft, kSoftThreads);
+            named_bar(kBarSoft, kSoftThreads); // the owners' factors are written
             epilogue(pend);
         }
     } else if (w == kMmaWarp) {
         // ================================================================ S warp
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
-            TileIt it;
-            tile_init(p, it, first);
-            // query tiles: one bulk copy per segment into buffer seg % QB.  With
-            // two buffers, the first two now and segment s + 1 once segment s
-            // has started (its buffer was segment s - 1's, free after that
-            // segment's last QK); with one, segment s + 1 after segment s ends.
-            constexpr int QB = L::QB;
-            auto load_q = [&](const Cursor &sc, int seg) {
-                const uint32_t bytes = (uint32_t)N * 512u;
+        // All 32 lanes run the loop (so every value is warp-uniform); one
+        // elected lane issues the MMAs, commits and query copies.
+        const bool leader = elect_one();
+        const uint32_t idesc_s = idesc_f16(128, N, false, false, false, false);
+        TileIt it;
+        tile_init(p, it, first);
+        // query tiles: one bulk copy per segment into buffer seg % QB.  With
+        // two buffers, the first two now and segment s + 1 once segment s
+        // has started (its buffer was segment s - 1's, free after that
+        // segment's last QK); with one, segment s + 1 after segment s ends.
+        constexpr int QB = L::QB;
+        int q_issued[2] = {0, 0}; // bulk copies issued into each buffer
+        auto load_q = [&](const Cursor &sc, int seg) {
+            const uint32_t bytes = (uint32_t)N * 512u;
+            if (leader) {
                 mbar_arrive_expect_tx(&ms.q_full[seg % QB], bytes);
                 bulk_g2s(smem + L::q + (size_t)(seg % QB) * N * 512,
                          static_cast<const uint8_t *>(p.q_img) + ((size_t)sc.b * p.G + sc.g) * N * 512, bytes,
                          &ms.q_full[seg % QB]);
-            };
-            Cursor qnext = first;
-            int qseg = 0; // next segment whose tile is to be loaded
-            if (it.valid && !p.q_inline) {
-                cudaGridDependencySynchronize(); // the tiles come from the staging kernel
-                for (; qseg < QB && qnext.remaining > 0; ++qseg) {
-                    load_q(qnext, qseg);
-                    qnext = next_segment(p, qnext);
-                }
             }
-            int cur_seg = -1;
-            for (int i = 0; it.valid; ++i) {
-                const int seg = it.seg;
-                const bool seg_start = seg != cur_seg;
-                if (seg_start) wait(&ms.q_full[seg % QB], (uint32_t)(seg / QB) & 1u);
-                cur_seg = seg;
-                wait(&ms.k_full, (uint32_t)i & 1u);
-                if (i >= 2) wait(&ms.s_empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u);
-                tc_fence_after();
-                const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg % QB) * N * 512u, 16, 1024);
-                const uint32_t sd = tmem + L::col_s(i & 1);
+            ++q_issued[seg % QB];
+        };
+        Cursor qnext = first;
+        int qseg = 0; // next segment whose tile is to be loaded
+        if (it.valid && !p.q_inline) {
+            cudaGridDependencySynchronize(); // the tiles come from the staging kernel
+            for (; qseg < QB && qnext.remaining > 0; ++qseg) {
+                load_q(qnext, qseg);
+                qnext = next_segment(p, qnext);
+            }
+        }
+        int cur_seg = -1;
+        for (int i = 0; it.valid; ++i) {
+            const int seg = it.seg;
+            const bool seg_start = seg != cur_seg;
+            if (seg_start) wait(&ms.q_full[seg % QB], (uint32_t)(seg / QB) & 1u);
+            cur_seg = seg;
+            const int kb = i % L::KB;
+            wait(&ms.k_full[kb], (uint32_t)(i / L::KB) & 1u);
+            if (i >= 2) wait(&ms.s_empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u);
+            tc_fence_after();
+            const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg % QB) * N * 512u, 16, 1024);
+            const uint32_t sd = tmem + L::col_s(i & 1);
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint64_t bd = qd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
-                    mma_f16_ts(sd, tmem + kColK + 8u * kk, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_f16_ts(sd, tmem + L::col_k(kb) + 8u * kk, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&ms.k_empty);
+                mma_commit(&ms.k_empty[kb]);
                 mma_commit(&ms.s_full[i & 1]);
-                tile_next(p, it);
-                const bool seg_end = !it.valid || it.seg != seg;
-                if (seg_end) mma_commit(&ms.q_empty[seg % QB]);
-                if (QB == 2 && seg_start && seg >= 1 && qnext.remaining > 0) {
-                    wait(&ms.q_empty[(seg - 1) & 1], (uint32_t)((seg - 1) >> 1) & 1u);
-                    load_q(qnext, qseg);
-                    ++qseg;
-                    qnext = next_segment(p, qnext);
-                }
-                if (QB == 1 && seg_end && qnext.remaining > 0) {
-                    wait(&ms.q_empty[0], (uint32_t)seg & 1u);
-                    load_q(qnext, qseg);
-                    ++qseg;
-                    qnext = next_segment(p, qnext);
-                }
             }
-            mma_commit(&ms.done);
-            wait(&ms.done, 0);
+            __syncwarp();
+            tile_next(p, it);
+            const bool seg_end = !it.valid || it.seg != seg;
+            if (seg_end && leader) mma_commit(&ms.q_empty[seg % QB]);
+            if (QB == 2 && seg_start && seg >= 1 && qnext.remaining > 0) {
+                wait(&ms.q_empty[(seg - 1) & 1], (uint32_t)((seg - 1) >> 1) & 1u);
+                load_q(qnext, qseg);
+                ++qseg;
+                qnext = next_segment(p, qnext);
+            }
+            if (QB == 1 && seg_end && qnext.remaining > 0) {
+                wait(&ms.q_empty[0], (uint32_t)seg & 1u);
+                load_q(qnext, qseg);
+                ++qseg;
+                qnext = next_segment(p, qnext);
+            }
         }
+        // before the CTA leaves (also after a time-out): every MMA of this
+        // warp complete, every query copy landed.  The k-th copy into a
+        // buffer completes phase k - 1 of its barrier, which nothing else
+        // arrives on.
+        if (leader) mma_commit(&ms.s_done);
         __syncwarp();
+        mbar_wait(&ms.s_done, 0, kDrainCycles);
+        if (!p.q_inline)
+            for (int bq = 0; bq < QB; ++bq)
+                if (q_issued[bq] > 0) mbar_wait(&ms.q_full[bq], (uint32_t)(q_issued[bq] - 1) & 1u, kDrainCycles);
     } else {
         // ================================================================ P.V warp
-        // A second issuing thread: one thread issues a tcgen05.mma every ~50-70
+        // A second issuing warp: one thread issues a tcgen05.mma every ~50-70
         // cycles on this GPU, so S of the next tile and P.V of the current one
-        // go out from two warps side by side.
-        if (lane == 0) {
-            const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
-            TileIt it;
-            tile_init(p, it, first);
-            int cp = -1;
-            for (int i = 0; it.valid; ++i) {
-                const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
-                if (first_t) ++cp;
-                wait(&ms.p_full[i % PB], (uint32_t)(i / PB) & 1u);
-                wait(&ms.v_full[i & 1], (uint32_t)(i >> 1) & 1u);
-                if (first_t && cp >= L::OB) wait(&ms.o_empty[cp % L::OB], (uint32_t)((cp - L::OB) / L::OB) & 1u);
-                tc_fence_after();
-                // descriptors built once; a K step only moves the start address
-                // (field [0,14) in 16-byte units, no carry for shared addresses)
-                const uint64_t ad0 = smem_desc(s_v + (uint32_t)(i & 1) * kStageBytes, 16384, 1024);
-                const uint64_t bd0 = smem_desc(s_p + (uint32_t)(i % PB) * N * 256u, 16, 1024);
-                const uint32_t d0 = tmem + L::col_o(cp, 0);
+        // go out from two warps side by side.  All lanes run the loop; one
+        // elected lane issues.
+        const bool leader = elect_one();
+        const uint32_t idesc_o = idesc_f16(128, N, false, false, true, false);
+        TileIt it;
+        tile_init(p, it, first);
+        int cp = -1;
+        for (int i = 0; it.valid; ++i) {
+            const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
+            if (first_t) ++cp;
+            wait(&ms.p_full[i % PB], (uint32_t)(i / PB) & 1u);
+            wait(&ms.v_full[i & 1], (uint32_t)(i >> 1) & 1u);
+            if (first_t && cp >= L::OB) wait(&ms.o_empty[cp % L::OB], (uint32_t)((cp - L::OB) / L::OB) & 1u);
+            tc_fence_after();
+            // descriptors built once; a K step only moves the start address
+            // (field [0,14) in 16-byte units, no carry for shared addresses)
+            const uint64_t ad0 = smem_desc(s_v + (uint32_t)(i & 1) * kStageBytes, 16384, 1024);
+            const uint64_t bd0 = smem_desc(s_p + (uint32_t)(i % PB) * N * 256u, 16, 1024);
+            const uint32_t d0 = tmem + L::col_o(cp, 0);
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk) {
                     // the two d halves interleaved: independent accumulators
@@ -1131,12 +1176,13 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 mma_commit(&ms.v_empty[i & 1]);
                 mma_commit(&ms.p_empty[i % PB]);
                 if (last_t) mma_commit(&ms.o_full[cp % L::OB]);
-                tile_next(p, it);
             }
-            mma_commit(&ms.done);
-            wait(&ms.done, 0);
+            __syncwarp();
+            tile_next(p, it);
         }
+        if (leader) mma_commit(&ms.pv_done);
         __syncwarp();
+        mbar_wait(&ms.pv_done, 0, kDrainCycles);
     }
     tc_fence_before();
     __syncthreads();

@@ -49,6 +49,7 @@ struct Params {
     int32_t pool_pages;        // pool_cells / P: valid page entries are 0 .. pool_pages - 1
     int32_t q_bf16;
     float scale_log2;          // softmax_scale * log2(e)
+    long long wait_cycles;     // bound of a device-side wait, SM clock cycles
 };
 
 // Tensor-core-ready operand images of the prompt-shaped path (workspace).

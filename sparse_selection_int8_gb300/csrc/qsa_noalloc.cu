@@ -11,10 +11,13 @@
 // library, until the process exits.
 //
 // The array's name is only a host-side stand-in in host code, so the device
-// address is obtained once per device with cudaGetSymbolAddress, with that
-// device current, on the first call made on that device.  That first call
-// should therefore happen before any stream capture.  Later calls only read
-// the cached address.
+// address is looked up with cudaGetSymbolAddress, with the device current.  A
+// symbol's address belongs to the CUDA context it was loaded into, so a call
+// on a stream that is not being captured looks it up again (a cheap call that
+// allocates nothing) and refreshes the per-device copy; a call made while its
+// stream is being captured into a CUDA graph uses that copy, so the first
+// call on each device, and the first after a cudaDeviceReset or a switch of
+// context, must happen outside capture.
 //
 // Every call shares the one array and leaves its contents behind; the chunk
 // kernels write every partial the merge reads, so nothing needs clearing.
@@ -35,18 +38,24 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices];
 
-// Device address of the scratch array on the current device (cached).
-qsa_status scratch_address(void **addr)
+// Device address of the scratch array on the current device: looked up
+// afresh unless the stream is being captured, when the copy from the last
+// lookup on this device is used.
+qsa_status scratch_address(cudaStream_t stream, void **addr)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return QSA_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return QSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
             return QSA_ERR_CUDA;
         g_scratch_addr[dev] = p;
+    } else if (g_scratch_addr[dev] == nullptr) {
+        return QSA_ERR_CUDA; // first call on this device inside a capture
     }
     *addr = g_scratch_addr[dev];
     return QSA_OK;
@@ -68,7 +77,7 @@ extern "C" qsa_status qsa_decode_attn_step_noalloc(const qsa_shape *shape, const
     if (st != QSA_OK) return st;
     if (need > qsa::kNoAllocScratchBytes) return QSA_ERR_WORKSPACE;
     void *scratch = nullptr;
-    st = qsa::scratch_address(&scratch);
+    st = qsa::scratch_address(static_cast<cudaStream_t>(stream), &scratch);
     if (st != QSA_OK) return st;
     return qsa_decode_attn_step(shape, q, k_pool, v_pool, k_scale, v_scale, page_table, sel,
                                 n_sel, out, scratch, qsa::kNoAllocScratchBytes, status, stream);

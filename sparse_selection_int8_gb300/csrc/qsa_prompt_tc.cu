@@ -173,6 +173,7 @@ constexpr int kLoadWarp = kMmaWarp + 1;       // 9: bulk copies of Q, K and the 
 constexpr int kVLoadWarp = kLoadWarp + 1;     // 10: bulk copies of V (one thread)
 constexpr int kThreads = kSoftThreads + 96;   // 352
 constexpr uint32_t kBarSoft = 1;              // named barrier of the softmax warps
+constexpr long long kDrainCycles = 1ll << 30; // bound of the waits before the CTA leaves
 
 // (Shared memory holds the Q, K and V tiles and this.)
 struct PromptSmem {
@@ -180,7 +181,7 @@ struct PromptSmem {
     float bias[kTile];          // 0 or -inf (masked cell)
     int32_t pos[kTile];         // the cells' logical positions (calls with causal limits)
     float rowmax[2][kTile];     // [column half][row]; the rows' sums at the end
-    uint64_t bar_q, k_full, k_empty, v_full, o_done, p_full, c_full;
+    uint64_t bar_q, k_full, k_empty, v_full, o_done, p_full, c_full, mma_done;
     uint64_t s_full[2], s_empty[2];
     uint32_t tmem;
     int32_t abort;
@@ -190,7 +191,7 @@ static_assert(sizeof(PromptSmem) <= 3072, "shared memory of the prompt kernel");
 __device__ __forceinline__ bool wait_bar(const Params &p, PromptSmem &ms, uint64_t *bar, uint32_t parity)
 {
     if (ms.abort) return false;
-    if (!mbar_wait(bar, parity)) {
+    if (!mbar_wait(bar, parity, p.wait_cycles)) {
         atomicExch(&ms.abort, 1);
         raise_status(p, QSA_STATUS_TIMEOUT);
         return false;
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
     // starts there.  The check keeps a misplaced window from being used.
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {
-        if (threadIdx.x == 0) raise_status(p, QSA_STATUS_TIMEOUT);
+        if (threadIdx.x == 0) raise_status(p, QSA_STATUS_LAUNCH);
         return;
     }
     const uint32_t s_q = smem_u32(smem), s_k = s_q + kTileBytes, s_v = s_k + kTileBytes;
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
         mbar_init(&ms.o_done, 1);
         mbar_init(&ms.p_full, kSoftThreads);
         mbar_init(&ms.c_full, 1);
+        mbar_init(&ms.mma_done, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.s_empty[i], kSoftThreads);
@@ -294,11 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 load_c(j + 1);
                 ++nc;
             }
-            if (ms.abort) {
-                // copies still in flight after a timeout must land before exit
-                mbar_wait(&ms.k_full, (uint32_t)(nk - 1) & 1u, 1ll << 26);
-                mbar_wait(&ms.c_full, (uint32_t)(nc - 1) & 1u, 1ll << 26);
-            }
+            // before the CTA leaves (also after a time-out): every copy of
+            // this thread landed.  The k-th copy on a barrier completes its
+            // phase k - 1, and nothing else arrives on these barriers.
+            mbar_wait(&ms.bar_q, 0, kDrainCycles);
+            mbar_wait(&ms.k_full, (uint32_t)(nk - 1) & 1u, kDrainCycles);
+            mbar_wait(&ms.c_full, (uint32_t)(nc - 1) & 1u, kDrainCycles);
         }
         __syncwarp();
     } else if (w == kVLoadWarp) {
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 load_v(j + 1);
                 ++nv;
             }
-            if (ms.abort) mbar_wait(&ms.v_full, (uint32_t)(nv - 1) & 1u, 1ll << 26);
+            mbar_wait(&ms.v_full, (uint32_t)(nv - 1) & 1u, kDrainCycles); // every copy landed
         }
         __syncwarp();
     } else if (w == kMmaWarp) {
@@ -357,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_prompt_tc_kernel(const Params
                 }
                 mma_commit(&ms.o_done);
             }
+            // before the CTA leaves (also after a time-out): every MMA of this
+            // thread complete, so tensor memory is idle when it is freed
+            mma_commit(&ms.mma_done);
+            mbar_wait(&ms.mma_done, 0, kDrainCycles);
         }
         __syncwarp();
     } else {

@@ -56,14 +56,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, ui
     return ok != 0;
 }
 
-// Bounded wait on phase `parity`: false once about `max_cycles` SM clock
-// cycles (default 2^32, about two seconds) have passed without completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          long long max_cycles = (1ll << 32))
+// Non-blocking test for completion of phase `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n"
+                 " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 " selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Default bound of a device-side wait: 2^32 SM clock cycles, about two
+// seconds at 2 GHz.
+constexpr long long kWaitCycles = 1ll << 32;
+
+// Bounded wait on phase `parity`: false once about `max_cycles` SM clock
+// cycles have passed without completion.  Long bounds suspend the waiting
+// thread between tests; short ones (below 2^24 cycles, used to exercise the
+// time-out path) poll without suspending, so the bound holds from the first
+// test on.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          long long max_cycles = kWaitCycles)
+{
+    if (max_cycles >= (1ll << 24)) {
+        if (mbar_try_wait(bar, parity, 20000u)) return true;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, parity, 200000u))
+            if (clock64() - t0 > max_cycles) return false;
+        return true;
+    }
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity, 200000u))
+    while (!mbar_test_wait(bar, parity))
         if (clock64() - t0 > max_cycles) return false;
     return true;
 }
@@ -295,10 +321,33 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // ------------------------------------------------------------- misc
 
+// True in exactly one lane of a converged warp (the lane that issues a
+// single-thread operation such as tcgen05.mma while the others follow).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t r;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(r));
+    return r != 0;
+}
+
 // Named barrier `id` over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier `id` over `count` threads that also ORs a predicate over
+// them: every participant gets true if any passed true.  Orders memory like
+// bar.sync.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool v)
+{
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n"
+                 " barrier.cta.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r)
+                 : "r"(id), "r"(count), "r"(v ? 1u : 0u)
+                 : "memory");
+    return r != 0;
 }
 
 // 16-byte asynchronous copy global -> shared (L2 only), no registers held.
@@ -337,6 +386,17 @@ __device__ __forceinline__ void ldg256_stream(const void *ptr, uint32_t *r)
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                    "=r"(r[6]), "=r"(r[7])
                  : "l"(ptr));
+}
+
+// The same load, predicated: when `on` is false nothing is read and the
+// registers keep their values.
+__device__ __forceinline__ void ldg256_stream_if(const void *ptr, uint32_t *r, bool on)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %9, 0;\n"
+                 " @p ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n}"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7])
+                 : "l"(ptr), "r"(on ? 1u : 0u));
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr)

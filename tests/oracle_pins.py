@@ -50,7 +50,9 @@ def load_golden(name):
     return {
         "D": int(fields["head_dim"]),
         "scale": float(fields["softmax_scale"]),
-        "q": np.array(nums(fields["q"]), dtype=np.float64),
+        "q": np.array(nums(fields["q"]), dtype=np.float64) if "q" in fields else None,
+        "q_bf16_bits": (np.array([int(x, 16) for x in fields["q_bf16_bits"].split()], dtype=np.uint16)
+                        if "q_bf16_bits" in fields else None),
         "page_table": np.array(nums(fields["page_table"], int), dtype=np.int32),
         "sel": np.array(nums(fields["sel"], int), dtype=np.int32),
         "k_codes": mat(fields["k_codes"], int).astype(np.int8),
@@ -136,6 +138,25 @@ def pin_golden_paged_mean(lib):
     g = load_golden("paged_mean.txt")
     out = oracle.attend_row(g["q"], g["k_codes"], g["v_codes"], g["k_scale"], g["v_scale"],
                             g["page_table"], g["sel"], g["scale"], lib=lib, page_cells=g["page_cells"])
+    assert np.abs(out - g["expected"]).max() <= g["tol"] + 1e-15, (out, g["expected"])
+
+
+def pin_golden_bf16_queries(lib, ora=oracle):
+    """bf16 query bit patterns go through the whole-call driver, whose
+    widening turns them into the exact values the hand-worked case uses.
+    ``ora`` is the oracle module (a test passes altered copies of it)."""
+    from types import SimpleNamespace
+    g = load_golden("bf16_queries.txt")
+    n_pool, D = g["k_codes"].shape
+    p = SimpleNamespace(
+        n_seq=1, n_kv_heads=1, q_per_kv=1, head_dim=D, n_queries=1, pool_cells=n_pool,
+        page_table_len=g["page_table"].shape[0], page_cells=1, softmax_scale=g["scale"],
+        q_dtype="bf16", q=g["q_bf16_bits"].reshape(1, 1, 1, D),
+        k_pool=g["k_codes"].reshape(1, 1, n_pool, D), v_pool=g["v_codes"].reshape(1, 1, n_pool, D),
+        k_scale=g["k_scale"].reshape(1, 1, n_pool), v_scale=g["v_scale"].reshape(1, 1, n_pool),
+        page_table=g["page_table"].reshape(1, -1), sel=g["sel"],
+        sel_offsets=np.array([0, g["sel"].shape[0]], np.int64), q_limit=None)
+    out = ora.decode_attn(p, lib=lib).reshape(D)
     assert np.abs(out - g["expected"]).max() <= g["tol"] + 1e-15, (out, g["expected"])
 
 
@@ -480,6 +501,7 @@ PINS = [
     pin_golden_masked_mean,
     pin_golden_dominant_cell,
     pin_golden_paged_mean,
+    pin_golden_bf16_queries,
     pin_page_relabelling,
     pin_one_page_is_the_pool,
     pin_golden_causal_window,

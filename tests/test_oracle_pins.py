@@ -88,3 +88,52 @@ def test_planted_mistake_is_caught(name, old, new):
         assert failed, f"no pin catches the planted mistake {name}"
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
+
+
+# Planted mistakes in the oracle's Python wrapper: the exact widening of bf16
+# query bit patterns (the prompt-shaped configuration's queries).  Each edit
+# is applied to a copy of oracle/__init__.py loaded as a separate module; the
+# C library stays the correct one.
+ORACLE_PY = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
+WIDEN_ANCHOR = "(np.asarray(q, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)"
+PY_MUTANTS = [
+    ("bf16_shift_by_8", WIDEN_ANCHOR,
+     "(np.asarray(q, dtype=np.uint16).astype(np.uint32) << np.uint32(8)).view(np.float32)"),
+    ("bf16_read_as_fp16", WIDEN_ANCHOR,
+     "np.asarray(q, dtype=np.uint16).view(np.float16).astype(np.float32)"),
+    ("bf16_low_mantissa_bit_dropped", WIDEN_ANCHOR,
+     "((np.asarray(q, dtype=np.uint16).astype(np.uint32) & np.uint32(0xFFFE)) << np.uint32(16)).view(np.float32)"),
+    ("bf16_sign_dropped", WIDEN_ANCHOR,
+     "((np.asarray(q, dtype=np.uint16).astype(np.uint32) & np.uint32(0x7FFF)) << np.uint32(16)).view(np.float32)"),
+]
+
+
+def _load_module_from_source(src: str, name: str):
+    import importlib.util
+    import sys
+    tmp = tempfile.mkdtemp(prefix="oracle_pymutant_")
+    path = os.path.join(tmp, "__init__.py")
+    with open(path, "w") as f:
+        f.write(src)
+    spec = importlib.util.spec_from_file_location(name, path)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[name] = mod
+    spec.loader.exec_module(mod)
+    return mod, tmp
+
+
+def test_widening_anchor_is_unique():
+    assert open(ORACLE_PY).read().count(WIDEN_ANCHOR) == 1
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_planted_widening_mistake_is_caught(name, old, new, oracle_lib):
+    from oracle_pins import pin_golden_bf16_queries
+    src = open(ORACLE_PY).read()
+    assert src.count(old) == 1
+    mod, tmp = _load_module_from_source(src.replace(old, new), f"oracle_mutant_{name}")
+    try:
+        with pytest.raises(AssertionError):
+            pin_golden_bf16_queries(oracle_lib, ora=mod)
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
