@@ -127,8 +127,8 @@ struct Lay {
     // halves x N columns.  Two K buffers let the loaders write the K codes of
     // tile i+1 while the MMAs of tile i read tile i's; two O buffers let a
     // chunk's epilogue overlap the next chunk's first P.V.  Up to 32 rows
-    // both fit; 48 and 64 rows keep two K buffers and one O; 80 rows one K
-    // and one O.
+    // both fit; 48 and 64 rows keep two K buffers and one O (at 48 rows this
+    // measured the same as one K and two O); 80 rows one K and one O.
     static constexpr int KB = N <= 64 ? 2 : 1;
     static constexpr int OB = N <= 32 ? 2 : 1;
     static constexpr uint32_t SW = (uint32_t)N;
@@ -586,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         // the rows of tile j+1 are loaded into registers; tile j is converted.
         // tile info per stage: bg = b * G + g, mt = cells of the tile (0 = none)
         int bg1 = 0, bg2 = 0, bg3 = 0, bg4 = 0, bg5 = 0, bg6 = 0;
+        int sq4 = 0, sq5 = 0, sq6 = 0; // sequence of the tile at stages 4-6 (its page-table row)
         int mt0 = 0, mt1 = 0, mt2 = 0, mt3 = 0, mt4 = 0, mt5 = 0, mt6 = 0;
         // slots (-1: masked) of the K cells A, B and the V cells A', B' at stages 1 and 2
         int kA1 = -1, kB1 = -1, vA1 = -1, vB1 = -1, kA2 = -1, kB2 = -1, vA2 = -1, vB2 = -1;
@@ -674,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             if (head.valid) {
                 const int nc = tile_cells(head);
                 bg6 = head.cur.b * p.G + head.cur.g;
+                sq6 = head.cur.b;
                 mt6 = nc;
                 if (res && cr < nc) cp_async4(smem_u32(&ms.rs_sel[(j + 6) & 3][cr]), p.sel + tile_base(p, head) + cr);
                 tile_next(p, head);
@@ -687,12 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 } else {
                     // position pos: page pos / P, offset pos % P (P = 1: the entry is the slot)
                     const int pos = ms.rs_sel[e4][cr], P = p.page_cells;
-                    const int32_t *prow = p.page_table + (size_t)(bg4 / p.G) * p.page_table_len;
+                    const int32_t *prow = p.page_table + (size_t)sq4 * p.page_table_len;
                     if (LIM && pos >= 0) {
                         // rows t*H.. of the queries whose limit is above pos see the
                         // cell: with limits non-decreasing in t, those are the rows
                         // from H * #{t : limit[t] <= pos} on
-                        const int32_t *lim = p.q_limit + (size_t)(bg4 / p.G) * p.T;
+                        const int32_t *lim = p.q_limit + (size_t)sq4 * p.T;
                         int below = 0;
                         for (int t = 0; t < p.T; ++t) below += __ldg(lim + t) <= pos;
                         ms.rs_r0[e4][cr] = (uint8_t)(below * p.H); // <= T * H <= 80
@@ -739,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             cp_async_commit();
             // shift the pipeline by one tile
             bg1 = bg2; bg2 = bg3; bg3 = bg4; bg4 = bg5; bg5 = bg6;
+            sq4 = sq5; sq5 = sq6;
             mt0 = mt1; mt1 = mt2; mt2 = mt3; mt3 = mt4; mt4 = mt5; mt5 = mt6;
             kA1 = kA2; kB1 = kB2; vA1 = vA2; vB1 = vB2;
         }
