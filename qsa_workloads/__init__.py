@@ -382,3 +382,77 @@ def prompt_append(seed_offset: int = 0) -> AppendProblem:
     sequence with 2 KV heads (the rows of a 32,768-token prefill)."""
     return make_append(n_seq=1, n_kv_heads=2, n_new=32768, pool_cells=32768,
                        seed=SEED_BASE + 17 + seed_offset, name="append_prompt")
+
+
+# ---------------------------------------------------------------- selection
+
+@dataclass
+class SelectProblem:
+    """One block-selection call (the QSA selection scorer and its top-k).
+
+    ``q_idx``   f32 ``[B][T][idx_heads * idx_dim]``: the window's indexer queries
+    ``pooled``  bf16 bit patterns ``[B][max_blocks][idx_heads * idx_dim]``: one
+                pooled indexer key per block of ``block_cells`` positions
+    ``n_live``  int32 ``[B]``: live positions per sequence
+    ``steps``   int32 ``[B][T]``: each query's position, or None
+    """
+
+    n_seq: int
+    n_queries: int
+    idx_heads: int
+    idx_dim: int
+    block_cells: int
+    max_blocks: int
+    top_k: int
+    q_idx: np.ndarray
+    pooled: np.ndarray
+    n_live: np.ndarray
+    steps: Optional[np.ndarray]
+    name: str = ""
+
+
+def make_selection(*, n_seq: int = 1, n_queries: int = 2, idx_heads: int = 4, idx_dim: int = 64,
+                   block_cells: int = 64, max_blocks: int = 256, top_k: int = 16,
+                   n_live: Sequence[int] | int | None = None, with_steps: bool = True,
+                   integer: bool = False, seed: int = SEED_BASE + 40, name: str = "") -> SelectProblem:
+    """Draw one seeded selection problem.
+
+    Pooled keys and queries are N(0,1) (keys rounded to bf16), or, with
+    ``integer``, whole numbers in [-8, 8] (every score is then an integer
+    below 2^24, exact in any summation order).  ``n_live`` defaults to the
+    full capacity; the window's queries sit at the last positions
+    (steps[b][t] = n_live[b] - T + t) when ``with_steps``.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    F = idx_heads * idx_dim
+    cap = max_blocks * block_cells
+    if n_live is None:
+        lives = [cap] * n_seq
+    elif isinstance(n_live, (int, np.integer)):
+        lives = [int(n_live)] * n_seq
+    else:
+        lives = [int(v) for v in n_live]
+    assert len(lives) == n_seq and all(0 <= v <= cap for v in lives)
+    if integer:
+        pooled_f = rng.integers(-8, 9, (n_seq, max_blocks, F)).astype(np.float32)
+        q_idx = rng.integers(-8, 9, (n_seq, n_queries, F)).astype(np.float32)
+    else:
+        pooled_f = rng.standard_normal((n_seq, max_blocks, F)).astype(np.float32)
+        q_idx = rng.standard_normal((n_seq, n_queries, F)).astype(np.float32)
+    steps = None
+    if with_steps:
+        steps = np.array([[max(v - n_queries + t, 0) for t in range(n_queries)] for v in lives], dtype=np.int32)
+    return SelectProblem(n_seq=n_seq, n_queries=n_queries, idx_heads=idx_heads, idx_dim=idx_dim,
+                         block_cells=block_cells, max_blocks=max_blocks, top_k=top_k, q_idx=q_idx,
+                         pooled=bf16_bits_from_f32(pooled_f), n_live=np.array(lives, dtype=np.int32),
+                         steps=steps, name=name)
+
+
+def long_selection(seed_offset: int = 0) -> SelectProblem:
+    """Selection in front of the long-context shape: 8 sequences of 131,072
+    live positions in blocks of 64 (2,048 pooled keys of 4 x 64 indexer
+    values each), 2 queries, 128 blocks kept per query: 8,192-16,384 cells
+    per sequence, the long-context configuration's selection size."""
+    return make_selection(n_seq=8, n_queries=2, idx_heads=4, idx_dim=64, block_cells=64,
+                          max_blocks=2048, top_k=128, seed=SEED_BASE + 41 + seed_offset,
+                          name="long_selection")
