@@ -92,6 +92,7 @@ typedef enum qsa_algo {
 #define QSA_STATUS_NOT_RESIDENT 0x10u /* qsa_kv_append: a position whose page entry is -1 */
 #define QSA_STATUS_BAD_LIMITS 0x20u  /* causal limits that decrease along a window */
 #define QSA_STATUS_LAUNCH 0x40u      /* a kernel's shared-memory window was misplaced: outputs invalid */
+#define QSA_STATUS_BAD_EXTENT 0x80u  /* qsa_select_blocks: a live extent outside [0, max_blocks * R] (clamped) */
 
 typedef struct qsa_shape {
     int32_t n_kv_heads;     /* G: KV heads per sequence (>= 1) */
@@ -277,6 +278,70 @@ qsa_status qsa_kv_append(const qsa_shape *shape, int32_t n_seq, int32_t n_new, i
                          const void *k_new, const void *v_new, const int32_t *positions,
                          const int32_t *page_table, int8_t *k_pool, int8_t *v_pool,
                          float *k_scale, float *v_scale, uint32_t *status, void *stream);
+
+/*
+ * QSA block selection: the scorer over pooled indexer keys and its top-k,
+ * which produce the selected-cell list a qsa_decode_attn_batch call reads.
+ * The step is the QSA selection scorer of "Strata issue #8, round 9:
+ * performance candidate set on v0.2.9" (R9-gpu-9: qsa_block_scores_rows over
+ * pooled keys, a dead tail, per-query indexer vectors and steps) and its
+ * top-k (the long-context select and TOPK_SPLIT on the same page).  The pages
+ * print no formula; this library's reading:
+ *   - block j of a sequence covers positions [j*R, (j+1)*R) and has one
+ *     pooled key of F = idx_heads * idx_dim values; it is live while
+ *     j*R < n_live, and a candidate for query t if also j*R <= steps[t];
+ *   - score s[t][j] = sum over f of q_idx[t][f] * pooled[j][f] (fp32
+ *     accumulation), -inf for a block that is not a candidate;
+ *   - query t keeps its top_k candidates by score, equal scores going to the
+ *     lower block id (all candidates if there are fewer);
+ *   - the sequence's list is the union of its queries' kept blocks, expanded
+ *     to their live positions in ascending order.
+ */
+typedef struct qsa_select_shape {
+    int32_t n_queries;   /* T: queries of the window (1..8) */
+    int32_t idx_heads;   /* indexer heads */
+    int32_t idx_dim;     /* values per indexer head; F = idx_heads * idx_dim is
+                            a multiple of 8 and at most 1024 */
+    int32_t block_cells; /* R: positions per block (>= 1) */
+    int32_t max_blocks;  /* pooled keys per sequence (1..16384); capacity
+                            max_blocks * R positions */
+    int32_t top_k;       /* blocks kept per query (1..max_blocks) */
+} qsa_select_shape;
+
+/* Workspace of a qsa_select_blocks call on n_seq sequences (block bitmaps and
+ * counts; 256-byte aligned base, no initialisation needed).  Errors as for
+ * qsa_select_blocks' shape checks. */
+qsa_status qsa_select_workspace_bytes(const qsa_select_shape *shape, int32_t n_seq, size_t *bytes);
+
+/*
+ * Score, keep and list.  All pointers device pointers (shape: host).
+ *   q_idx       [n_seq][T][F] fp32, 16-byte aligned.
+ *   pooled      [n_seq][max_blocks][F] bf16 bit patterns, 16-byte aligned;
+ *               rows of dead blocks are not read.
+ *   n_live      [n_seq] int32 live positions (a value outside
+ *               [0, max_blocks * R] is clamped and raises QSA_STATUS_BAD_EXTENT).
+ *   steps       [n_seq][T] int32 position of each query, or NULL (every live
+ *               block is a candidate).
+ *   scores      [n_seq][T][max_blocks] fp32, written (-inf off candidates).
+ *   kept        [n_seq][T][top_k] int32, written: kept block ids ascending,
+ *               then -1.
+ *   sel         positions, written: sequence b's list at
+ *               sel[sel_offsets[b] .. sel_offsets[b+1]); capacity needed
+ *               n_seq * min(T * top_k, max_blocks) * R entries.
+ *   sel_offsets [n_seq + 1] int32, written (CSR; sel_offsets[0] = 0): pass
+ *               sel and sel_offsets, with max_selected =
+ *               min(T * top_k, max_blocks) * R, to qsa_decode_attn_batch.
+ *   workspace   >= qsa_select_workspace_bytes(shape, n_seq) bytes.
+ * Four kernel launches on `stream`; allocates nothing.  Errors:
+ * QSA_ERR_INVALID_ARG (null or misaligned pointer, non-positive field),
+ * QSA_ERR_UNSUPPORTED (T > 8, F not a multiple of 8 or above 1024,
+ * max_blocks above 16384, top_k above max_blocks), QSA_ERR_WORKSPACE,
+ * QSA_ERR_CUDA.
+ */
+qsa_status qsa_select_blocks(const qsa_select_shape *shape, int32_t n_seq, const float *q_idx,
+                             const uint16_t *pooled, const int32_t *n_live, const int32_t *steps,
+                             float *scores, int32_t *kept, int32_t *sel, int32_t *sel_offsets,
+                             void *workspace, size_t workspace_bytes, uint32_t *status, void *stream);
 
 /*
  * Testing aid: the bound, in SM clock cycles, of every device-side wait of the

@@ -36,6 +36,7 @@ QSA_STATUS_TIMEOUT = 0x8
 QSA_STATUS_NOT_RESIDENT = 0x10
 QSA_STATUS_BAD_LIMITS = 0x20
 QSA_STATUS_LAUNCH = 0x40
+QSA_STATUS_BAD_EXTENT = 0x80
 
 HEAD_DIM = 256
 
@@ -59,6 +60,17 @@ class qsa_shape(ctypes.Structure):
         ("q_dtype", ctypes.c_int32),
         ("algo", ctypes.c_int32),
         ("page_cells", ctypes.c_int32),
+    ]
+
+
+class qsa_select_shape(ctypes.Structure):
+    _fields_ = [
+        ("n_queries", ctypes.c_int32),
+        ("idx_heads", ctypes.c_int32),
+        ("idx_dim", ctypes.c_int32),
+        ("block_cells", ctypes.c_int32),
+        ("max_blocks", ctypes.c_int32),
+        ("top_k", ctypes.c_int32),
     ]
 
 
@@ -94,6 +106,10 @@ _SIG = {
     "qsa_kv_append": ([ctypes.POINTER(qsa_shape), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                        _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int32),
     "qsa_set_wait_limit": ([ctypes.c_int64], None),
+    "qsa_select_workspace_bytes": ([ctypes.POINTER(qsa_select_shape), ctypes.c_int32,
+                                    ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int32),
+    "qsa_select_blocks": ([ctypes.POINTER(qsa_select_shape), ctypes.c_int32, _VP, _VP, _VP, _VP, _VP,
+                           _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP], ctypes.c_int32),
 }
 
 
@@ -229,4 +245,22 @@ def qsa_kv_append(shape: qsa_shape, n_seq: int, n_new: int, kv_dtype: int, k_new
         _ptr(v_scale), _ptr(status), _stream(stream)), "qsa_kv_append")
 
 
-from .device import DeviceAppend, DeviceProblem, run_problem, partials_of  # noqa: E402,F401
+
+
+def qsa_select_workspace_bytes(shape: qsa_select_shape, n_seq: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().qsa_select_workspace_bytes(ctypes.byref(shape), int(n_seq), ctypes.byref(out)),
+           "qsa_select_workspace_bytes")
+    return int(out.value)
+
+
+def qsa_select_blocks(shape: qsa_select_shape, n_seq: int, q_idx, pooled, n_live, steps, scores, kept,
+                      sel, sel_offsets, workspace, workspace_bytes: int, status=None, stream=None) -> None:
+    """Block scores, top-k and the selected-cell list (see include/qsa.h)."""
+    _check(load_library().qsa_select_blocks(
+        ctypes.byref(shape), int(n_seq), _ptr(q_idx), _ptr(pooled), _ptr(n_live), _ptr(steps),
+        _ptr(scores), _ptr(kept), _ptr(sel), _ptr(sel_offsets), _ptr(workspace), int(workspace_bytes),
+        _ptr(status), _stream(stream)), "qsa_select_blocks")
+
+
+from .device import DeviceAppend, DeviceProblem, DeviceSelection, run_problem, partials_of  # noqa: E402,F401

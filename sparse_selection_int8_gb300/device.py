@@ -12,7 +12,8 @@ import numpy as np
 
 from . import (QSA_ALGO_AUTO, QSA_BF16, QSA_F32, make_shape, qsa_decode_attn_batch,
                qsa_decode_attn_batch_limited, qsa_decode_attn_step, qsa_kv_append,
-               qsa_partials_view, qsa_workspace_bytes)
+               qsa_partials_view, qsa_select_blocks, qsa_select_shape, qsa_select_workspace_bytes,
+               qsa_workspace_bytes)
 
 
 def _to_dev(torch, a: np.ndarray, device, pin: bool = False):
@@ -119,6 +120,41 @@ class DeviceAppend:
         qsa_kv_append(self.shape, a.n_seq, a.n_new, self.kv_dtype, self.k_new, self.v_new,
                       self.positions, self.page_table, self.k_pool, self.v_pool, self.k_scale,
                       self.v_scale, self.status, stream)
+
+
+class DeviceSelection:
+    """A block-selection call (as drawn by the input generator) resident in
+    device memory, with its outputs: scores, kept block ids, the list and
+    its offsets."""
+
+    def __init__(self, sp, device: str = "cuda"):
+        import torch
+        self.sp = sp
+        self.q_idx = _to_dev(torch, sp.q_idx.astype(np.float32), device)
+        self.pooled = _to_dev(torch, np.asarray(sp.pooled).view(np.int16), device)
+        self.n_live = _to_dev(torch, sp.n_live.astype(np.int32), device)
+        self.steps = None if sp.steps is None else _to_dev(torch, sp.steps.astype(np.int32), device)
+        self.shape = qsa_select_shape(sp.n_queries, sp.idx_heads, sp.idx_dim, sp.block_cells,
+                                      sp.max_blocks, sp.top_k)
+        B, T = sp.n_seq, sp.n_queries
+        self.max_selected = min(T * sp.top_k, sp.max_blocks) * sp.block_cells
+        self.scores = torch.empty((B, T, sp.max_blocks), dtype=torch.float32, device=device)
+        self.kept = torch.empty((B, T, sp.top_k), dtype=torch.int32, device=device)
+        self.sel = torch.empty(max(B * self.max_selected, 1), dtype=torch.int32, device=device)
+        self.sel_offsets = torch.empty(B + 1, dtype=torch.int32, device=device)
+        self.ws_bytes = qsa_select_workspace_bytes(self.shape, B)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run(self, stream=None):
+        qsa_select_blocks(self.shape, self.sp.n_seq, self.q_idx, self.pooled, self.n_live, self.steps,
+                          self.scores, self.kept, self.sel, self.sel_offsets, self.workspace, self.ws_bytes,
+                          self.status, stream)
+
+    def result(self):
+        """(scores, kept, sel, sel_offsets) copied to host."""
+        off = self.sel_offsets.cpu().numpy()
+        return (self.scores.cpu().numpy(), self.kept.cpu().numpy(), self.sel[:int(off[-1])].cpu().numpy(), off)
 
 
 def run_problem(p, algo: int = QSA_ALGO_AUTO, batch: Optional[bool] = None) -> np.ndarray:

@@ -220,3 +220,27 @@ def test_binding_has_no_cpu_path():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "qsa_oracle" not in text, f
+
+
+def test_select_rejects_before_launch(lib):
+    """qsa_select_blocks checks its shape and pointers before any launch."""
+    s = qsa.qsa_select_shape(2, 4, 64, 64, 2048, 128)
+    size = ctypes.c_size_t(0)
+    assert lib.qsa_select_workspace_bytes(ctypes.byref(s), 8, ctypes.byref(size)) == qsa.QSA_OK
+    assert size.value > 0
+    args = lambda sh, n=8: [ctypes.byref(sh), n, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            size.value, None, None]
+    for field, value, code in (("n_queries", 9, qsa.QSA_ERR_UNSUPPORTED), ("n_queries", 0, qsa.QSA_ERR_INVALID_ARG),
+                               ("idx_dim", 63, qsa.QSA_ERR_UNSUPPORTED), ("idx_dim", 512, qsa.QSA_ERR_UNSUPPORTED),
+                               ("max_blocks", 16385, qsa.QSA_ERR_UNSUPPORTED),
+                               ("top_k", 2049, qsa.QSA_ERR_UNSUPPORTED), ("block_cells", 0, qsa.QSA_ERR_INVALID_ARG)):
+        bad = qsa.qsa_select_shape(2, 4, 64, 64, 2048, 128)
+        setattr(bad, field, value)
+        assert lib.qsa_select_blocks(*args(bad)) == code, field
+    assert lib.qsa_select_blocks(*args(s, 0)) == qsa.QSA_ERR_INVALID_ARG
+    small = args(s)
+    small[11] = size.value - 1
+    assert lib.qsa_select_blocks(*small) == qsa.QSA_ERR_WORKSPACE
+    misaligned = args(s)
+    misaligned[3] = FAKE + 8  # pooled keys must be 16-byte aligned
+    assert lib.qsa_select_blocks(*misaligned) == qsa.QSA_ERR_INVALID_ARG
