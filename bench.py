@@ -68,7 +68,7 @@ def parse():
                     help="run one workload --reps times and exit (for profiler captures): "
                          "tiny_decode, qsa_decode1..4, qsa_decode_sweep (T = 1, 2, 3, 4 in turn), "
                          "batched_decode, long_context, prompt_shaped, prompt_append, "
-                         "decode_step_append")
+                         "decode_step_append, long_selection")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tcgen05"])
     return ap.parse_args()
@@ -82,6 +82,13 @@ def run_case(args):
     qsa_build.build()
     import sparse_selection_int8_gb300 as qsa
     name = args.case
+    if name == "long_selection":
+        d = qsa.DeviceSelection(wl.long_selection())
+        for _ in range(args.reps):
+            d.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"case": name, "reps": args.reps, "status": [int(d.status.item())]}))
+        return 0
     if name.endswith("_append"):
         d = qsa.DeviceAppend(getattr(wl, name)())
         for _ in range(args.reps):
@@ -207,7 +214,7 @@ def source_digest(*names) -> str:
 # only while the kernel source hashes to the recorded digest.
 TRAFFIC = {
     # qsa_decode T = 1..4, chunk kernel, sum of the four launches (ncu dram__bytes_read + write)
-    "91369a909f44003b": 6110720,
+    "900b70e576d91dd9": 6102016,
 }
 
 # Sources of the chunk kernel the recorded traffic belongs to.
@@ -611,6 +618,115 @@ def measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=64, what=None):
     return res
 
 
+def select_bytes(sp) -> int:
+    """Algorithmic bytes of one block-selection call: the pooled keys of the
+    live blocks and the queries read; scores, kept ids, the list and its
+    offsets written."""
+    F = sp.idx_heads * sp.idx_dim
+    live_blocks = sum(-(-int(v) // sp.block_cells) for v in sp.n_live)
+    return (live_blocks * F * 2 + sp.n_seq * sp.n_queries * F * 4
+            + sp.n_seq * sp.n_queries * (sp.max_blocks + sp.top_k) * 4 + 4 * (sp.n_seq + 1))
+
+
+def measure_selection(torch, qsa, wl, stream, hbm_peak, flush):
+    """The QSA block selection in front of the long-context shape (scores,
+    top-k, list): one call per graph, L2 flushed before each; and the
+    selection followed by the attention over its list in one graph."""
+    sp = wl.long_selection()
+    ds = qsa.DeviceSelection(sp)
+    g = capture(torch, ds, stream)
+    with torch.cuda.stream(stream):
+        per = time_graphs(torch, [g], flush, 50, 5, stream)
+    us = statistics.median([x[0] for x in per]) * 1e3
+    if int(ds.status.item()):
+        raise RuntimeError(f"selection status {int(ds.status.item()):#x}")
+    torch.cuda.synchronize()
+    off = ds.sel_offsets.cpu().numpy()
+    ab = select_bytes(sp) + 4 * int(off[-1])
+    res = {"us_per_call": round(us, 2), "algorithmic_bytes": ab, "hbm_gbs": ab / (us * 1e-6) / 1e9,
+           "hbm_frac": ab / (us * 1e-6) / 1e9 / hbm_peak, "selected_cells": int(off[-1]),
+           "kernels": 4}
+    # the attention of the long-context shape over the list it just made
+    p = wl.long_context()
+    dp = qsa.DeviceProblem(p, max_selected=ds.max_selected)
+
+    class SelectThenAttend:
+        def run(self, stream=None):
+            ds.run(stream=stream)
+            qsa.qsa_decode_attn_batch(dp.shape, p.n_seq, dp.q, dp.k_pool, dp.v_pool, dp.k_scale, dp.v_scale,
+                                      dp.page_table, ds.sel, ds.sel_offsets, ds.max_selected, dp.out,
+                                      dp.workspace, dp.ws_bytes, dp.status, stream)
+
+    g2 = capture(torch, SelectThenAttend(), stream)
+    with torch.cuda.stream(stream):
+        per2 = time_graphs(torch, [g2], flush, 20, 3, stream)
+    us2 = statistics.median([x[0] for x in per2]) * 1e3
+    res["with_attention"] = {"us_per_call": round(us2, 2), "selected_cells": int(off[-1]),
+                             "what": "selection, then qsa_decode_attn_batch over its list on the long-context "
+                                     "pools (8 x 2 KV heads x 24 rows), one graph, L2 flushed before each"}
+    res["what"] = ("qsa_select_blocks on 8 sequences of 131,072 live positions in blocks of 64 (2,048 pooled keys "
+                   "of 4 x 64 bf16 values), 2 queries, 128 blocks kept per query; one call per graph, L2 flushed")
+    del g, g2, ds, dp
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_per_config(torch, qsa, wl, extra, budget_s=75.0):
+    """Every configuration: the GPU output against the fp64 oracle (max abs
+    error, max error relative to each output row's norm), and the oracle
+    timed on the host cores, single-threaded and with all threads (median of
+    up to five runs within the budget); the prompt-shaped case on 24 sampled
+    rows, its time scaled to the whole call."""
+    import oracle
+    oracle.build()
+    n_all = oracle.threads()
+    res = {}
+    cfgs = [("tiny_decode", wl.tiny_decode(), None)] + [
+        (f"qsa_decode_T{T}", wl.qsa_decode(T), None) for T in SWEEP] + [
+        ("batched_decode", wl.batched_decode(), None), ("long_context", wl.long_context(), None),
+        ("prompt_shaped", wl.prompt_shaped(), np.arange(0, 24))]
+    t_start = time.perf_counter()
+    per_cfg = budget_s / len(cfgs)
+    for name, p, rows in cfgs:
+        dp = qsa.DeviceProblem(p)
+        dp.run()
+        torch.cuda.synchronize()
+        got = dp.out.cpu().numpy().reshape(-1, p.head_dim).astype(np.float64)
+        del dp
+        total_rows = got.shape[0]
+        if rows is not None:
+            got = got[rows]
+        scale = 1.0 if rows is None else total_rows / len(rows)
+
+        def timed(threads):
+            oracle.set_threads(threads)
+            ts, out = [], None
+            t0 = time.perf_counter()
+            while len(ts) < 5 and (not ts or time.perf_counter() - t0 < per_cfg / 2):
+                a = time.perf_counter()
+                out = oracle.decode_attn(p, rows=rows)
+                ts.append(time.perf_counter() - a)
+            return statistics.median(ts) * scale * 1e3, len(ts), out
+        ms_n, runs_n, ref = timed(n_all)
+        ms_1, runs_1, _ = timed(1)
+        oracle.set_threads(n_all)
+        ref = np.asarray(ref).reshape(-1, p.head_dim)
+        d = np.abs(got - ref)
+        rn = np.linalg.norm(ref, axis=1)
+        rel = np.linalg.norm(got - ref, axis=1) / np.where(rn > 0, rn, 1.0)
+        res[name] = {"oracle_ms_1thread": round(ms_1, 3), "oracle_ms_all_threads": round(ms_n, 3),
+                     "threads": n_all, "runs": [runs_1, runs_n], "max_abs_err": float(d.max()),
+                     "max_rel_err_row_norm": float(rel.max()), "mean_rel_err_row_norm": float(rel.mean())}
+        if rows is not None:
+            res[name]["sample"] = f"{len(rows)} of {total_rows} rows, times scaled to the whole call"
+        if name in extra and isinstance(extra[name], dict) and "us_per_call" in extra[name]:
+            res[name]["gpu_us_per_call"] = extra[name]["us_per_call"]
+            res[name]["gpu_over_oracle_all_threads"] = ms_n * 1e3 / extra[name]["us_per_call"]
+        if time.perf_counter() - t_start > 3 * budget_s:
+            break
+    return res
+
+
 def run_ours(args, world, rank, local):
     import torch
     if not torch.cuda.is_available():
@@ -726,7 +842,7 @@ def run_ours(args, world, rank, local):
     e2e_ms = dist_max(statistics.mean(e2e_times), world)
     e2e_value = world * cells_step / (e2e_ms * 1e-3)
 
-    extra, steady, layers, windows, append = {}, {}, {}, {}, {}
+    extra, steady, layers, windows, append, selection, per_config = {}, {}, {}, {}, {}, {}, {}
     if rank == 0 and not args.no_extra:
         steady = measure_steady(torch, qsa, wl, stream, hbm_peak)
         layers = measure_steady(torch, qsa, wl, stream, hbm_peak, n_seq=12, what=(
@@ -735,6 +851,10 @@ def run_ours(args, world, rank, local):
         windows = measure_windows(torch, qsa, wl, stream, hbm_peak)
         append = measure_append(torch, qsa, wl, stream, hbm_peak, flush)
         extra = measure_extra(torch, qsa, wl, stream, hbm_peak, tflops_peak, flush)
+        selection = measure_selection(torch, qsa, wl, stream, hbm_peak, flush)
+        for T in SWEEP:
+            extra[f"qsa_decode_T{T}"] = {"us_per_call": per_T[f"T{T}"]}
+        per_config = oracle_per_config(torch, qsa, wl, extra)
 
     cpu = None
     if rank == 0 and world == 1:
@@ -776,6 +896,8 @@ def run_ours(args, world, rank, local):
             "wide_windows": windows,
             "kv_append": append,
             "other_workloads": extra,
+            "selection": selection,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     dist_barrier(world)

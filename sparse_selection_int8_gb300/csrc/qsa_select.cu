@@ -15,16 +15,19 @@
 //   the list is the union over the window's queries, expanded to the live
 //   positions of the kept blocks in ascending order (CSR over sequences).
 //
-// Four launches on the stream, each a plain grid:
-//   scores   one warp per block: 16-byte loads of the pooled key, the
-//            queries from shared memory, a warp butterfly per query; dead
-//            and future blocks read nothing
+// Three launches on the stream (the second and third programmatic
+// dependents of the one before, so each launches while its predecessor runs
+// and waits for it before it reads its results):
+//   scores   two blocks per warp, both pooled keys loaded before either is
+//            used (16-byte loads), the queries from shared memory, a warp
+//            butterfly per query; dead and future blocks read nothing
 //   top-k    one CTA per (sequence, query): an exact four-pass radix select
-//            over order-preserving 32-bit keys of the scores (shared memory),
-//            ties ranked by block id with a block scan; kept ids ascending,
-//            their bits OR-ed into the sequence's block bitmap
-//   count    one CTA per sequence: cells of every bitmap word, a scan; the
-//            last CTA to finish scans the sequences into the CSR offsets
+//            over order-preserving 32-bit keys of the scores (shared memory;
+//            a warp's histogram adds aggregated per digit), ties ranked by
+//            block id with a block scan; kept ids ascending, their bits OR-ed
+//            into the sequence's block bitmap.  The last of a sequence's CTAs
+//            counts its positions per bitmap word; the last sequence counted
+//            scans the sequences into the CSR offsets.
 //   expand   one warp per bitmap word: the kept blocks' live positions
 #include <float.h>
 
@@ -51,7 +54,7 @@ struct SelParams {
     uint32_t *bitmap;        // [B][W]
     int32_t *word_pre;       // [B][W] positions before the word
     int32_t *seq_cells;      // [B]
-    uint32_t *ticket;        // one word
+    uint32_t *ticket;        // [1 + B]: sequences counted, then each sequence's finished queries
     uint32_t *status;
     int32_t n_seq, T, F, R, NB, K, W;
 };
@@ -69,64 +72,90 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as
 
 // ---------------------------------------------------------------- scores
 
+constexpr int kScoreBlocksPerCta = 2 * kScoreWarps;          // two blocks per warp
+constexpr int kMaxChunksPerLane = kMaxSelFeatures / 8 / 32; // 16-byte pieces of a key per lane
+
 __global__ void __launch_bounds__(kScoreWarps * 32) qsa_block_scores_kernel(const SelParams p)
 {
     extern __shared__ __align__(16) float s_q[]; // [T][F]
     const int b = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j0 = blockIdx.x * 64;
+    const int j0 = blockIdx.x * kScoreBlocksPerCta;
     const int live = live_of(p, b);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         const int v = __ldg(p.n_live + b);
         if ((v < 0 || (long long)v > (long long)p.NB * p.R) && p.status) atomicOr(p.status, QSA_STATUS_BAD_EXTENT);
-        if (b == 0) *p.ticket = 0; // the count kernel's completion ticket
+        p.ticket[1 + b] = 0u;      // the top-k's per-sequence completion ticket
+        if (b == 0) *p.ticket = 0; // and the sequences' ticket
     }
-    // this CTA's blocks start with empty bitmap words (the top-k OR-s into them)
-    if (threadIdx.x < 2 && j0 / 32 + (int)threadIdx.x < p.W) p.bitmap[(size_t)b * p.W + j0 / 32 + threadIdx.x] = 0u;
+    // the top-k may launch now: it waits for this grid before it reads
+    cudaTriggerProgrammaticLaunchCompletion();
+    // empty bitmap words for the top-k to OR into: a word spans two CTAs'
+    // blocks, the one holding its first block clears it
+    if (threadIdx.x == 0 && (j0 & 31) == 0) p.bitmap[(size_t)b * p.W + j0 / 32] = 0u;
     const float *q = p.q_idx + (size_t)b * p.T * p.F;
     for (int e = threadIdx.x; e < p.T * p.F; e += blockDim.x) s_q[e] = __ldg(q + e);
     __syncthreads();
     const int nchunk = p.F / 8; // 16-byte pieces of a pooled key
-    for (int j = j0 + warp; j < min(j0 + 64, p.NB); j += kScoreWarps) {
+    int jb[2];
+    bool live_blk[2];
+    uint4 kw[2][kMaxChunksPerLane];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        jb[u] = j0 + warp + kScoreWarps * u;
+        live_blk[u] = jb[u] < p.NB && (long long)jb[u] * p.R < live;
+        const uint16_t *key = p.pooled + ((size_t)b * p.NB + (live_blk[u] ? jb[u] : 0)) * p.F;
+#pragma unroll
+        for (int c = 0; c < kMaxChunksPerLane; ++c) {
+            const int ch = lane + 32 * c;
+            kw[u][c] = make_uint4(0, 0, 0, 0);
+            if (live_blk[u] && ch < nchunk) kw[u][c] = ldg_nc_v4(key + 8 * ch);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int j = jb[u];
+        if (j >= p.NB) continue;
         float acc[kMaxSelQueries];
 #pragma unroll
         for (int t = 0; t < kMaxSelQueries; ++t) acc[t] = 0.f;
-        const bool live_blk = (long long)j * p.R < live;
-        if (live_blk) {
-            const uint16_t *key = p.pooled + ((size_t)b * p.NB + j) * p.F;
-            for (int ch = lane; ch < nchunk; ch += 32) {
-                const uint4 w = ldg_nc_v4(key + 8 * ch);
-                const float k8[8] = {bf16_to_f32(w.x & 0xffffu), bf16_to_f32(w.x >> 16),
-                                     bf16_to_f32(w.y & 0xffffu), bf16_to_f32(w.y >> 16),
-                                     bf16_to_f32(w.z & 0xffffu), bf16_to_f32(w.z >> 16),
-                                     bf16_to_f32(w.w & 0xffffu), bf16_to_f32(w.w >> 16)};
+        if (live_blk[u]) {
 #pragma unroll
-                for (int t = 0; t < kMaxSelQueries; ++t) {
-                    if (t < p.T) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(s_q + t * p.F + 8 * ch);
-                        const float4 qb = *reinterpret_cast<const float4 *>(s_q + t * p.F + 8 * ch + 4);
-                        float a = acc[t];
-                        a = fmaf(qa.x, k8[0], a); a = fmaf(qa.y, k8[1], a);
-                        a = fmaf(qa.z, k8[2], a); a = fmaf(qa.w, k8[3], a);
-                        a = fmaf(qb.x, k8[4], a); a = fmaf(qb.y, k8[5], a);
-                        a = fmaf(qb.z, k8[6], a); a = fmaf(qb.w, k8[7], a);
-                        acc[t] = a;
+            for (int c = 0; c < kMaxChunksPerLane; ++c) {
+                const int ch = lane + 32 * c;
+                if (ch < nchunk) {
+                    const uint4 w = kw[u][c];
+                    const float k8[8] = {bf16_to_f32(w.x & 0xffffu), bf16_to_f32(w.x >> 16),
+                                         bf16_to_f32(w.y & 0xffffu), bf16_to_f32(w.y >> 16),
+                                         bf16_to_f32(w.z & 0xffffu), bf16_to_f32(w.z >> 16),
+                                         bf16_to_f32(w.w & 0xffffu), bf16_to_f32(w.w >> 16)};
+#pragma unroll
+                    for (int t = 0; t < kMaxSelQueries; ++t) {
+                        if (t < p.T) {
+                            const float4 qa = *reinterpret_cast<const float4 *>(s_q + t * p.F + 8 * ch);
+                            const float4 qb = *reinterpret_cast<const float4 *>(s_q + t * p.F + 8 * ch + 4);
+                            float a = acc[t];
+                            a = fmaf(qa.x, k8[0], a); a = fmaf(qa.y, k8[1], a);
+                            a = fmaf(qa.z, k8[2], a); a = fmaf(qa.w, k8[3], a);
+                            a = fmaf(qb.x, k8[4], a); a = fmaf(qb.y, k8[5], a);
+                            a = fmaf(qb.z, k8[6], a); a = fmaf(qb.w, k8[7], a);
+                            acc[t] = a;
+                        }
                     }
                 }
             }
 #pragma unroll
             for (int t = 0; t < kMaxSelQueries; ++t)
+                if (t < p.T)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+                    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
         }
         if (lane < p.T) {
-            float v = -INFINITY;
             float a = acc[0];
 #pragma unroll
             for (int t = 1; t < kMaxSelQueries; ++t)
                 if (lane == t) a = acc[t];
-            const bool cand = live_blk && (p.steps == nullptr || (long long)j * p.R <= (long long)__ldg(p.steps + (size_t)b * p.T + lane));
-            if (cand) v = a;
-            p.scores[((size_t)b * p.T + lane) * p.NB + j] = v;
+            const bool cand = live_blk[u] && (p.steps == nullptr || (long long)j * p.R <= (long long)__ldg(p.steps + (size_t)b * p.T + lane));
+            p.scores[((size_t)b * p.T + lane) * p.NB + j] = cand ? a : -INFINITY;
         }
     }
 }
@@ -171,6 +200,18 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int *tot
     return r;
 }
 
+// Positions of the kept blocks in bitmap word w of sequence b.
+__device__ __forceinline__ int word_cells(const SelParams &p, uint32_t bits, int w, int live)
+{
+    if (!bits) return 0;
+    int cells = __popc(bits) * p.R;
+    // only the last live block can be partial
+    const int last = (live + p.R - 1) / p.R - 1; // last live block (live > 0 when bits != 0)
+    if (last >= 32 * w && last < 32 * w + 32 && (bits >> (last - 32 * w)) & 1u)
+        cells -= (last + 1) * p.R - live;
+    return cells;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) qsa_topk_kernel(const SelParams p)
 {
     extern __shared__ __align__(16) uint32_t s_key[]; // [NB]
@@ -178,8 +219,13 @@ __global__ void __launch_bounds__(kTopkThreads) qsa_topk_kernel(const SelParams 
     __shared__ int s_warp[33];
     __shared__ uint32_t s_bits[kMaxSelBlocks / 32];
     __shared__ int s_pick[2];
+    __shared__ bool s_last;
     const int bt = blockIdx.x, b = bt / p.T;
     const int n = p.NB;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    // the expansion may launch now; it waits for this grid before it reads
+    cudaTriggerProgrammaticLaunchCompletion();
+    cudaGridDependencySynchronize(); // the scores, the cleared bitmap and tickets
     const float *sc = p.scores + (size_t)bt * n;
     // keys, and the number of candidates (finite scores)
     int fin = 0;
@@ -200,19 +246,45 @@ __global__ void __launch_bounds__(kTopkThreads) qsa_topk_kernel(const SelParams 
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = threadIdx.x; i < 256; i += blockDim.x) s_hist[i] = 0;
             __syncthreads();
-            for (int j = threadIdx.x; j < n; j += blockDim.x) {
-                const uint32_t k = s_key[j];
-                if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 0xFFu], 1);
+            // a warp's lanes with the same digit add once, together
+            for (int jw = 32 * warp; jw < n; jw += 32 * nwarps) {
+                const int j = jw + lane;
+                const uint32_t k = j < n ? s_key[j] : 0u;
+                const bool in = j < n && (k & mask) == prefix;
+                const uint32_t d = in ? (k >> shift) & 0xFFu : 256u + (uint32_t)lane;
+                const unsigned grp = __match_any_sync(0xffffffffu, d);
+                if (in && lane == __ffs(grp) - 1) atomicAdd(&s_hist[d], __popc(grp));
             }
             __syncthreads();
-            if (threadIdx.x == 0) {
-                int above = 0, d = 255;
-                for (; d > 0; --d) {
-                    if (above + s_hist[d] >= need) break;
-                    above += s_hist[d];
+            if (warp == 0) {
+                // lane l holds digits 8l..8l+7: the digit at which the keys
+                // counted from 255 down first reach `need`, and the count above it
+                int c[8], lsum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = s_hist[8 * lane + i];
+                    lsum += c[i];
                 }
-                s_pick[0] = d;
-                s_pick[1] = above;
+                int suf = lsum; // keys with digits >= 8 * lane
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_down_sync(0xffffffffu, suf, o);
+                    if (lane + o < 32) suf += v;
+                }
+                int above = suf - lsum;
+                if (above < need && need <= suf) {
+                    int d = 8 * lane;
+#pragma unroll
+                    for (int i = 7; i >= 0; --i) {
+                        if (above + c[i] >= need) {
+                            d = 8 * lane + i;
+                            break;
+                        }
+                        above += c[i];
+                    }
+                    s_pick[0] = d;
+                    s_pick[1] = above;
+                }
             }
             __syncthreads();
             prefix |= (uint32_t)s_pick[0] << shift;
@@ -254,40 +326,29 @@ __global__ void __launch_bounds__(kTopkThreads) qsa_topk_kernel(const SelParams 
     __syncthreads();
     for (int w = threadIdx.x; w < (n + 31) / 32; w += blockDim.x)
         if (s_bits[w]) atomicOr(p.bitmap + (size_t)b * p.W + w, s_bits[w]);
-}
-
-// ---------------------------------------------------------------- count
-
-// Positions of the kept blocks in bitmap word w of sequence b.
-__device__ __forceinline__ int word_cells(const SelParams &p, uint32_t bits, int w, int live)
-{
-    if (!bits) return 0;
-    int cells = __popc(bits) * p.R;
-    // only the last live block can be partial
-    const int last = (live + p.R - 1) / p.R - 1; // last live block (live > 0 when bits != 0)
-    if (last >= 32 * w && last < 32 * w + 32 && (bits >> (last - 32 * w)) & 1u)
-        cells -= (last + 1) * p.R - live;
-    return cells;
-}
-
-__global__ void __launch_bounds__(256) qsa_select_count_kernel(const SelParams p)
-{
-    __shared__ int s_warp[33];
-    __shared__ bool s_last;
-    const int b = blockIdx.x;
+    // the last of the sequence's T CTAs counts its positions (per bitmap
+    // word, a scan); the last sequence counted scans the sequences into
+    // the CSR offsets
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(p.ticket + 1 + b, 1u) == (unsigned)p.T - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
     const int live = live_of(p, b);
-    int run = 0; // positions before this pass of words
+    int run = 0;
     for (int w0 = 0; w0 < p.W; w0 += blockDim.x) {
         const int w = w0 + threadIdx.x;
-        const int c = w < p.W ? word_cells(p, p.bitmap[(size_t)b * p.W + w], w, live) : 0;
-        int total;
-        const int before = block_exclusive_scan(c, s_warp, &total);
+        const uint32_t bits = w < p.W ? *reinterpret_cast<volatile uint32_t *>(p.bitmap + (size_t)b * p.W + w) : 0u;
+        const int c = w < p.W ? word_cells(p, bits, w, live) : 0;
+        int tot;
+        const int before = block_exclusive_scan(c, s_warp, &tot);
         if (w < p.W) p.word_pre[(size_t)b * p.W + w] = run + before;
-        run += total;
+        run += tot;
     }
     if (threadIdx.x == 0) p.seq_cells[b] = run;
-    // the last CTA to finish turns the sequences' counts into CSR offsets
     __threadfence();
+    __syncthreads();
     if (threadIdx.x == 0) s_last = atomicAdd(p.ticket, 1u) == (unsigned)p.n_seq - 1;
     __syncthreads();
     if (!s_last) return;
@@ -296,10 +357,10 @@ __global__ void __launch_bounds__(256) qsa_select_count_kernel(const SelParams p
     for (int b0 = 0; b0 < p.n_seq; b0 += blockDim.x) {
         const int i = b0 + threadIdx.x;
         const int c = i < p.n_seq ? *reinterpret_cast<volatile int32_t *>(p.seq_cells + i) : 0;
-        int total;
-        const int before = block_exclusive_scan(c, s_warp, &total);
+        int tot;
+        const int before = block_exclusive_scan(c, s_warp, &tot);
         if (i < p.n_seq) p.sel_offsets[i] = base + before;
-        base += total;
+        base += tot;
     }
     if (threadIdx.x == 0) p.sel_offsets[p.n_seq] = base;
 }
@@ -310,6 +371,7 @@ __global__ void __launch_bounds__(256) qsa_select_expand_kernel(const SelParams 
 {
     const int b = blockIdx.y, lane = threadIdx.x & 31;
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+    cudaGridDependencySynchronize(); // the bitmap, the word prefixes and the offsets
     if (w >= p.W) return;
     uint32_t bits = p.bitmap[(size_t)b * p.W + w];
     if (!bits) return;
@@ -337,7 +399,7 @@ SelWorkspace sel_carve(const qsa_select_shape *s, int n_seq)
     w.off_pre = align_up(w.off_bitmap + (size_t)n_seq * W * 4, 256);
     w.off_cells = align_up(w.off_pre + (size_t)n_seq * W * 4, 256);
     w.off_ticket = align_up(w.off_cells + (size_t)n_seq * 4, 256);
-    w.total = align_up(w.off_ticket + 4, 256);
+    w.total = align_up(w.off_ticket + 4 * ((size_t)n_seq + 1), 256);
     return w;
 }
 
@@ -409,17 +471,29 @@ qsa_status qsa_select_blocks(const qsa_select_shape *shape, int32_t n_seq, const
     p.W = (p.NB + 31) / 32;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const size_t q_smem = (size_t)p.T * p.F * sizeof(float);
-    qsa_block_scores_kernel<<<dim3((unsigned)((p.NB + 63) / 64), (unsigned)n_seq), kScoreWarps * 32, q_smem, cs>>>(p);
+    // the scorer waits for everything before it on the stream (it clears the
+    // bitmap and tickets the previous call's kernels read)
+    qsa_block_scores_kernel<<<dim3((unsigned)((p.NB + kScoreBlocksPerCta - 1) / kScoreBlocksPerCta), (unsigned)n_seq),
+                              kScoreWarps * 32, q_smem, cs>>>(p);
     if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
     const int key_smem = p.NB * 4;
     if (cudaFuncSetAttribute(qsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, key_smem) != cudaSuccess)
         return QSA_ERR_CUDA;
-    qsa_topk_kernel<<<(unsigned)(n_seq * p.T), kTopkThreads, key_smem, cs>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
-    qsa_select_count_kernel<<<(unsigned)n_seq, 256, 0, cs>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
-    qsa_select_expand_kernel<<<dim3((unsigned)((p.W + 7) / 8), (unsigned)n_seq), 256, 0, cs>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_seq * p.T));
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = (size_t)key_smem;
+    cfg.stream = cs;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, qsa_topk_kernel, p) != cudaSuccess) return QSA_ERR_CUDA;
+    cfg.gridDim = dim3((unsigned)((p.W + 7) / 8), (unsigned)n_seq);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, qsa_select_expand_kernel, p) != cudaSuccess) return QSA_ERR_CUDA;
     return QSA_OK;
 }
 
