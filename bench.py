@@ -717,6 +717,16 @@ def oracle_per_config(torch, qsa, wl, extra, budget_s=75.0):
         res[name] = {"oracle_ms_1thread": round(ms_1, 3), "oracle_ms_all_threads": round(ms_n, 3),
                      "threads": n_all, "runs": [runs_1, runs_n], "max_abs_err": float(d.max()),
                      "max_rel_err_row_norm": float(rel.max()), "mean_rel_err_row_norm": float(rel.mean())}
+        if p.q_dtype == "f32":
+            # the share of the error that the f16 rounding of the queries
+            # causes: the oracle on the rounded queries against the oracle
+            p16 = copy.copy(p)
+            p16.q = np.asarray(p.q, np.float32).astype(np.float16).astype(np.float32)
+            r16 = np.asarray(oracle.decode_attn(p16, rows=rows)).reshape(-1, p.head_dim)
+            res[name]["q_f16_rel_err_row_norm"] = float(
+                (np.linalg.norm(r16 - ref, axis=1) / np.where(rn > 0, rn, 1.0)).max())
+            res[name]["rest_rel_err_row_norm"] = float(
+                (np.linalg.norm(got - r16, axis=1) / np.where(rn > 0, rn, 1.0)).max())
         if rows is not None:
             res[name]["sample"] = f"{len(rows)} of {total_rows} rows, times scaled to the whole call"
         if name in extra and isinstance(extra[name], dict) and "us_per_call" in extra[name]:
@@ -868,7 +878,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16 (int8 codes exact) x f16 -> f32", "data": "synthetic",
+            "dtype": "f16 x f16 -> f32 (fp32 queries rounded to f16; INT8 codes exact in f16; P' in f16; fp32 sums, scales and output)", "data": "synthetic",
             "config": {"workload": WORKLOAD,
                        "l2": (f"inputs larger than L2: calls rotate over {ROTATION} distinct input sets "
                               f"per T ({ROTATION * bytes_step / L2_BYTES:.1f}x L2 of algorithmic bytes "

@@ -1,0 +1,155 @@
+"""Error bounds of the tensor-core decode path, derived from its arithmetic.
+
+The decode chunk kernel ("Strata PR #2220, attn_chunk_q8_v3_kernel": chunk
+partials m, l, o of the softmax over a chunk's cells, merged by log-sum-exp)
+computes, for one query row against the cells i of its (sequence, KV head):
+
+  1. q16 = f16(q)                           round to nearest even (u16 = 2^-11)
+  2. S_i = sum_d q16_d * kcode_d            products exact, summed in fp32 by
+                                            the MMA (|err| <= 2 * 256 * u32 * sum|q16 k|,
+                                            taken for any order and truncating adds)
+  3. x_i = fma(S_i, f32(k_scale_i * scale * log2 e), 0)   two fp32 roundings
+  4. p_i = ex2.approx(x_i - mref)           relative error <= 2^-20 (taken
+                                            generously above the instruction's
+                                            documented accuracy)
+  5. P'_i = f16(p_i * v_scale_i / sigma)    relative u16 while P' is a normal
+                                            f16; absolute 2^-25 when subnormal
+  6. o = sigma * sum_i P'_i vcode_i, l = sum_i p_i in fp32, merged in fp32.
+
+Step 1 is removed exactly by comparing with the fp64 oracle run on the
+f16-rounded queries (``ref16``).  Steps 2-6 perturb cell i of a row by a
+relative error eta_i of its P' and an error eps_i of its score (natural-log
+units, |eps_i| <= E_i).  With softmax weights w_i and values v_id = v_scale_i *
+vcode_id, to first order
+
+  o'_d - o_d = sum_i w_i v_id eta_i + sum_i w_i (v_id - o_d) eps_i.
+
+Bound A (any rounding):  |o'_d - o_d| <= 1.01 * (u16 * S1_d + sum_i w_i E_i (|v_id| + |o_d|)
+                                              + subnormal terms) + acc_d
+Bound B (rounding errors as independent mean-zero variables; Hoeffding with
+lambda = 7, i.e. a chance below 5e-11 per element of exceeding it):
+  |o'_d - o_d| <= 7 * (u16 * sqrt(sum_i w_i^2 v_id^2) + sqrt(sum_i w_i^2 E_i^2 (v_id - o_d)^2)
+                       + subnormal terms) + acc_d
+with S1_d = sum_i w_i |v_id| and acc_d = (C + 8) * 2 u32 * (S1_d + |o_d|) for
+the fp32 sums of a chunk of C cells and the merge.  The factor 1.01 covers
+second-order terms while max E_i < 1e-3 (checked).
+
+The query rounding itself (ref16 - ref64) has the a-priori bound
+  A_q,d = 1.01 * sum_i w_i |v_id - o_d| * scale * k_scale_i * u16 * sum_d |q_d kcode_d|.
+
+P' can be subnormal only where 2^(x_i - M) * v_scale_i / max v_scale < 2^-14
+(the reference mref never exceeds the row's maximum M and sigma never exceeds
+the largest V scale); such a cell adds max v_scale * |vcode_id| * 2^-25 / L
+(L = sum_i 2^(x_i - M) >= 1) to A, and its square to B's sum.
+
+Everything here is test infrastructure: numpy in fp64 over the problem's
+inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+U16 = 2.0 ** -11
+U32 = 2.0 ** -24
+EXP2_REL = 2.0 ** -20
+LAMBDA = 7.0
+SUB_MIN = 2.0 ** -14   # smallest normal f16
+SUB_HALF_ULP = 2.0 ** -25
+
+
+def f16_round(q: np.ndarray) -> np.ndarray:
+    """Queries as the kernel rounds them (f16, nearest even), as float64."""
+    return np.asarray(q, np.float32).astype(np.float16).astype(np.float64)
+
+
+def cells_of(p, b: int, g: int):
+    """Codes and scales of the valid cells of (sequence b, KV head g), in list order."""
+    sel = p.sel_of(b).astype(np.int64)
+    P = int(getattr(p, "page_cells", 1))
+    ok = (sel >= 0) & (sel < p.page_table_len * P)
+    pos = sel[ok]
+    ent = p.page_table[b][pos // P].astype(np.int64)
+    ok2 = (ent >= 0) & (ent < p.pool_cells // P)
+    slot = ent[ok2] * P + pos[ok2] % P
+    kc = p.k_pool[b, g, slot].astype(np.float64)
+    vc = p.v_pool[b, g, slot].astype(np.float64)
+    ks = p.k_scale[b, g, slot].astype(np.float64)
+    vs = p.v_scale[b, g, slot].astype(np.float64)
+    return kc, vc, ks, vs
+
+
+def bounds(p, q_rows: np.ndarray, b: int, g: int):
+    """Bounds A, B (steps 2-6) and A_q (step 1) for the query rows q_rows
+    [R][D] (fp32 values) of (sequence b, KV head g): arrays [R][D], plus the
+    largest E_i."""
+    kc, vc, ks, vs = cells_of(p, b, g)
+    R, D = q_rows.shape
+    if kc.shape[0] == 0:
+        z = np.zeros((R, D))
+        return z, z, z, 0.0
+    q64 = np.asarray(q_rows, np.float64)
+    q16 = f16_round(q_rows)
+    scale = float(p.softmax_scale)
+    x = scale * (q16 @ kc.T) * ks[None, :]               # natural-log units, [R][n]
+    M = x.max(axis=1, keepdims=True)
+    e = np.exp(x - M)
+    L = e.sum(axis=1, keepdims=True)
+    w = e / L
+    v = vc * vs[:, None]                                  # [n][D]
+    av = np.abs(v)
+    o = w @ v
+    S1 = w @ av
+    # score error per (row, cell): MMA sum, the two fp32 roundings, the exponential
+    E = (scale * ks[None, :] * 2 * 256 * U32 * (np.abs(q16) @ np.abs(kc).T)
+         + 2 * U32 * np.abs(x) + EXP2_REL)
+    WE = w * E
+    # subnormal P': possible only where this lower bound of P' is below 2^-14
+    vmax = float(np.abs(vs).max())
+    flag = (e * np.abs(vs)[None, :] / vmax) < SUB_MIN
+    a_scale = vmax * SUB_HALF_ULP
+    A_sub = a_scale * ((flag / L) @ np.abs(vc))
+    B_sub = a_scale * np.sqrt((flag / L ** 2) @ (vc * vc))
+    C = int(p.chunk_cells)
+    acc = (C + 8) * 2 * U32 * (S1 + np.abs(o))
+    A = 1.01 * (U16 * S1 + WE @ av + np.abs(o) * WE.sum(axis=1, keepdims=True) + A_sub) + acc
+    WE2 = WE * WE
+    cterm = (WE2 @ (v * v)) - 2 * o * (WE2 @ v) + o * o * WE2.sum(axis=1, keepdims=True)
+    B = LAMBDA * (U16 * np.sqrt((w * w) @ (v * v)) + np.sqrt(np.maximum(cterm, 0.0)) + B_sub) + acc
+    # step 1, a priori: |x16 - x| <= scale * ks * u16 * sum |q k|
+    Eq = scale * ks[None, :] * U16 * (np.abs(q64) @ np.abs(kc).T)
+    Aq = 1.01 * ((w * Eq) @ av + np.abs(o) * (w * Eq).sum(axis=1, keepdims=True))
+    return A, B, Aq, float(E.max())
+
+
+def problem_bounds(p):
+    """Bounds for every output row of a decode problem (f32 queries, no causal
+    limits): A, B, A_q shaped like the output [B][T][G*H][D], and max E."""
+    T, G, H, D = p.n_queries, p.n_kv_heads, p.q_per_kv, p.head_dim
+    shp = (p.n_seq, T, G * H, D)
+    A, B, Aq = np.zeros(shp), np.zeros(shp), np.zeros(shp)
+    emax = 0.0
+    q = np.asarray(p.q, np.float32)
+    for b in range(p.n_seq):
+        for g in range(G):
+            rows = q[b, :, g * H:(g + 1) * H, :].reshape(T * H, D)
+            a, bb, aq, em = bounds(p, rows, b, g)
+            A[b, :, g * H:(g + 1) * H, :] = a.reshape(T, H, D)
+            B[b, :, g * H:(g + 1) * H, :] = bb.reshape(T, H, D)
+            Aq[b, :, g * H:(g + 1) * H, :] = aq.reshape(T, H, D)
+            emax = max(emax, em)
+    return A, B, Aq, emax
+
+
+def with_f16_queries(p):
+    """A copy of problem p whose fp32 queries are the f16-rounded values."""
+    import copy
+    p16 = copy.copy(p)
+    p16.q = f16_round(p.q).astype(np.float32)
+    return p16
+
+
+def row_norm_errors(out, ref):
+    """Per output row ||out - ref|| / ||ref|| (rows of D values)."""
+    out = np.asarray(out, np.float64).reshape(-1, np.shape(out)[-1])
+    ref = np.asarray(ref, np.float64).reshape(-1, np.shape(ref)[-1])
+    return np.linalg.norm(out - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-300)
