@@ -189,11 +189,12 @@ __device__ __forceinline__ void divmod_nn(long long a, long long b, long long &q
     }
 }
 
-// Position of this CTA's first item, computed by one full warp: lanes read
-// the sequences' list offsets in parallel, a warp scan finds the sequence
-// that holds item `lo`.  Items are (sequence, KV head, chunk) in that order;
-// each CTA takes a contiguous range (consecutive chunks share their queries).
-__device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
+// Position of the first item of CTA `cta` of `ncta` (the CTAs of one row
+// block), computed by one full warp: lanes read the sequences' list offsets
+// in parallel, a warp scan finds the sequence that holds item `lo`.  Items
+// are (sequence, KV head, chunk) in that order; each CTA takes a contiguous
+// range (consecutive chunks share their queries).
+__device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane, int cta, int ncta)
 {
     cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
     cur.remaining = 0;
@@ -203,8 +204,8 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
         int s, n;
         const int nch = seq_chunks(p, 0, &s, &n);
         const long long total = (long long)p.G * nch;
-        divmod_nn(total + gridDim.x - 1, gridDim.x, per, rem);
-        const long long lo = per * blockIdx.x;
+        divmod_nn(total + ncta - 1, ncta, per, rem);
+        const long long lo = per * cta;
         const long long hi = min(lo + per, total);
         if (lo >= hi) return;
         cur.remaining = (int)(hi - lo);
@@ -221,8 +222,8 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane)
     for (int b = lane; b < p.n_seq; b += 32) total += (long long)p.G * seq_chunks(p, b, &s, &n);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-    divmod_nn(total + gridDim.x - 1, gridDim.x, per, rem);
-    const long long lo = per * blockIdx.x;
+    divmod_nn(total + ncta - 1, ncta, per, rem);
+    const long long lo = per * cta;
     const long long hi = min(lo + per, total);
     if (lo >= hi) return;
     cur.remaining = (int)(hi - lo);
@@ -485,6 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
     // in uniform registers and warp-wide tcgen05 operations need no per-lane
     // fallback
     const int w = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
+    // Row block: the CTAs of block rb take rows row0 .. row0 + Rl - 1 of every
+    // item (all rows when the rows are not split).
+    const int n_rb = p.row_blocks > 1 ? p.row_blocks : 1;
+    const int cta_per_rb = (int)gridDim.x / n_rb;
+    const int rblk = (int)blockIdx.x / cta_per_rb;
+    const int row0 = n_rb > 1 ? rblk * p.rb_rows : 0;
+    const int Rl = n_rb > 1 ? min(p.rb_rows, p.R - row0) : p.R;
     const uint32_t s_v = smem_u32(smem + L::v);
     const uint32_t s_q = smem_u32(smem + L::q);
     const uint32_t s_p = smem_u32(smem + L::pb);
@@ -517,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         tmem_alloc(&ms.tmem, kTmemCols);
         tmem_relinquish();
     }
-    if (w == kLoadWarps) cursor_init_warp(p, ms.first, lane);
+    if (w == kLoadWarps) cursor_init_warp(p, ms.first, lane, (int)blockIdx.x - rblk * cta_per_rb, cta_per_rb);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -778,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         auto epilogue = [&](const Pend &e) {
             wait(&ms.o_full[e.cp % L::OB], (uint32_t)(e.cp / L::OB) & 1u);
             tc_fence_after();
-            const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R;
+            const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R + row0;
             const float *fin = ms.st_fin[e.cp & 1];
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
@@ -798,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
                         const int r = 8 * k + jj; // rows R..N-1 are MMA padding
-                        if (r < p.R) dst[(size_t)r * kHeadDim] = v[r] * fr[jj];
+                        if (r < Rl) dst[(size_t)r * kHeadDim] = v[r] * fr[jj];
                     }
                 }
             }
@@ -834,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 }
             }
             named_bar(kBarSoft, kSoftThreads);
-            if (orow < p.R) {
+            if (orow < Rl) {
                 const float m = fmaxf(fmaxf(ms.ch_max[0][orow], ms.ch_max[1][orow]),
                                       fmaxf(ms.ch_max[2][orow], ms.ch_max[3][orow]));
                 const float l = ((ms.ch_sum[0][orow] + ms.ch_sum[1][orow]) + ms.ch_sum[2][orow]) +
@@ -842,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 // (a row with a valid score has a finite reference)
                 const float fin = m > -INFINITY ? fast_exp2(ms.ch_ref[orow] - m) : 0.f;
                 ms.st_fin[cpar][orow] = fin * sig;
-                const size_t base = (((size_t)b * p.G + g) * p.n_chunks + cc) * p.R;
+                const size_t base = (((size_t)b * p.G + g) * p.n_chunks + cc) * p.R + row0;
                 p.part_m[base + orow] = m > -INFINITY ? m * kLn2 : -INFINITY;
                 p.part_l[base + orow] = l * fin;
             }
@@ -858,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             for (int e = c; e < N * 32; e += kSoftThreads) {
                 const int r = e >> 5, pc = e & 31;
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (r < p.R) v = q_piece_f16(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, first.b, first.g, r) * esz, pc);
+                if (r < Rl) v = q_piece_f16(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, first.b, first.g, row0 + r) * esz, pc);
                 *reinterpret_cast<uint4 *>(smem + L::q + kmajor_sw128_off(r, pc * 8, N)) = v;
             }
             fence_proxy_async_smem();
@@ -926,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                             const int ci = 2 * L2 + B;
                             float &xv = x[L2][4 * k + 2 * B + e];
                             xv = __fmaf_rn(xv, ksc[ci], kbias[ci]); // = the rounded product, or -inf
-                            if (LIM && 8 * k + 2 * u + e < r0[ci]) xv = -INFINITY; // beyond its query's limit
+                            if (LIM && row0 + 8 * k + 2 * u + e < r0[ci]) xv = -INFINITY; // beyond its query's limit
                             m = fmaxf(m, xv);
                         }
                     }
@@ -1008,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 #pragma unroll 1
                     for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll 1
-                        for (int rb = 0; rb < p.R; rb += 16) {
+                        for (int rb = 0; rb < Rl; rb += 16) {
                             const uint32_t ta = tmem + t_lane + L::col_o(cp, hh) + rb;
                             float v[16];
                             tmem_ld16(ta, v);
@@ -1221,9 +1229,14 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
         scfg.numAttrs = 1;
         if ((e = cudaLaunchKernelEx(&scfg, qsa_query_stage_kernel<N>, p)) != cudaSuccess) return e;
     }
+    // one persistent CTA per SM at most; with split rows, each row block gets
+    // the same number of CTAs
     const long long items = (long long)p.n_seq * p.G * p.n_chunks;
+    const int n_rb = p.row_blocks > 1 ? p.row_blocks : 1;
+    const long long per_rb = items < sms / n_rb ? items : sms / n_rb;
+    if (per_rb < 1) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
+    cfg.gridDim = dim3((unsigned)(per_rb * n_rb));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = stream;
@@ -1247,6 +1260,31 @@ cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
     // converts it itself, so the call is two kernels (chunk, merge)
     Params p = p_in;
     p.q_inline = p.n_seq * p.G == 1 ? 1 : 0;
+    p.row_blocks = 1;
+    p.rb_rows = p.R;
+    if (p.q_inline && !p.q_limit) {
+        // Few chunks on one query tile (a decode window of one sequence):
+        // the SMs the chunks leave idle take blocks of the rows instead, so
+        // each CTA's chain of softmax, P' and epilogue work covers fewer
+        // rows.  Each block re-reads the chunk's cells (from L2, mostly).
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        for (int rb = 16; rb < p.R; rb += 16) {
+            const int n_rb = (p.R + rb - 1) / rb;
+            if ((long long)p.n_chunks * n_rb <= sms) {
+                p.row_blocks = n_rb;
+                p.rb_rows = rb;
+                switch (rb) {
+                case 16: return launch_n<16, 2>(p, stream);
+                case 32: return launch_n<32, 4>(p, stream);
+                case 48: return launch_n<48, 6>(p, stream);
+                default: return launch_n<64, 8>(p, stream);
+                }
+            }
+        }
+    }
     if (p.q_limit) { // causal limits: one instantiation per N (padding rows cost a little)
         switch ((p.R + 15) / 16) {
         case 1: return launch_n<16, 2, true>(p, stream);

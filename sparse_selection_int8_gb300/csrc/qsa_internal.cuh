@@ -42,6 +42,8 @@ struct Params {
     void *q_img;               // decode tensor-core path: [n_seq][G] f16 query tiles (workspace)
     int32_t q_inline;          // decode tensor-core path, one (sequence, KV head): the chunk
                                // kernel converts the queries itself (no staging kernel)
+    int32_t row_blocks;        // decode tensor-core path: the rows are split into this many
+    int32_t rb_rows;           // blocks of rb_rows rows, each on its own CTAs (0 or 1: no split)
     int32_t n_sel_single;      // list length when sel_offsets == nullptr
     int32_t n_seq, G, H, T, R; // R = T*H rows per KV head
     int32_t pool_cells, page_table_len, chunk_cells, n_chunks, max_selected;
