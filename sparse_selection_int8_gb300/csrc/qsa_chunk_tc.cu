@@ -1267,16 +1267,19 @@ cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
         // the SMs the chunks leave idle take blocks of the rows instead, so
         // each CTA's chain of softmax, P' and epilogue work covers fewer
         // rows.  Each block re-reads the chunk's cells (from L2, mostly).
+        // Blocks of 8 rows (one 8-row score block, MMA N = 16), else the
+        // smallest multiple of 16 whose blocks fit beside the chunks.
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        for (int rb = 16; rb < p.R; rb += 16) {
+        for (int rb = 8; rb < p.R; rb += (rb == 8 ? 8 : 16)) {
             const int n_rb = (p.R + rb - 1) / rb;
             if ((long long)p.n_chunks * n_rb <= sms) {
                 p.row_blocks = n_rb;
                 p.rb_rows = rb;
                 switch (rb) {
+                case 8: return launch_n<16, 1>(p, stream);
                 case 16: return launch_n<16, 2>(p, stream);
                 case 32: return launch_n<32, 4>(p, stream);
                 case 48: return launch_n<48, 6>(p, stream);
