@@ -72,14 +72,18 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as
 
 // ---------------------------------------------------------------- scores
 
-constexpr int kScoreBlocksPerCta = 2 * kScoreWarps;          // two blocks per warp
 constexpr int kMaxChunksPerLane = kMaxSelFeatures / 8 / 32; // 16-byte pieces of a key per lane
 
-__global__ void __launch_bounds__(kScoreWarps * 32) qsa_block_scores_kernel(const SelParams p)
+// CPL: 16-byte pieces of a key per lane (F / 256, rounded up); BPW: blocks
+// per warp, all their keys loaded before any is used.  BPW * CPL stays at 4,
+// so a warp has 2 KB of keys in flight and the grid (NB / (8 BPW) CTAs per
+// sequence) fits the SMs in one wave at the sizes of a long context.
+template <int CPL, int BPW>
+__global__ void __launch_bounds__(kScoreWarps * 32, 1) qsa_block_scores_kernel(const SelParams p)
 {
     extern __shared__ __align__(16) float s_q[]; // [T][F]
     const int b = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j0 = blockIdx.x * kScoreBlocksPerCta;
+    const int j0 = blockIdx.x * (BPW * kScoreWarps);
     const int live = live_of(p, b);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         const int v = __ldg(p.n_live + b);
@@ -89,30 +93,30 @@ __global__ void __launch_bounds__(kScoreWarps * 32) qsa_block_scores_kernel(cons
     }
     // the top-k may launch now: it waits for this grid before it reads
     cudaTriggerProgrammaticLaunchCompletion();
-    // empty bitmap words for the top-k to OR into: a word spans two CTAs'
-    // blocks, the one holding its first block clears it
+    // empty bitmap words for the top-k to OR into: the CTA that holds a
+    // word's first block clears it
     if (threadIdx.x == 0 && (j0 & 31) == 0) p.bitmap[(size_t)b * p.W + j0 / 32] = 0u;
     const float *q = p.q_idx + (size_t)b * p.T * p.F;
     for (int e = threadIdx.x; e < p.T * p.F; e += blockDim.x) s_q[e] = __ldg(q + e);
     __syncthreads();
     const int nchunk = p.F / 8; // 16-byte pieces of a pooled key
-    int jb[2];
-    bool live_blk[2];
-    uint4 kw[2][kMaxChunksPerLane];
+    int jb[BPW];
+    bool live_blk[BPW];
+    uint4 kw[BPW][CPL];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < BPW; ++u) {
         jb[u] = j0 + warp + kScoreWarps * u;
         live_blk[u] = jb[u] < p.NB && (long long)jb[u] * p.R < live;
         const uint16_t *key = p.pooled + ((size_t)b * p.NB + (live_blk[u] ? jb[u] : 0)) * p.F;
 #pragma unroll
-        for (int c = 0; c < kMaxChunksPerLane; ++c) {
+        for (int c = 0; c < CPL; ++c) {
             const int ch = lane + 32 * c;
             kw[u][c] = make_uint4(0, 0, 0, 0);
             if (live_blk[u] && ch < nchunk) kw[u][c] = ldg_nc_v4(key + 8 * ch);
         }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < BPW; ++u) {
         const int j = jb[u];
         if (j >= p.NB) continue;
         float acc[kMaxSelQueries];
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) qsa_block_scores_kernel(cons
         for (int t = 0; t < kMaxSelQueries; ++t) acc[t] = 0.f;
         if (live_blk[u]) {
 #pragma unroll
-            for (int c = 0; c < kMaxChunksPerLane; ++c) {
+            for (int c = 0; c < CPL; ++c) {
                 const int ch = lane + 32 * c;
                 if (ch < nchunk) {
                     const uint4 w = kw[u][c];
@@ -251,7 +255,9 @@ __global__ void __launch_bounds__(kTopkThreads) qsa_topk_kernel(const SelParams 
                 const int j = jw + lane;
                 const uint32_t k = j < n ? s_key[j] : 0u;
                 const bool in = j < n && (k & mask) == prefix;
-                const uint32_t d = in ? (k >> shift) & 0xFFu : 256u + (uint32_t)lane;
+                if (!__any_sync(0xffffffffu, in)) continue;
+                // (the lanes out of the prefix form one group, which adds nothing)
+                const uint32_t d = in ? (k >> shift) & 0xFFu : 0xFFFFFFFFu;
                 const unsigned grp = __match_any_sync(0xffffffffu, d);
                 if (in && lane == __ffs(grp) - 1) atomicAdd(&s_hist[d], __popc(grp));
             }
@@ -473,8 +479,15 @@ qsa_status qsa_select_blocks(const qsa_select_shape *shape, int32_t n_seq, const
     const size_t q_smem = (size_t)p.T * p.F * sizeof(float);
     // the scorer waits for everything before it on the stream (it clears the
     // bitmap and tickets the previous call's kernels read)
-    qsa_block_scores_kernel<<<dim3((unsigned)((p.NB + kScoreBlocksPerCta - 1) / kScoreBlocksPerCta), (unsigned)n_seq),
-                              kScoreWarps * 32, q_smem, cs>>>(p);
+    auto sgrid = [&](int bpw) {
+        return dim3((unsigned)((p.NB + bpw * kScoreWarps - 1) / (bpw * kScoreWarps)), (unsigned)n_seq);
+    };
+    switch ((p.F / 8 + 31) / 32) {
+    case 1: qsa_block_scores_kernel<1, 4><<<sgrid(4), kScoreWarps * 32, q_smem, cs>>>(p); break;
+    case 2: qsa_block_scores_kernel<2, 2><<<sgrid(2), kScoreWarps * 32, q_smem, cs>>>(p); break;
+    case 3: qsa_block_scores_kernel<3, 1><<<sgrid(1), kScoreWarps * 32, q_smem, cs>>>(p); break;
+    default: qsa_block_scores_kernel<kMaxChunksPerLane, 1><<<sgrid(1), kScoreWarps * 32, q_smem, cs>>>(p); break;
+    }
     if (cudaGetLastError() != cudaSuccess) return QSA_ERR_CUDA;
     const int key_smem = p.NB * 4;
     if (cudaFuncSetAttribute(qsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, key_smem) != cudaSuccess)
