@@ -360,6 +360,37 @@ def time_graphs(torch, graphs, flush, steps, warmup, stream):
     return per_step
 
 
+_CUDART = []
+
+
+def graph_upload(torch, g, stream):
+    """Upload an instantiated graph to the device (cudaGraphUpload), so that
+    its first replay carries no upload: a fresh 80-call graph's first replay
+    measured about 3.6 us per step slower than later ones.  A no-op where
+    torch does not expose the executable graph or no CUDA runtime library is
+    found."""
+    if not hasattr(g, "raw_cuda_graph_exec"):
+        return
+    if not _CUDART:
+        import ctypes
+        lib = None
+        for name in ("libcudart.so", "libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        _CUDART.append(lib)
+    lib = _CUDART[0]
+    if lib is None:
+        return
+    import ctypes
+    rc = lib.cudaGraphUpload(ctypes.c_void_p(g.raw_cuda_graph_exec()), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"cudaGraphUpload failed ({rc})")
+    stream.synchronize()
+
+
 def capture(torch, dp, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -367,6 +398,7 @@ def capture(torch, dp, stream):
     stream.synchronize()
     with torch.cuda.graph(g, stream=stream):
         dp.run()
+    graph_upload(torch, g, stream)
     return g
 
 
@@ -397,6 +429,7 @@ def capture_calls(torch, calls, stream):
     with torch.cuda.graph(g, stream=stream):
         for c in calls:
             c()
+    graph_upload(torch, g, stream)
     return g
 
 
@@ -717,16 +750,21 @@ def oracle_per_config(torch, qsa, wl, extra, budget_s=75.0):
         res[name] = {"oracle_ms_1thread": round(ms_1, 3), "oracle_ms_all_threads": round(ms_n, 3),
                      "threads": n_all, "runs": [runs_1, runs_n], "max_abs_err": float(d.max()),
                      "max_rel_err_row_norm": float(rel.max()), "mean_rel_err_row_norm": float(rel.mean())}
-        if p.q_dtype == "f32":
-            # the share of the error that the f16 rounding of the queries
-            # causes: the oracle on the rounded queries against the oracle
-            p16 = copy.copy(p)
-            p16.q = np.asarray(p.q, np.float32).astype(np.float16).astype(np.float32)
-            r16 = np.asarray(oracle.decode_attn(p16, rows=rows)).reshape(-1, p.head_dim)
-            res[name]["q_f16_rel_err_row_norm"] = float(
-                (np.linalg.norm(r16 - ref, axis=1) / np.where(rn > 0, rn, 1.0)).max())
+        if p.q_dtype == "f32" and name != "prompt_shaped":
+            # the share of the error that the rounding of the queries causes:
+            # the oracle on the queries the decode kernel multiplies (f16
+            # hi + lo parts; hi alone for windows over 64 rows on several
+            # pairs) against the oracle on the caller's
+            q32 = np.asarray(p.q, np.float32)
+            hi = q32.astype(np.float16).astype(np.float32)
+            split = p.n_seq * p.n_kv_heads == 1 or p.rows_per_kv <= 64
+            pq = copy.copy(p)
+            pq.q = (hi + (q32 - hi).astype(np.float16).astype(np.float32)) if split else hi
+            rq = np.asarray(oracle.decode_attn(pq, rows=rows)).reshape(-1, p.head_dim)
+            res[name]["q_round_rel_err_row_norm"] = float(
+                (np.linalg.norm(rq - ref, axis=1) / np.where(rn > 0, rn, 1.0)).max())
             res[name]["rest_rel_err_row_norm"] = float(
-                (np.linalg.norm(got - r16, axis=1) / np.where(rn > 0, rn, 1.0)).max())
+                (np.linalg.norm(got - rq, axis=1) / np.where(rn > 0, rn, 1.0)).max())
         if rows is not None:
             res[name]["sample"] = f"{len(rows)} of {total_rows} rows, times scaled to the whole call"
         if name in extra and isinstance(extra[name], dict) and "us_per_call" in extra[name]:
@@ -878,12 +916,13 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16 x f16 -> f32 (fp32 queries rounded to f16; INT8 codes exact in f16; P' in f16; fp32 sums, scales and output)", "data": "synthetic",
+            "dtype": "f16 x f16 -> f32 (fp32 queries as f16 hi + lo parts, about 22 bits; INT8 codes exact in f16; P' in f16; fp32 sums, scales and output)", "data": "synthetic",
             "config": {"workload": WORKLOAD,
                        "l2": (f"inputs larger than L2: calls rotate over {ROTATION} distinct input sets "
                               f"per T ({ROTATION * bytes_step / L2_BYTES:.1f}x L2 of algorithmic bytes "
                               "touched per rotation)"),
-                       "launch": (f"back to back: one CUDA graph of {ROTATION} steps (4 calls each), "
+                       "launch": (f"back to back: CUDA graphs of up to {ROTATION} steps (4 calls each), "
+                                  "uploaded to the device before the timed region (cudaGraphUpload), "
                                   "replayed; the pages' method (µs per call over a run of calls)"),
                        "parallelism": f"replica per GPU x{world}" if world > 1 else "1 GPU"},
             "us_per_call": per_T,

@@ -16,7 +16,12 @@
 // softmax scale and log2 e) multiplies the fp32 score after the MMA; the V
 // scale, divided by a reference sigma, multiplies the probability before it
 // is rounded to f16 (P' = p * v_scale / sigma), and sigma multiplies the fp32
-// result.  Queries are rounded to f16.
+// result.  A query element q is split into f16 parts hi = f16(q) and
+// lo = f16(q - hi), and S = K.hi + K.lo (two MMAs per 16-wide contraction
+// step into one fp32 accumulator): the query then carries about 22 bits
+// instead of f16's 11.  Windows of more than 64 rows on calls over several
+// (sequence, KV head) pairs have no shared memory left for the low part and
+// use hi alone.
 //
 // Probabilities are formed against a reference maximum per row (mref) that
 // moves only when a score exceeds it by more than 2^8, so P' <= 2^8 * 16 stays
@@ -121,7 +126,13 @@ struct Misc {
 template <int N>
 struct Lay {
     static constexpr int PB = N <= 48 ? 2 : 1; // P' buffers
-    static constexpr int QB = N <= 48 ? 2 : 1; // query tile buffers
+    static constexpr int QSF = N <= 64 ? 2 : 1; // query tile parts (hi, lo)
+    // Query tile buffers: two (the next segment's tile loads while this one
+    // runs) where that keeps the layout within 196 KB, the size above which
+    // the SM's L1 carve-out halves (measured: the split query tiles with
+    // two buffers at 32 rows, 224 KB, cost 13% on long contexts; one
+    // buffer, 192 KB, 3.5%).
+    static constexpr int QB = N <= (QSF == 2 ? 16 : 48) ? 2 : 1;
     // Tensor memory (512 columns): KB buffers of K codes (128 columns each),
     // two score buffers of N columns, then O^T in OB chunk buffers x two d
     // halves x N columns.  Two K buffers let the loaders write the K codes of
@@ -144,7 +155,7 @@ struct Lay {
     static_assert(colO + OB * 2 * SW <= kTmemCols, "tensor memory columns");
     static constexpr uint32_t v = 0;
     static constexpr uint32_t q = 2 * kStageBytes;
-    static constexpr uint32_t pb = q + QB * N * 512u;
+    static constexpr uint32_t pb = q + QB * N * 512u * QSF;
     static constexpr uint32_t misc = pb + PB * N * 256u;
     static constexpr uint32_t total = misc + (uint32_t)((sizeof(Misc) + 127) / 128 * 128);
 };
@@ -401,8 +412,9 @@ __device__ __forceinline__ QRaw q_piece_load(const Params &p, const uint8_t *row
     return q;
 }
 
-// Raw query piece -> f16x8.
-__device__ __forceinline__ uint4 q_piece_cvt(const Params &p, const QRaw &q)
+// Raw query piece -> its f16 high parts hi and the f16 rounding lo of what
+// they leave (q - hi is exact in fp32; bf16 elements are exact in f16, lo = 0).
+__device__ __forceinline__ void q_piece_cvt2(const Params &p, const QRaw &q, uint4 &hi, uint4 &lo)
 {
     float f[8];
     if (p.q_bf16) {
@@ -416,21 +428,20 @@ __device__ __forceinline__ uint4 q_piece_cvt(const Params &p, const QRaw &q)
         f[4] = __uint_as_float(q.b.x); f[5] = __uint_as_float(q.b.y);
         f[6] = __uint_as_float(q.b.z); f[7] = __uint_as_float(q.b.w);
     }
-    return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-                      pack_f16x2(f[6], f[7]));
+    float r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = f[i] - __half2float(__float2half_rn(f[i]));
+    hi = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
+    lo = make_uint4(pack_f16x2(r[0], r[1]), pack_f16x2(r[2], r[3]), pack_f16x2(r[4], r[5]), pack_f16x2(r[6], r[7]));
 }
 
-// Query piece pc of the row at `row` (f32 or bf16 elements) -> f16x8.
-__device__ __forceinline__ uint4 q_piece_f16(const Params &p, const uint8_t *row, int pc)
-{
-    return q_piece_cvt(p, q_piece_load(p, row, pc));
-}
 
 // Query tiles of every (sequence, KV head) pair, written once per call into
 // the workspace in exactly the shared-memory layout the MMA reads (f16,
 // K-major, 128-byte swizzle, contraction index permuted as above, rows >= R
-// zero), so the chunk kernel brings a pair's tile in with one bulk copy.
-// One thread per 16-byte piece.
+// zero; the high parts, then the low parts where the layout has them), so
+// the chunk kernel brings a pair's tile in with one bulk copy.  One thread
+// per 16-byte piece.
 template <int N>
 __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
 {
@@ -449,12 +460,15 @@ __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
     if (e >= pieces) return;
     const int bg = (int)(e / (N * 32));
     const int r = (int)((e / 32) % N), pc = (int)(e % 32);
-    uint4 v = make_uint4(0, 0, 0, 0);
+    uint4 v = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
     if (r < p.R) {
         const int esz = p.q_bf16 ? 2 : 4;
-        v = q_piece_f16(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, r) * esz, pc);
+        q_piece_cvt2(p, q_piece_load(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, r) * esz, pc), v, lo);
     }
-    *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.q_img) + (size_t)bg * N * 512 + kmajor_sw128_off(r, pc * 8, N)) = v;
+    constexpr int QSF = Lay<N>::QSF;
+    uint8_t *img = static_cast<uint8_t *>(p.q_img) + (size_t)bg * N * 512 * QSF + kmajor_sw128_off(r, pc * 8, N);
+    *reinterpret_cast<uint4 *>(img) = v;
+    if (QSF == 2) *reinterpret_cast<uint4 *>(img + N * 512) = lo;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -858,16 +872,18 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 
         if (p.q_inline && it.valid) {
             // One (sequence, KV head) in the whole call: this CTA converts its
-            // query tile itself into buffer 0, in the layout of the staged
-            // images (f16, K-major, 128-byte swizzle, permuted contraction
-            // index, rows >= R zero), while the loaders resolve the first
-            // tiles.  Nothing of the previous call is read or written here.
+            // rows of the query tile itself into buffer 0, in the layout of
+            // the staged images (f16 high and low parts, K-major, 128-byte
+            // swizzle, permuted contraction index, rows past its block zero),
+            // while the loaders resolve the first tiles.  Nothing of the
+            // previous call is read or written here.
             const int esz = p.q_bf16 ? 2 : 4;
             for (int e = c; e < N * 32; e += kSoftThreads) {
                 const int r = e >> 5, pc = e & 31;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (r < Rl) v = q_piece_f16(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, first.b, first.g, row0 + r) * esz, pc);
+                uint4 v = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+                if (r < Rl) q_piece_cvt2(p, q_piece_load(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, first.b, first.g, row0 + r) * esz, pc), v, lo);
                 *reinterpret_cast<uint4 *>(smem + L::q + kmajor_sw128_off(r, pc * 8, N)) = v;
+                if (L::QSF == 2) *reinterpret_cast<uint4 *>(smem + L::q + N * 512 + kmajor_sw128_off(r, pc * 8, N)) = lo;
             }
             fence_proxy_async_smem();
             mbar_arrive(&ms.q_full[0]);
@@ -1084,11 +1100,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         constexpr int QB = L::QB;
         int q_issued[2] = {0, 0}; // bulk copies issued into each buffer
         auto load_q = [&](const Cursor &sc, int seg) {
-            const uint32_t bytes = (uint32_t)N * 512u;
+            const uint32_t bytes = (uint32_t)N * 512u * L::QSF;
             if (leader) {
                 mbar_arrive_expect_tx(&ms.q_full[seg % QB], bytes);
-                bulk_g2s(smem + L::q + (size_t)(seg % QB) * N * 512,
-                         static_cast<const uint8_t *>(p.q_img) + ((size_t)sc.b * p.G + sc.g) * N * 512, bytes,
+                bulk_g2s(smem + L::q + (size_t)(seg % QB) * N * 512 * L::QSF,
+                         static_cast<const uint8_t *>(p.q_img) + ((size_t)sc.b * p.G + sc.g) * N * 512 * L::QSF, bytes,
                          &ms.q_full[seg % QB]);
             }
             ++q_issued[seg % QB];
@@ -1112,13 +1128,15 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             wait(&ms.k_full[kb], (uint32_t)(i / L::KB) & 1u);
             if (i >= 2) wait(&ms.s_empty[i & 1], (uint32_t)((i - 2) >> 1) & 1u);
             tc_fence_after();
-            const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg % QB) * N * 512u, 16, 1024);
+            const uint64_t qd0 = smem_desc(s_q + (uint32_t)(seg % QB) * N * 512u * L::QSF, 16, 1024);
             const uint32_t sd = tmem + L::col_s(i & 1);
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint64_t bd = qd0 + (uint64_t)(((uint32_t)(kk >> 2) * N * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
                     mma_f16_ts(sd, tmem + L::col_k(kb) + 8u * kk, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    if (L::QSF == 2)
+                        mma_f16_ts(sd, tmem + L::col_k(kb) + 8u * kk, bd + (uint64_t)((N * 512u) >> 4), idesc_s, 1u);
                 }
                 mma_commit(&ms.k_empty[kb]);
                 mma_commit(&ms.s_full[i & 1]);
@@ -1250,7 +1268,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
 size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
 {
     const size_t N = (size_t)(R + 15) / 16 * 16;
-    return (size_t)n_seq * G * N * 512;
+    return (size_t)n_seq * G * N * 512 * 2;
 }
 
 cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)

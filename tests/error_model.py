@@ -4,9 +4,14 @@ The decode chunk kernel ("Strata PR #2220, attn_chunk_q8_v3_kernel": chunk
 partials m, l, o of the softmax over a chunk's cells, merged by log-sum-exp)
 computes, for one query row against the cells i of its (sequence, KV head):
 
-  1. q16 = f16(q)                           round to nearest even (u16 = 2^-11)
-  2. S_i = sum_d q16_d * kcode_d            products exact, summed in fp32 by
-                                            the MMA (|err| <= 2 * 256 * u32 * sum|q16 k|,
+  1. hi = f16(q), lo = f16(q - hi)         round to nearest even; the kernel's
+                                            query is q' = hi + lo (|q - q'| <= 2^-22 |q|,
+                                            or 2^-25 where lo is subnormal).  Windows
+                                            of more than 64 rows on calls over several
+                                            (sequence, KV head) pairs use q' = hi alone
+                                            (u16 = 2^-11).
+  2. S_i = sum_d (hi_d + lo_d) * kcode_d    products exact, summed in fp32 by
+                                            the MMA (|err| <= 2 * 512 * u32 * sum(|hi| + |lo|)|k|,
                                             taken for any order and truncating adds)
   3. x_i = fma(S_i, f32(k_scale_i * scale * log2 e), 0)   two fp32 roundings
   4. p_i = ex2.approx(x_i - mref)           relative error <= 2^-20 (taken
@@ -17,7 +22,7 @@ computes, for one query row against the cells i of its (sequence, KV head):
   6. o = sigma * sum_i P'_i vcode_i, l = sum_i p_i in fp32, merged in fp32.
 
 Step 1 is removed exactly by comparing with the fp64 oracle run on the
-f16-rounded queries (``ref16``).  Steps 2-6 perturb cell i of a row by a
+kernel's queries q' (``refq``).  Steps 2-6 perturb cell i of a row by a
 relative error eta_i of its P' and an error eps_i of its score (natural-log
 units, |eps_i| <= E_i).  With softmax weights w_i and values v_id = v_scale_i *
 vcode_id, to first order
@@ -26,16 +31,22 @@ vcode_id, to first order
 
 Bound A (any rounding):  |o'_d - o_d| <= 1.01 * (u16 * S1_d + sum_i w_i E_i (|v_id| + |o_d|)
                                               + subnormal terms) + acc_d
-Bound B (rounding errors as independent mean-zero variables; Hoeffding with
-lambda = 7, i.e. a chance below 5e-11 per element of exceeding it):
-  |o'_d - o_d| <= 7 * (u16 * sqrt(sum_i w_i^2 v_id^2) + sqrt(sum_i w_i^2 E_i^2 (v_id - o_d)^2)
-                       + subnormal terms) + acc_d
+Bound B (every rounding error an independent mean-zero variable, the
+probabilistic model of rounding-error analysis; 7 standard deviations):
+  |o'_d - o_d| <= 7 * sqrt(u16^2 sum_i w_i^2 v_id^2 + sum_i w_i^2 s_i^2 (v_id - o_d)^2)
+                  + subnormal terms + acc_d
+where s_i bounds the standard deviation of cell i's score error: the MMA's
+sum of n products has a rounding error sum_k delta_k S_k (S_k its partial
+sums, |delta_k| <= u32), of standard deviation <= sqrt(n) * u32 * sum |terms|,
+plus the fp32 scaling and the exponential as in E_i.
 with S1_d = sum_i w_i |v_id| and acc_d = (C + 8) * 2 u32 * (S1_d + |o_d|) for
 the fp32 sums of a chunk of C cells and the merge.  The factor 1.01 covers
-second-order terms while max E_i < 1e-3 (checked).
+second-order terms while max E_i < 1e-2 (e^E - 1 - E <= E^2 < E / 100;
+checked).
 
-The query rounding itself (ref16 - ref64) has the a-priori bound
-  A_q,d = 1.01 * sum_i w_i |v_id - o_d| * scale * k_scale_i * u16 * sum_d |q_d kcode_d|.
+The query rounding itself (refq - ref64) has the a-priori bound
+  A_q,d = 1.01 * sum_i w_i |v_id - o_d| * scale * k_scale_i * sum_d (u_q |q_d| + a_q) |kcode_d|
+with u_q = 2^-22, a_q = 2^-25 for the split and u_q = u16, a_q = 2^-25 for hi alone.
 
 P' can be subnormal only where 2^(x_i - M) * v_scale_i / max v_scale < 2^-14
 (the reference mref never exceeds the row's maximum M and sigma never exceeds
@@ -58,8 +69,25 @@ SUB_HALF_ULP = 2.0 ** -25
 
 
 def f16_round(q: np.ndarray) -> np.ndarray:
-    """Queries as the kernel rounds them (f16, nearest even), as float64."""
+    """Queries rounded to f16 (nearest even), as float64."""
     return np.asarray(q, np.float32).astype(np.float16).astype(np.float64)
+
+
+def split_applies(p) -> bool:
+    """Whether the decode kernel splits the queries into f16 hi + lo: every
+    call but windows of more than 64 rows over several (sequence, KV head)
+    pairs (a single pair's rows go to blocks of at most 64)."""
+    return p.n_seq * p.n_kv_heads == 1 or p.rows_per_kv <= 64
+
+
+def kernel_queries(q: np.ndarray, split: bool) -> np.ndarray:
+    """The query values the kernel multiplies, as float64: hi + lo, or hi."""
+    q32 = np.asarray(q, np.float32)
+    hi = q32.astype(np.float16).astype(np.float32)
+    if not split:
+        return hi.astype(np.float64)
+    lo = (q32 - hi).astype(np.float16).astype(np.float64)  # q - hi is exact in fp32
+    return hi.astype(np.float64) + lo
 
 
 def cells_of(p, b: int, g: int):
@@ -78,7 +106,7 @@ def cells_of(p, b: int, g: int):
     return kc, vc, ks, vs
 
 
-def bounds(p, q_rows: np.ndarray, b: int, g: int):
+def bounds(p, q_rows: np.ndarray, b: int, g: int, split: bool = True):
     """Bounds A, B (steps 2-6) and A_q (step 1) for the query rows q_rows
     [R][D] (fp32 values) of (sequence b, KV head g): arrays [R][D], plus the
     largest E_i."""
@@ -88,7 +116,7 @@ def bounds(p, q_rows: np.ndarray, b: int, g: int):
         z = np.zeros((R, D))
         return z, z, z, 0.0
     q64 = np.asarray(q_rows, np.float64)
-    q16 = f16_round(q_rows)
+    q16 = kernel_queries(q_rows, split)
     scale = float(p.softmax_scale)
     x = scale * (q16 @ kc.T) * ks[None, :]               # natural-log units, [R][n]
     M = x.max(axis=1, keepdims=True)
@@ -100,7 +128,10 @@ def bounds(p, q_rows: np.ndarray, b: int, g: int):
     o = w @ v
     S1 = w @ av
     # score error per (row, cell): MMA sum, the two fp32 roundings, the exponential
-    E = (scale * ks[None, :] * 2 * 256 * U32 * (np.abs(q16) @ np.abs(kc).T)
+    nsum = 512 if split else 256  # products the MMA sums per score
+    hi = kernel_queries(q_rows, False)
+    mag = np.abs(hi) + np.abs(q16 - hi)  # |hi| + |lo| (lo = 0 for hi alone)
+    E = (scale * ks[None, :] * 2 * nsum * U32 * (mag @ np.abs(kc).T)
          + 2 * U32 * np.abs(x) + EXP2_REL)
     WE = w * E
     # subnormal P': possible only where this lower bound of P' is below 2^-14
@@ -112,18 +143,24 @@ def bounds(p, q_rows: np.ndarray, b: int, g: int):
     C = int(p.chunk_cells)
     acc = (C + 8) * 2 * U32 * (S1 + np.abs(o))
     A = 1.01 * (U16 * S1 + WE @ av + np.abs(o) * WE.sum(axis=1, keepdims=True) + A_sub) + acc
-    WE2 = WE * WE
-    cterm = (WE2 @ (v * v)) - 2 * o * (WE2 @ v) + o * o * WE2.sum(axis=1, keepdims=True)
-    B = LAMBDA * (U16 * np.sqrt((w * w) @ (v * v)) + np.sqrt(np.maximum(cterm, 0.0)) + B_sub) + acc
-    # step 1, a priori: |x16 - x| <= scale * ks * u16 * sum |q k|
-    Eq = scale * ks[None, :] * U16 * (np.abs(q64) @ np.abs(kc).T)
+    sd = (scale * ks[None, :] * np.sqrt(nsum) * U32 * (mag @ np.abs(kc).T)
+          + 2 * U32 * np.abs(x) + EXP2_REL)
+    WS2 = (w * sd) ** 2
+    cterm = (WS2 @ (v * v)) - 2 * o * (WS2 @ v) + o * o * WS2.sum(axis=1, keepdims=True)
+    B = LAMBDA * np.sqrt(U16 * U16 * ((w * w) @ (v * v)) + np.maximum(cterm, 0.0)) + LAMBDA * B_sub + acc
+    # step 1, a priori: |x' - x| <= scale * ks * sum (u_q |q| + a_q) |k|
+    u_q = 2.0 ** -22 if split else U16
+    Eq = scale * ks[None, :] * ((u_q * np.abs(q64) + SUB_HALF_ULP) @ np.abs(kc).T)
     Aq = 1.01 * ((w * Eq) @ av + np.abs(o) * (w * Eq).sum(axis=1, keepdims=True))
     return A, B, Aq, float(E.max())
 
 
-def problem_bounds(p):
+def problem_bounds(p, split: bool = None):
     """Bounds for every output row of a decode problem (f32 queries, no causal
-    limits): A, B, A_q shaped like the output [B][T][G*H][D], and max E."""
+    limits): A, B, A_q shaped like the output [B][T][G*H][D], and max E.
+    ``split``: the kernel's query split (default: as the kernel takes it)."""
+    if split is None:
+        split = split_applies(p)
     T, G, H, D = p.n_queries, p.n_kv_heads, p.q_per_kv, p.head_dim
     shp = (p.n_seq, T, G * H, D)
     A, B, Aq = np.zeros(shp), np.zeros(shp), np.zeros(shp)
@@ -132,7 +169,7 @@ def problem_bounds(p):
     for b in range(p.n_seq):
         for g in range(G):
             rows = q[b, :, g * H:(g + 1) * H, :].reshape(T * H, D)
-            a, bb, aq, em = bounds(p, rows, b, g)
+            a, bb, aq, em = bounds(p, rows, b, g, split)
             A[b, :, g * H:(g + 1) * H, :] = a.reshape(T, H, D)
             B[b, :, g * H:(g + 1) * H, :] = bb.reshape(T, H, D)
             Aq[b, :, g * H:(g + 1) * H, :] = aq.reshape(T, H, D)
@@ -140,12 +177,15 @@ def problem_bounds(p):
     return A, B, Aq, emax
 
 
-def with_f16_queries(p):
-    """A copy of problem p whose fp32 queries are the f16-rounded values."""
+def with_kernel_queries(p, split: bool = None):
+    """A copy of problem p whose fp32 queries are the values the kernel
+    multiplies (hi + lo, exact in fp32, or hi)."""
     import copy
-    p16 = copy.copy(p)
-    p16.q = f16_round(p.q).astype(np.float32)
-    return p16
+    if split is None:
+        split = split_applies(p)
+    pq = copy.copy(p)
+    pq.q = kernel_queries(p.q, split).astype(np.float32)
+    return pq
 
 
 def row_norm_errors(out, ref):
@@ -153,3 +193,12 @@ def row_norm_errors(out, ref):
     out = np.asarray(out, np.float64).reshape(-1, np.shape(out)[-1])
     ref = np.asarray(ref, np.float64).reshape(-1, np.shape(ref)[-1])
     return np.linalg.norm(out - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-300)
+
+
+def split_visible(out, ref_split, ref_hi) -> bool:
+    """Whether an output follows the queries' hi + lo (True) or hi alone
+    (False): the mean absolute error against the oracle on each, compared."""
+    out = np.asarray(out, np.float64)
+    a = float(np.mean(np.abs(out - np.asarray(ref_split))))
+    b = float(np.mean(np.abs(out - np.asarray(ref_hi))))
+    return a < b
