@@ -887,10 +887,14 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             }
             fence_proxy_async_smem();
             mbar_arrive(&ms.q_full[0]);
-            // the call before may still be reading the workspace (partials) or
-            // writing the output: wait for it before this CTA writes anything
-            cudaGridDependencySynchronize();
         }
+        // The call before may still be reading the workspace (the partials):
+        // a single-pair call waits for it just before its first partial
+        // write, so its first tile's scores, softmax and P.V run under the
+        // previous call's merge.  (The softmax threads write nothing else to
+        // global memory; with staged queries the S warp's wait for the
+        // staging grid, which waited for the call before, comes first.)
+        bool prev_done = !p.q_inline;
         for (int i = 0; it.valid; ++i) {
             const int par = i & 1;
             const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
@@ -1076,6 +1080,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 pend.on = false;
             }
             if (last_t) {
+                if (!prev_done) {
+                    cudaGridDependencySynchronize();
+                    prev_done = true;
+                }
                 chunk_end(cp, it.cur.b, it.cur.g, it.cur.c);
                 pend = Pend{it.cur.b, it.cur.g, it.cur.c, cp, true};
             }
