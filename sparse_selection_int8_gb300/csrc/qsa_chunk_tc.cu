@@ -1293,19 +1293,27 @@ cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
         // the SMs the chunks leave idle take blocks of the rows instead, so
         // each CTA's chain of softmax, P' and epilogue work covers fewer
         // rows.  Each block re-reads the chunk's cells (from L2, mostly).
-        // Blocks of 8 rows (one 8-row score block, MMA N = 16), else the
-        // smallest multiple of 16 whose blocks fit beside the chunks.
+        // Blocks of the smallest multiple of 16 rows such that the call's
+        // CTAs take at most half the SMs: back to back, a call's CTAs start
+        // under the previous call's (and its merge's), and CTAs beyond the
+        // free SMs would start only when those end (measured, 2,051 cells:
+        // 8-row blocks on 85 and 102 CTAs for 36 and 48 rows, 6.63 and 6.75
+        // us per call; 16-row blocks on 51 CTAs, 6.20 and 6.15 us).  Blocks
+        // of 16 rows also keep windows of 12 to 64 rows on one instantiation
+        // (N = 16, two 8-row score blocks), so a run of calls with different
+        // window sizes does not alternate kernels (8-row blocks up to 24 rows
+        // beside 16-row ones above: 6.42 us per call over windows of 1-4
+        // queries; one instantiation: 5.68).
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        for (int rb = 8; rb < p.R; rb += (rb == 8 ? 8 : 16)) {
+        for (int rb = 16; rb < p.R; rb += 16) {
             const int n_rb = (p.R + rb - 1) / rb;
-            if ((long long)p.n_chunks * n_rb <= sms) {
+            if ((long long)p.n_chunks * n_rb <= sms / 2) {
                 p.row_blocks = n_rb;
                 p.rb_rows = rb;
                 switch (rb) {
-                case 8: return launch_n<16, 1>(p, stream);
                 case 16: return launch_n<16, 2>(p, stream);
                 case 32: return launch_n<32, 4>(p, stream);
                 case 48: return launch_n<48, 6>(p, stream);
