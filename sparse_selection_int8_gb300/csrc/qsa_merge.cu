@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
             if (ok[u]) gm = fmaxf(gm, mu[u]);
         }
         if (gm > M) {
-            const float f = M == -INFINITY ? 0.f : expf(M - gm);
+            const float f = M == -INFINITY ? 0.f : __expf(M - gm);
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] *= f;
             Lpart *= f;
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
 #pragma unroll
         for (int u = 0; u < kRound; ++u) {
             if (!ok[u]) continue;
-            const float wu = mu[u] == M ? 1.f : expf(mu[u] - M);
+            const float wu = mu[u] == M ? 1.f : __expf(mu[u] - M);
             Lpart = fmaf(lu[u], wu, Lpart);
             acc[0] = fmaf(ou[u][0].x, wu, acc[0]);
             acc[1] = fmaf(ou[u][0].y, wu, acc[1]);
@@ -110,8 +110,9 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
         float4 *dst = reinterpret_cast<float4 *>(orow + lane * 8);
         const float L = Lpart;
         if (L > 0.f) {
-            dst[0] = make_float4(acc[0] / L, acc[1] / L, acc[2] / L, acc[3] / L);
-            dst[1] = make_float4(acc[4] / L, acc[5] / L, acc[6] / L, acc[7] / L);
+            const float iL = 1.f / L;
+            dst[0] = make_float4(acc[0] * iL, acc[1] * iL, acc[2] * iL, acc[3] * iL);
+            dst[1] = make_float4(acc[4] * iL, acc[5] * iL, acc[6] * iL, acc[7] * iL);
         } else {
             dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -139,16 +140,17 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
     for (int x = 0; x < kWarps; ++x) {
         fx[x] = 0.f;
         if (Mt > -INFINITY && s_l[x] > 0.f) {
-            fx[x] = s_m[x] == Mt ? 1.f : expf(s_m[x] - Mt);
+            fx[x] = s_m[x] == Mt ? 1.f : __expf(s_m[x] - Mt);
             L = fmaf(s_l[x], fx[x], L);
         }
     }
+    const float iL = L > 0.f ? 1.f / L : 0.f;
     for (int d = threadIdx.x; d < kHeadDimMerge; d += WPR * 32) {
         float o = 0.f;
 #pragma unroll
         for (int x = 0; x < kWarps; ++x)
             if (fx[x] != 0.f) o = fmaf(s_acc[x][d], fx[x], o);
-        orow[d] = L > 0.f ? o / L : 0.f;
+        orow[d] = L > 0.f ? o * iL : 0.f;
     }
 }
 

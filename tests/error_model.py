@@ -19,7 +19,8 @@ computes, for one query row against the cells i of its (sequence, KV head):
                                             documented accuracy)
   5. P'_i = f16(p_i * v_scale_i / sigma)    relative u16 while P' is a normal
                                             f16; absolute 2^-25 when subnormal
-  6. o = sigma * sum_i P'_i vcode_i, l = sum_i p_i in fp32, merged in fp32.
+  6. o = sigma * sum_i P'_i vcode_i, l = sum_i p_i in fp32, merged in fp32
+     with approximate exponentials (relative error <= 2^-20 per chunk weight).
 
 Step 1 is removed exactly by comparing with the fp64 oracle run on the
 kernel's queries q' (``refq``).  Steps 2-6 perturb cell i of a row by a
@@ -39,8 +40,9 @@ where s_i bounds the standard deviation of cell i's score error: the MMA's
 sum of n products has a rounding error sum_k delta_k S_k (S_k its partial
 sums, |delta_k| <= u32), of standard deviation <= sqrt(n) * u32 * sum |terms|,
 plus the fp32 scaling and the exponential as in E_i.
-with S1_d = sum_i w_i |v_id| and acc_d = (C + 8) * 2 u32 * (S1_d + |o_d|) for
-the fp32 sums of a chunk of C cells and the merge.  The factor 1.01 covers
+with S1_d = sum_i w_i |v_id| and acc_d = ((C + 8) * 2 u32 + 2 * 2^-20) * (S1_d + |o_d|)
+for the fp32 sums of a chunk of C cells and the merge (its weights in numerator
+and denominator).  The factor 1.01 covers
 second-order terms while max E_i < 1e-2 (e^E - 1 - E <= E^2 < E / 100;
 checked).
 
@@ -141,7 +143,7 @@ def bounds(p, q_rows: np.ndarray, b: int, g: int, split: bool = True):
     A_sub = a_scale * ((flag / L) @ np.abs(vc))
     B_sub = a_scale * np.sqrt((flag / L ** 2) @ (vc * vc))
     C = int(p.chunk_cells)
-    acc = (C + 8) * 2 * U32 * (S1 + np.abs(o))
+    acc = ((C + 8) * 2 * U32 + 2 * EXP2_REL) * (S1 + np.abs(o))
     A = 1.01 * (U16 * S1 + WE @ av + np.abs(o) * WE.sum(axis=1, keepdims=True) + A_sub) + acc
     sd = (scale * ks[None, :] * np.sqrt(nsum) * U32 * (mag @ np.abs(kc).T)
           + 2 * U32 * np.abs(x) + EXP2_REL)
