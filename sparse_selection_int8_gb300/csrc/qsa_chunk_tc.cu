@@ -114,6 +114,8 @@ struct Misc {
     __align__(16) float ch_sum[4][kMaxRows];
     __align__(16) float ch_ref[kMaxRows];
     __align__(16) float st_fin[2][kMaxRows];
+    __align__(16) float st_m[2][kMaxRows]; // the chunk's partial m and l, per chunk parity,
+    __align__(16) float st_l[2][kMaxRows]; // stored with its O by the epilogue
     Cursor first;
     uint32_t tmem;
     int abort;
@@ -797,6 +799,16 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         tile_init(p, it, first);
 
         // partials of chunk e.cp: O read out of tensor memory, times sigma * 2^(mref - m)
+        // The call before may still be reading the workspace (the partials):
+        // a single-pair call waits for it just before its first partial
+        // store, so its first tile runs under the previous call's merge.
+        // (The softmax threads store nothing else to global memory; with
+        // staged queries the S warp's wait for the staging grid, which
+        // waited for the call before, comes first.)
+        bool prev_done = !p.q_inline;
+
+        // partials of chunk e.cp: O read out of tensor memory, times sigma *
+        // 2^(mref - m), and the m and l that the chunk's end left in shared memory
         auto epilogue = [&](const Pend &e) {
             wait(&ms.o_full[e.cp % L::OB], (uint32_t)(e.cp / L::OB) & 1u);
             tc_fence_after();
@@ -811,6 +823,10 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     tmem_ld8(tmem + t_lane + L::col_o(e.cp, hh) + 8u * k, v + 8 * k);
                 tmem_wait_ld();
                 regs_after_wait<8 * KR>(v);
+                if (!prev_done) {
+                    cudaGridDependencySynchronize();
+                    prev_done = true;
+                }
                 float *dst = p.part_o + base * kHeadDim + 128 * hh + c;
 #pragma unroll
                 for (int k = 0; k < KR; ++k) {
@@ -824,13 +840,18 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     }
                 }
             }
+            if (c < Rl) {
+                p.part_m[base + c] = ms.st_m[e.cp & 1][c];
+                p.part_l[base + c] = ms.st_l[e.cp & 1][c];
+            }
             tc_fence_before();
             mbar_arrive(&ms.o_empty[e.cp % L::OB]);
         };
 
         // end of chunk cp: the rows' true maxima and sums across the CTA; the
-        // row's owner writes m and l and the factor its O is read out with
-        auto chunk_end = [&](int chunk, int b, int g, int cc) {
+        // row's owner leaves m, l and the factor its O is read out with in
+        // shared memory for the epilogue
+        auto chunk_end = [&](int chunk) {
             const int cpar = chunk & 1;
             float cm[NR], cs[NR];
 #pragma unroll
@@ -864,9 +885,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 // (a row with a valid score has a finite reference)
                 const float fin = m > -INFINITY ? fast_exp2(ms.ch_ref[orow] - m) : 0.f;
                 ms.st_fin[cpar][orow] = fin * sig;
-                const size_t base = (((size_t)b * p.G + g) * p.n_chunks + cc) * p.R + row0;
-                p.part_m[base + orow] = m > -INFINITY ? m * kLn2 : -INFINITY;
-                p.part_l[base + orow] = l * fin;
+                ms.st_m[cpar][orow] = m > -INFINITY ? m * kLn2 : -INFINITY;
+                ms.st_l[cpar][orow] = l * fin;
             }
         };
 
@@ -888,13 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             fence_proxy_async_smem();
             mbar_arrive(&ms.q_full[0]);
         }
-        // The call before may still be reading the workspace (the partials):
-        // a single-pair call waits for it just before its first partial
-        // write, so its first tile's scores, softmax and P.V run under the
-        // previous call's merge.  (The softmax threads write nothing else to
-        // global memory; with staged queries the S warp's wait for the
-        // staging grid, which waited for the call before, comes first.)
-        bool prev_done = !p.q_inline;
+
         for (int i = 0; it.valid; ++i) {
             const int par = i & 1;
             const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
@@ -1080,11 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 pend.on = false;
             }
             if (last_t) {
-                if (!prev_done) {
-                    cudaGridDependencySynchronize();
-                    prev_done = true;
-                }
-                chunk_end(cp, it.cur.b, it.cur.g, it.cur.c);
+                chunk_end(cp);
                 pend = Pend{it.cur.b, it.cur.g, it.cur.c, cp, true};
             }
             tile_next(p, it);
