@@ -6,9 +6,9 @@
 //   M = max_{c: l_c > 0} m_c,  L = sum_c l_c e^{m_c - M},
 //   out = sum_c o_c e^{m_c - M} / L   (zeros when no chunk holds a cell).
 // A CTA of four warps covers four query rows with one warp each when a row
-// has at most four chunks; otherwise a CTA of 4 (up to 16 chunks) or 16
-// warps takes one row (warp w takes chunks w, w + WPR, ...), so one round of
-// loads covers up to 64 chunks.  Lane k owns output dimensions 8k..8k+7.
+// has at most four chunks; otherwise a CTA of 4, 8 or 16 warps takes one row
+// (warp w takes chunks w, w + WPR, ...), so one round of loads covers up to
+// 4 * WPR chunks.  Lane k owns output dimensions 8k..8k+7.
 // Each warp forms its own (M_w, L_w, acc_w), four chunks at a time with all
 // their loads in flight together and a running maximum; the warps' results
 // are then combined in shared memory.  Every sum runs in a fixed order, so
@@ -21,7 +21,7 @@ namespace {
 constexpr int kHeadDimMerge = 256;
 
 // WPR warps per row: 1 (a CTA of four warps takes four rows, a warp per
-// row), or 4 / 16 (a CTA per row; warp w takes chunks w, w + WPR, ...).
+// row), or 4 / 8 / 16 (a CTA per row; warp w takes chunks w, w + WPR, ...).
 template <int WPR>
 __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(const Params p)
 {
@@ -159,13 +159,16 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
     // a warp per row when rows have few chunks; otherwise a CTA per row with
-    // enough warps that one round of loads covers every chunk when possible
-    // (16 warps per row only while the whole grid stays within about 48
-    // warps per SM; more rows take 4 warps each)
+    // enough warps that one round of loads covers every chunk when possible:
+    // 16, 8 or 4 warps per row, the most that keep the grid within 32 warps
+    // per SM (16-warp CTAs hold 32 K registers, two per SM: more rows would
+    // run a second wave)
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long rows = (long long)p.R * p.G * p.n_seq;
-    const int wpr = p.n_chunks <= 4 ? 1 : (p.n_chunks > 16 && rows * 16 <= 48ll * sms) ? 16 : 4;
+    const int wpr = p.n_chunks <= 4 ? 1
+                    : (p.n_chunks > 16 && rows * 16 <= 32ll * sms) ? 16
+                    : (p.n_chunks > 16 && rows * 8 <= 32ll * sms) ? 8 : 4;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(wpr == 1 ? (p.R + 3) / 4 : p.R), (unsigned)p.G, (unsigned)p.n_seq);
     cfg.blockDim = dim3(wpr == 1 ? 128 : wpr * 32);
@@ -178,6 +181,7 @@ cudaError_t launch_merge(const Params &p, cudaStream_t stream)
     cfg.numAttrs = 1;
     if (wpr == 1) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1>, p);
     if (wpr == 4) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<4>, p);
+    if (wpr == 8) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<8>, p);
     return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<16>, p);
 }
 
