@@ -753,11 +753,10 @@ def oracle_per_config(torch, qsa, wl, extra, budget_s=75.0):
         if p.q_dtype == "f32" and name != "prompt_shaped":
             # the share of the error that the rounding of the queries causes:
             # the oracle on the queries the decode kernel multiplies (f16
-            # hi + lo parts; hi alone for windows over 64 rows on several
-            # pairs) against the oracle on the caller's
+            # hi + lo parts) against the oracle on the caller's
             q32 = np.asarray(p.q, np.float32)
             hi = q32.astype(np.float16).astype(np.float32)
-            split = p.n_seq * p.n_kv_heads == 1 or p.rows_per_kv <= 64
+            split = True  # (hi alone only for windows over 64 rows with causal limits)
             pq = copy.copy(p)
             pq.q = (hi + (q32 - hi).astype(np.float16).astype(np.float32)) if split else hi
             rq = np.asarray(oracle.decode_attn(pq, rows=rows)).reshape(-1, p.head_dim)

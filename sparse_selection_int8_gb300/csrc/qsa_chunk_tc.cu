@@ -19,9 +19,10 @@
 // result.  A query element q is split into f16 parts hi = f16(q) and
 // lo = f16(q - hi), and S = K.hi + K.lo (two MMAs per 16-wide contraction
 // step into one fp32 accumulator): the query then carries about 22 bits
-// instead of f16's 11.  Windows of more than 64 rows on calls over several
-// (sequence, KV head) pairs have no shared memory left for the low part and
-// use hi alone.
+// instead of f16's 11.  Calls split their rows into blocks of at most 64
+// (16-row multiples for one (sequence, KV head), 24 rows for several);
+// windows of more than 64 rows with causal limits, which are not split, have
+// no shared memory left for the low part and use hi alone.
 //
 // Probabilities are formed against a reference maximum per row (mref) that
 // moves only when a score exceeds it by more than 2^8, so P' <= 2^8 * 16 stays
@@ -457,18 +458,23 @@ __global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
     // writes as well.
     cudaTriggerProgrammaticLaunchCompletion();
     cudaGridDependencySynchronize();
+    // one image per (pair, row block): rows rb * rb_rows .. of the pair
+    const int n_rb = p.row_blocks > 1 ? p.row_blocks : 1;
+    const int rb_rows = n_rb > 1 ? p.rb_rows : p.R;
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long pieces = (long long)p.n_seq * p.G * N * 32;
+    const long long pieces = (long long)p.n_seq * p.G * n_rb * N * 32;
     if (e >= pieces) return;
-    const int bg = (int)(e / (N * 32));
+    const int img_i = (int)(e / (N * 32));
+    const int bg = img_i / n_rb, rblk = img_i % n_rb;
     const int r = (int)((e / 32) % N), pc = (int)(e % 32);
+    const int row = rblk * rb_rows + r;
     uint4 v = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-    if (r < p.R) {
+    if (r < rb_rows && row < p.R) {
         const int esz = p.q_bf16 ? 2 : 4;
-        q_piece_cvt2(p, q_piece_load(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, r) * esz, pc), v, lo);
+        q_piece_cvt2(p, q_piece_load(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, row) * esz, pc), v, lo);
     }
     constexpr int QSF = Lay<N>::QSF;
-    uint8_t *img = static_cast<uint8_t *>(p.q_img) + (size_t)bg * N * 512 * QSF + kmajor_sw128_off(r, pc * 8, N);
+    uint8_t *img = static_cast<uint8_t *>(p.q_img) + (size_t)img_i * N * 512 * QSF + kmajor_sw128_off(r, pc * 8, N);
     *reinterpret_cast<uint4 *>(img) = v;
     if (QSF == 2) *reinterpret_cast<uint4 *>(img + N * 512) = lo;
 }
@@ -1122,7 +1128,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             if (leader) {
                 mbar_arrive_expect_tx(&ms.q_full[seg % QB], bytes);
                 bulk_g2s(smem + L::q + (size_t)(seg % QB) * N * 512 * L::QSF,
-                         static_cast<const uint8_t *>(p.q_img) + ((size_t)sc.b * p.G + sc.g) * N * 512 * L::QSF, bytes,
+                         static_cast<const uint8_t *>(p.q_img) +
+                             (((size_t)sc.b * p.G + sc.g) * n_rb + rblk) * N * 512 * L::QSF, bytes,
                          &ms.q_full[seg % QB]);
             }
             ++q_issued[seg % QB];
@@ -1252,7 +1259,7 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     if ((e = cudaFuncSetAttribute(qsa_chunk_tc_kernel<N, KR, LIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)bytes)) != cudaSuccess)
         return e;
-    const long long pieces = (long long)p.n_seq * p.G * N * 32;
+    const long long pieces = (long long)p.n_seq * p.G * (p.row_blocks > 1 ? p.row_blocks : 1) * N * 32;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1285,8 +1292,10 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
 
 size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
 {
+    // the rows of a pair in row blocks of up to 64 rows, each padded to its
+    // MMA N: at most N + 48 padded rows in all
     const size_t N = (size_t)(R + 15) / 16 * 16;
-    return (size_t)n_seq * G * N * 512 * 2;
+    return (size_t)n_seq * G * (N + 48) * 512 * 2;
 }
 
 cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
@@ -1331,6 +1340,17 @@ cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
                 }
             }
         }
+    }
+    if (!p.q_inline && !p.q_limit && p.R > 24) {
+        // Calls over several pairs with more than 24 rows: blocks of 24 rows
+        // (MMA N = 32), each with its own CTAs and query images.  The softmax
+        // warps' per-tile chain grows with the rows while the loaders' work
+        // does not, and with 48 rows it set the pace (16 sequences x 2 KV
+        // heads x 48 rows, one-tile chunks: 35.9 -> 30.5 us per call on
+        // GB300; blocks of 16 rows, 34.3).  Each block re-reads the cells.
+        p.row_blocks = (p.R + 23) / 24;
+        p.rb_rows = 24;
+        return launch_n<32, 3>(p, stream);
     }
     if (p.q_limit) { // causal limits: one instantiation per N (padding rows cost a little)
         switch ((p.R + 15) / 16) {

@@ -7,9 +7,8 @@ computes, for one query row against the cells i of its (sequence, KV head):
   1. hi = f16(q), lo = f16(q - hi)         round to nearest even; the kernel's
                                             query is q' = hi + lo (|q - q'| <= 2^-22 |q|,
                                             or 2^-25 where lo is subnormal).  Windows
-                                            of more than 64 rows on calls over several
-                                            (sequence, KV head) pairs use q' = hi alone
-                                            (u16 = 2^-11).
+                                            of more than 64 rows with causal limits
+                                            use q' = hi alone (u16 = 2^-11).
   2. S_i = sum_d (hi_d + lo_d) * kcode_d    products exact, summed in fp32 by
                                             the MMA (|err| <= 2 * 512 * u32 * sum(|hi| + |lo|)|k|,
                                             taken for any order and truncating adds)
@@ -77,9 +76,10 @@ def f16_round(q: np.ndarray) -> np.ndarray:
 
 def split_applies(p) -> bool:
     """Whether the decode kernel splits the queries into f16 hi + lo: every
-    call but windows of more than 64 rows over several (sequence, KV head)
-    pairs (a single pair's rows go to blocks of at most 64)."""
-    return p.n_seq * p.n_kv_heads == 1 or p.rows_per_kv <= 64
+    call but windows of more than 64 rows with causal limits (the rows of
+    other calls go to blocks of at most 64: 16-row multiples for one
+    (sequence, KV head), 24 rows for several)."""
+    return getattr(p, "q_limit", None) is None or p.rows_per_kv <= 64
 
 
 def kernel_queries(q: np.ndarray, split: bool) -> np.ndarray:

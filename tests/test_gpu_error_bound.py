@@ -5,8 +5,8 @@ For every output element: |gpu - refq| <= B (the probabilistic bound of the
 kernel's fp32/f16 arithmetic after the query rounding) and <= A (its worst
 case), and |gpu - ref64| <= A + A_q, where ref64 is the fp64 oracle on the
 caller's queries and refq the oracle on the queries the kernel multiplies
-(f16 hi + lo; hi alone for windows of more than 64 rows over several pairs,
-the T = 6 batch case here).  Per output row, relative to the row's norm:
+(f16 hi + lo; hi alone only for windows of more than 64 rows with causal
+limits, which these calls do not have).  Per output row, relative to the row's norm:
 ||gpu - ref64|| <= ||refq - ref64|| + ||B||, the exact cost of the query
 rounding plus the bound of the rest.  Whether the kernel applied the low
 part shows in the mean error: the output is nearer the oracle on the
