@@ -6,7 +6,7 @@
 //   M = max_{c: l_c > 0} m_c,  L = sum_c l_c e^{m_c - M},
 //   out = sum_c o_c e^{m_c - M} / L   (zeros when no chunk holds a cell).
 // A CTA of four warps covers four query rows with one warp each when a row
-// has at most four chunks; otherwise a CTA of 4, 8 or 16 warps takes one row
+// has at most four chunks; otherwise a CTA of 2, 4 or 8 warps takes one row
 // (warp w takes chunks w, w + WPR, ...), so one round of loads covers up to
 // 4 * WPR chunks.  Lane k owns output dimensions 8k..8k+7.
 // Each warp forms its own (M_w, L_w, acc_w), four chunks at a time with all
@@ -21,7 +21,7 @@ namespace {
 constexpr int kHeadDimMerge = 256;
 
 // WPR warps per row: 1 (a CTA of four warps takes four rows, a warp per
-// row), or 2 / 4 / 8 / 16 (a CTA per row; warp w takes chunks w, w + WPR, ...).
+// row), or 2 / 4 / 8 (a CTA per row; warp w takes chunks w, w + WPR, ...).
 template <int WPR>
 __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(const Params p)
 {
@@ -158,18 +158,18 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
 
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
-    // a warp per row when rows have few chunks; otherwise a CTA per row with
-    // enough warps that one round of loads covers every chunk when possible:
-    // 16, 8 or 4 warps per row, the most that keep the grid within 32 warps
-    // per SM (16-warp CTAs hold 32 K registers, two per SM: more rows would
-    // run a second wave); with more rows than 4-warp CTAs fit in one wave
-    // (7 per SM), 2 warps per row (1,536 rows of 17 chunks: 30.4 -> 29.4 us
-    // per call)
+    // a warp per row when rows have few chunks; otherwise a CTA per row: 8
+    // warps for more than 16 chunks (one round of loads covers 32) while the
+    // grid stays within 32 warps per SM, else 4; with more rows than 4-warp
+    // CTAs fit in one wave (7 per SM), 2 warps per row (1,536 rows of 17
+    // chunks: 30.4 -> 29.4 us per call).  No wider CTA: the merge runs beside
+    // the next call's chunk kernel (it lets that grid launch at once), and a
+    // 16-warp CTA's 32 K registers kept chunk CTAs off its SM (one pair, 17
+    // chunks: 4.6 -> 3.8 us per call with 8 warps; 64 chunks: 5.8 -> 5.2)
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long rows = (long long)p.R * p.G * p.n_seq;
     const int wpr = p.n_chunks <= 4 ? 1
-                    : (p.n_chunks > 16 && rows * 16 <= 32ll * sms) ? 16
                     : (p.n_chunks > 16 && rows * 8 <= 32ll * sms) ? 8
                     : (rows * 4 <= 28ll * sms) ? 4 : 2;
     cudaLaunchConfig_t cfg = {};
@@ -185,8 +185,7 @@ cudaError_t launch_merge(const Params &p, cudaStream_t stream)
     if (wpr == 1) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1>, p);
     if (wpr == 4) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<4>, p);
     if (wpr == 8) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<8>, p);
-    if (wpr == 2) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<2>, p);
-    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<16>, p);
+    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<2>, p);
 }
 
 } // namespace qsa
