@@ -67,8 +67,10 @@ Workspace carve(const qsa_shape *s, int n_seq, int max_selected)
     w.off_o = align_up(w.off_l + rows * sizeof(float), kWorkspaceAlign);
     w.off_extra = align_up(w.off_o + rows * kHeadDim * sizeof(float), 1024);
     w.total = w.off_extra;
-    if (select_path(s) == kPathDecodeTc && n_chunks > 0)
-        w.total = w.off_extra + align_up(chunk_tc_query_image_bytes(n_seq, s->n_kv_heads, (int)R), 1024);
+    if (select_path(s) == kPathDecodeTc && n_chunks > 0) {
+        w.off_runs = w.off_extra + align_up(chunk_tc_query_image_bytes(n_seq, s->n_kv_heads, (int)R), 1024);
+        w.total = w.off_runs + align_up((size_t)n_seq * s->n_kv_heads * sizeof(int32_t), kWorkspaceAlign);
+    }
     if (select_path(s) == kPathPromptTc && n_chunks > 0) {
         size_t kb, qb, cb;
         prompt_image_bytes(n_seq, s->n_kv_heads, (int)R, s->chunk_cells, (int)n_chunks, &kb, &qb, &cb);
@@ -144,6 +146,7 @@ qsa_status run(const qsa_shape *s, int n_seq, const void *q, const int8_t *k_poo
     p.part_o = reinterpret_cast<float *>(ws + w.off_o);
     p.status = status;
     p.q_img = ws + w.off_extra;
+    p.part_runs = w.off_runs > 0 ? reinterpret_cast<int32_t *>(ws + w.off_runs) : nullptr;
     p.n_sel_single = n_sel_single;
     p.n_seq = n_seq;
     p.G = s->n_kv_heads;

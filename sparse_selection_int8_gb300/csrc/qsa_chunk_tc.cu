@@ -60,6 +60,7 @@
 // ends.  Before the CTA leaves, each issuing thread waits (with a bound of its
 // own) for its tensor-core operations and bulk copies, and each loader for its
 // asynchronous copies, so nothing is in flight when tensor memory is freed.
+#include <algorithm>
 #include <cuda_fp16.h>
 #include <float.h>
 
@@ -88,11 +89,23 @@ constexpr float kRescaleLog2 = 8.f; // the reference moves when a score exceeds 
 constexpr float kSigmaGrow = 16.f;  // ... sigma when a V scale exceeds 16 x sigma
 constexpr long long kDrainCycles = 1ll << 30; // bound of the waits before the CTA leaves
 
-// Position in the work list (see cursor_init_warp / cursor_next).
+// Position in the work list (see cursor_init_warp / cursor_next); lo and
+// per (the CTA's first item and the items per CTA) are set for the first item.
 struct Cursor {
     int b, g, c, nch, start, n;
     int remaining;
+    int per;
+    long long lo;
 };
+
+// Runs: a CTA accumulates up to kRunChunks consecutive chunks of one
+// (sequence, KV head) in one partial (m, l, o), so the partials written and
+// merged per row drop from the chunk count to about the number of CTAs that
+// share the pair.  Item y (of a row block's list) starts a run when its
+// offset in its CTA's range, y mod per, is a multiple of kRunChunks, or when
+// it is its pair's first chunk.  The k-th run of a pair is stored at partial
+// slot k; the pair's run count goes to part_runs for the merge.
+constexpr int kRunChunks = 8;
 
 struct Misc {
     // resolution rings (tile t in entry t % 4), filled by asynchronous copies
@@ -212,6 +225,8 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane, 
 {
     cur.b = cur.g = cur.c = cur.nch = cur.start = cur.n = 0;
     cur.remaining = 0;
+    cur.per = 1;
+    cur.lo = 0;
     long long per, rem, q, r;
     if (p.sel_offsets == nullptr) {
         // one sequence (the step entry): closed form, no scan
@@ -223,6 +238,8 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane, 
         const long long hi = min(lo + per, total);
         if (lo >= hi) return;
         cur.remaining = (int)(hi - lo);
+        cur.per = (int)per;
+        cur.lo = lo;
         cur.nch = nch;
         cur.start = s;
         cur.n = n;
@@ -241,6 +258,8 @@ __device__ inline void cursor_init_warp(const Params &p, Cursor &cur, int lane, 
     const long long hi = min(lo + per, total);
     if (lo >= hi) return;
     cur.remaining = (int)(hi - lo);
+    cur.per = (int)per;
+    cur.lo = lo;
     long long before = 0;
     for (int b0 = 0; b0 < p.n_seq; b0 += 32) {
         const int b = b0 + lane;
@@ -349,6 +368,43 @@ __device__ __forceinline__ int tile_cells(const TileIt &t) { return min(kTile, t
 __device__ __forceinline__ int tile_base(const Params &p, const TileIt &t)
 {
     return t.cur.start + t.cur.c * p.chunk_cells + t.ti * kTile;
+}
+
+// First / last tile of a run (rem0: the CTA's item count; rem0 - remaining
+// is the item's offset in the CTA's range).
+__device__ __forceinline__ bool run_first(const TileIt &t, int rem0)
+{
+    return t.ti == 0 && (t.cur.c == 0 || (rem0 - t.cur.remaining) % kRunChunks == 0);
+}
+
+__device__ __forceinline__ bool run_last(const TileIt &t, int rem0)
+{
+    return t.ti == t.nt - 1 &&
+           (t.cur.c == t.cur.nch - 1 || t.cur.remaining == 1 || (rem0 - t.cur.remaining + 1) % kRunChunks == 0);
+}
+
+// Items y in [0, n) whose offset in their CTA's range is a multiple of
+// kRunChunks: full ranges of per items hold ceil(per / kRunChunks) each.
+__device__ __forceinline__ long long run_starts_below(long long n, int per)
+{
+    long long q, r;
+    divmod_nn(n, per, q, r);
+    return q * ((per + kRunChunks - 1) / kRunChunks) + (r + kRunChunks - 1) / kRunChunks;
+}
+
+// Slot of the run that starts at item x, chunk c of its pair (the pair's
+// first item is x - c, a run start whatever its offset), and the pair's run
+// count.
+__device__ __forceinline__ int run_slot(long long x, int c, int per)
+{
+    if (c == 0 || per == 1) return c; // (an item per CTA: a run per chunk)
+    return (int)(1 + run_starts_below(x, per) - run_starts_below(x - c + 1, per));
+}
+
+__device__ __forceinline__ int run_count(long long pair0, int nch, int per)
+{
+    if (per == 1) return nch;
+    return (int)(1 + run_starts_below(pair0 + nch, per) - run_starts_below(pair0 + 1, per));
 }
 
 // ---------------------------------------------------------------- step a1
@@ -784,10 +840,11 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         constexpr int NK = N / 8;               // 16x256b repetitions over the score columns
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
         struct Pend {
-            int b, g, c, cp;
+            int b, g, k, cp, runs; // partial slot k; the pair's run count when k == 0
             bool on;
         };
-        Pend pend{0, 0, 0, 0, false};
+        Pend pend{0, 0, 0, 0, 0, false};
+        int run_k = 0, run_n = 0; // slot of the current run; its pair's run count (slot 0)
         // per row (index 2k + e = row 8k + 2u + e): the reference maximum (log2
         // units, the same in every thread that holds the row; -FLT_MAX until
         // the row's first valid score, when all its scores are -inf), and this
@@ -813,12 +870,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         // waited for the call before, comes first.)
         bool prev_done = !p.q_inline;
 
-        // partials of chunk e.cp: O read out of tensor memory, times sigma *
-        // 2^(mref - m), and the m and l that the chunk's end left in shared memory
+        // partials of run e.cp: O read out of tensor memory, times sigma *
+        // 2^(mref - m), and the m and l that the run's end left in shared memory
         auto epilogue = [&](const Pend &e) {
             wait(&ms.o_full[e.cp % L::OB], (uint32_t)(e.cp / L::OB) & 1u);
             tc_fence_after();
-            const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.c) * p.R + row0;
+            const size_t base = (((size_t)e.b * p.G + e.g) * p.n_chunks + e.k) * p.R + row0;
             const float *fin = ms.st_fin[e.cp & 1];
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
@@ -850,14 +907,15 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 p.part_m[base + c] = ms.st_m[e.cp & 1][c];
                 p.part_l[base + c] = ms.st_l[e.cp & 1][c];
             }
+            if (e.k == 0 && c == 0 && rblk == 0) p.part_runs[(size_t)e.b * p.G + e.g] = e.runs;
             tc_fence_before();
             mbar_arrive(&ms.o_empty[e.cp % L::OB]);
         };
 
-        // end of chunk cp: the rows' true maxima and sums across the CTA; the
+        // end of run cp: the rows' true maxima and sums across the CTA; the
         // row's owner leaves m, l and the factor its O is read out with in
         // shared memory for the epilogue
-        auto chunk_end = [&](int chunk) {
+        auto run_end = [&](int chunk) {
             const int cpar = chunk & 1;
             float cm[NR], cs[NR];
 #pragma unroll
@@ -915,9 +973,12 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
             mbar_arrive(&ms.q_full[0]);
         }
 
+        const int rem0 = first.remaining;
         for (int i = 0; it.valid; ++i) {
             const int par = i & 1;
-            const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
+            // first / last tile of a run (O, the row sums and maxima start
+            // afresh at a run's first tile; its partials go out after the last)
+            const bool first_t = run_first(it, rem0), last_t = run_last(it, rem0);
             if (it.seg != cur_seg) { // new (sequence, KV head): new rows, no reference yet
                 cur_seg = it.seg;
 #pragma unroll
@@ -931,6 +992,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     lsum[r] = 0.f;
                     cmax[r] = -INFINITY;
                 }
+                const long long x = ms.first.lo + (rem0 - it.cur.remaining);
+                run_k = run_slot(x, it.cur.c, ms.first.per);
+                run_n = run_k == 0 ? run_count(x - it.cur.c, it.cur.nch, ms.first.per) : 0;
             }
             wait(&ms.sc_full[par], (uint32_t)(i >> 1) & 1u);
             // this thread's four cells (16x256b layout): cell(ci) = 32q + 8ci + t/4,
@@ -1011,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 }
                 named_bar(kBarSoft, kSoftThreads);
                 // every thread takes the same decisions for the rows it holds;
-                // O of this chunk (if any is accumulated) is rescaled by rows
+                // O of this run (if any is accumulated) is rescaled by rows
                 bool resc = false;
 #pragma unroll
                 for (int k = 0; k < KR; ++k) {
@@ -1049,7 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                     inv_sig = 1.f / st;
                 }
                 if (named_bar_or(kBarSoft, kSoftThreads, resc)) {
-                    // P.V of the previous tile (same chunk) must be done
+                    // P.V of the previous tile (same run) must be done
                     if (PB == 2) wait(&ms.p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u);
                     else wait(&ms.p_empty[0], (uint32_t)(i - 1) & 1u);
                     tc_fence_after();
@@ -1100,8 +1164,8 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
                 pend.on = false;
             }
             if (last_t) {
-                chunk_end(cp);
-                pend = Pend{it.cur.b, it.cur.g, it.cur.c, cp, true};
+                run_end(cp);
+                pend = Pend{it.cur.b, it.cur.g, run_k, cp, run_n, true};
             }
             tile_next(p, it);
         }
@@ -1204,8 +1268,9 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
         TileIt it;
         tile_init(p, it, first);
         int cp = -1;
+        const int rem0 = first.remaining;
         for (int i = 0; it.valid; ++i) {
-            const bool first_t = it.ti == 0, last_t = it.ti == it.nt - 1;
+            const bool first_t = run_first(it, rem0), last_t = run_last(it, rem0); // of a run
             if (first_t) ++cp;
             wait(&ms.p_full[i % PB], (uint32_t)(i / PB) & 1u);
             wait(&ms.v_full[i & 1], (uint32_t)(i >> 1) & 1u);
@@ -1245,7 +1310,7 @@ __global__ void __launch_bounds__(kThreads, 1) qsa_chunk_tc_kernel(const Params 
 }
 
 template <int N, int KR, bool LIM = false>
-cudaError_t launch_n(const Params &p, cudaStream_t stream)
+cudaError_t launch_n(Params &p, cudaStream_t stream)
 {
     int dev = 0, sms = 0, max_smem = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1278,6 +1343,13 @@ cudaError_t launch_n(const Params &p, cudaStream_t stream)
     const int n_rb = p.row_blocks > 1 ? p.row_blocks : 1;
     const long long per_rb = items < sms / n_rb ? items : sms / n_rb;
     if (per_rb < 1) return cudaErrorInvalidConfiguration;
+    // items per CTA when every list is full (the kernel's count is at most
+    // this): above one, CTAs combine runs of chunks and the merge reads the
+    // run counts; its CTA shape follows the slots a row then has
+    const long long per = (items + per_rb - 1) / per_rb;
+    const long long run = per < kRunChunks ? per : kRunChunks;
+    p.runs = per > 1 ? 1 : 0;
+    p.merge_slots = (int)(per > 1 ? std::min<long long>(p.n_chunks, (p.n_chunks + run - 1) / run + 1) : p.n_chunks);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(per_rb * n_rb));
     cfg.blockDim = dim3(kThreads);
@@ -1298,12 +1370,11 @@ size_t chunk_tc_query_image_bytes(int n_seq, int G, int R)
     return (size_t)n_seq * G * (N + 48) * 512 * 2;
 }
 
-cudaError_t launch_chunk_tc(const Params &p_in, cudaStream_t stream)
+cudaError_t launch_chunk_tc(Params &p, cudaStream_t stream)
 {
-    if (p_in.n_chunks == 0) return cudaSuccess;
+    if (p.n_chunks == 0) return cudaSuccess;
     // one (sequence, KV head): every CTA works on the same query tile and
     // converts it itself, so the call is two kernels (chunk, merge)
-    Params p = p_in;
     p.q_inline = p.n_seq * p.G == 1 ? 1 : 0;
     p.row_blocks = 1;
     p.rb_rows = p.R;

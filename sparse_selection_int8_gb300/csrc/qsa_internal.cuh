@@ -38,6 +38,10 @@ struct Params {
     float *part_m;             // [n_seq][G][n_chunks][R]
     float *part_l;
     float *part_o;             // [n_seq][G][n_chunks][R][D]
+    int32_t *part_runs;        // decode tensor-core path: [n_seq][G] partial slots written
+    int32_t runs;              // 1: slot k of a pair holds its k-th run of chunks (part_runs
+                               // slots), 0: slot c holds chunk c
+    int32_t merge_slots;       // slots per row the merge expects (its CTA shape; 0: n_chunks)
     uint32_t *status;          // optional
     void *q_img;               // decode tensor-core path: [n_seq][G] f16 query tiles (workspace)
     int32_t q_inline;          // decode tensor-core path, one (sequence, KV head): the chunk
@@ -68,7 +72,7 @@ struct PromptImages {
 
 // Workspace carve-up shared by the host code of every path.
 struct Workspace {
-    size_t off_m, off_l, off_o, off_extra, total;
+    size_t off_m, off_l, off_o, off_extra, off_runs, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -149,7 +153,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16)
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_chunk_simt(const Params &p, cudaStream_t stream);
 size_t chunk_tc_query_image_bytes(int n_seq, int G, int R);
-cudaError_t launch_chunk_tc(const Params &p, cudaStream_t stream);
+cudaError_t launch_chunk_tc(Params &p, cudaStream_t stream); // sets p.runs, p.merge_slots
 size_t prompt_image_bytes(int n_seq, int G, int R, int chunk_cells, int n_chunks, size_t *k_bytes,
                           size_t *q_bytes, size_t *cell_bytes);
 cudaError_t launch_prompt_tc(const Params &p, const PromptImages &im, cudaStream_t stream);

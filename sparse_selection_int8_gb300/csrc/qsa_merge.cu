@@ -5,8 +5,12 @@
 // of a row carries (m_c, l_c, o_c) with m in natural-log units; the merge is
 //   M = max_{c: l_c > 0} m_c,  L = sum_c l_c e^{m_c - M},
 //   out = sum_c o_c e^{m_c - M} / L   (zeros when no chunk holds a cell).
+// The tensor-core decode kernel may combine a run of consecutive chunks of a
+// (sequence, KV head) into one partial (same m, l, o over the run's cells);
+// then slots 0 .. part_runs[b][g] - 1 of the pair hold its runs, and the
+// merge is the same over those slots.
 // A CTA of four warps covers four query rows with one warp each when a row
-// has at most four chunks; otherwise a CTA of 2, 4 or 8 warps takes one row
+// has at most four slots; otherwise a CTA of 2, 4 or 8 warps takes one row
 // (warp w takes chunks w, w + WPR, ...), so one round of loads covers up to
 // 4 * WPR chunks.  Lane k owns output dimensions 8k..8k+7.
 // Each warp forms its own (M_w, L_w, acc_w), four chunks at a time with all
@@ -21,8 +25,10 @@ namespace {
 constexpr int kHeadDimMerge = 256;
 
 // WPR warps per row: 1 (a CTA of four warps takes four rows, a warp per
-// row), or 2 / 4 / 8 (a CTA per row; warp w takes chunks w, w + WPR, ...).
-template <int WPR>
+// row), or 2 / 4 / 8 (a CTA per row; warp w takes slots w, w + WPR, ...).
+// RUNS: the slots are the pair's runs (their count is read first) rather
+// than its chunks (loaded at once, masked by the list length when it comes).
+template <int WPR, bool RUNS>
 __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(const Params p)
 {
     constexpr int kWarps = WPR == 1 ? 4 : WPR;
@@ -49,14 +55,17 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
     }
     const size_t base = ((size_t)b * p.G + g) * p.n_chunks * p.R + r;
     const size_t stride = (size_t)p.R; // chunk stride of m and l
-    // a round: kRound chunks per warp, every load issued together (the list
-    // length is only needed to mask them, so its read overlaps the loads),
-    // then folded in with a running maximum
+    // a round: kRound slots per warp, every load issued together (with a
+    // slot per chunk the list length is only needed to mask them, so its
+    // read overlaps the loads), then folded in with a running maximum
     int start, n;
     seq_range(p, b, &start, &n);
+    // slots that may be loaded: every chunk slot, or the pair's runs
+    const int lim = !RUNS ? p.n_chunks
+                    : n > 0 ? min(max(p.part_runs[(size_t)b * p.G + g], 0), p.n_chunks) : 0;
     float M = -INFINITY, Lpart = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c0 = w; c0 < p.n_chunks; c0 += kRound * WPR) {
+    for (int c0 = w; c0 < lim; c0 += kRound * WPR) {
         float mu[kRound], lu[kRound];
         float4 ou[kRound][2];
 #pragma unroll
@@ -64,7 +73,7 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
             const int c = c0 + u * WPR;
             mu[u] = -INFINITY;
             lu[u] = 0.f;
-            if (c < p.n_chunks) {
+            if (c < lim) {
                 const size_t idx = base + (size_t)c * stride;
                 mu[u] = p.part_m[idx];
                 lu[u] = p.part_l[idx];
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
                 ou[u][1] = src[1];
             }
         }
-        const int n_chunks = n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0;
+        const int n_chunks = RUNS ? lim : n > 0 ? (n + p.chunk_cells - 1) / p.chunk_cells : 0; // valid slots
         bool ok[kRound];
         float gm = -INFINITY;
 #pragma unroll
@@ -169,8 +178,9 @@ cudaError_t launch_merge(const Params &p, cudaStream_t stream)
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long rows = (long long)p.R * p.G * p.n_seq;
-    const int wpr = p.n_chunks <= 4 ? 1
-                    : (p.n_chunks > 16 && rows * 8 <= 32ll * sms) ? 8
+    const int slots = p.merge_slots > 0 ? p.merge_slots : p.n_chunks; // expected per row
+    const int wpr = slots <= 4 ? 1
+                    : (slots > 16 && rows * 8 <= 32ll * sms) ? 8
                     : (rows * 4 <= 28ll * sms) ? 4 : 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(wpr == 1 ? (p.R + 3) / 4 : p.R), (unsigned)p.G, (unsigned)p.n_seq);
@@ -182,10 +192,16 @@ cudaError_t launch_merge(const Params &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (wpr == 1) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1>, p);
-    if (wpr == 4) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<4>, p);
-    if (wpr == 8) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<8>, p);
-    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<2>, p);
+    if (p.runs) {
+        if (wpr == 1) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1, true>, p);
+        if (wpr == 4) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<4, true>, p);
+        if (wpr == 8) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<8, true>, p);
+        return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<2, true>, p);
+    }
+    if (wpr == 1) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<1, false>, p);
+    if (wpr == 4) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<4, false>, p);
+    if (wpr == 8) return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<8, false>, p);
+    return cudaLaunchKernelEx(&cfg, qsa_merge_kernel<2, false>, p);
 }
 
 } // namespace qsa

@@ -18,8 +18,10 @@ computes, for one query row against the cells i of its (sequence, KV head):
                                             documented accuracy)
   5. P'_i = f16(p_i * v_scale_i / sigma)    relative u16 while P' is a normal
                                             f16; absolute 2^-25 when subnormal
-  6. o = sigma * sum_i P'_i vcode_i, l = sum_i p_i in fp32, merged in fp32
-     with approximate exponentials (relative error <= 2^-20 per chunk weight).
+  6. o = sigma * sum_i P'_i vcode_i, l = sum_i p_i in fp32 over a partial's
+     cells (a chunk, or a run of up to RUN_CHUNKS consecutive chunks that one
+     CTA accumulates), merged in fp32 with approximate exponentials (relative
+     error <= 2^-20 per partial's weight).
 
 Step 1 is removed exactly by comparing with the fp64 oracle run on the
 kernel's queries q' (``refq``).  Steps 2-6 perturb cell i of a row by a
@@ -39,9 +41,10 @@ where s_i bounds the standard deviation of cell i's score error: the MMA's
 sum of n products has a rounding error sum_k delta_k S_k (S_k its partial
 sums, |delta_k| <= u32), of standard deviation <= sqrt(n) * u32 * sum |terms|,
 plus the fp32 scaling and the exponential as in E_i.
-with S1_d = sum_i w_i |v_id| and acc_d = ((C + 8) * 2 u32 + 2 * 2^-20) * (S1_d + |o_d|)
-for the fp32 sums of a chunk of C cells and the merge (its weights in numerator
-and denominator).  The factor 1.01 covers
+with S1_d = sum_i w_i |v_id| and acc_d = ((U + n_c) * 2 u32 + 2 * 2^-20) * (S1_d + |o_d|)
+for the fp32 sums of a partial of at most U = min(RUN_CHUNKS * C, n) cells (n
+the pair's cells, C the chunk size) and the merge of at most n_c = ceil(n / C)
+partials (its weights in numerator and denominator), in any order.  The factor 1.01 covers
 second-order terms while max E_i < 1e-2 (e^E - 1 - E <= E^2 < E / 100;
 checked).
 
@@ -67,6 +70,7 @@ EXP2_REL = 2.0 ** -20
 LAMBDA = 7.0
 SUB_MIN = 2.0 ** -14   # smallest normal f16
 SUB_HALF_ULP = 2.0 ** -25
+RUN_CHUNKS = 8         # chunks a CTA may accumulate into one partial
 
 
 def f16_round(q: np.ndarray) -> np.ndarray:
@@ -108,10 +112,10 @@ def cells_of(p, b: int, g: int):
     return kc, vc, ks, vs
 
 
-def bounds(p, q_rows: np.ndarray, b: int, g: int, split: bool = True):
+def bounds(p, q_rows: np.ndarray, b: int, g: int, split: bool = True, run_chunks: int = RUN_CHUNKS):
     """Bounds A, B (steps 2-6) and A_q (step 1) for the query rows q_rows
     [R][D] (fp32 values) of (sequence b, KV head g): arrays [R][D], plus the
-    largest E_i."""
+    largest E_i.  run_chunks: chunks that one partial may span."""
     kc, vc, ks, vs = cells_of(p, b, g)
     R, D = q_rows.shape
     if kc.shape[0] == 0:
@@ -143,7 +147,9 @@ def bounds(p, q_rows: np.ndarray, b: int, g: int, split: bool = True):
     A_sub = a_scale * ((flag / L) @ np.abs(vc))
     B_sub = a_scale * np.sqrt((flag / L ** 2) @ (vc * vc))
     C = int(p.chunk_cells)
-    acc = ((C + 8) * 2 * U32 + 2 * EXP2_REL) * (S1 + np.abs(o))
+    n = kc.shape[0]
+    U = min(run_chunks * C, n)
+    acc = ((U + -(-n // C)) * 2 * U32 + 2 * EXP2_REL) * (S1 + np.abs(o))
     A = 1.01 * (U16 * S1 + WE @ av + np.abs(o) * WE.sum(axis=1, keepdims=True) + A_sub) + acc
     sd = (scale * ks[None, :] * np.sqrt(nsum) * U32 * (mag @ np.abs(kc).T)
           + 2 * U32 * np.abs(x) + EXP2_REL)
@@ -157,10 +163,11 @@ def bounds(p, q_rows: np.ndarray, b: int, g: int, split: bool = True):
     return A, B, Aq, float(E.max())
 
 
-def problem_bounds(p, split: bool = None):
+def problem_bounds(p, split: bool = None, run_chunks: int = RUN_CHUNKS):
     """Bounds for every output row of a decode problem (f32 queries, no causal
     limits): A, B, A_q shaped like the output [B][T][G*H][D], and max E.
-    ``split``: the kernel's query split (default: as the kernel takes it)."""
+    ``split``: the kernel's query split (default: as the kernel takes it);
+    ``run_chunks``: chunks that one partial may span (1: a partial per chunk)."""
     if split is None:
         split = split_applies(p)
     T, G, H, D = p.n_queries, p.n_kv_heads, p.q_per_kv, p.head_dim
@@ -171,7 +178,7 @@ def problem_bounds(p, split: bool = None):
     for b in range(p.n_seq):
         for g in range(G):
             rows = q[b, :, g * H:(g + 1) * H, :].reshape(T * H, D)
-            a, bb, aq, em = bounds(p, rows, b, g, split)
+            a, bb, aq, em = bounds(p, rows, b, g, split, run_chunks)
             A[b, :, g * H:(g + 1) * H, :] = a.reshape(T, H, D)
             B[b, :, g * H:(g + 1) * H, :] = bb.reshape(T, H, D)
             Aq[b, :, g * H:(g + 1) * H, :] = aq.reshape(T, H, D)

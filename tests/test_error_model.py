@@ -3,7 +3,8 @@
 A numpy emulation of the tensor-core kernel's arithmetic (queries split into
 f16 hi + lo, fp32 scores, f16 P', fp32 sums and merge) must stay inside bounds
 A and B against the fp64 oracle on the kernel's queries hi + lo, and inside
-A + A_q against the oracle on the caller's queries.  Planted changes of the
+A + A_q against the oracle on the caller's queries, with a partial per chunk
+and with partials over runs of chunks.  Planted changes of the
 arithmetic (P' rounded to bf16; queries rounded to bf16) must leave bound B:
 it is not vacuous.  Queries rounded to f16 with no low part stay inside B (the
 query rounding is about as large as the P' rounding), so whether the low part
@@ -25,9 +26,10 @@ def _built():
     oracle.build()
 
 
-def emulate(p, p_round=np.float16, q_round="split"):
-    """The kernel's arithmetic in numpy: chunk partials against the chunk's
-    maximum with sigma = the chunk's largest V scale, merged in fp32."""
+def emulate(p, p_round=np.float16, q_round="split", run_chunks=1):
+    """The kernel's arithmetic in numpy: partials over runs of run_chunks
+    chunks (one chunk by default) against the run's maximum with sigma = the
+    run's largest V scale, merged in fp32."""
     T, G, H, D = p.n_queries, p.n_kv_heads, p.q_per_kv, p.head_dim
     out = np.zeros((p.n_seq, T, G * H, D), np.float32)
     log2e = np.float32(1.0 / np.log(2.0))
@@ -52,7 +54,7 @@ def emulate(p, p_round=np.float16, q_round="split"):
             else:
                 S = q16 @ kc.astype(np.float32).T                # fp32 sums
             x = (S * ksc[None, :]).astype(np.float32)            # log2 units
-            C = p.chunk_cells
+            C = p.chunk_cells * run_chunks
             ms, ls, os_ = [], [], []
             for c0 in range(0, kc.shape[0], C):
                 xc = x[:, c0:c0 + C]
@@ -85,7 +87,7 @@ PROBLEMS = {
 @pytest.fixture(scope="module", params=sorted(PROBLEMS))
 def case(request):
     p = PROBLEMS[request.param]()
-    A, B, Aq, emax = em.problem_bounds(p)
+    A, B, Aq, emax = em.problem_bounds(p, run_chunks=1)  # the emulation: a partial per chunk
     ref64 = oracle.decode_attn(p)
     ref16 = oracle.decode_attn(em.with_kernel_queries(p))
     return request.param, p, A, B, Aq, emax, ref64, ref16
@@ -101,6 +103,18 @@ def test_emulated_kernel_inside_bounds(case):
     assert np.all(np.abs(out - ref64) <= A + Aq), name
     # the query rounding alone stays inside its a-priori bound
     assert np.all(np.abs(ref16 - ref64) <= Aq), name
+
+
+@pytest.mark.parametrize("run_chunks", [3, 8])
+def test_emulated_runs_inside_the_default_bounds(case, run_chunks):
+    """Partials over runs of up to RUN_CHUNKS chunks (as one CTA accumulates
+    them) stay inside the bounds taken for such runs."""
+    name, p, A, B, Aq, emax, ref64, ref16 = case
+    A8, B8, Aq8, _ = em.problem_bounds(p)
+    out = emulate(p, run_chunks=run_chunks)
+    d16 = np.abs(out - ref16)
+    assert np.all(d16 <= B8) and np.all(d16 <= A8), (name, float((d16 / B8).max()))
+    assert np.all(np.abs(out - ref64) <= A8 + Aq8), name
 
 
 def test_p_in_bf16_leaves_the_bounds(case):
@@ -132,7 +146,7 @@ def test_f16_only_model_holds_for_f16_only_arithmetic(case):
     """The bounds for hi alone (windows of more than 64 rows over several
     pairs) hold for the emulation that uses hi alone."""
     name, p, A, B, Aq, emax, ref64, ref16 = case
-    A1, B1, Aq1, _ = em.problem_bounds(p, split=False)
+    A1, B1, Aq1, _ = em.problem_bounds(p, split=False, run_chunks=1)
     r1 = oracle.decode_attn(em.with_kernel_queries(p, split=False))
     out = emulate(p, q_round=np.float16)
     d = np.abs(out - r1)
