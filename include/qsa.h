@@ -206,6 +206,12 @@ qsa_status qsa_decode_attn_batch_limited(const qsa_shape *shape, int32_t n_seq, 
  * b: m = max score (natural-log units, -inf when the chunk has no valid
  * cell), l = sum exp(s - m), o = sum exp(s - m) * v_hat.  Chunks at or past
  * ceil(n_b / C) are not written.  Any of m, l, o may be NULL.
+ * A decode-window call (at most 80 rows per KV head, tensor-core path) with
+ * more chunks than its CTAs (n_seq * G * n_chunks above the SM count, per
+ * block of rows) lets a CTA accumulate up to eight consecutive chunks of a
+ * (sequence, KV head) into one partial, the same m, l, o over those cells:
+ * slot k then holds the pair's k-th such run, in chunk order, and the slots
+ * past its last run are not written.
  */
 qsa_status qsa_partials_view(const qsa_shape *shape, int32_t n_seq, int32_t max_selected,
                              const void *workspace, const float **m, const float **l,

@@ -3,7 +3,12 @@
 // What it computes is the chunk step of "Strata PR #2220,
 // attn_chunk_q8_v3_kernel": each chunk of the selected list yields partials
 // (max m, sum of exponentials l, unnormalised P.V o) for every query row
-// (T queries x H heads of one KV head).  The pages' Turing kernel reads each
+// (T queries x H heads of one KV head).  Where a CTA takes several
+// consecutive chunks of one (sequence, KV head) -- more chunks than CTAs --
+// it accumulates up to eight of them into one partial: the same m, l, o
+// over the run's cells, which the merge combines exactly as it would the
+// chunks' own (the pages' split into chunks is the unit of work; partials
+// per chunk only add stores and merge reads).  The pages' Turing kernel reads each
 // cell once for all 12 heads and does the dot products with warp shuffles;
 // here both contractions run on the 5th-generation tensor cores with the
 // cells on the MMA's M dimension, because a decode window has only 12-80
@@ -32,8 +37,8 @@
 // leaves the reference's range; only then (the first tile of a pair, or a
 // score that jumps by 2^8) do they reduce the tile's true row maxima and move
 // the reference, rescaling l and O.  Row sums and row maxima are kept per
-// thread and reduced across the CTA once per chunk, where the partials are
-// brought to the chunk's true maximum: m = max score, l = sum 2^(s - m),
+// thread and reduced across the CTA once per run, where the partials are
+// brought to the run's true maximum: m = max score, l = sum 2^(s - m),
 // o = sum 2^(s - m) v_hat.
 //
 // One persistent CTA per SM walks a contiguous range of non-empty (sequence,
