@@ -507,37 +507,60 @@ __device__ __forceinline__ void q_piece_cvt2(const Params &p, const QRaw &q, uin
 // the chunk kernel brings a pair's tile in with one bulk copy.  One thread
 // per 16-byte piece.
 template <int N>
-__global__ void __launch_bounds__(256) qsa_query_stage_kernel(const Params p)
+__global__ void __launch_bounds__(128) qsa_query_stage_kernel(const Params p)
 {
     // Launched as a programmatic dependent of the kernel before the call on
     // the stream (if any, the previous call's merge).  The chunk kernel may
     // launch at once: before it waits for this grid it only reads the
-    // caller's inputs (list, page table, pools).  This kernel then waits for
-    // the kernel before it, whose chunk kernel may still be reading the query
-    // images, before it rewrites them; so once this grid is complete the call
-    // before is too, and the chunk kernel's wait for it covers its partial
-    // writes as well.
+    // caller's inputs (list, page table, pools).  This kernel reads and
+    // converts its pieces of the caller's queries, then waits for the kernel
+    // before it, whose chunk kernel may still be reading the query images,
+    // before it writes them; so once this grid is complete the call before
+    // is too, and the chunk kernel's wait for it covers its partial writes as
+    // well.  A grid of at most one 128-thread CTA per SM (each thread takes
+    // pieces e, e + stride, ...), so the grid is soon resident and lets the
+    // chunk kernel launch.
     cudaTriggerProgrammaticLaunchCompletion();
-    cudaGridDependencySynchronize();
     // one image per (pair, row block): rows rb * rb_rows .. of the pair
     const int n_rb = p.row_blocks > 1 ? p.row_blocks : 1;
     const int rb_rows = n_rb > 1 ? p.rb_rows : p.R;
-    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long pieces = (long long)p.n_seq * p.G * n_rb * N * 32;
-    if (e >= pieces) return;
-    const int img_i = (int)(e / (N * 32));
-    const int bg = img_i / n_rb, rblk = img_i % n_rb;
-    const int r = (int)((e / 32) % N), pc = (int)(e % 32);
-    const int row = rblk * rb_rows + r;
-    uint4 v = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-    if (r < rb_rows && row < p.R) {
-        const int esz = p.q_bf16 ? 2 : 4;
-        q_piece_cvt2(p, q_piece_load(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, row) * esz, pc), v, lo);
-    }
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long e0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     constexpr int QSF = Lay<N>::QSF;
-    uint8_t *img = static_cast<uint8_t *>(p.q_img) + (size_t)img_i * N * 512 * QSF + kmajor_sw128_off(r, pc * 8, N);
-    *reinterpret_cast<uint4 *>(img) = v;
-    if (QSF == 2) *reinterpret_cast<uint4 *>(img + N * 512) = lo;
+    auto convert = [&](long long e, uint4 &v, uint4 &lo) {
+        const int img_i = (int)(e / (N * 32));
+        const int bg = img_i / n_rb, rblk = img_i % n_rb;
+        const int r = (int)((e / 32) % N), pc = (int)(e % 32);
+        const int row = rblk * rb_rows + r;
+        v = make_uint4(0, 0, 0, 0);
+        lo = make_uint4(0, 0, 0, 0);
+        if (r < rb_rows && row < p.R) {
+            const int esz = p.q_bf16 ? 2 : 4;
+            q_piece_cvt2(p, q_piece_load(p, static_cast<const uint8_t *>(p.q) + q_row_offset(p, bg / p.G, bg % p.G, row) * esz, pc), v, lo);
+        }
+    };
+    auto store = [&](long long e, const uint4 &v, const uint4 &lo) {
+        const int img_i = (int)(e / (N * 32));
+        const int r = (int)((e / 32) % N), pc = (int)(e % 32);
+        uint8_t *img = static_cast<uint8_t *>(p.q_img) + (size_t)img_i * N * 512 * QSF + kmajor_sw128_off(r, pc * 8, N);
+        *reinterpret_cast<uint4 *>(img) = v;
+        if (QSF == 2) *reinterpret_cast<uint4 *>(img + N * 512) = lo;
+    };
+    constexpr int kEarly = 4; // pieces per thread converted before the wait
+    uint4 hv[kEarly], lv[kEarly];
+#pragma unroll
+    for (int k = 0; k < kEarly; ++k)
+        if (e0 + k * stride < pieces) convert(e0 + k * stride, hv[k], lv[k]);
+    cudaGridDependencySynchronize();
+#pragma unroll
+    for (int k = 0; k < kEarly; ++k)
+        if (e0 + k * stride < pieces) store(e0 + k * stride, hv[k], lv[k]);
+    for (long long e = e0 + kEarly * stride; e < pieces; e += stride) {
+        uint4 v, lo;
+        convert(e, v, lo);
+        store(e, v, lo);
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -1335,8 +1358,9 @@ cudaError_t launch_n(Params &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (!p.q_inline) {
         cudaLaunchConfig_t scfg = {};
-        scfg.gridDim = dim3((unsigned)((pieces + 255) / 256));
-        scfg.blockDim = dim3(256);
+        const long long blocks = (pieces + 127) / 128;
+        scfg.gridDim = dim3((unsigned)(blocks < sms ? blocks : sms));
+        scfg.blockDim = dim3(128);
         scfg.stream = stream;
         scfg.attrs = attr;
         scfg.numAttrs = 1;
