@@ -167,11 +167,12 @@ __global__ void __launch_bounds__(WPR == 1 ? 128 : WPR * 32) qsa_merge_kernel(co
 
 cudaError_t launch_merge(const Params &p, cudaStream_t stream)
 {
-    // a warp per row when rows have few chunks; otherwise a CTA per row: 8
-    // warps for more than 16 chunks (one round of loads covers 32) while the
-    // grid stays within 32 warps per SM, else 4; with more rows than 4-warp
-    // CTAs fit in one wave (7 per SM), 2 warps per row (1,536 rows of 17
-    // chunks: 30.4 -> 29.4 us per call).  No wider CTA: the merge runs beside
+    // a warp per row when rows have few slots (chunks, or the runs the chunk
+    // kernel expects to form); otherwise a CTA per row: 8 warps for more than
+    // 16 slots (one round of loads covers 32) while the grid stays within 32
+    // warps per SM, else 4; with more rows than 4-warp CTAs fit in one wave
+    // (7 per SM), 2 warps per row (1,536 rows of 17 chunks: 30.4 -> 29.4 us
+    // per call).  No wider CTA: the merge runs beside
     // the next call's chunk kernel (it lets that grid launch at once), and a
     // 16-warp CTA's 32 K registers kept chunk CTAs off its SM (one pair, 17
     // chunks: 4.6 -> 3.8 us per call with 8 warps; 64 chunks: 5.8 -> 5.2)
