@@ -30,6 +30,7 @@ import copy
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -203,10 +204,13 @@ class ClockSampler:
 
 
 def source_digest(*names) -> str:
+    """Digest of the sources' code: line comments and blank lines left out,
+    so an edit of comments alone keeps a recorded figure valid."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "sparse_selection_int8_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sparse_selection_int8_gb300", "csrc", n), encoding="utf-8") as f:
+            lines = (re.sub(r"//.*$", "", line).rstrip() for line in f.read().splitlines())
+            h.update("\n".join(line for line in lines if line.strip()).encode())
     return h.hexdigest()[:16]
 
 
@@ -214,7 +218,7 @@ def source_digest(*names) -> str:
 # only while the kernel source hashes to the recorded digest.
 TRAFFIC = {
     # qsa_decode T = 1..4, chunk kernel, sum of the four launches (ncu dram__bytes_read + write)
-    "b65686c4a939d7da": 6085632,
+    "5f55a077cff0d480": 6085632,
 }
 
 # Sources of the chunk kernel the recorded traffic belongs to.

@@ -499,13 +499,12 @@ __device__ __forceinline__ void q_piece_cvt2(const Params &p, const QRaw &q, uin
     lo = make_uint4(pack_f16x2(r[0], r[1]), pack_f16x2(r[2], r[3]), pack_f16x2(r[4], r[5]), pack_f16x2(r[6], r[7]));
 }
 
-
 // Query tiles of every (sequence, KV head) pair, written once per call into
 // the workspace in exactly the shared-memory layout the MMA reads (f16,
 // K-major, 128-byte swizzle, contraction index permuted as above, rows >= R
 // zero; the high parts, then the low parts where the layout has them), so
-// the chunk kernel brings a pair's tile in with one bulk copy.  One thread
-// per 16-byte piece.
+// the chunk kernel brings a pair's tile in with one bulk copy.  A thread
+// converts 16-byte pieces (eight elements) of it.
 template <int N>
 __global__ void __launch_bounds__(128) qsa_query_stage_kernel(const Params p)
 {
