@@ -59,6 +59,20 @@ def test_workspace_bytes_layout(lib):
     assert qsa.qsa_workspace_bytes(s, 8, 2051) >= 8 * rows * 258 * 4
 
 
+@pytest.mark.parametrize("n_seq,G,T", [(1, 1, 4), (8, 2, 2), (16, 2, 4), (3, 3, 1)])
+def test_decode_workspace_holds_query_images_and_run_counts(lib, n_seq, G, T):
+    """The tensor-core decode path's workspace is the partials (as the
+    CUDA-core path's) plus the staged query images, (N + 48) rows of 1 KB per
+    (sequence, KV head) with N the rows rounded up to 16 (1,024-byte aligned),
+    plus one int32 run count per (sequence, KV head) (256-byte aligned)."""
+    def align(v, a):
+        return -(-v // a) * a
+    tc = qsa.qsa_workspace_bytes(shape(n_queries=T, n_kv_heads=G, algo=qsa.QSA_ALGO_TCGEN05), n_seq, 2051)
+    simt = qsa.qsa_workspace_bytes(shape(n_queries=T, n_kv_heads=G, algo=qsa.QSA_ALGO_SIMT), n_seq, 2051)
+    N = -(-(12 * T) // 16) * 16
+    assert tc - simt == align(n_seq * G * (N + 48) * 512 * 2, 1024) + align(n_seq * G * 4, 256)
+
+
 def test_partials_view_offsets(lib):
     s = shape(n_queries=2, chunk_cells=256, n_kv_heads=2)
     base = 1 << 20
