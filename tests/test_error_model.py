@@ -162,3 +162,14 @@ def test_row_norm_bound(case):
     lhs = np.linalg.norm((out - ref64).reshape(-1, D), axis=1)
     rhs = np.linalg.norm((ref16 - ref64).reshape(-1, D), axis=1) + np.linalg.norm(B.reshape(-1, D), axis=1)
     assert np.all(lhs <= rhs), name
+
+
+def test_run_cap_matches_the_kernel():
+    """The bounds take a partial's fp32 sums over at most RUN_CHUNKS chunks:
+    the decode kernel's own cap on the chunks a CTA accumulates."""
+    import os
+    import re
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "sparse_selection_int8_gb300", "csrc", "qsa_chunk_tc.cu")
+    m = re.search(r"constexpr int kRunChunks = (\d+);", open(src).read())
+    assert m and int(m.group(1)) == em.RUN_CHUNKS
